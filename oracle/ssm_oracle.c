@@ -1,0 +1,173 @@
+/*
+ * ssm_oracle.c -- fp64 CPU oracle for the selective-scan linear recurrence.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, strictly
+ * sequential definition of what the GPU library computes.  Only the tests,
+ * the smoke check and the benchmark's CPU-baseline leg may load it.  It
+ * shares no code, header or constant with the CUDA path.
+ *
+ * Sources (web pages, by title and section):
+ *   [P1] "scan output is different between sequential and parallel
+ *        versions" (alxndrTL/mamba.py issue 26): the shape API of
+ *        selective_scan / selective_scan_seq -- x, delta (Bs,L,ED),
+ *        A (ED,N), B, C (Bs,L,N), D (ED) -> y (Bs,L,ED) -- and the
+ *        sequential form selective_scan_seq that this file writes out.
+ *   [P2] "Some questions of Bi-Mamba2 and Hydra" (Hprairie/Bi-Mamba2
+ *        issue 1): the chunked scalar-decay scan's argument list
+ *        (x, dt, A, B, C, chunk_size, D, ...) and the bidirectional
+ *        reading "the addition of two separate SSMs, plus D x(t)" with
+ *        weights shared between the two scans.
+ *
+ * The recurrence itself is not printed on the pages; the plainest reading
+ * that they support (Mamba zero-order-hold discretisation) is used:
+ *
+ *   diagonal A, per (b, e, n):
+ *     h_t[n] = exp(delta_t * A[e,n]) * h_{t-1}[n] + delta_t * B_t[n] * x_t
+ *     y_t    = sum_n C_t[n] * h_t[n] + D[e] * x_t,          h_{-1} = 0
+ *
+ *   scalar A per head (SSD form), per (b, h), state H_t in R^{P x N}:
+ *     H_t[p][n] = exp(dt_t * A_h) * H_{t-1}[p][n] + dt_t * x_t[p] * B_t[n]
+ *     y_t[p]    = sum_n H_t[p][n] * C_t[n] + D_h * x_t[p],   H_{-1} = 0
+ *
+ *   bidirectional: y = F(x) + flip(F(flip(x))) + D x, where F is the SSD
+ *   recurrence above without the D term and flip reverses the time axis
+ *   of x, dt, B and C together.  D x is added once.
+ *
+ * All arrays are dense row-major (last index fastest) fp64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Diagonal selective scan, sequential over t for every (b, e) channel.
+ * x, delta, y: (Bs, L, ED); A: (ED, N); B, C: (Bs, L, N); D: (ED) or NULL.
+ * Channels listed in [c_begin, c_end) of the flattened (b, e) index are
+ * computed; the rest of y is left untouched (lets a caller time a sample).
+ */
+void oracle_diag_scan_range(const double *x, const double *delta,
+                            const double *A, const double *B, const double *C,
+                            const double *D, double *y, int64_t Bs, int64_t L,
+                            int64_t ED, int64_t N, int64_t c_begin,
+                            int64_t c_end, int nthreads) {
+    set_threads(nthreads);
+    if (c_end > Bs * ED) c_end = Bs * ED;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t c = c_begin; c < c_end; ++c) {
+        const int64_t b = c / ED, e = c % ED;
+        double *h = (double *)calloc((size_t)N, sizeof(double));
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t i = (b * L + t) * ED + e;   /* x, delta, y */
+            const int64_t r = (b * L + t) * N;        /* B, C row     */
+            const double dl = delta[i], xv = x[i];
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double a = exp(dl * A[e * N + n]);
+                h[n] = a * h[n] + dl * B[r + n] * xv;
+                acc += C[r + n] * h[n];
+            }
+            y[i] = acc + (D ? D[e] * xv : 0.0);
+        }
+        free(h);
+    }
+}
+
+void oracle_diag_scan(const double *x, const double *delta, const double *A,
+                      const double *B, const double *C, const double *D,
+                      double *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
+                      int nthreads) {
+    oracle_diag_scan_range(x, delta, A, B, C, D, y, Bs, L, ED, N, 0, Bs * ED,
+                           nthreads);
+}
+
+/*
+ * One direction of the SSD recurrence for a single (b, h), written into
+ * y (accumulating).  `rev` = 0 walks t = 0..L-1; `rev` = 1 walks the
+ * flipped sequence, i.e. t = L-1..0, which is F applied to flip(inputs)
+ * and flipped back.
+ * x, y: (Bs, L, H, P); dt: (Bs, L, H); B, C: (Bs, L, N).
+ */
+static void ssd_one_direction(const double *x, const double *dt, double Ah,
+                              const double *B, const double *C, double *y,
+                              int64_t b, int64_t h, int64_t L, int64_t H,
+                              int64_t P, int64_t N, int rev, double *state) {
+    memset(state, 0, (size_t)(P * N) * sizeof(double));
+    for (int64_t k = 0; k < L; ++k) {
+        const int64_t t = rev ? (L - 1 - k) : k;
+        const double d = dt[(b * L + t) * H + h];
+        const double a = exp(d * Ah);
+        const double *xt = x + ((b * L + t) * H + h) * P;
+        const double *Bt = B + (b * L + t) * N;
+        const double *Ct = C + (b * L + t) * N;
+        double *yt = y + ((b * L + t) * H + h) * P;
+        for (int64_t p = 0; p < P; ++p) {
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double *s = state + p * N + n;
+                *s = a * (*s) + d * xt[p] * Bt[n];
+                acc += (*s) * Ct[n];
+            }
+            yt[p] += acc;
+        }
+    }
+}
+
+/*
+ * Scalar-per-head (SSD) scan, optionally bidirectional, for the (b, h)
+ * pairs in [u_begin, u_end) of the flattened index u = b * H + h.
+ * x, y: (Bs, L, H, P); dt: (Bs, L, H); A_head: (H); B, C: (Bs, L, N)
+ * (one group shared by all heads); D: (H) or NULL.
+ */
+void oracle_ssd_scan_range(const double *x, const double *dt,
+                           const double *A_head, const double *B,
+                           const double *C, const double *D, double *y,
+                           int64_t Bs, int64_t L, int64_t H, int64_t P,
+                           int64_t N, int bidirectional, int64_t u_begin,
+                           int64_t u_end, int nthreads) {
+    set_threads(nthreads);
+    if (u_end > Bs * H) u_end = Bs * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = u_begin; u < u_end; ++u) {
+        const int64_t b = u / H, h = u % H;
+        double *state = (double *)malloc((size_t)(P * N) * sizeof(double));
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t o = ((b * L + t) * H + h) * P;
+            for (int64_t p = 0; p < P; ++p)
+                y[o + p] = D ? D[h] * x[o + p] : 0.0;
+        }
+        ssd_one_direction(x, dt, A_head[h], B, C, y, b, h, L, H, P, N, 0,
+                          state);
+        if (bidirectional)
+            ssd_one_direction(x, dt, A_head[h], B, C, y, b, h, L, H, P, N, 1,
+                              state);
+        free(state);
+    }
+}
+
+void oracle_ssd_scan(const double *x, const double *dt, const double *A_head,
+                     const double *B, const double *C, const double *D,
+                     double *y, int64_t Bs, int64_t L, int64_t H, int64_t P,
+                     int64_t N, int bidirectional, int nthreads) {
+    oracle_ssd_scan_range(x, dt, A_head, B, C, D, y, Bs, L, H, P, N,
+                          bidirectional, 0, Bs * H, nthreads);
+}
