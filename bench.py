@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective-scan hot path on GB300.
+
+A step is one call of the scan on one batch of synthetic input resident in
+HBM.  The default workload is the diagonal selective scan with bf16 inputs,
+Bs=8 L=2048 ED=1536 N=16 (the shape the throughput metric is quoted on);
+``--workload`` selects any of the five workloads in ``workloads.py``.
+
+Prints ONE JSON line (rank 0).  ``value`` is element-steps/s (Bs*L*ED*N per
+step, ED = H*P for the chunked scan, both directions counted when
+bidirectional) over all ranks.  Inputs rotate over several resident sets so
+no step finds its inputs in L2 (> 2x L2 bytes between reuses).
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload on this host's cores (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = "diag_bf16_Bs8_L2048_ED1536_N16"
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "scan throughput (Bs·L·ED·N element-steps/s) and HBM GB/s vs roofline, 1 GB300"
+UNIT = "element-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.BY_NAME))
+    p.add_argument("--no-cpu-baseline", action="store_true",
+                   help="skip the CPU oracle leg (used for profiler runs)")
+    p.add_argument("--quick", action="store_true",
+                   help="timed steps only: no clock sampling, pre/post roll or e2e leg "
+                        "(used for profiler runs)")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target wall time of the CPU oracle sample")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS,
+                    bf16_tflops_sustained=1700.0, sm_max_mhz=2070.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# Traffic figures from the committed ncu summaries
+# ---------------------------------------------------------------------------
+
+def kernel_source_hash(kind: str) -> str:
+    src = os.path.join(ROOT, "linear_recurrence_ssm_gb300", "csrc",
+                       "diag_scan.cu" if kind == "diag" else "ssd_chunk_scan.cu")
+    h = hashlib.sha256()
+    for p in (src, os.path.join(ROOT, "linear_recurrence_ssm_gb300", "csrc", "ssm_common.cuh")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, kind: str):
+    """dram read+write bytes per launch recorded in profiles/, if the kernel
+    source still hashes to the value recorded with the counters."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    want = kernel_source_hash(kind)
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(".md"):
+            continue
+        text = open(os.path.join(pdir, name)).read()
+        for m in re.finditer(r"traffic_per_launch\[(?P<w>[^\]]+)\]\s*=\s*(?P<b>[0-9]+)\s*bytes"
+                             r"\s*source_hash=(?P<h>[0-9a-f]+)", text):
+            if m.group("w") == workload and m.group("h") == want:
+                return int(m.group("b"))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling (nvidia-smi) around the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# The hot path
+# ---------------------------------------------------------------------------
+
+def kernels_per_call(w) -> int:
+    """Kernels one library call launches (the diagonal scan is one kernel;
+    the chunked scan is one kernel per call in either direction mode)."""
+    return 1
+
+
+def make_step(w, lrs, bufs):
+    s = w.shape
+    if w.kind == "diag":
+        def step(i):
+            b = bufs[i % len(bufs)]
+            lrs.ssm_scan_fwd(b["x"], b["delta"], b["A"], b["B"], b["C"], b["D"], y=b["y"])
+    else:
+        def step(i):
+            b = bufs[i % len(bufs)]
+            lrs.ssd_chunk_scan_fwd(b["x"], b["dt"], b["A_head"], b["B"], b["C"], b["D"],
+                                   chunk=s["chunk"], bidirectional=s["bidirectional"], y=b["y"])
+    return step
+
+
+def out_shape(w):
+    s = w.shape
+    if w.kind == "diag":
+        return (s["Bs"], s["L"], s["ED"])
+    return (s["Bs"], s["L"], s["H"], s["P"])
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    import linear_recurrence_ssm_gb300 as lrs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = workloads.BY_NAME[args.workload]
+    lrs.library()
+
+    # Resident input/output sets; each rank draws its own batch (weak scaling).
+    host = workloads.workload_inputs(
+        workloads.Workload(w.name, w.kind, w.dtype, w.shape, seed=w.seed + 1000 * rank))
+    per_set = w.algorithmic_bytes
+    nsets = max(3, -(-3 * L2_BYTES // per_set))
+    bufs = []
+    for k in range(nsets):
+        b = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
+        b["y"] = torch.empty(out_shape(w), dtype=torch.float32, device=dev)
+        bufs.append(b)
+    step = make_step(w, lrs, bufs)
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    # Busy pre-roll so that clocks are sampled under load around the timed region.
+    sampler = ClockSampler(local)
+    roll = 0.0 if args.quick else 0.6
+    if not args.quick:
+        sampler.start()
+    t_roll = time.time()
+    i = 0
+    while time.time() - t_roll < roll:
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize(dev)
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    # Busy post-roll, then stop sampling.
+    t_roll = time.time()
+    while time.time() - t_roll < (0.0 if args.quick else 0.4):
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize(dev)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0 - 0.6, t_wall1 + 0.4)
+
+    # End to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, the call, D2H of y, every step.
+    pinned = {n: (t.pin_memory() if t is not None else None) for n, t in host.items()}
+    y_host = torch.empty(out_shape(w), dtype=torch.float32).pin_memory()
+    dbuf = bufs[0]
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values() if t is not None)
+    d2h = y_host.numel() * 4
+    k_e2e = 0 if args.quick else max(1, min(args.steps, 200))
+    for _ in range(0 if args.quick else 2):
+        for n, t in pinned.items():
+            if t is not None:
+                dbuf[n].copy_(t, non_blocking=True)
+        step(0)
+        y_host.copy_(dbuf["y"], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(k_e2e):
+        for n, t in pinned.items():
+            if t is not None:
+                dbuf[n].copy_(t, non_blocking=True)
+        step(0)
+        y_host.copy_(dbuf["y"], non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = f0.elapsed_time(f1) if k_e2e else float("nan")
+
+    if world > 1:
+        t = torch.tensor([ms, ms_e2e], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+
+    units = w.element_steps
+    value = units * args.steps * world / (ms / 1e3)
+    e2e_value = units * k_e2e * world / (ms_e2e / 1e3) if k_e2e else None
+    peaks = load_peaks()
+    per_launch_s = ms / 1e3 / (args.steps * kernels_per_call(w))
+    achieved = w.algorithmic_bytes / per_launch_s / 1e9
+    roofline = {
+        "bound": "hbm",
+        "achieved": round(achieved, 1),
+        "peak": peaks["hbm_gbs"],
+        "unit": "GB/s",
+        "frac": round(achieved / peaks["hbm_gbs"], 4),
+        "traffic": ncu_traffic(w.name, w.kind),
+        "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+        "algorithmic_bytes_per_launch": w.algorithmic_bytes,
+        "launch_us": round(per_launch_s * 1e6, 3),
+    }
+    s = w.shape
+    config = {"workload": w.name, **{k: v for k, v in s.items()},
+              "input_dtype": w.dtype, "state_dtype": "f32", "output_dtype": "f32",
+              "l2": "inputs rotate over %d resident sets (%.0f MB each, > 2x L2 between reuses)"
+                    % (nsets, per_set / 1e6),
+              "parallelism": "replica per GPU (batch shards, no collective)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded, distributions of the workload definition)",
+        "config": config,
+        "hbm_gbs": round(achieved, 1),
+        "roofline": roofline,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": k_e2e},
+        "gpu_launches": args.steps * kernels_per_call(w),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (the reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(w, host, units_per_call_target):
+    """Slice a contiguous block of channels (diag) or heads (SSD) of every batch
+    row; returns (callable, element-steps it computes, description)."""
+    import oracle
+    s = w.shape
+    if w.kind == "diag":
+        Bs, L, ED, N = s["Bs"], s["L"], s["ED"], s["N"]
+        per_chan = L * N
+        ne = max(1, min(ED, int(units_per_call_target // (per_chan * Bs))))
+        sl = dict(x=host["x"][:, :, :ne].contiguous(), delta=host["delta"][:, :, :ne].contiguous(),
+                  A=host["A"][:ne].contiguous(), B=host["B"], C=host["C"],
+                  D=host["D"][:ne].contiguous())
+        sl = {k: oracle._f64(v) for k, v in sl.items()}
+        fn = lambda: oracle.diag_scan(**sl)
+        return fn, Bs * L * ne * N, "%d of %d channels (e < %d) of all %d batch rows" % (
+            ne * Bs, Bs * ED, ne, Bs)
+    Bs, L, H, P, N = s["Bs"], s["L"], s["H"], s["P"], s["N"]
+    dirs = 2 if s["bidirectional"] else 1
+    per_head = L * P * N * dirs
+    nb = max(1, min(Bs, int(units_per_call_target // (per_head * H)) or 1))
+    nh = H if nb > 1 else max(1, min(H, int(units_per_call_target // per_head)))
+    sl = dict(x=host["x"][:nb, :, :nh].contiguous(), dt=host["dt"][:nb, :, :nh].contiguous(),
+              A_head=host["A_head"][:nh].contiguous(), B=host["B"][:nb], C=host["C"][:nb],
+              D=host["D"][:nh].contiguous())
+    sl = {k: oracle._f64(v) for k, v in sl.items()}
+    fn = lambda: oracle.ssd_scan(**sl, bidirectional=s["bidirectional"])
+    return fn, nb * L * nh * P * N * dirs, "%d of %d (batch, head) pairs" % (nb * nh, Bs * H)
+
+
+def cpu_baseline(w, seconds: float):
+    import oracle
+    host = workloads.workload_inputs(w)
+    cores = oracle.max_threads()
+    # Calibrate on a small sample, then size the sample to ~`seconds`.
+    fn, units, _ = _oracle_sample(w, host, 2e6)
+    t0 = time.perf_counter()
+    fn()
+    rate = units / max(1e-6, time.perf_counter() - t0)
+    fn, units, desc = _oracle_sample(w, host, rate * seconds)
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    return {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%s; %.3g element-steps in %.2f s (fp64 sequential C, OpenMP)"
+                      % (desc, units, dt)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    w = workloads.BY_NAME[args.workload]
+    host = workloads.workload_inputs(w)
+    cores = oracle.max_threads()
+    budget = 150.0  # seconds for the whole warm-up + timed run
+    fn, units, _ = _oracle_sample(w, host, 2e6)
+    t0 = time.perf_counter()
+    fn()
+    rate = units / max(1e-6, time.perf_counter() - t0)
+    per_step = max(0.05, budget / max(1, args.steps + args.warmup))
+    fn, units, desc = _oracle_sample(w, host, rate * per_step)
+    for _ in range(args.warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn()
+    dt = time.perf_counter() - t0
+    value = units * args.steps / dt
+    s = w.shape
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, distributions of the workload definition)",
+        "config": {"workload": w.name, **{k: v for k, v in s.items()}, "input_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,126 @@
+/*
+ * ssm_scan.h -- C ABI of the GB300 (sm_103a) selective-scan library
+ * (libssmscan.so).
+ *
+ * The library computes the forward linear recurrence at the core of
+ * Mamba-style state-space layers, in two forms:
+ *
+ *   ssm_scan_fwd / ssm_scan_fwd_bf16  -- diagonal A (one decay per channel
+ *       and state).  Shape API of selective_scan / selective_scan_seq in
+ *       "scan output is different between sequential and parallel
+ *       versions" (mamba.py issue 26, the test script's comment block):
+ *       x, delta (Bs, L, ED); A (ED, N); B, C (Bs, L, N); D (ED);
+ *       y (Bs, L, ED).  Per channel (b, e) and state n, with h_{-1} = 0:
+ *         h_t[n] = exp(delta_t * A[e,n]) * h_{t-1}[n] + delta_t * B_t[n] * x_t
+ *         y_t    = sum_n C_t[n] * h_t[n] + D[e] * x_t
+ *
+ *   ssd_chunk_scan_fwd  -- one scalar decay per head (chunked "SSD" form),
+ *       argument subset (x, dt, A, B, C, chunk_size, D) of the chunked scan
+ *       in "Some questions of Bi-Mamba2 and Hydra" (Bi-Mamba2 issue 1, the
+ *       MambaChunkScanCombinedFn.forward signature), with z, dt_bias and
+ *       dt_softplus off and one group of B, C shared by all heads.
+ *       x (Bs, L, H, P); dt (Bs, L, H); A_head (H); B, C (Bs, L, N) -- the
+ *       same memory as (Bs, L, 1, N); D (H); y (Bs, L, H, P).  Per (b, h):
+ *         H_t = exp(dt_t * A_h) * H_{t-1} + dt_t * x_t (outer) B_t   (P x N)
+ *         y_t = H_t C_t + D_h * x_t
+ *       With bidirectional != 0 the reversed scan (same x, dt, A, B, C, the
+ *       time axis walked from the end) is added, and D x once: "the addition
+ *       of two separate SSMs, plus D x(t)" on the same page.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, dense
+ *     row-major with the last index fastest.  Inputs are only read; y is
+ *     fully overwritten (never accumulated into).  The library keeps no
+ *     pointer after the call returns.
+ *   - A, A_head and D are fp32.  D may be NULL (read as D = 0).  y is fp32.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work
+ *     is enqueued on it and the call never synchronises; faults raised by
+ *     the kernels surface at the caller's next synchronisation.
+ *   - Errors are returned as ssm_status_t; nothing is launched when the
+ *     status is not SSM_OK.  No entry point aborts or throws.
+ *   - Calls are reentrant and thread-safe; the only global state is a
+ *     per-device cache of attributes.
+ *   - Sizes are int64; every size must be >= 1 and every tensor's element
+ *     count must fit in int64.
+ *   - Results are deterministic: the same inputs give bitwise-equal y.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,     /* NULL pointer, size < 1, size overflow */
+    SSM_ERR_UNSUPPORTED = 2,     /* a size outside what the kernels handle */
+    SSM_ERR_ALIGNMENT = 3,       /* a pointer not aligned to its element size */
+    SSM_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed */
+    SSM_ERR_DEVICE_TIMEOUT = 5,  /* reserved: a bounded device wait ran out */
+    SSM_ERR_NO_DEVICE = 6        /* no CUDA device, or not an sm_103 device */
+} ssm_status_t;
+
+/*
+ * Diagonal selective scan, fp32 x / delta / B / C.
+ *   x, delta : (Bs, L, ED) fp32        A : (ED, N) fp32
+ *   B, C     : (Bs, L, N)  fp32        D : (ED) fp32 or NULL
+ *   y        : (Bs, L, ED) fp32 output
+ * Supported: 1 <= N <= 64.  Every pointer must be 4-byte aligned
+ * (SSM_ERR_ALIGNMENT otherwise).  Any Bs, L, ED >= 1.
+ */
+SSM_API ssm_status_t ssm_scan_fwd(const float *x, const float *delta, const float *A,
+                          const float *B, const float *C, const float *D,
+                          float *y, int64_t Bs, int64_t L, int64_t ED,
+                          int64_t N, void *stream);
+
+/*
+ * Diagonal selective scan, bf16 x / delta / B / C (passed as raw 16-bit
+ * bfloat16 storage); A, D fp32; state and y fp32.  Same shapes and rules as
+ * ssm_scan_fwd; x, delta, B, C must be 2-byte aligned.
+ */
+SSM_API ssm_status_t ssm_scan_fwd_bf16(const void *x, const void *delta,
+                               const float *A, const void *B, const void *C,
+                               const float *D, float *y, int64_t Bs,
+                               int64_t L, int64_t ED, int64_t N,
+                               void *stream);
+
+/*
+ * Chunked scalar-decay (SSD) scan, bf16 x / dt / B / C (raw bfloat16
+ * storage), fp32 A_head, D, state and y.
+ *   x  : (Bs, L, H, P) bf16        dt : (Bs, L, H) bf16
+ *   A_head : (H) fp32              B, C : (Bs, L, N) bf16 (one group)
+ *   D  : (H) fp32 or NULL          y  : (Bs, L, H, P) fp32 output
+ *   chunk : time-chunk length Q of the chunked algorithm.
+ *   bidirectional : 0 = forward scan; != 0 = forward + reversed scan + D x.
+ * Supported: P == 64; N in {16, 32, 64, 128}; chunk in {64, 128, 256};
+ * any Bs, L, H >= 1 (L need not be a multiple of chunk).  x, B, C and y
+ * must be 16-byte aligned, dt 2-byte aligned (SSM_ERR_ALIGNMENT otherwise).
+ * The result does not depend on `chunk` beyond rounding.
+ */
+SSM_API ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt,
+                                const float *A_head, const void *B,
+                                const void *C, const float *D, float *y,
+                                int64_t Bs, int64_t L, int64_t H, int64_t P,
+                                int64_t N, int64_t chunk, int bidirectional,
+                                void *stream);
+
+/* Static, human-readable name of a status code. */
+SSM_API const char *ssm_status_string(ssm_status_t status);
+
+/* Version of the library as MAJOR * 10000 + MINOR * 100 + PATCH. */
+SSM_API int ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

@@ -1,0 +1,177 @@
+"""GB300-native selective-scan linear recurrence: a thin Python binding of
+libssmscan.so (C ABI declared in include/ssm_scan.h).
+
+Every call marshals torch CUDA tensors into raw device pointers plus the
+current CUDA stream and calls the C entry point of the same name; all of the
+computation runs in the library's sm_103a kernels.  There is no fallback: if
+the library is missing or fails to load, importing a function raises.
+
+Functions
+---------
+ssm_scan_fwd(x, delta, A, B, C, D=None, y=None)
+    Diagonal-A selective scan (shape API of selective_scan in "scan output is
+    different between sequential and parallel versions", mamba.py issue 26).
+    x, delta: (Bs, L, ED); A: (ED, N) fp32; B, C: (Bs, L, N); D: (ED) fp32.
+    fp32 inputs call the C ``ssm_scan_fwd``; bf16 inputs call
+    ``ssm_scan_fwd_bf16``.  Returns y (Bs, L, ED) fp32.
+ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, bidirectional=False, y=None)
+    Chunked scalar-decay scan ("Some questions of Bi-Mamba2 and Hydra",
+    Bi-Mamba2 issue 1).  x: (Bs, L, H, P) bf16; dt: (Bs, L, H) bf16;
+    A_head: (H) fp32; B, C: (Bs, L, N) or (Bs, L, 1, N) bf16; D: (H) fp32.
+    Returns y (Bs, L, H, P) fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+__all__ = ["ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssd_chunk_scan_fwd", "SsmError", "library",
+           "build", "status_string", "STATUS"]
+
+STATUS = {
+    0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED", 3: "SSM_ERR_ALIGNMENT",
+    4: "SSM_ERR_CUDA", 5: "SSM_ERR_DEVICE_TIMEOUT", 6: "SSM_ERR_NO_DEVICE",
+}
+
+# Every symbol include/ssm_scan.h declares, with its ctypes signature.
+_VP = ctypes.c_void_p
+_I64 = ctypes.c_int64
+SIGNATURES = {
+    "ssm_scan_fwd": ([_VP] * 7 + [_I64] * 4 + [_VP], ctypes.c_int),
+    "ssm_scan_fwd_bf16": ([_VP] * 7 + [_I64] * 4 + [_VP], ctypes.c_int),
+    "ssd_chunk_scan_fwd": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP], ctypes.c_int),
+    "ssm_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "ssm_version": ([], ctypes.c_int),
+}
+
+_lib = None
+
+
+class SsmError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__("%s failed: %s" % (fn, status_string(status)))
+
+
+def build(force: bool = False) -> str:
+    """Compile libssmscan.so in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force)
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C library (built first if its sources are newer)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB_PATH
+        if _build.needs_build():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError("libssmscan.so is missing and could not be built")
+        lib = ctypes.CDLL(path)
+        for name, (argtypes, restype) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = argtypes
+            fn.restype = restype
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().ssm_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(dev):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _check(t, name, dtypes, dev, ndim=None):
+    import torch
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device != dev:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, dev))
+    if t.dtype not in dtypes:
+        raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() not in ndim:
+        raise ValueError("%s must have %s dims, got %d" % (name, ndim, t.dim()))
+
+
+def ssm_scan_fwd(x, delta, A, B, C, D=None, y=None):
+    """Diagonal selective scan on the current CUDA stream; returns y (fp32)."""
+    import torch
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    ins = (torch.float32, torch.bfloat16)
+    for t, n in ((x, "x"), (delta, "delta"), (B, "B"), (C, "C")):
+        _check(t, n, (x.dtype,) if x.dtype in ins else ins, dev, (3,))
+    _check(A, "A", (torch.float32,), dev, (2,))
+    _check(D, "D", (torch.float32,), dev, (1,))
+    Bs, L, ED = x.shape
+    N = A.shape[1]
+    if delta.shape != x.shape or tuple(A.shape) != (ED, N) or tuple(B.shape) != (Bs, L, N) \
+            or tuple(C.shape) != (Bs, L, N) or (D is not None and tuple(D.shape) != (ED,)):
+        raise ValueError("shape mismatch: x, delta (Bs,L,ED); A (ED,N); B, C (Bs,L,N); D (ED)")
+    if y is None:
+        y = torch.empty((Bs, L, ED), dtype=torch.float32, device=dev)
+    _check(y, "y", (torch.float32,), dev, (3,))
+    name = "ssm_scan_fwd" if x.dtype == torch.float32 else "ssm_scan_fwd_bf16"
+    fn = getattr(library(), name)
+    st = fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y),
+            Bs, L, ED, N, _stream(dev))
+    if st != 0:
+        raise SsmError(name, st)
+    return y
+
+
+def ssm_scan_fwd_bf16(x, delta, A, B, C, D=None, y=None):
+    """Same as ``ssm_scan_fwd`` but requires bf16 x, delta, B, C."""
+    import torch
+    if x.dtype != torch.bfloat16:
+        raise TypeError("ssm_scan_fwd_bf16 takes bf16 x, delta, B, C")
+    return ssm_scan_fwd(x, delta, A, B, C, D, y)
+
+
+def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
+                       bidirectional: bool = False, y=None):
+    """Chunked scalar-decay scan on the current CUDA stream; returns y (fp32)."""
+    import torch
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    bf = (torch.bfloat16,)
+    _check(x, "x", bf, dev, (4,))
+    _check(dt, "dt", bf, dev, (3,))
+    _check(B, "B", bf, dev, (3, 4))
+    _check(C, "C", bf, dev, (3, 4))
+    _check(A_head, "A_head", (torch.float32,), dev, (1,))
+    _check(D, "D", (torch.float32,), dev, (1,))
+    Bs, L, H, P = x.shape
+    if B.dim() == 4:
+        if B.shape[2] != 1 or C.dim() != 4 or C.shape[2] != 1:
+            raise ValueError("B, C must have one group: (Bs, L, 1, N)")
+    N = B.shape[-1]
+    if tuple(dt.shape) != (Bs, L, H) or tuple(A_head.shape) != (H,) \
+            or B.shape[0] != Bs or B.shape[1] != L or tuple(C.shape) != tuple(B.shape) \
+            or (D is not None and tuple(D.shape) != (H,)):
+        raise ValueError("shape mismatch: x (Bs,L,H,P); dt (Bs,L,H); A_head (H); B, C (Bs,L,[1,]N)")
+    if y is None:
+        y = torch.empty((Bs, L, H, P), dtype=torch.float32, device=dev)
+    _check(y, "y", (torch.float32,), dev, (4,))
+    st = library().ssd_chunk_scan_fwd(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D),
+                                      _ptr(y), Bs, L, H, P, N, int(chunk), int(bool(bidirectional)),
+                                      _stream(dev))
+    if st != 0:
+        raise SsmError("ssd_chunk_scan_fwd", st)
+    return y

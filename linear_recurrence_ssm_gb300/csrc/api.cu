@@ -1,0 +1,164 @@
+// api.cu -- the C ABI of libssmscan.so: argument validation, device checks
+// and dispatch to the kernels.  See include/ssm_scan.h for the contract.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <limits.h>
+#include <mutex>
+
+#include "ssm_common.cuh"
+
+namespace ssm {
+namespace diag {
+template <typename Tin>
+cudaError_t launch(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
+                   const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
+                   int num_sms, cudaStream_t st);
+}
+namespace ssd {
+cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
+                   const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
+                   int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N, int64_t chunk,
+                   bool bidirectional, int num_sms, cudaStream_t st);
+}
+}  // namespace ssm
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ok = false;
+    int num_sms = 0;
+};
+
+std::once_flag g_dev_once[kMaxDevices];
+DeviceInfo g_dev[kMaxDevices];
+
+// Device attributes, queried once per device.  A device that is not
+// compute capability 10.3 cannot run this library's sm_103a code.
+ssm_status_t current_device(DeviceInfo *out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return SSM_ERR_NO_DEVICE;
+    }
+    std::call_once(g_dev_once[dev], [dev]() {
+        int major = 0, minor = 0, sms = 0;
+        bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+        g_dev[dev].ok = ok && major == 10 && minor == 3;
+        g_dev[dev].num_sms = sms;
+    });
+    *out = g_dev[dev];
+    return out->ok ? SSM_OK : SSM_ERR_NO_DEVICE;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+// Every size >= 1 and the product of all of them fits in int64.
+bool sizes_ok(std::initializer_list<int64_t> dims) {
+    int64_t prod = 1;
+    for (int64_t d : dims) {
+        if (d < 1) return false;
+        if (!mul_ok(prod, d, &prod)) return false;
+    }
+    return true;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ssm_status_t from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return SSM_OK;
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorNoDevice ||
+        e == cudaErrorInsufficientDriver)
+        return SSM_ERR_NO_DEVICE;
+    if (e == cudaErrorInvalidConfiguration) return SSM_ERR_UNSUPPORTED;
+    return SSM_ERR_CUDA;
+}
+
+template <typename Tin>
+ssm_status_t diag_entry(const Tin *x, const Tin *delta, const float *A, const Tin *B, const Tin *C,
+                        const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
+                        void *stream) {
+    if (!x || !delta || !A || !B || !C || !y) return SSM_ERR_INVALID_ARG;
+    if (!sizes_ok({Bs, L, ED}) || !sizes_ok({Bs, L, N}) || !sizes_ok({ED, N}))
+        return SSM_ERR_INVALID_ARG;
+    if (N > 64) return SSM_ERR_UNSUPPORTED;
+    if (L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    const size_t es = sizeof(Tin);
+    if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
+        !aligned(A, 4) || !aligned(y, 4) || (D && !aligned(D, 4)))
+        return SSM_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    ssm_status_t s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    return from_cuda(ssm::diag::launch<Tin>(x, delta, A, B, C, D, y, Bs, L, ED, N, dev.num_sms,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status_t ssm_scan_fwd(const float *x, const float *delta, const float *A, const float *B,
+                          const float *C, const float *D, float *y, int64_t Bs, int64_t L,
+                          int64_t ED, int64_t N, void *stream) {
+    return diag_entry<float>(x, delta, A, B, C, D, y, Bs, L, ED, N, stream);
+}
+
+ssm_status_t ssm_scan_fwd_bf16(const void *x, const void *delta, const float *A, const void *B,
+                               const void *C, const float *D, float *y, int64_t Bs, int64_t L,
+                               int64_t ED, int64_t N, void *stream) {
+    using bf = __nv_bfloat16;
+    return diag_entry<bf>(static_cast<const bf *>(x), static_cast<const bf *>(delta), A,
+                          static_cast<const bf *>(B), static_cast<const bf *>(C), D, y, Bs, L, ED,
+                          N, stream);
+}
+
+ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt, const float *A_head, const void *B,
+                                const void *C, const float *D, float *y, int64_t Bs, int64_t L,
+                                int64_t H, int64_t P, int64_t N, int64_t chunk, int bidirectional,
+                                void *stream) {
+    if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_INVALID_ARG;
+    if (!sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, N}) || chunk < 1) return SSM_ERR_INVALID_ARG;
+    if (P != 64) return SSM_ERR_UNSUPPORTED;
+    if (N != 16 && N != 32 && N != 64 && N != 128) return SSM_ERR_UNSUPPORTED;
+    if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
+    if (L > INT_MAX || H > 65535 || Bs > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+        !aligned(dt, 2) || !aligned(A_head, 4) || (D && !aligned(D, 4)))
+        return SSM_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    ssm_status_t s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    using bf = __nv_bfloat16;
+    return from_cuda(ssm::ssd::launch(static_cast<const bf *>(x), static_cast<const bf *>(dt),
+                                      A_head, static_cast<const bf *>(B),
+                                      static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
+                                      bidirectional != 0, dev.num_sms,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+const char *ssm_status_string(ssm_status_t status) {
+    switch (status) {
+        case SSM_OK: return "SSM_OK";
+        case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG: null pointer or size < 1 / overflow";
+        case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED: size outside the supported set";
+        case SSM_ERR_ALIGNMENT: return "SSM_ERR_ALIGNMENT: pointer not aligned as required";
+        case SSM_ERR_CUDA: return "SSM_ERR_CUDA: a CUDA call or kernel launch failed";
+        case SSM_ERR_DEVICE_TIMEOUT: return "SSM_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
+        case SSM_ERR_NO_DEVICE: return "SSM_ERR_NO_DEVICE: no sm_103 CUDA device is current";
+    }
+    return "unknown ssm_status_t";
+}
+
+int ssm_version(void) { return 100; }
+
+}  // extern "C"

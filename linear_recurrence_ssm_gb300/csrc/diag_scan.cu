@@ -1,0 +1,277 @@
+// diag_scan.cu -- diagonal-A selective scan (Mamba-1 style) for sm_103a.
+//
+// Computes, per channel (b, e) and state n, with h_{-1} = 0,
+//     h_t[n] = exp(delta_t * A[e,n]) * h_{t-1}[n] + delta_t * B_t[n] * x_t
+//     y_t    = sum_n C_t[n] * h_t[n] + D[e] * x_t
+// -- the sequential form selective_scan_seq of "scan output is different
+// between sequential and parallel versions" (mamba.py issue 26), with the
+// shape API given there (x, delta (Bs,L,ED); A (ED,N); B, C (Bs,L,N); D (ED)).
+//
+// Design (one pass over HBM, state never leaves registers):
+//   * A CTA of 128 threads owns ET = 128 / G consecutive channels of one
+//     batch row b for the whole sequence.  G lanes share a channel, each
+//     holding S = NP / G of its (padded) states in registers, so the work
+//     per thread is S independent fp32 recurrences (instruction-level
+//     parallelism) and the y reduction over the G lanes is a shuffle.
+//   * Time is walked in tiles of TT steps.  x and delta tiles (TT x ET) and
+//     the B, C rows of the tile (TT x N, contiguous in memory) are staged
+//     into shared memory by 16-byte cp.async copies, two tiles ahead of the
+//     compute (double buffered), so HBM latency overlaps the recurrence.
+//   * B and C are converted once per tile to fp32 (zero padded to NP) and
+//     read back as broadcast float4 loads by every channel's lanes.
+//   * exp(delta*A) is one MUFU ex2 per element-step: A is pre-scaled by
+//     log2(e) once per (e, n) in registers.
+//   * y is stored from registers: per step a warp writes 32/G consecutive
+//     fp32 values of one row.
+#include "ssm_common.cuh"
+
+namespace ssm {
+namespace diag {
+
+constexpr int kThreads = 128;
+constexpr int kTileT = 32;
+
+template <typename Tin, int S, int G>
+struct Shape {
+    static constexpr int ET = kThreads / G;  // channels per CTA
+    static constexpr int NP = S * G;         // padded state count
+    static constexpr size_t raw_x = size_t(kTileT) * ET;     // elements per x tile
+    static constexpr size_t raw_bc = size_t(kTileT) * NP;    // elements per B tile
+    static constexpr size_t smem_bytes =
+        (2 * 2 * raw_x + 2 * 2 * raw_bc) * sizeof(Tin) + 2 * raw_bc * sizeof(float);
+};
+
+// Stage one time tile of x, delta, B, C into shared-memory buffer `stage`.
+template <typename Tin, int S, int G, bool VEC>
+__device__ __forceinline__ void load_tile(Tin *sx, Tin *sd, Tin *sB, Tin *sC,
+                                          const Tin *__restrict__ x, const Tin *__restrict__ dlt,
+                                          const Tin *__restrict__ Bm, const Tin *__restrict__ Cm,
+                                          int64_t b, int t0, int L, int e0, int ED, int N) {
+    using Sh = Shape<Tin, S, G>;
+    constexpr int ET = Sh::ET;
+    const int tid = threadIdx.x;
+    const int rows = min(kTileT, L - t0);
+    if constexpr (VEC) {
+        constexpr int EPC = 16 / sizeof(Tin);       // elements per 16-byte chunk
+        constexpr int CPR = ET / EPC;               // chunks per x row
+        for (int i = tid; i < kTileT * CPR; i += kThreads) {
+            const int t = i / CPR, c = i % CPR;
+            const int e = e0 + c * EPC;
+            const bool ok = (t < rows) && (e < ED);
+            const int64_t g = ok ? ((b * L + t0 + t) * ED + e) : 0;
+            cp_async16(sx + t * ET + c * EPC, x + g, ok ? 16 : 0);
+            cp_async16(sd + t * ET + c * EPC, dlt + g, ok ? 16 : 0);
+        }
+        // B, C rows t0..t0+rows-1 are one contiguous block of rows*N elements.
+        const int nchunk = kTileT * N / EPC;
+        const int valid = rows * N / EPC;
+        const int64_t base = (b * L + t0) * N;
+        for (int i = tid; i < nchunk; i += kThreads) {
+            const bool ok = i < valid;
+            const int64_t g = ok ? base + int64_t(i) * EPC : 0;
+            cp_async16(sB + i * EPC, Bm + g, ok ? 16 : 0);
+            cp_async16(sC + i * EPC, Cm + g, ok ? 16 : 0);
+        }
+    } else {
+        // Any alignment: element-wise synchronous copies.
+        for (int i = tid; i < kTileT * ET; i += kThreads) {
+            const int t = i / ET, c = i % ET;
+            const int e = e0 + c;
+            const bool ok = (t < rows) && (e < ED);
+            const int64_t g = (b * L + t0 + t) * ED + e;
+            sx[i] = ok ? x[g] : Tin(0.0f);
+            sd[i] = ok ? dlt[g] : Tin(0.0f);
+        }
+        const int64_t base = (b * L + t0) * N;
+        for (int i = tid; i < kTileT * N; i += kThreads) {
+            const bool ok = i < rows * N;
+            sB[i] = ok ? Bm[base + i] : Tin(0.0f);
+            sC[i] = ok ? Cm[base + i] : Tin(0.0f);
+        }
+    }
+}
+
+template <typename Tin, int S, int G, bool VEC>
+__global__ void __launch_bounds__(kThreads)
+diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
+                 const float *__restrict__ A, const Tin *__restrict__ Bm,
+                 const Tin *__restrict__ Cm, const float *__restrict__ D,
+                 float *__restrict__ y, int L, int ED, int N, int n_etiles) {
+    using Sh = Shape<Tin, S, G>;
+    constexpr int ET = Sh::ET;
+    constexpr int NP = Sh::NP;
+    static_assert(S % 4 == 0, "states per thread must be a multiple of 4");
+
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Tin *sx = reinterpret_cast<Tin *>(smem_raw);     // [2][TT][ET]
+    Tin *sd = sx + 2 * Sh::raw_x;                    // [2][TT][ET]
+    Tin *sB = sd + 2 * Sh::raw_x;                    // [2][TT*N] (dense rows)
+    Tin *sC = sB + 2 * Sh::raw_bc;                   // [2][TT*N]
+    float *fB = reinterpret_cast<float *>(sC + 2 * Sh::raw_bc);  // [TT][NP]
+    float *fC = fB + Sh::raw_bc;                                  // [TT][NP]
+
+    const int64_t b = blockIdx.x / n_etiles;
+    const int e0 = (blockIdx.x % n_etiles) * ET;
+    const int tid = threadIdx.x;
+    const int ch = tid / G;
+    const int g = tid % G;
+    const int e = e0 + ch;
+    const bool e_ok = e < ED;
+
+    float A2[S], h[S];
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+        const int n = g * S + j;
+        A2[j] = (e_ok && n < N) ? A[int64_t(e) * N + n] * SSM_LOG2E : 0.0f;
+        h[j] = 0.0f;
+    }
+    const float Dv = (D != nullptr && e_ok) ? D[e] : 0.0f;
+
+    const int n_tiles = (L + kTileT - 1) / kTileT;
+    load_tile<Tin, S, G, VEC>(sx, sd, sB, sC, x, dlt, Bm, Cm, b, 0, L, e0, ED, N);
+    cp_async_commit();
+    if (n_tiles > 1)
+        load_tile<Tin, S, G, VEC>(sx + Sh::raw_x, sd + Sh::raw_x, sB + Sh::raw_bc, sC + Sh::raw_bc,
+                                  x, dlt, Bm, Cm, b, kTileT, L, e0, ED, N);
+    cp_async_commit();
+
+    for (int k = 0; k < n_tiles; ++k) {
+        const int st = k & 1;
+        cp_async_wait<1>();
+        __syncthreads();
+        // B, C of this tile -> fp32, zero padded to NP states.
+        {
+            const Tin *rb = sB + st * Sh::raw_bc;
+            const Tin *rc = sC + st * Sh::raw_bc;
+            for (int i = tid; i < kTileT * NP; i += kThreads) {
+                const int t = i / NP, n = i % NP;
+                fB[i] = n < N ? to_f32(rb[t * N + n]) : 0.0f;
+                fC[i] = n < N ? to_f32(rc[t * N + n]) : 0.0f;
+            }
+        }
+        __syncthreads();
+
+        const int t0 = k * kTileT;
+        const int tl = min(kTileT, L - t0);
+        const Tin *xs = sx + st * Sh::raw_x + ch;
+        const Tin *ds = sd + st * Sh::raw_x + ch;
+        float *yp = y + (b * L + t0) * ED + e;
+        for (int t = 0; t < tl; ++t) {
+            const float dl = to_f32(ds[t * ET]);
+            const float xv = to_f32(xs[t * ET]);
+            const float dlx = dl * xv;
+            const float *bq = fB + t * NP + g * S;
+            const float *cq = fC + t * NP + g * S;
+            float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
+#pragma unroll
+            for (int q = 0; q < S / 4; ++q) {
+                const float4 bb = *reinterpret_cast<const float4 *>(bq + 4 * q);
+                const float4 cc = *reinterpret_cast<const float4 *>(cq + 4 * q);
+                float a;
+                a = ex2(dl * A2[4 * q + 0]);
+                h[4 * q + 0] = fmaf(a, h[4 * q + 0], dlx * bb.x);
+                acc0 = fmaf(cc.x, h[4 * q + 0], acc0);
+                a = ex2(dl * A2[4 * q + 1]);
+                h[4 * q + 1] = fmaf(a, h[4 * q + 1], dlx * bb.y);
+                acc1 = fmaf(cc.y, h[4 * q + 1], acc1);
+                a = ex2(dl * A2[4 * q + 2]);
+                h[4 * q + 2] = fmaf(a, h[4 * q + 2], dlx * bb.z);
+                acc2 = fmaf(cc.z, h[4 * q + 2], acc2);
+                a = ex2(dl * A2[4 * q + 3]);
+                h[4 * q + 3] = fmaf(a, h[4 * q + 3], dlx * bb.w);
+                acc3 = fmaf(cc.w, h[4 * q + 3], acc3);
+            }
+            float yv = (acc0 + acc1) + (acc2 + acc3);
+#pragma unroll
+            for (int o = 1; o < G; o <<= 1) yv += __shfl_xor_sync(0xffffffffu, yv, o);
+            if (g == 0 && e_ok) yp[int64_t(t) * ED] = fmaf(Dv, xv, yv);
+        }
+        __syncthreads();
+        if (k + 2 < n_tiles)
+            load_tile<Tin, S, G, VEC>(sx + st * Sh::raw_x, sd + st * Sh::raw_x, sB + st * Sh::raw_bc,
+                                      sC + st * Sh::raw_bc, x, dlt, Bm, Cm, b, (k + 2) * kTileT, L,
+                                      e0, ED, N);
+        cp_async_commit();
+    }
+}
+
+template <typename Tin, int S, int G, bool VEC>
+static cudaError_t launch_one(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm,
+                              const Tin *Cm, const float *D, float *y, int64_t Bs, int L, int ED,
+                              int N, cudaStream_t stream) {
+    using Sh = Shape<Tin, S, G>;
+    const int n_etiles = (ED + Sh::ET - 1) / Sh::ET;
+    const int64_t grid = Bs * n_etiles;
+    if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    auto kern = diag_scan_kernel<Tin, S, G, VEC>;
+    const int smem = int(Sh::smem_bytes);
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+    }
+    kern<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(x, dlt, A, Bm, Cm, D, y, L, ED, N,
+                                                                n_etiles);
+    return cudaGetLastError();
+}
+
+template <typename Tin, bool VEC>
+static cudaError_t dispatch_sg(int S, int G, const Tin *x, const Tin *dlt, const float *A,
+                               const Tin *Bm, const Tin *Cm, const float *D, float *y, int64_t Bs,
+                               int L, int ED, int N, cudaStream_t st) {
+#define SSM_DIAG_CASE(s_, g_)                                                                    \
+    if (S == s_ && G == g_)                                                                      \
+        return launch_one<Tin, s_, g_, VEC>(x, dlt, A, Bm, Cm, D, y, Bs, L, ED, N, st);
+    SSM_DIAG_CASE(16, 1)
+    SSM_DIAG_CASE(8, 2)
+    SSM_DIAG_CASE(4, 4)
+    SSM_DIAG_CASE(16, 2)
+    SSM_DIAG_CASE(8, 4)
+    SSM_DIAG_CASE(16, 4)
+#undef SSM_DIAG_CASE
+    return cudaErrorInvalidValue;
+}
+
+// Pick states-per-thread S and lanes-per-channel G.  More lanes per channel
+// give more warps (needed to fill 152 SMs x 4 schedulers when Bs*ED is
+// small) at the price of a shuffle reduction and less reuse of each
+// channel's x/delta/B/C loads per lane.
+static void choose_split(int64_t channels, int N, int num_sms, int *S, int *G) {
+    const int NP = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
+    const int64_t want_warps = int64_t(num_sms) * 4 * 4;  // ~4 warps per scheduler
+    int s = 16;
+    for (;;) {
+        const int64_t warps = (channels * (NP / s) + 31) / 32;
+        if (warps >= want_warps || s == 4 || NP / (s / 2) > 4) break;
+        s /= 2;
+    }
+    *S = s;
+    *G = NP / s;
+}
+
+template <typename Tin>
+cudaError_t launch(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
+                   const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
+                   int num_sms, cudaStream_t st) {
+    int S, G;
+    choose_split(Bs * ED, int(N), num_sms, &S, &G);
+    const int esz = int(sizeof(Tin));
+    const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(dlt) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(Bm) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(Cm) % 16 == 0) && ((ED * esz) % 16 == 0) &&
+                     ((N * esz) % 16 == 0);
+    if (vec)
+        return dispatch_sg<Tin, true>(S, G, x, dlt, A, Bm, Cm, D, y, Bs, int(L), int(ED), int(N), st);
+    return dispatch_sg<Tin, false>(S, G, x, dlt, A, Bm, Cm, D, y, Bs, int(L), int(ED), int(N), st);
+}
+
+template cudaError_t launch<float>(const float *, const float *, const float *, const float *,
+                                   const float *, const float *, float *, int64_t, int64_t, int64_t,
+                                   int64_t, int, cudaStream_t);
+template cudaError_t launch<__nv_bfloat16>(const __nv_bfloat16 *, const __nv_bfloat16 *,
+                                           const float *, const __nv_bfloat16 *,
+                                           const __nv_bfloat16 *, const float *, float *, int64_t,
+                                           int64_t, int64_t, int64_t, int, cudaStream_t);
+
+}  // namespace diag
+}  // namespace ssm

@@ -1,0 +1,95 @@
+"""Host-side checks of the C ABI (CPU only: no kernel is launched).
+
+The library must load, export every function include/ssm_scan.h declares,
+and reject bad arguments with status codes before touching any device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_recurrence_ssm_gb300 as lrs
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "ssm_scan.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = "\n".join(l for l in text.splitlines() if not l.lstrip().startswith("#"))
+    return sorted(set(re.findall(r"SSM_API\s+[^;(]*?\b([a-z_][a-z0-9_]*)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssd_chunk_scan_fwd", "ssm_status_string",
+              "ssm_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = lrs.library()
+    for name in declared_functions():
+        assert hasattr(lib, name), "missing export " + name
+    assert set(declared_functions()) == set(lrs.SIGNATURES)
+
+
+def test_status_strings():
+    for code, name in lrs.STATUS.items():
+        assert lrs.status_string(code).startswith(name)
+    assert "unknown" in lrs.status_string(99)
+
+
+P = ctypes.c_void_p(0x10000)       # never dereferenced: validation fails first
+P_ODD = ctypes.c_void_p(0x10001)
+
+
+def diag(fn="ssm_scan_fwd", ptrs=None, Bs=2, L=8, ED=4, N=16):
+    p = ptrs or [P] * 7
+    return getattr(lrs.library(), fn)(*p, Bs, L, ED, N, None)
+
+
+def ssd(ptrs=None, Bs=1, L=8, H=2, P_=64, N=64, chunk=128, bidir=0):
+    p = ptrs or [P] * 7
+    return lrs.library().ssd_chunk_scan_fwd(*p, Bs, L, H, P_, N, chunk, bidir, None)
+
+
+@pytest.mark.parametrize("fn", ["ssm_scan_fwd", "ssm_scan_fwd_bf16"])
+def test_diag_rejects_bad_arguments(fn):
+    for i in (0, 1, 2, 3, 4, 6):          # every pointer but D is required
+        ptrs = [P] * 7
+        ptrs[i] = None
+        assert diag(fn, ptrs) == 1
+    assert diag(fn, Bs=0) == 1
+    assert diag(fn, L=0) == 1
+    assert diag(fn, ED=-3) == 1
+    assert diag(fn, N=0) == 1
+    assert diag(fn, Bs=2 ** 40, L=2 ** 40) == 1      # element count overflows int64
+    assert diag(fn, N=65) == 2
+    ptrs = [P] * 7
+    ptrs[6] = P_ODD                       # y not 4-byte aligned
+    assert diag(fn, ptrs) == 3
+
+
+def test_ssd_rejects_bad_arguments():
+    ptrs = [P] * 7
+    ptrs[0] = None
+    assert ssd(ptrs) == 1
+    assert ssd(L=0) == 1
+    assert ssd(chunk=0) == 1
+    assert ssd(P_=32) == 2
+    assert ssd(N=48) == 2
+    assert ssd(chunk=96) == 2
+    ptrs = [P] * 7
+    ptrs[3] = P_ODD                       # B not 16-byte aligned
+    assert ssd(ptrs) == 3
+
+
+def test_valid_call_without_device_reports_no_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert diag() == 6
+    assert ssd() == 6
