@@ -65,7 +65,7 @@ typedef enum {
     SSM_ERR_UNSUPPORTED = 2,     /* a size outside what the kernels handle */
     SSM_ERR_ALIGNMENT = 3,       /* a pointer not aligned to its element size */
     SSM_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed */
-    SSM_ERR_DEVICE_TIMEOUT = 5,  /* reserved: a bounded device wait ran out */
+    SSM_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device wait ran out (see ssm_check_device_errors) */
     SSM_ERR_NO_DEVICE = 6        /* no CUDA device, or not an sm_103 device */
 } ssm_status_t;
 
@@ -101,10 +101,17 @@ SSM_API ssm_status_t ssm_scan_fwd_bf16(const void *x, const void *delta,
  *   D  : (H) fp32 or NULL          y  : (Bs, L, H, P) fp32 output
  *   chunk : time-chunk length Q of the chunked algorithm.
  *   bidirectional : 0 = forward scan; != 0 = forward + reversed scan + D x.
- * Supported: P == 64; N in {16, 32, 64, 128}; chunk in {64, 128, 256};
- * any Bs, L, H >= 1 (L need not be a multiple of chunk).  x, B, C and y
- * must be 16-byte aligned, dt 2-byte aligned (SSM_ERR_ALIGNMENT otherwise).
- * The result does not depend on `chunk` beyond rounding.
+ * Supported: P == 64; N in {64, 128}; chunk in {64, 128, 256}; any
+ * Bs, L, H >= 1 (L need not be a multiple of chunk).  x, B, C and y must be
+ * 16-byte aligned, dt 2-byte aligned (SSM_ERR_ALIGNMENT otherwise).
+ * The chunked result equals the recurrence for every chunk length (up to
+ * rounding).  The kernel passes the state between 128-row tiles -- the
+ * tensor-core tile height -- so a chunk of 256 rows is computed as two
+ * 128-row tiles and a chunk of 64 as half of one; `chunk` is validated and
+ * does not change the result beyond rounding.
+ * Bidirectional calls with L > 128 take a stream-ordered scratch buffer of
+ * Bs*H*ceil(L/128)*P*N*2 bytes (cudaMallocAsync / cudaFreeAsync on
+ * `stream`) for the reverse scan's entering states.
  */
 SSM_API ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt,
                                 const float *A_head, const void *B,
@@ -112,6 +119,16 @@ SSM_API ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt,
                                 int64_t Bs, int64_t L, int64_t H, int64_t P,
                                 int64_t N, int64_t chunk, int bidirectional,
                                 void *stream);
+
+/*
+ * Synchronise `stream` and report whether a kernel of this library running on
+ * the current device gave up a bounded wait (SSM_ERR_DEVICE_TIMEOUT) since
+ * the previous check; the record is cleared by the call.  Kernels never hang
+ * or trap: a wait that runs out abandons the kernel's work (y is then
+ * unspecified) and is reported here.  Also returns SSM_ERR_CUDA if the
+ * stream holds an earlier asynchronous CUDA error.
+ */
+SSM_API ssm_status_t ssm_check_device_errors(void *stream);
 
 /* Static, human-readable name of a status code. */
 SSM_API const char *ssm_status_string(ssm_status_t status);

@@ -27,8 +27,8 @@ import os
 
 from . import _build
 
-__all__ = ["ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssd_chunk_scan_fwd", "SsmError", "library",
-           "build", "status_string", "STATUS"]
+__all__ = ["ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssd_chunk_scan_fwd", "ssm_check_device_errors",
+           "SsmError", "library", "build", "status_string", "STATUS"]
 
 STATUS = {
     0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED", 3: "SSM_ERR_ALIGNMENT",
@@ -42,6 +42,7 @@ SIGNATURES = {
     "ssm_scan_fwd": ([_VP] * 7 + [_I64] * 4 + [_VP], ctypes.c_int),
     "ssm_scan_fwd_bf16": ([_VP] * 7 + [_I64] * 4 + [_VP], ctypes.c_int),
     "ssd_chunk_scan_fwd": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP], ctypes.c_int),
+    "ssm_check_device_errors": ([_VP], ctypes.c_int),
     "ssm_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "ssm_version": ([], ctypes.c_int),
 }
@@ -175,3 +176,13 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
     if st != 0:
         raise SsmError("ssd_chunk_scan_fwd", st)
     return y
+
+
+def ssm_check_device_errors(device=None) -> None:
+    """Synchronise the current stream and raise SsmError if a kernel of the
+    library abandoned its work after a bounded device wait ran out."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    st = library().ssm_check_device_errors(_stream(dev))
+    if st != 0:
+        raise SsmError("ssm_check_device_errors", st)

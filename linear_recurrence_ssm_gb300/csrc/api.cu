@@ -20,6 +20,7 @@ cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float 
                    const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
                    int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N, int64_t chunk,
                    bool bidirectional, int num_sms, cudaStream_t st);
+cudaError_t take_device_error(unsigned int *out);
 }
 }  // namespace ssm
 
@@ -129,7 +130,7 @@ ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt, const float *A_he
     if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_INVALID_ARG;
     if (!sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, N}) || chunk < 1) return SSM_ERR_INVALID_ARG;
     if (P != 64) return SSM_ERR_UNSUPPORTED;
-    if (N != 16 && N != 32 && N != 64 && N != 128) return SSM_ERR_UNSUPPORTED;
+    if (N != 64 && N != 128) return SSM_ERR_UNSUPPORTED;
     if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
     if (L > INT_MAX || H > 65535 || Bs > INT_MAX) return SSM_ERR_UNSUPPORTED;
     if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
@@ -144,6 +145,16 @@ ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt, const float *A_he
                                       static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
                                       bidirectional != 0, dev.num_sms,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+ssm_status_t ssm_check_device_errors(void *stream) {
+    DeviceInfo dev;
+    ssm_status_t s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSM_ERR_CUDA;
+    unsigned int flag = 0;
+    if (ssm::ssd::take_device_error(&flag) != cudaSuccess) return SSM_ERR_CUDA;
+    return flag ? SSM_ERR_DEVICE_TIMEOUT : SSM_OK;
 }
 
 const char *ssm_status_string(ssm_status_t status) {

@@ -29,7 +29,8 @@ namespace ssm {
 namespace diag {
 
 constexpr int kThreads = 128;
-constexpr int kTileT = 32;
+constexpr int kTileT = 32;   // time steps per shared-memory tile
+constexpr int kStages = 3;   // tiles in flight (cp.async ring)
 
 template <typename Tin, int S, int G>
 struct Shape {
@@ -38,10 +39,12 @@ struct Shape {
     static constexpr size_t raw_x = size_t(kTileT) * ET;     // elements per x tile
     static constexpr size_t raw_bc = size_t(kTileT) * NP;    // elements per B tile
     static constexpr size_t smem_bytes =
-        (2 * 2 * raw_x + 2 * 2 * raw_bc) * sizeof(Tin) + 2 * raw_bc * sizeof(float);
+        (kStages * 2 * raw_x + kStages * 2 * raw_bc) * sizeof(Tin) + 2 * raw_bc * sizeof(float);
 };
 
-// Stage one time tile of x, delta, B, C into shared-memory buffer `stage`.
+// Stage one time tile of x, delta, B, C into a shared-memory ring slot.
+// Rows past the end of the sequence are zero filled: delta = 0 there makes
+// exp(delta*A) = 1 and delta*B*x = 0, so the state passes through unchanged.
 template <typename Tin, int S, int G, bool VEC>
 __device__ __forceinline__ void load_tile(Tin *sx, Tin *sd, Tin *sB, Tin *sC,
                                           const Tin *__restrict__ x, const Tin *__restrict__ dlt,
@@ -50,7 +53,7 @@ __device__ __forceinline__ void load_tile(Tin *sx, Tin *sd, Tin *sB, Tin *sC,
     using Sh = Shape<Tin, S, G>;
     constexpr int ET = Sh::ET;
     const int tid = threadIdx.x;
-    const int rows = min(kTileT, L - t0);
+    const int rows = max(0, min(kTileT, L - t0));
     if constexpr (VEC) {
         constexpr int EPC = 16 / sizeof(Tin);       // elements per 16-byte chunk
         constexpr int CPR = ET / EPC;               // chunks per x row
@@ -78,7 +81,7 @@ __device__ __forceinline__ void load_tile(Tin *sx, Tin *sd, Tin *sB, Tin *sC,
             const int t = i / ET, c = i % ET;
             const int e = e0 + c;
             const bool ok = (t < rows) && (e < ED);
-            const int64_t g = (b * L + t0 + t) * ED + e;
+            const int64_t g = ok ? (b * L + t0 + t) * ED + e : 0;
             sx[i] = ok ? x[g] : Tin(0.0f);
             sd[i] = ok ? dlt[g] : Tin(0.0f);
         }
@@ -100,15 +103,16 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
     using Sh = Shape<Tin, S, G>;
     constexpr int ET = Sh::ET;
     constexpr int NP = Sh::NP;
+    constexpr int S2 = S / 2;
     static_assert(S % 4 == 0, "states per thread must be a multiple of 4");
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    Tin *sx = reinterpret_cast<Tin *>(smem_raw);     // [2][TT][ET]
-    Tin *sd = sx + 2 * Sh::raw_x;                    // [2][TT][ET]
-    Tin *sB = sd + 2 * Sh::raw_x;                    // [2][TT*N] (dense rows)
-    Tin *sC = sB + 2 * Sh::raw_bc;                   // [2][TT*N]
-    float *fB = reinterpret_cast<float *>(sC + 2 * Sh::raw_bc);  // [TT][NP]
-    float *fC = fB + Sh::raw_bc;                                  // [TT][NP]
+    Tin *sx = reinterpret_cast<Tin *>(smem_raw);     // [kStages][TT][ET]
+    Tin *sd = sx + kStages * Sh::raw_x;              // [kStages][TT][ET]
+    Tin *sB = sd + kStages * Sh::raw_x;              // [kStages][TT*N] (dense rows)
+    Tin *sC = sB + kStages * Sh::raw_bc;             // [kStages][TT*N]
+    float *fB = reinterpret_cast<float *>(sC + kStages * Sh::raw_bc);  // [TT][NP]
+    float *fC = fB + Sh::raw_bc;                                        // [TT][NP]
 
     const int64_t b = blockIdx.x / n_etiles;
     const int e0 = (blockIdx.x % n_etiles) * ET;
@@ -118,27 +122,41 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
     const int e = e0 + ch;
     const bool e_ok = e < ED;
 
-    float A2[S], h[S];
+    // State pairs and A * log2(e) pairs, so that the per-step arithmetic runs
+    // as packed fp32x2 multiplies / fused multiply-adds.
+    float2 A2[S2], h[S2];
 #pragma unroll
-    for (int j = 0; j < S; ++j) {
-        const int n = g * S + j;
-        A2[j] = (e_ok && n < N) ? A[int64_t(e) * N + n] * SSM_LOG2E : 0.0f;
-        h[j] = 0.0f;
+    for (int j = 0; j < S2; ++j) {
+        const int n = g * S + 2 * j;
+        A2[j].x = (e_ok && n < N) ? A[int64_t(e) * N + n] * SSM_LOG2E : 0.0f;
+        A2[j].y = (e_ok && n + 1 < N) ? A[int64_t(e) * N + n + 1] * SSM_LOG2E : 0.0f;
+        h[j] = make_float2(0.0f, 0.0f);
     }
     const float Dv = (D != nullptr && e_ok) ? D[e] : 0.0f;
 
     const int n_tiles = (L + kTileT - 1) / kTileT;
-    load_tile<Tin, S, G, VEC>(sx, sd, sB, sC, x, dlt, Bm, Cm, b, 0, L, e0, ED, N);
-    cp_async_commit();
-    if (n_tiles > 1)
-        load_tile<Tin, S, G, VEC>(sx + Sh::raw_x, sd + Sh::raw_x, sB + Sh::raw_bc, sC + Sh::raw_bc,
-                                  x, dlt, Bm, Cm, b, kTileT, L, e0, ED, N);
-    cp_async_commit();
+#pragma unroll
+    for (int k = 0; k < kStages - 1; ++k) {
+        if (k < n_tiles)
+            load_tile<Tin, S, G, VEC>(sx + k * Sh::raw_x, sd + k * Sh::raw_x, sB + k * Sh::raw_bc,
+                                      sC + k * Sh::raw_bc, x, dlt, Bm, Cm, b, k * kTileT, L, e0,
+                                      ED, N);
+        cp_async_commit();
+    }
 
     for (int k = 0; k < n_tiles; ++k) {
-        const int st = k & 1;
-        cp_async_wait<1>();
-        __syncthreads();
+        const int st = k % kStages;
+        cp_async_wait<kStages - 2>();
+        __syncthreads();   // tile k landed everywhere; tile k-1 fully consumed
+        {
+            const int kn = k + kStages - 1;
+            const int sn = kn % kStages;
+            if (kn < n_tiles)
+                load_tile<Tin, S, G, VEC>(sx + sn * Sh::raw_x, sd + sn * Sh::raw_x,
+                                          sB + sn * Sh::raw_bc, sC + sn * Sh::raw_bc, x, dlt, Bm,
+                                          Cm, b, kn * kTileT, L, e0, ED, N);
+            cp_async_commit();
+        }
         // B, C of this tile -> fp32, zero padded to NP states.
         {
             const Tin *rb = sB + st * Sh::raw_bc;
@@ -156,43 +174,38 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
         const Tin *xs = sx + st * Sh::raw_x + ch;
         const Tin *ds = sd + st * Sh::raw_x + ch;
         float *yp = y + (b * L + t0) * ED + e;
-        for (int t = 0; t < tl; ++t) {
+#pragma unroll 8
+        for (int t = 0; t < kTileT; ++t) {
             const float dl = to_f32(ds[t * ET]);
             const float xv = to_f32(xs[t * ET]);
             const float dlx = dl * xv;
-            const float *bq = fB + t * NP + g * S;
-            const float *cq = fC + t * NP + g * S;
-            float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
+            const float2 dl2 = make_float2(dl, dl);
+            const float2 dlx2 = make_float2(dlx, dlx);
+            const float4 *bq = reinterpret_cast<const float4 *>(fB + t * NP + g * S);
+            const float4 *cq = reinterpret_cast<const float4 *>(fC + t * NP + g * S);
+            float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int q = 0; q < S / 4; ++q) {
-                const float4 bb = *reinterpret_cast<const float4 *>(bq + 4 * q);
-                const float4 cc = *reinterpret_cast<const float4 *>(cq + 4 * q);
-                float a;
-                a = ex2(dl * A2[4 * q + 0]);
-                h[4 * q + 0] = fmaf(a, h[4 * q + 0], dlx * bb.x);
-                acc0 = fmaf(cc.x, h[4 * q + 0], acc0);
-                a = ex2(dl * A2[4 * q + 1]);
-                h[4 * q + 1] = fmaf(a, h[4 * q + 1], dlx * bb.y);
-                acc1 = fmaf(cc.y, h[4 * q + 1], acc1);
-                a = ex2(dl * A2[4 * q + 2]);
-                h[4 * q + 2] = fmaf(a, h[4 * q + 2], dlx * bb.z);
-                acc2 = fmaf(cc.z, h[4 * q + 2], acc2);
-                a = ex2(dl * A2[4 * q + 3]);
-                h[4 * q + 3] = fmaf(a, h[4 * q + 3], dlx * bb.w);
-                acc3 = fmaf(cc.w, h[4 * q + 3], acc3);
+                const float4 bb = bq[q];
+                const float4 cc = cq[q];
+                const float2 z0 = __fmul2_rn(dl2, A2[2 * q]);
+                const float2 z1 = __fmul2_rn(dl2, A2[2 * q + 1]);
+                const float2 a0 = make_float2(ex2(z0.x), ex2(z0.y));
+                const float2 a1 = make_float2(ex2(z1.x), ex2(z1.y));
+                const float2 u0 = __fmul2_rn(dlx2, make_float2(bb.x, bb.y));
+                const float2 u1 = __fmul2_rn(dlx2, make_float2(bb.z, bb.w));
+                h[2 * q] = __ffma2_rn(a0, h[2 * q], u0);
+                h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], u1);
+                acc0 = __ffma2_rn(make_float2(cc.x, cc.y), h[2 * q], acc0);
+                acc1 = __ffma2_rn(make_float2(cc.z, cc.w), h[2 * q + 1], acc1);
             }
-            float yv = (acc0 + acc1) + (acc2 + acc3);
+            float yv = (acc0.x + acc0.y) + (acc1.x + acc1.y);
 #pragma unroll
             for (int o = 1; o < G; o <<= 1) yv += __shfl_xor_sync(0xffffffffu, yv, o);
-            if (g == 0 && e_ok) yp[int64_t(t) * ED] = fmaf(Dv, xv, yv);
+            if (g == 0 && e_ok && t < tl) yp[int64_t(t) * ED] = fmaf(Dv, xv, yv);
         }
-        __syncthreads();
-        if (k + 2 < n_tiles)
-            load_tile<Tin, S, G, VEC>(sx + st * Sh::raw_x, sd + st * Sh::raw_x, sB + st * Sh::raw_bc,
-                                      sC + st * Sh::raw_bc, x, dlt, Bm, Cm, b, (k + 2) * kTileT, L,
-                                      e0, ED, N);
-        cp_async_commit();
     }
+    cp_async_wait<0>();
 }
 
 template <typename Tin, int S, int G, bool VEC>

@@ -1,13 +1,574 @@
-// ssd_chunk_scan.cu -- chunked scalar-decay (SSD) scan for sm_103a.
+// ssd_chunk_scan.cu -- chunked scalar-decay ("SSD") scan on 5th-generation
+// tensor cores (tcgen05, TMEM accumulators, TMA-fed bf16 tiles) for sm_103a.
+//
+// Computes, per batch row b and head h (state H_t in R^{P x N}, H_{-1} = 0),
+//     H_t = exp(dt_t A_h) H_{t-1} + dt_t x_t (outer) B_t,   y_t = H_t C_t + D_h x_t
+// and, when bidirectional, adds the same recurrence run from the end of the
+// sequence (shared x, dt, A, B, C), counting D_h x_t once: "the addition of
+// two separate SSMs, plus D x(t)" with shared weights, from "Some questions of
+// Bi-Mamba2 and Hydra" (Bi-Mamba2 issue 1), whose chunked forward pass names
+// the stages used here (dA cumulative sums per direction, chunk states,
+// state passing, chunk-scan output).
+//
+// Chunked form, for a tile of Q = 128 rows with dA_r = dt_r A_h,
+// cum = inclusive prefix sum of dA in the tile, excl = cum - dA, tot = cum
+// at the tile's end (every exponent below is a difference of cumulative sums
+// and is <= 0 when dt A_h <= 0 -- the subtraction-based "stable segsum"):
+//   G     = C B^T                                   (tensor core, Q x Q)
+//   M[t,s]= G[t,s] dt_s (exp(cum_t - cum_s) [s <= t] + exp(excl_s - excl_t) [s >= t, reverse])
+//   Y     = M X                                     (tensor core, Q x P)
+//   Zf    = C S_in^T,  Zr = C R_in^T                (tensor core, Q x P)
+//   y[t]  = Y[t] + exp(cum_t) Zf[t] + exp(tot - excl_t) Zr[t] + D_h x[t]
+//   S_c   = B^T (w x), w_s = dt_s exp(tot - cum_s)   (tensor core, N x P)
+//   S_in <- exp(tot) S_in + S_c                      (fp32, in registers)
+// The reverse direction's entering states R_in come from a first sweep over
+// the tiles from the last to the first: R_in <- exp(tot) R_in + B^T (w' x),
+// w'_s = dt_s exp(excl_s).  Both directions read each tile of x, dt, B, C in
+// place -- no reversed copy of any input is materialised.
+//
+// One CTA of 128 threads owns one (b, h) and walks its tiles in order; thread
+// t owns tile row t (and TMEM lane t).  Thread 0 issues the TMA copies and
+// the tensor-core MMAs; every wait is bounded in time and reports through an
+// error word instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "ssm_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace ssm {
 namespace ssd {
 
-cudaError_t launch(const __nv_bfloat16 *, const __nv_bfloat16 *, const float *,
-                   const __nv_bfloat16 *, const __nv_bfloat16 *, const float *, float *, int64_t,
-                   int64_t, int64_t, int64_t, int64_t, int64_t, bool, int, cudaStream_t) {
+using namespace ssm::tc;
+
+constexpr int kQ = 128;          // tile rows (MMA M)
+constexpr int kP = 64;           // head dimension
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColG = 0;    // G: 128 columns
+constexpr uint32_t kColY = 128;  // Y: 64 columns
+constexpr uint32_t kColZf = 192; // Zf: 64
+constexpr uint32_t kColZr = 256; // Zr: 64
+constexpr uint32_t kColS = 320;  // chunk state S_c^T: 64
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kTile = kQ * 128;      // bytes of a 128-row x 128-byte tile region
+constexpr uint32_t kStateRegion = kP * 128;
+
+__device__ unsigned int g_device_error;   // non-zero once a bounded wait ran out
+
+template <int NB>  // NB = N / 64
+struct __align__(1024) Smem {
+    uint8_t C[NB][kTile];       // C tile, K-major: row t, 64 n per region (128B swizzle)
+    uint8_t B[2][kTile];        // B tile, rows s; region 1 stays zero when N = 64
+    uint8_t X[kTile];           // x tile, rows s, 64 p (MN-major B operand)
+    uint8_t Xw[kTile];          // weighted x rows
+    uint8_t M[2][kTile];        // masked G, K-major: row t, s in two 64-wide regions
+    uint8_t S[NB][kStateRegion];  // forward entering state (bf16), K-major: row p, n
+    uint8_t R[NB][kStateRegion];  // reverse entering state (bf16), same layout
+    float cum[kQ];
+    float excl[kQ];
+    float dtv[kQ];
+    float wsum[kThreads / 32];
+    uint64_t bar_tma;
+    uint64_t bar_mma;
+    uint32_t tmem_base;
+};
+
+struct Params {
+    const __nv_bfloat16 *dt;
+    const float *A;
+    const float *D;
+    float *y;
+    uint8_t *rstate;   // reverse entering states, [Bs*H][nc][NB * kStateRegion] (bidirectional)
+    int L, H, nc, bidir;
+};
+
+// Byte offset of element (row, col) of a 128-byte-swizzled tile whose rows
+// are 128 bytes (64 bf16): the 16-byte chunk index is XORed with row % 8.
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+    return uint32_t(row) * 128u + ((uint32_t((col >> 3) ^ (row & 7))) << 4) + uint32_t(col & 7) * 2u;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t w) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&w);
+    return __bfloat1622float2(v);
+}
+
+// Inclusive prefix sum over the CTA's 128 threads; also returns the total.
+__device__ __forceinline__ float cta_inclusive_scan(float v, float *wsum, float *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    float off = 0.0f, tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        const float s = wsum[w];
+        off += (w < warp) ? s : 0.0f;
+        tot += s;
+    }
+    *total = tot;
+    return v + off;
+}
+
+// Scale row s of the x tile by w into the Xw tile.  Both tiles share the
+// same swizzle, and the scale is uniform along the row, so the 16-byte
+// chunks are processed in their physical order.
+__device__ __forceinline__ void scale_row(const uint8_t *X, uint8_t *Xw, int s, float w) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(X + s * 128);
+    uint4 *dst = reinterpret_cast<uint4 *>(Xw + s * 128);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint4 v = src[j];
+        float2 a = unpack_bf16(v.x), b = unpack_bf16(v.y), c = unpack_bf16(v.z), d = unpack_bf16(v.w);
+        v.x = pack_bf16(a.x * w, a.y * w);
+        v.y = pack_bf16(b.x * w, b.y * w);
+        v.z = pack_bf16(c.x * w, c.y * w);
+        v.w = pack_bf16(d.x * w, d.y * w);
+        dst[j] = v;
+    }
+}
+
+// Store a P-vector state column (thread n owns column n) as bf16 into a
+// K-major state image: row p, K index n.
+template <int NB>
+__device__ __forceinline__ void store_state_bf16(uint8_t (*img)[kStateRegion], int n,
+                                                 const float (&s)[kP]) {
+    uint8_t *reg = img[n >> 6];
+    const int nc = n & 63;
+#pragma unroll
+    for (int p = 0; p < kP; ++p) {
+        __nv_bfloat16 v = __float2bfloat16_rn(s[p]);
+        *reinterpret_cast<__nv_bfloat16 *>(reg + swz(p, nc)) = v;
+    }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kThreads, 1)
+ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmX, const Params prm) {
+    constexpr int N = NB * 64;
+    extern __shared__ uint8_t smem_raw[];
+    Smem<NB> &sm = *reinterpret_cast<Smem<NB> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int bh = blockIdx.x;
+    const int b = bh / prm.H;
+    const int h = bh % prm.H;
+    const int L = prm.L;
+    const float Ah = prm.A[h] * SSM_LOG2E;        // decays are exp2 of log2e-scaled sums
+    const float Dh = prm.D ? prm.D[h] : 0.0f;
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(&sm.bar_tma, 1);
+        mbar_init(&sm.bar_mma, 1);
+        mbar_fence_init();
+        prefetch_tmap(&tmC);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    // The second B region (n = 64..127) is read as zero rows when N = 64.
+    if (NB == 1) {
+        uint4 *z = reinterpret_cast<uint4 *>(sm.B[1]);
+        for (int i = tid; i < int(kTile / 16); i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = sm.tmem_base;
+    uint32_t ph_tma = 0, ph_mma = 0;
+    bool ok = true;
+
+    const uint32_t sC = smem_addr(sm.C), sB = smem_addr(sm.B), sX = smem_addr(sm.X);
+    const uint32_t sXw = smem_addr(sm.Xw), sM = smem_addr(sm.M), sS = smem_addr(sm.S);
+    const uint32_t sR = smem_addr(sm.R);
+    constexpr uint32_t idG = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idZ = idesc_bf16_f32(128, 64, false, false);
+    constexpr uint32_t idY = idesc_bf16_f32(128, 64, false, true);
+    constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);
+
+    // Per-tile cumulative sums of dt * A (log2 units); fills sm.cum/excl/dtv.
+    auto tile_cumsum = [&](int c0, float *tot_out) {
+        const int row = c0 + tid;
+        const float dv = row < L ? __bfloat162float(prm.dt[(int64_t(b) * L + row) * prm.H + h]) : 0.0f;
+        const float dA = dv * Ah;
+        float tot;
+        const float cum = cta_inclusive_scan(dA, sm.wsum, &tot);
+        sm.cum[tid] = cum;
+        sm.excl[tid] = cum - dA;
+        sm.dtv[tid] = dv;
+        *tot_out = tot;
+    };
+    // Chunk-state MMA: S^T[n, p] = sum_s B[s, n] * Xw[s, p] into TMEM kColS.
+    auto issue_state_mma = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk) {
+            const uint64_t a = smem_desc(sB + kk * 2048, kTile, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(sXw + kk * 2048, kTile, 1024, kSwizzle128B);
+            mma_bf16_ss(tmem + kColS, a, bd, idS, kk > 0);
+        }
+    };
+
+    float st[kP];   // this thread's state column (n = tid), fp32
+    const int nc = prm.nc;
+    const size_t rstride = size_t(NB) * kStateRegion;
+
+    // ---------------- reverse sweep: entering states of the reverse scan -------------
+    if (prm.bidir) {
+#pragma unroll
+        for (int p = 0; p < kP; ++p) st[p] = 0.0f;
+        for (int c = nc - 1; c >= 0 && ok; --c) {
+            const int c0 = c * kQ;
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&sm.bar_tma, NB * kTile + kTile);
+#pragma unroll
+                for (int r = 0; r < NB; ++r) tma_load_3d(sm.B[r], &tmB, &sm.bar_tma, r * 64, c0, b);
+                tma_load_4d(sm.X, &tmX, &sm.bar_tma, 0, h, c0, b);
+            }
+            float tot;
+            tile_cumsum(c0, &tot);
+            // R_in of this tile (state entering from the right) -> scratch.
+            if (c < nc - 1) {
+                if (tid < N) store_state_bf16<NB>(sm.R, tid, st);
+                __syncthreads();
+                uint4 *dst = reinterpret_cast<uint4 *>(prm.rstate + (size_t(bh) * nc + c) * rstride);
+                const uint4 *src = reinterpret_cast<const uint4 *>(sm.R);
+                for (int i = tid; i < int(rstride / 16); i += kThreads) dst[i] = src[i];
+                fence_proxy_async_all();
+            }
+            ok = mbar_wait_bounded(&sm.bar_tma, ph_tma, &abort_flag, kWaitLimitNs);
+            ph_tma ^= 1;
+            if (__syncthreads_or(!ok)) { ok = false; break; }
+            scale_row(sm.X, sm.Xw, tid, exp2f(sm.excl[tid]) * sm.dtv[tid]);
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after_sync();
+                issue_state_mma();
+                mma_commit(&sm.bar_mma);
+            }
+            ok = mbar_wait_bounded(&sm.bar_mma, ph_mma, &abort_flag, kWaitLimitNs);
+            ph_mma ^= 1;
+            if (__syncthreads_or(!ok)) { ok = false; break; }
+            tc_fence_after_sync();
+            if (tid < N) {
+                const float e = exp2f(tot);
+#pragma unroll
+                for (int q = 0; q < kP / 32; ++q) {
+                    float v[32];
+                    tmem_ld_32x32b_x32(tmem + lane_base + kColS + q * 32, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) st[q * 32 + j] = fmaf(e, st[q * 32 + j], v[j]);
+                }
+            }
+            tc_fence_before_sync();
+            __syncthreads();
+        }
+    }
+
+    // ---------------- forward sweep with the outputs ----------------------------------
+#pragma unroll
+    for (int p = 0; p < kP; ++p) st[p] = 0.0f;
+    for (int c = 0; c < nc && ok; ++c) {
+        const int c0 = c * kQ;
+        const bool has_s = c > 0;
+        const bool has_r = prm.bidir && (c < nc - 1);
+        if (tid == 0) {
+            uint32_t bytes = NB * kTile * 2 + kTile;
+            if (has_r) bytes += uint32_t(rstride);
+            mbar_arrive_expect_tx(&sm.bar_tma, bytes);
+#pragma unroll
+            for (int r = 0; r < NB; ++r) {
+                tma_load_3d(sm.C[r], &tmC, &sm.bar_tma, r * 64, c0, b);
+                tma_load_3d(sm.B[r], &tmB, &sm.bar_tma, r * 64, c0, b);
+            }
+            tma_load_4d(sm.X, &tmX, &sm.bar_tma, 0, h, c0, b);
+            if (has_r)
+                bulk_load(sm.R, prm.rstate + (size_t(bh) * nc + c) * rstride, uint32_t(rstride),
+                          &sm.bar_tma);
+        }
+        float tot;
+        tile_cumsum(c0, &tot);
+        ok = mbar_wait_bounded(&sm.bar_tma, ph_tma, &abort_flag, kWaitLimitNs);
+        ph_tma ^= 1;
+        if (__syncthreads_or(!ok)) { ok = false; break; }
+
+        // MMA group 1: G = C B^T, Zf = C S_in^T, Zr = C R_in^T.
+        if (tid == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < N / 16; ++kk) {
+                const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;
+                const uint64_t a = smem_desc(sC + koff, 16, 1024, kSwizzle128B);
+                mma_bf16_ss(tmem + kColG, a, smem_desc(sB + koff, 16, 1024, kSwizzle128B), idG, kk > 0);
+                const uint32_t soff = (kk >> 2) * kStateRegion + (kk & 3) * 32;
+                if (has_s)
+                    mma_bf16_ss(tmem + kColZf, a, smem_desc(sS + soff, 16, 1024, kSwizzle128B), idZ, kk > 0);
+                if (has_r)
+                    mma_bf16_ss(tmem + kColZr, a, smem_desc(sR + soff, 16, 1024, kSwizzle128B), idZ, kk > 0);
+            }
+            mma_commit(&sm.bar_mma);
+        }
+        // Meanwhile: weighted x rows for this tile's forward chunk state.
+        scale_row(sm.X, sm.Xw, tid, exp2f(tot - sm.cum[tid]) * sm.dtv[tid]);
+        fence_proxy_async_smem();
+        ok = mbar_wait_bounded(&sm.bar_mma, ph_mma, &abort_flag, kWaitLimitNs);
+        ph_mma ^= 1;
+        if (__syncthreads_or(!ok)) { ok = false; break; }
+        tc_fence_after_sync();
+
+        // Decay mask on row t of G -> bf16 M (K-major, swizzled).
+        {
+            const int t = tid;
+            const float cum_t = sm.cum[t], excl_t = sm.excl[t];
+#pragma unroll 1
+            for (int sb = 0; sb < kQ / 32; ++sb) {
+                float g[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + kColG + sb * 32, g);
+                uint32_t packed[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    float m2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int s = sb * 32 + j + u;
+                        const float ds = sm.dtv[s];
+                        float m = 0.0f;
+                        if (s <= t) m = exp2f(cum_t - sm.cum[s]);
+                        if (prm.bidir && s >= t) m += exp2f(sm.excl[s] - excl_t);
+                        m2[u] = g[j + u] * m * ds;
+                    }
+                    packed[j >> 1] = pack_bf16(m2[0], m2[1]);
+                }
+                uint8_t *reg = sm.M[sb >> 1];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int col = (sb & 1) * 32 + q * 8;   // column inside the 64-wide region
+                    *reinterpret_cast<uint4 *>(reg + swz(t, col)) =
+                        make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // MMA group 2: Y = M X, S_c^T = B^T Xw.
+        if (tid == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < kQ / 16; ++kk) {
+                const uint64_t a = smem_desc(sM + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                const uint64_t bd = smem_desc(sX + kk * 2048, kTile, 1024, kSwizzle128B);
+                mma_bf16_ss(tmem + kColY, a, bd, idY, kk > 0);
+            }
+            issue_state_mma();
+            mma_commit(&sm.bar_mma);
+        }
+        ok = mbar_wait_bounded(&sm.bar_mma, ph_mma, &abort_flag, kWaitLimitNs);
+        ph_mma ^= 1;
+        if (__syncthreads_or(!ok)) { ok = false; break; }
+        tc_fence_after_sync();
+
+        // Epilogue: row t of y.
+        {
+            const int t = tid;
+            const int row = c0 + t;
+            const float ef = exp2f(sm.cum[t]);
+            const float er = exp2f(tot - sm.excl[t]);
+            float *yrow = prm.y + ((int64_t(b) * L + row) * prm.H + h) * kP;
+            const uint4 *xs = reinterpret_cast<const uint4 *>(sm.X + t * 128);
+#pragma unroll 1
+            for (int q = 0; q < kP / 32; ++q) {
+                float xr[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 v = xs[(q * 4 + j) ^ (t & 7)];
+                    const float2 a = unpack_bf16(v.x), bb = unpack_bf16(v.y),
+                                 cc = unpack_bf16(v.z), dd = unpack_bf16(v.w);
+                    xr[8 * j + 0] = a.x; xr[8 * j + 1] = a.y; xr[8 * j + 2] = bb.x; xr[8 * j + 3] = bb.y;
+                    xr[8 * j + 4] = cc.x; xr[8 * j + 5] = cc.y; xr[8 * j + 6] = dd.x; xr[8 * j + 7] = dd.y;
+                }
+                float yv[32], zf[32], zr[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + kColY + q * 32, yv);
+                if (has_s) tmem_ld_32x32b_x32(tmem + lane_base + kColZf + q * 32, zf);
+                if (has_r) tmem_ld_32x32b_x32(tmem + lane_base + kColZr + q * 32, zr);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float v = fmaf(Dh, xr[j], yv[j]);
+                    if (has_s) v = fmaf(ef, zf[j], v);
+                    if (has_r) v = fmaf(er, zr[j], v);
+                    yv[j] = v;
+                }
+                if (row < L) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(yrow + q * 32 + j) =
+                            make_float4(yv[j], yv[j + 1], yv[j + 2], yv[j + 3]);
+                }
+            }
+        }
+        // State passing: column n = tid of S_in.
+        if (tid < N) {
+            const float e = exp2f(tot);
+#pragma unroll
+            for (int q = 0; q < kP / 32; ++q) {
+                float v[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + kColS + q * 32, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) st[q * 32 + j] = fmaf(e, st[q * 32 + j], v[j]);
+            }
+            store_state_bf16<NB>(sm.S, tid, st);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+    }
+
+    if (!ok && tid == 0) {
+        abort_flag = 1;
+        atomicOr(&g_device_error, 1u);
+    }
+    // An MMA still in flight after a timeout: give it a bounded chance to land
+    // before the tensor memory is released.
+    if (!ok && tid == 0) {
+        volatile int never = 0;
+        (void)mbar_wait_bounded(&sm.bar_mma, ph_mma, &never, 100000000ull);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+static bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+                     const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void *>(base),
+                    dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int NB>
+static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A,
+                             const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D,
+                             float *y, int64_t Bs, int64_t L, int64_t H, bool bidir,
+                             cudaStream_t stream) {
+    constexpr int N = NB * 64;
+    CUtensorMap tmC, tmB, tmX;
+    const cuuint64_t dbc[3] = {cuuint64_t(N), cuuint64_t(L), cuuint64_t(Bs)};
+    const cuuint64_t sbc[2] = {cuuint64_t(N) * 2, cuuint64_t(L) * N * 2};
+    const cuuint32_t boxbc[3] = {64, kQ, 1};
+    const cuuint64_t dx[4] = {cuuint64_t(kP), cuuint64_t(H), cuuint64_t(L), cuuint64_t(Bs)};
+    const cuuint64_t sx[3] = {cuuint64_t(kP) * 2, cuuint64_t(H) * kP * 2, cuuint64_t(L) * H * kP * 2};
+    const cuuint32_t boxx[4] = {64, 1, kQ, 1};
+    if (!make_map(&tmC, Cm, 3, dbc, sbc, boxbc) || !make_map(&tmB, Bm, 3, dbc, sbc, boxbc) ||
+        !make_map(&tmX, x, 4, dx, sx, boxx))
+        return cudaErrorInvalidValue;
+
+    Params prm;
+    prm.dt = dt;
+    prm.A = A;
+    prm.D = D;
+    prm.y = y;
+    prm.rstate = nullptr;
+    prm.L = int(L);
+    prm.H = int(H);
+    prm.nc = int((L + kQ - 1) / kQ);
+    prm.bidir = bidir ? 1 : 0;
+    const int64_t grid = Bs * H;
+    if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+
+    const size_t smem = sizeof(Smem<NB>) + 1024;
+    auto kern = ssd_chunk_scan_kernel<NB>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (err != cudaSuccess) return err;
+
+    void *scratch = nullptr;
+    if (bidir && prm.nc > 1) {
+        const size_t bytes = size_t(grid) * prm.nc * NB * kStateRegion;
+        err = cudaMallocAsync(&scratch, bytes, stream);
+        if (err != cudaSuccess) return err;
+        prm.rstate = static_cast<uint8_t *>(scratch);
+    }
+    kern<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tmC, tmB, tmX, prm);
+    err = cudaGetLastError();
+    if (scratch) {
+        cudaError_t e2 = cudaFreeAsync(scratch, stream);
+        if (err == cudaSuccess) err = e2;
+    }
+    return err;
+}
+
+cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
+                   const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
+                   int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N, int64_t chunk,
+                   bool bidirectional, int num_sms, cudaStream_t stream) {
+    (void)num_sms;
+    (void)chunk;
+    if (P != kP) return cudaErrorNotSupported;
+    if (N == 64)
+        return launch_nb<1>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream);
+    if (N == 128)
+        return launch_nb<2>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream);
     return cudaErrorNotSupported;
+}
+
+// Read and clear the device error word (host side, synchronous).
+cudaError_t take_device_error(unsigned int *out) {
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    }
+    *out = v;
+    return e;
 }
 
 }  // namespace ssd

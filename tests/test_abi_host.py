@@ -25,7 +25,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssd_chunk_scan_fwd", "ssm_status_string",
-              "ssm_version"):
+              "ssm_version", "ssm_check_device_errors"):
         assert n in names
 
 
@@ -81,6 +81,7 @@ def test_ssd_rejects_bad_arguments():
     assert ssd(chunk=0) == 1
     assert ssd(P_=32) == 2
     assert ssd(N=48) == 2
+    assert ssd(N=32) == 2
     assert ssd(chunk=96) == 2
     ptrs = [P] * 7
     ptrs[3] = P_ODD                       # B not 16-byte aligned
@@ -93,3 +94,4 @@ def test_valid_call_without_device_reports_no_device():
         pytest.skip("a device is present")
     assert diag() == 6
     assert ssd() == 6
+    assert lrs.library().ssm_check_device_errors(None) == 6

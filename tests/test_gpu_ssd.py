@@ -1,0 +1,117 @@
+"""GPU parity of the chunked scalar-decay (SSD) scan, one and two directions,
+against the fp64 oracle on the same bf16-rounded inputs.
+
+Tolerance: max|y - y_ref| <= 2e-2 * max|y_ref| (bf16 inputs, bf16 tensor-core
+operands with fp32 accumulation and fp32 state).
+"""
+import numpy as np
+import pytest
+import torch
+
+import linear_recurrence_ssm_gb300 as lrs
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+def _dev(inp, dev):
+    return {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+
+
+def _check(y, ref):
+    y = y.double().cpu().numpy()
+    assert np.all(np.isfinite(y))
+    scale = float(np.max(np.abs(ref)))
+    err = float(np.max(np.abs(y - ref)))
+    assert err <= TOL * scale, "max abs err %.3e > %.3e (scale %.3e)" % (err, TOL * scale, scale)
+    return err / scale
+
+
+@pytest.mark.parametrize("bidir", [False, True])
+@pytest.mark.parametrize("Bs,L,H,N,chunk", [
+    (1, 128, 1, 64, 128),     # exactly one tile
+    (2, 300, 3, 64, 128),     # ragged last tile
+    (1, 1, 2, 128, 256),      # L = 1
+    (2, 257, 2, 128, 256),    # one row into a third tile
+    (1, 400, 2, 64, 64),
+    (1, 640, 1, 128, 128),    # five tiles
+])
+def test_ssd_matches_oracle(cuda_device, Bs, L, H, N, chunk, bidir):
+    inp = workloads.ssd_inputs(Bs, L, H, 64, N, "bf16", seed=L + H + N + int(bidir))
+    ref = oracle.ssd_scan(**inp, bidirectional=bidir)
+    y = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=chunk, bidirectional=bidir)
+    _check(y, ref)
+    lrs.ssm_check_device_errors()
+
+
+def test_ssd_without_D(cuda_device):
+    inp = workloads.ssd_inputs(2, 200, 2, 64, 64, "bf16", seed=21, with_D=False)
+    ref = oracle.ssd_scan(**inp)
+    y = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=128)
+    _check(y, ref)
+
+
+def test_chunk_lengths_agree(cuda_device):
+    inp = _dev(workloads.ssd_inputs(1, 300, 2, 64, 128, "bf16", seed=5), cuda_device)
+    ys = [lrs.ssd_chunk_scan_fwd(**inp, chunk=q) for q in (64, 128, 256)]
+    for y in ys[1:]:
+        assert torch.allclose(y, ys[0], rtol=0, atol=1e-3 * ys[0].abs().max().item())
+
+
+def test_bidirectional_reversal_equivariance(cuda_device):
+    inp = workloads.ssd_inputs(2, 333, 2, 64, 64, "bf16", seed=8)
+    flip = {k: (v.flip(1).contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in inp.items()}
+    y = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=128, bidirectional=True)
+    yf = lrs.ssd_chunk_scan_fwd(**_dev(flip, cuda_device), chunk=128, bidirectional=True)
+    scale = y.abs().max().item()
+    assert (yf.flip(1) - y).abs().max().item() <= TOL * scale
+
+
+@pytest.mark.parametrize("name", ["ssd_bf16_Bs4_L4096_H32_P64_N128_Q256",
+                                  "bissd_bf16_Bs32_L400_H8_P64_N64_Q128"])
+def test_benchmark_shape_sampled_heads(cuda_device, name):
+    """Full benchmark size in the benchmark's launch configuration; the oracle
+    recomputes a spread-out sample of (batch, head) pairs one by one."""
+    w = workloads.BY_NAME[name]
+    s = w.shape
+    inp = workloads.workload_inputs(w)
+    y = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=s["chunk"],
+                               bidirectional=s["bidirectional"]).cpu().double().numpy()
+    assert np.all(np.isfinite(y))
+    Bs, H = s["Bs"], s["H"]
+    pairs = [(0, 0), (Bs - 1, H - 1), (Bs // 2, H // 3), (1 % Bs, H - 2), (Bs - 2, 1)]
+    for b, h in pairs:
+        one = dict(x=inp["x"][b:b + 1, :, h:h + 1], dt=inp["dt"][b:b + 1, :, h:h + 1],
+                   A_head=inp["A_head"][h:h + 1], B=inp["B"][b:b + 1], C=inp["C"][b:b + 1],
+                   D=inp["D"][h:h + 1])
+        ref = oracle.ssd_scan(**one, bidirectional=s["bidirectional"])[0, :, 0]
+        err = np.max(np.abs(y[b, :, h] - ref))
+        assert err <= TOL * np.max(np.abs(ref)), (b, h, err)
+    lrs.ssm_check_device_errors()
+
+
+def test_deterministic_and_guard_bands(cuda_device):
+    inp = _dev(workloads.ssd_inputs(2, 260, 3, 64, 64, "bf16", seed=9), cuda_device)
+    Bs, L, H, P = inp["x"].shape
+    n = Bs * L * H * P
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), float("nan"), device=cuda_device)
+    y1 = buf[guard:guard + n].view(Bs, L, H, P)
+    lrs.ssd_chunk_scan_fwd(**inp, chunk=128, bidirectional=True, y=y1)
+    y2 = lrs.ssd_chunk_scan_fwd(**inp, chunk=128, bidirectional=True)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:guard]).all() and torch.isnan(buf[guard + n:]).all()
+    assert torch.equal(y1, y2)
+
+
+def test_runs_on_caller_stream(cuda_device):
+    inp = _dev(workloads.ssd_inputs(1, 256, 2, 64, 128, "bf16", seed=3), cuda_device)
+    ref = lrs.ssd_chunk_scan_fwd(**inp, chunk=128, bidirectional=True)
+    s = torch.cuda.Stream(cuda_device)
+    with torch.cuda.stream(s):
+        y = lrs.ssd_chunk_scan_fwd(**inp, chunk=128, bidirectional=True)
+    s.synchronize()
+    assert torch.equal(y, ref)
