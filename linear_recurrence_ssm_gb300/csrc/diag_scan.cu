@@ -25,6 +25,8 @@
 //     fp32 values of one row.
 #include "ssm_common.cuh"
 
+#include <algorithm>
+
 namespace ssm {
 namespace diag {
 
@@ -49,11 +51,12 @@ template <typename Tin, int S, int G, bool VEC>
 __device__ __forceinline__ void load_tile(Tin *sx, Tin *sd, Tin *sB, Tin *sC,
                                           const Tin *__restrict__ x, const Tin *__restrict__ dlt,
                                           const Tin *__restrict__ Bm, const Tin *__restrict__ Cm,
-                                          int64_t b, int t0, int L, int e0, int ED, int N) {
+                                          int64_t b, int t0, int te, int L, int e0, int ED,
+                                          int N) {
     using Sh = Shape<Tin, S, G>;
     constexpr int ET = Sh::ET;
     const int tid = threadIdx.x;
-    const int rows = max(0, min(kTileT, L - t0));
+    const int rows = max(0, min(kTileT, te - t0));   // rows of this segment (te <= L)
     if constexpr (VEC) {
         constexpr int EPC = 16 / sizeof(Tin);       // elements per 16-byte chunk
         constexpr int CPR = ET / EPC;               // chunks per x row
@@ -94,12 +97,22 @@ __device__ __forceinline__ void load_tile(Tin *sx, Tin *sd, Tin *sB, Tin *sC,
     }
 }
 
-template <typename Tin, int S, int G, bool VEC>
+// Summary of one time segment of one channel, written when the sequence is
+// split into K > 1 segments: the segment's end state started from zero, the
+// sum of its deltas, and its smallest delta.
+struct SegSummary {
+    float *h_end;   // [K][Bs][ED][16]
+    float *dsum;    // [K][Bs][ED]
+    float *dmin;    // [K][Bs][ED]
+};
+
+template <typename Tin, int S, int G, bool VEC, bool SPLIT>
 __global__ void __launch_bounds__(kThreads)
 diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
                  const float *__restrict__ A, const Tin *__restrict__ Bm,
                  const Tin *__restrict__ Cm, const float *__restrict__ D,
-                 float *__restrict__ y, int L, int ED, int N, int n_etiles) {
+                 float *__restrict__ y, int L, int ED, int N, int n_etiles, int seg_len,
+                 SegSummary summ) {
     using Sh = Shape<Tin, S, G>;
     constexpr int ET = Sh::ET;
     constexpr int NP = Sh::NP;
@@ -116,6 +129,9 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
 
     const int64_t b = blockIdx.x / n_etiles;
     const int e0 = (blockIdx.x % n_etiles) * ET;
+    const int seg = blockIdx.y;
+    const int tb = seg * seg_len;                    // this CTA's time range [tb, te)
+    const int te = min(L, tb + seg_len);
     const int tid = threadIdx.x;
     const int ch = tid / G;
     const int g = tid % G;
@@ -133,14 +149,15 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
         h[j] = make_float2(0.0f, 0.0f);
     }
     const float Dv = (D != nullptr && e_ok) ? D[e] : 0.0f;
+    float dsum = 0.0f, dmin = 3.0e38f;
 
-    const int n_tiles = (L + kTileT - 1) / kTileT;
+    const int n_tiles = (te - tb + kTileT - 1) / kTileT;
 #pragma unroll
     for (int k = 0; k < kStages - 1; ++k) {
         if (k < n_tiles)
             load_tile<Tin, S, G, VEC>(sx + k * Sh::raw_x, sd + k * Sh::raw_x, sB + k * Sh::raw_bc,
-                                      sC + k * Sh::raw_bc, x, dlt, Bm, Cm, b, k * kTileT, L, e0,
-                                      ED, N);
+                                      sC + k * Sh::raw_bc, x, dlt, Bm, Cm, b, tb + k * kTileT, te,
+                                      L, e0, ED, N);
         cp_async_commit();
     }
 
@@ -154,7 +171,7 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
             if (kn < n_tiles)
                 load_tile<Tin, S, G, VEC>(sx + sn * Sh::raw_x, sd + sn * Sh::raw_x,
                                           sB + sn * Sh::raw_bc, sC + sn * Sh::raw_bc, x, dlt, Bm,
-                                          Cm, b, kn * kTileT, L, e0, ED, N);
+                                          Cm, b, tb + kn * kTileT, te, L, e0, ED, N);
             cp_async_commit();
         }
         // B, C of this tile -> fp32, zero padded to NP states.
@@ -169,113 +186,381 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
         }
         __syncthreads();
 
-        const int t0 = k * kTileT;
-        const int tl = min(kTileT, L - t0);
+        const int t0 = tb + k * kTileT;
+        const int tl = min(kTileT, te - t0);
         const Tin *xs = sx + st * Sh::raw_x + ch;
         const Tin *ds = sd + st * Sh::raw_x + ch;
+        const float *bq = fB + g * S;
+        const float *cq = fC + g * S;
         float *yp = y + (b * L + t0) * ED + e;
-#pragma unroll 8
+        const bool store_ok = (g == 0) && e_ok;
+        // Operands of the next step are read from shared memory before this
+        // step's result is stored: y is a generic pointer, and the compiler
+        // may not move shared loads across a store that could alias them.
+        float n_dl = to_f32(ds[0]), n_xv = to_f32(xs[0]);
+        float4 n_b[S / 4], n_c[S / 4];
+        float2 n_a[S2];   // next step's decays, exp2(delta * A * log2 e)
+#pragma unroll
+        for (int q = 0; q < S / 4; ++q) {
+            n_b[q] = reinterpret_cast<const float4 *>(bq)[q];
+            n_c[q] = reinterpret_cast<const float4 *>(cq)[q];
+        }
+        {
+            const float2 dl2 = make_float2(n_dl, n_dl);
+#pragma unroll
+            for (int j = 0; j < S2; ++j) {
+                const float2 z = __fmul2_rn(dl2, A2[j]);
+                n_a[j] = make_float2(ex2(z.x), ex2(z.y));
+            }
+        }
+#pragma unroll 2
         for (int t = 0; t < kTileT; ++t) {
-            const float dl = to_f32(ds[t * ET]);
-            const float xv = to_f32(xs[t * ET]);
+            const float dl = n_dl, xv = n_xv;
+            float4 cb[S / 4], cc[S / 4];
+            float2 a[S2];
+#pragma unroll
+            for (int q = 0; q < S / 4; ++q) {
+                cb[q] = n_b[q];
+                cc[q] = n_c[q];
+            }
+#pragma unroll
+            for (int j = 0; j < S2; ++j) a[j] = n_a[j];
+            if (t + 1 < kTileT) {
+                // Operands and exponentials of step t+1 come first: the
+                // exponentials keep the MUFU pipe busy while this step's
+                // state update waits on them.
+                n_dl = to_f32(ds[(t + 1) * ET]);
+                n_xv = to_f32(xs[(t + 1) * ET]);
+#pragma unroll
+                for (int q = 0; q < S / 4; ++q) {
+                    n_b[q] = reinterpret_cast<const float4 *>(bq + (t + 1) * NP)[q];
+                    n_c[q] = reinterpret_cast<const float4 *>(cq + (t + 1) * NP)[q];
+                }
+                const float2 dl2 = make_float2(n_dl, n_dl);
+#pragma unroll
+                for (int j = 0; j < S2; ++j) {
+                    const float2 z = __fmul2_rn(dl2, A2[j]);
+                    n_a[j] = make_float2(ex2(z.x), ex2(z.y));
+                }
+            }
             const float dlx = dl * xv;
-            const float2 dl2 = make_float2(dl, dl);
+            if constexpr (SPLIT) {
+                dsum += dl;
+                dmin = (t < tl) ? fminf(dmin, dl) : dmin;
+            }
             const float2 dlx2 = make_float2(dlx, dlx);
-            const float4 *bq = reinterpret_cast<const float4 *>(fB + t * NP + g * S);
-            const float4 *cq = reinterpret_cast<const float4 *>(fC + t * NP + g * S);
             float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int q = 0; q < S / 4; ++q) {
-                const float4 bb = bq[q];
-                const float4 cc = cq[q];
-                const float2 z0 = __fmul2_rn(dl2, A2[2 * q]);
-                const float2 z1 = __fmul2_rn(dl2, A2[2 * q + 1]);
-                const float2 a0 = make_float2(ex2(z0.x), ex2(z0.y));
-                const float2 a1 = make_float2(ex2(z1.x), ex2(z1.y));
-                const float2 u0 = __fmul2_rn(dlx2, make_float2(bb.x, bb.y));
-                const float2 u1 = __fmul2_rn(dlx2, make_float2(bb.z, bb.w));
-                h[2 * q] = __ffma2_rn(a0, h[2 * q], u0);
-                h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], u1);
-                acc0 = __ffma2_rn(make_float2(cc.x, cc.y), h[2 * q], acc0);
-                acc1 = __ffma2_rn(make_float2(cc.z, cc.w), h[2 * q + 1], acc1);
+                const float2 u0 = __fmul2_rn(dlx2, make_float2(cb[q].x, cb[q].y));
+                const float2 u1 = __fmul2_rn(dlx2, make_float2(cb[q].z, cb[q].w));
+                h[2 * q] = __ffma2_rn(a[2 * q], h[2 * q], u0);
+                h[2 * q + 1] = __ffma2_rn(a[2 * q + 1], h[2 * q + 1], u1);
+                acc0 = __ffma2_rn(make_float2(cc[q].x, cc[q].y), h[2 * q], acc0);
+                acc1 = __ffma2_rn(make_float2(cc[q].z, cc[q].w), h[2 * q + 1], acc1);
             }
             float yv = (acc0.x + acc0.y) + (acc1.x + acc1.y);
 #pragma unroll
             for (int o = 1; o < G; o <<= 1) yv += __shfl_xor_sync(0xffffffffu, yv, o);
-            if (g == 0 && e_ok && t < tl) yp[int64_t(t) * ED] = fmaf(Dv, xv, yv);
+            if (store_ok && t < tl) yp[int64_t(t) * ED] = fmaf(Dv, xv, yv);
         }
+    }
+    cp_async_wait<0>();
+
+    if constexpr (SPLIT) {
+        // Rows past the segment's end were zero filled (delta = 0), so h and
+        // dsum are exactly the segment's end state and delta sum.
+        if (e_ok) {
+            const int64_t c = (int64_t(seg) * (gridDim.x / n_etiles) + b) * ED + e;
+#pragma unroll
+            for (int j = 0; j < S2; ++j) {
+                const int n = g * S + 2 * j;
+                summ.h_end[c * 16 + n] = h[j].x;
+                summ.h_end[c * 16 + n + 1] = h[j].y;
+            }
+            if (g == 0) {
+                summ.dsum[c] = dsum;
+                summ.dmin[c] = dmin;
+            }
+        }
+    }
+}
+
+// Copy rows [t0, t0 + kTileT) x channels [e0, e0 + 128) of a (Bs, L, ED)
+// tensor into shared memory [kTileT][128]; rows >= te and channels >= ED
+// are zero filled.  VEC: 16-byte cp.async chunks (caller checked alignment).
+template <typename T, bool VEC>
+__device__ __forceinline__ void stage_rows(T *dst, const T *__restrict__ src, int64_t b, int t0,
+                                           int te, int L, int e0, int ED) {
+    constexpr int EPC = 16 / sizeof(T);
+    const int rows = max(0, min(kTileT, te - t0));
+    if constexpr (VEC) {
+        constexpr int CPR = 128 / EPC;
+        for (int i = threadIdx.x; i < kTileT * CPR; i += kThreads) {
+            const int t = i / CPR, c = i % CPR;
+            const int e = e0 + c * EPC;
+            const bool ok = (t < rows) && (e < ED);
+            const int64_t g = ok ? ((b * L + t0 + t) * ED + e) : 0;
+            cp_async16(dst + t * 128 + c * EPC, src + g, ok ? 16 : 0);
+        }
+    } else {
+        for (int i = threadIdx.x; i < kTileT * 128; i += kThreads) {
+            const int t = i / 128, c = i % 128;
+            const int e = e0 + c;
+            const bool ok = (t < rows) && (e < ED);
+            dst[i] = ok ? src[(b * L + t0 + t) * ED + e] : T(0.0f);
+        }
+    }
+}
+
+// Second pass of a time-split scan (16 padded states, one channel per
+// thread): for every segment k >= 1, fold the summaries of segments 0..k-1
+// into the state entering segment k, h_in, and add its contribution
+//     y_t += sum_n C_t[n] * exp(A[e,n] * (delta_{tb} + ... + delta_t)) * h_in[n]
+// to the segment's outputs, which the first pass computed from a zero state.
+// exp2 flushes results below 2^-126 to zero, so once A*cumsum + log2|h_in|
+// is below -126 for a group of states the group adds exactly zero, and it
+// stays so while delta >= 0 and A <= 0 (checked per segment and channel):
+// such groups are dropped, and the CTA stops when no warp has one left.
+// delta, C and y are staged through shared memory one tile ahead.
+template <typename Tin, bool VEC>
+__global__ void __launch_bounds__(kThreads)
+diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
+                  const Tin *__restrict__ Cm, float *__restrict__ y, int Bs, int L, int ED, int N,
+                  int seg_len, SegSummary summ) {
+    constexpr int NP = 16;
+    extern __shared__ __align__(16) unsigned char fx_smem[];
+    float (*s_y)[kTileT * 128] = reinterpret_cast<float (*)[kTileT * 128]>(fx_smem);
+    Tin (*s_d)[kTileT * 128] = reinterpret_cast<Tin (*)[kTileT * 128]>(fx_smem + 2 * kTileT * 128 * 4);
+    Tin (*s_c)[kTileT * NP] = reinterpret_cast<Tin (*)[kTileT * NP]>(
+        fx_smem + 2 * kTileT * 128 * (4 + sizeof(Tin)));
+    const int tid = threadIdx.x;
+    const int e0 = blockIdx.x * kThreads;
+    const int e = e0 + tid;
+    const int64_t b = blockIdx.y;
+    const int seg = blockIdx.z + 1;
+    const bool e_ok = e < ED;
+    const int ec = e_ok ? e : ED - 1;    // lanes past ED mirror a valid channel, store nothing
+
+    float A2[NP], hin[NP], lh[NP];
+    bool mono = true;
+#pragma unroll
+    for (int n = 0; n < NP; ++n) {
+        A2[n] = n < N ? A[int64_t(ec) * N + n] * SSM_LOG2E : 0.0f;
+        mono = mono && (A2[n] <= 0.0f);
+        hin[n] = 0.0f;
+    }
+    for (int j = 0; j < seg; ++j) {
+        const int64_t c = (int64_t(j) * Bs + b) * ED + ec;
+        const float d = summ.dsum[c];
+#pragma unroll
+        for (int n = 0; n < NP; ++n) hin[n] = fmaf(ex2(A2[n] * d), hin[n], summ.h_end[c * 16 + n]);
+    }
+    mono = mono && (summ.dmin[(int64_t(seg) * Bs + b) * ED + ec] >= 0.0f);
+#pragma unroll
+    for (int n = 0; n < NP; ++n) lh[n] = __log2f(fabsf(hin[n]));   // -inf for a zero state
+    const bool all_mono = __all_sync(0xffffffffu, mono);
+
+    const int tb = seg * seg_len;
+    const int te = min(L, tb + seg_len);
+    const int n_tiles = (te - tb + kTileT - 1) / kTileT;
+    auto stage = [&](int k, int buf) {
+        const int t0 = tb + k * kTileT;
+        stage_rows<Tin, VEC>(s_d[buf], dlt, b, t0, te, L, e0, ED);
+        stage_rows<float, VEC>(s_y[buf], y, b, t0, te, L, e0, ED);
+        const int rows = max(0, min(kTileT, te - t0));
+        const int64_t base = (b * L + t0) * N;
+        for (int i = tid; i < kTileT * NP; i += kThreads) {
+            const int t = i / NP, n = i % NP;
+            s_c[buf][i] = (t < rows && n < N) ? Cm[base + t * N + n] : Tin(0.0f);
+        }
+    };
+    uint32_t live = 0xFu;    // this warp's groups of four states that can still contribute
+    float cum = 0.0f;
+    stage(0, 0);
+    cp_async_commit();
+    for (int k = 0; k < n_tiles; ++k) {
+        const int buf = k & 1;
+        if (k + 1 < n_tiles) stage(k + 1, buf ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const int t0 = tb + k * kTileT;
+        const int tl = min(kTileT, te - t0);
+#pragma unroll 2
+        for (int t = 0; t < kTileT; ++t) {
+            cum += to_f32(s_d[buf][t * 128 + tid]);
+            float acc = 0.0f;
+            uint32_t alive = 0;
+#pragma unroll
+            for (int gi = 0; gi < NP / 4; ++gi) {
+                if (live & (1u << gi)) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int n = 4 * gi + j;
+                        const float z = fmaf(A2[n], cum, lh[n]);
+                        const float v = copysignf(ex2(z), hin[n]);
+                        acc = fmaf(to_f32(s_c[buf][t * NP + n]), v, acc);
+                        alive |= (z >= -126.0f ? 1u : 0u) << gi;
+                    }
+                }
+            }
+            if (e_ok && t < tl) y[(b * L + t0 + t) * ED + e] = s_y[buf][t * 128 + tid] + acc;
+            if (all_mono && (t & 7) == 7) {
+#pragma unroll
+                for (int gi = 0; gi < NP / 4; ++gi)
+                    if ((live & (1u << gi)) && !__any_sync(0xffffffffu, (alive >> gi) & 1u))
+                        live &= ~(1u << gi);
+            }
+        }
+        if (!__syncthreads_or(live != 0)) break;   // every warp's carried state has decayed to zero
     }
     cp_async_wait<0>();
 }
 
-template <typename Tin, int S, int G, bool VEC>
+template <typename Tin, int S, int G, bool VEC, bool SPLIT>
 static cudaError_t launch_one(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm,
                               const Tin *Cm, const float *D, float *y, int64_t Bs, int L, int ED,
-                              int N, cudaStream_t stream) {
+                              int N, int K, int seg_len, SegSummary summ, cudaStream_t stream) {
     using Sh = Shape<Tin, S, G>;
     const int n_etiles = (ED + Sh::ET - 1) / Sh::ET;
     const int64_t grid = Bs * n_etiles;
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    auto kern = diag_scan_kernel<Tin, S, G, VEC>;
+    auto kern = diag_scan_kernel<Tin, S, G, VEC, SPLIT>;
     const int smem = int(Sh::smem_bytes);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err != cudaSuccess) return err;
     }
-    kern<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(x, dlt, A, Bm, Cm, D, y, L, ED, N,
-                                                                n_etiles);
+    kern<<<dim3(unsigned(grid), unsigned(K)), dim3(kThreads), smem, stream>>>(
+        x, dlt, A, Bm, Cm, D, y, L, ED, N, n_etiles, seg_len, summ);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess || !SPLIT) return err;
+    const dim3 fgrid(unsigned((ED + kThreads - 1) / kThreads), unsigned(Bs), unsigned(K - 1));
+    const bool yvec = (reinterpret_cast<uintptr_t>(y) % 16 == 0) && (ED % 4 == 0);
+    const int fsmem = 2 * kTileT * 128 * (4 + int(sizeof(Tin))) + 2 * kTileT * 16 * int(sizeof(Tin));
+    auto fk = (VEC && yvec) ? diag_fixup_kernel<Tin, true> : diag_fixup_kernel<Tin, false>;
+    err = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, fsmem);
+    if (err != cudaSuccess) return err;
+    fk<<<fgrid, dim3(kThreads), fsmem, stream>>>(dlt, A, Cm, y, int(Bs), L, ED, N, seg_len, summ);
     return cudaGetLastError();
 }
 
-template <typename Tin, bool VEC>
+template <typename Tin, bool VEC, bool SPLIT>
 static cudaError_t dispatch_sg(int S, int G, const Tin *x, const Tin *dlt, const float *A,
                                const Tin *Bm, const Tin *Cm, const float *D, float *y, int64_t Bs,
-                               int L, int ED, int N, cudaStream_t st) {
+                               int L, int ED, int N, int K, int seg_len, SegSummary summ,
+                               cudaStream_t st) {
 #define SSM_DIAG_CASE(s_, g_)                                                                    \
     if (S == s_ && G == g_)                                                                      \
-        return launch_one<Tin, s_, g_, VEC>(x, dlt, A, Bm, Cm, D, y, Bs, L, ED, N, st);
+        return launch_one<Tin, s_, g_, VEC, SPLIT>(x, dlt, A, Bm, Cm, D, y, Bs, L, ED, N, K,      \
+                                                   seg_len, summ, st);
     SSM_DIAG_CASE(16, 1)
     SSM_DIAG_CASE(8, 2)
     SSM_DIAG_CASE(4, 4)
-    SSM_DIAG_CASE(16, 2)
-    SSM_DIAG_CASE(8, 4)
-    SSM_DIAG_CASE(16, 4)
+    if constexpr (!SPLIT) {
+        SSM_DIAG_CASE(16, 2)
+        SSM_DIAG_CASE(8, 4)
+        SSM_DIAG_CASE(16, 4)
+    }
 #undef SSM_DIAG_CASE
     return cudaErrorInvalidValue;
 }
 
-// Pick states-per-thread S and lanes-per-channel G.  More lanes per channel
-// give more warps (needed to fill 152 SMs x 4 schedulers when Bs*ED is
-// small) at the price of a shuffle reduction and less reuse of each
-// channel's x/delta/B/C loads per lane.
-static void choose_split(int64_t channels, int N, int num_sms, int *S, int *G) {
+// Work decomposition.  A warp owns 32/G channels for a time segment; the
+// 152 x 4 schedulers must all get (nearly) the same number of warps.  More
+// lanes per channel (G) or more time segments (K) add warps; G costs a
+// shuffle reduction and less reuse of each step's loads, K costs a second
+// pass over the first steps of each later segment (usually short: it stops
+// once the carried state has decayed to zero).  The estimate below is in
+// issue slots per scheduler.
+struct Plan {
+    int S, G, K, seg_len;
+};
+
+static Plan choose_plan(int64_t Bs, int64_t L, int64_t ED, int N, int num_sms, int max_ctas_per_sm) {
     const int NP = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
-    const int64_t want_warps = int64_t(num_sms) * 4 * 4;  // ~4 warps per scheduler
-    int s = 16;
-    for (;;) {
-        const int64_t warps = (channels * (NP / s) + 31) / 32;
-        if (warps >= want_warps || s == 4 || NP / (s / 2) > 4) break;
-        s /= 2;
+    Plan best{16, NP / 16, 1, int(L)};
+    double best_cost = 1e300;
+    for (int s = 16; s >= 4; s /= 2) {
+        const int g = NP / s;
+        if (g > 4) continue;
+        const int et = kThreads / g;
+        const double per_step = 3.0 * s + (s == 16 ? 18.0 : s == 8 ? 15.0 : 13.0);  // issue / lane-step
+        for (int k = 1; k <= 8; ++k) {
+            if (k > 1 && NP != 16) break;
+            int64_t seg = (L + k - 1) / k;
+            seg = (seg + kTileT - 1) / kTileT * kTileT;
+            const int kk = int((L + seg - 1) / seg);
+            if (kk != k) continue;
+            if (k > 1 && seg < 128) break;
+            const int64_t ctas = (ED + et - 1) / et * Bs * kk;
+            const int64_t per_sm = (ctas + num_sms - 1) / num_sms;   // CTAs on the busiest SM
+            if (per_sm > max_ctas_per_sm) continue;                  // would need a second wave
+            // one warp of each CTA per scheduler; latency hiding improves with warps
+            const double eff = per_sm >= 3 ? 0.95 : per_sm == 2 ? 0.85 : 0.6;
+            double cost = double(per_sm) * double(seg) * per_step / eff;
+            if (kk > 1) {
+                // later segments redo ~min(seg, 96) steps of MUFU-bound work
+                const int64_t fctas = (ED + kThreads - 1) / kThreads * Bs * (kk - 1);
+                const int64_t fper_sm = (fctas + num_sms - 1) / num_sms;
+                cost += double(fper_sm) * double(std::min<int64_t>(seg, 96)) * 16.0 * 4.0 / 4.0;
+            }
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = Plan{s, g, kk, int(seg)};
+            }
+        }
     }
-    *S = s;
-    *G = NP / s;
+    return best;
 }
 
 template <typename Tin>
 cudaError_t launch(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
                    const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
                    int num_sms, cudaStream_t st) {
-    int S, G;
-    choose_split(Bs * ED, int(N), num_sms, &S, &G);
     const int esz = int(sizeof(Tin));
+    const int NP = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
+    // CTAs per SM allowed by shared memory for each split (228 KB per SM,
+    // 1 KB reserved per CTA), capped by the 16-warp-per-scheduler limit.
+    auto ctas_per_sm = [&](int s) {
+        const int g = NP / s, et = kThreads / g;
+        const int smem = (kStages * 2 * kTileT * et + kStages * 2 * kTileT * NP) * esz +
+                         2 * kTileT * NP * 4;
+        return std::min(16, (228 * 1024) / (smem + 1024));
+    };
+    Plan p = choose_plan(Bs, L, ED, int(N), num_sms, ctas_per_sm(16));
+    (void)ctas_per_sm;
     const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(dlt) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(Bm) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(Cm) % 16 == 0) && ((ED * esz) % 16 == 0) &&
                      ((N * esz) % 16 == 0);
+    SegSummary summ{nullptr, nullptr, nullptr};
+    if (p.K == 1) {
+        if (vec)
+            return dispatch_sg<Tin, true, false>(p.S, p.G, x, dlt, A, Bm, Cm, D, y, Bs, int(L),
+                                                 int(ED), int(N), 1, int(L), summ, st);
+        return dispatch_sg<Tin, false, false>(p.S, p.G, x, dlt, A, Bm, Cm, D, y, Bs, int(L),
+                                              int(ED), int(N), 1, int(L), summ, st);
+    }
+    // Per-segment summaries: stream-ordered scratch, released after the
+    // second pass is enqueued.
+    const size_t nsum = size_t(p.K) * size_t(Bs) * size_t(ED);
+    void *scratch = nullptr;
+    cudaError_t err = cudaMallocAsync(&scratch, nsum * (16 + 2) * sizeof(float), st);
+    if (err != cudaSuccess) return err;
+    summ.h_end = static_cast<float *>(scratch);
+    summ.dsum = summ.h_end + nsum * 16;
+    summ.dmin = summ.dsum + nsum;
     if (vec)
-        return dispatch_sg<Tin, true>(S, G, x, dlt, A, Bm, Cm, D, y, Bs, int(L), int(ED), int(N), st);
-    return dispatch_sg<Tin, false>(S, G, x, dlt, A, Bm, Cm, D, y, Bs, int(L), int(ED), int(N), st);
+        err = dispatch_sg<Tin, true, true>(p.S, p.G, x, dlt, A, Bm, Cm, D, y, Bs, int(L), int(ED),
+                                           int(N), p.K, p.seg_len, summ, st);
+    else
+        err = dispatch_sg<Tin, false, true>(p.S, p.G, x, dlt, A, Bm, Cm, D, y, Bs, int(L),
+                                            int(ED), int(N), p.K, p.seg_len, summ, st);
+    cudaError_t e2 = cudaFreeAsync(scratch, st);
+    return err != cudaSuccess ? err : e2;
 }
 
 template cudaError_t launch<float>(const float *, const float *, const float *, const float *,

@@ -62,7 +62,7 @@ template <int NB>  // NB = N / 64
 struct __align__(1024) Smem {
     uint8_t C[NB][kTile];       // C tile, K-major: row t, 64 n per region (128B swizzle)
     uint8_t B[2][kTile];        // B tile, rows s; region 1 stays zero when N = 64
-    uint8_t X[kTile];           // x tile, rows s, 64 p (MN-major B operand)
+    uint8_t X[2][kTile];        // x tiles (double buffered), rows s, 64 p (MN-major B operand)
     uint8_t Xw[kTile];          // weighted x rows
     uint8_t M[2][kTile];        // masked G, K-major: row t, s in two 64-wide regions
     uint8_t S[NB][kStateRegion];  // forward entering state (bf16), K-major: row p, n
@@ -70,9 +70,13 @@ struct __align__(1024) Smem {
     float cum[kQ];
     float excl[kQ];
     float dtv[kQ];
+    float csf[kQ];              // column factors of the forward decay mask
+    float csr[kQ];              // column factors of the reverse decay mask
     float wsum[kThreads / 32];
-    uint64_t bar_tma;
-    uint64_t bar_mma;
+    uint64_t bar_x[2];          // x tile landed (one per buffer)
+    uint64_t bar_c;             // C tile (and the reverse entering state) landed
+    uint64_t bar_b;             // B tile landed
+    uint64_t bar_mma;           // tensor-core group finished
     uint32_t tmem_base;
 };
 
@@ -153,6 +157,18 @@ __device__ __forceinline__ void store_state_bf16(uint8_t (*img)[kStateRegion], i
     }
 }
 
+// Waits of the CTA: every thread polls the mbarrier (bounded in time), and
+// the CTA agrees on the outcome so that all threads leave together.
+#define SSM_CTA_WAIT(bar, ph)                                                             \
+    do {                                                                                  \
+        ok = mbar_wait_bounded(&(bar), (ph), &abort_flag, kWaitLimitNs);                  \
+        (ph) ^= 1u;                                                                       \
+        if (__syncthreads_or(!ok)) {                                                      \
+            ok = false;                                                                   \
+            goto done;                                                                    \
+        }                                                                                 \
+    } while (0)
+
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
@@ -169,13 +185,19 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     const int b = bh / prm.H;
     const int h = bh % prm.H;
     const int L = prm.L;
+    const int nc = prm.nc;
+    const bool bidir = prm.bidir != 0;
     const float Ah = prm.A[h] * SSM_LOG2E;        // decays are exp2 of log2e-scaled sums
     const float Dh = prm.D ? prm.D[h] : 0.0f;
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    const size_t rstride = size_t(NB) * kStateRegion;
 
     if (tid == 0) {
         abort_flag = 0;
-        mbar_init(&sm.bar_tma, 1);
+        mbar_init(&sm.bar_x[0], 1);
+        mbar_init(&sm.bar_x[1], 1);
+        mbar_init(&sm.bar_c, 1);
+        mbar_init(&sm.bar_b, 1);
         mbar_init(&sm.bar_mma, 1);
         mbar_fence_init();
         prefetch_tmap(&tmC);
@@ -196,10 +218,10 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
-    uint32_t ph_tma = 0, ph_mma = 0;
+    uint32_t ph_x[2] = {0, 0}, ph_c = 0, ph_b = 0, ph_mma = 0;
     bool ok = true;
 
-    const uint32_t sC = smem_addr(sm.C), sB = smem_addr(sm.B), sX = smem_addr(sm.X);
+    const uint32_t sC = smem_addr(sm.C), sB = smem_addr(sm.B);
     const uint32_t sXw = smem_addr(sm.Xw), sM = smem_addr(sm.M), sS = smem_addr(sm.S);
     const uint32_t sR = smem_addr(sm.R);
     constexpr uint32_t idG = idesc_bf16_f32(128, 128, false, false);
@@ -207,10 +229,31 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     constexpr uint32_t idY = idesc_bf16_f32(128, 64, false, true);
     constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);
 
-    // Per-tile cumulative sums of dt * A (log2 units); fills sm.cum/excl/dtv.
-    auto tile_cumsum = [&](int c0, float *tot_out) {
-        const int row = c0 + tid;
-        const float dv = row < L ? __bfloat162float(prm.dt[(int64_t(b) * L + row) * prm.H + h]) : 0.0f;
+    // ---- copies issued by thread 0 -------------------------------------------------
+    auto load_x = [&](int c, int buf) {
+        mbar_arrive_expect_tx(&sm.bar_x[buf], kTile);
+        tma_load_4d(sm.X[buf], &tmX, &sm.bar_x[buf], 0, h, c * kQ, b);
+    };
+    auto load_b = [&](int c) {
+        mbar_arrive_expect_tx(&sm.bar_b, NB * kTile);
+#pragma unroll
+        for (int r = 0; r < NB; ++r) tma_load_3d(sm.B[r], &tmB, &sm.bar_b, r * 64, c * kQ, b);
+    };
+    auto load_c = [&](int c, bool with_r) {
+        mbar_arrive_expect_tx(&sm.bar_c, NB * kTile + (with_r ? uint32_t(rstride) : 0u));
+#pragma unroll
+        for (int r = 0; r < NB; ++r) tma_load_3d(sm.C[r], &tmC, &sm.bar_c, r * 64, c * kQ, b);
+        if (with_r)
+            bulk_load(sm.R, prm.rstate + (size_t(bh) * nc + c) * rstride, uint32_t(rstride),
+                      &sm.bar_c);
+    };
+    auto load_dt = [&](int c) {
+        const int row = c * kQ + tid;
+        return row < L ? __bfloat162float(prm.dt[(int64_t(b) * L + row) * prm.H + h]) : 0.0f;
+    };
+    // Per-tile cumulative sums of dt * A (log2 units) and the column factors
+    // of the decay masks.  Rows past L have dt = 0 (no decay, no input).
+    auto tile_prep = [&](float dv, float *tot_out) {
         const float dA = dv * Ah;
         float tot;
         const float cum = cta_inclusive_scan(dA, sm.wsum, &tot);
@@ -219,7 +262,6 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         sm.dtv[tid] = dv;
         *tot_out = tot;
     };
-    // Chunk-state MMA: S^T[n, p] = sum_s B[s, n] * Xw[s, p] into TMEM kColS.
     auto issue_state_mma = [&]() {
 #pragma unroll
         for (int kk = 0; kk < kQ / 16; ++kk) {
@@ -230,23 +272,22 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     };
 
     float st[kP];   // this thread's state column (n = tid), fp32
-    const int nc = prm.nc;
-    const size_t rstride = size_t(NB) * kStateRegion;
 
     // ---------------- reverse sweep: entering states of the reverse scan -------------
-    if (prm.bidir) {
+    if (bidir) {
 #pragma unroll
         for (int p = 0; p < kP; ++p) st[p] = 0.0f;
-        for (int c = nc - 1; c >= 0 && ok; --c) {
-            const int c0 = c * kQ;
-            if (tid == 0) {
-                mbar_arrive_expect_tx(&sm.bar_tma, NB * kTile + kTile);
-#pragma unroll
-                for (int r = 0; r < NB; ++r) tma_load_3d(sm.B[r], &tmB, &sm.bar_tma, r * 64, c0, b);
-                tma_load_4d(sm.X, &tmX, &sm.bar_tma, 0, h, c0, b);
-            }
+        if (tid == 0) {
+            load_x(nc - 1, (nc - 1) & 1);
+            load_b(nc - 1);
+        }
+        float dv = load_dt(nc - 1);
+        for (int c = nc - 1; c >= 0; --c) {
+            const int xb = c & 1;
+            if (tid == 0 && c >= 1) load_x(c - 1, xb ^ 1);
             float tot;
-            tile_cumsum(c0, &tot);
+            tile_prep(dv, &tot);
+            if (c >= 1) dv = load_dt(c - 1);
             // R_in of this tile (state entering from the right) -> scratch.
             if (c < nc - 1) {
                 if (tid < N) store_state_bf16<NB>(sm.R, tid, st);
@@ -256,23 +297,20 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                 for (int i = tid; i < int(rstride / 16); i += kThreads) dst[i] = src[i];
                 fence_proxy_async_all();
             }
-            ok = mbar_wait_bounded(&sm.bar_tma, ph_tma, &abort_flag, kWaitLimitNs);
-            ph_tma ^= 1;
-            if (__syncthreads_or(!ok)) { ok = false; break; }
-            scale_row(sm.X, sm.Xw, tid, exp2f(sm.excl[tid]) * sm.dtv[tid]);
+            SSM_CTA_WAIT(sm.bar_x[xb], ph_x[xb]);
+            scale_row(sm.X[xb], sm.Xw, tid, ex2(sm.excl[tid]) * sm.dtv[tid]);
             fence_proxy_async_smem();
-            __syncthreads();
+            SSM_CTA_WAIT(sm.bar_b, ph_b);
             if (tid == 0) {
                 tc_fence_after_sync();
                 issue_state_mma();
                 mma_commit(&sm.bar_mma);
             }
-            ok = mbar_wait_bounded(&sm.bar_mma, ph_mma, &abort_flag, kWaitLimitNs);
-            ph_mma ^= 1;
-            if (__syncthreads_or(!ok)) { ok = false; break; }
+            SSM_CTA_WAIT(sm.bar_mma, ph_mma);
             tc_fence_after_sync();
+            if (tid == 0 && c >= 1) load_b(c - 1);
             if (tid < N) {
-                const float e = exp2f(tot);
+                const float e = ex2(tot);
 #pragma unroll
                 for (int q = 0; q < kP / 32; ++q) {
                     float v[32];
@@ -281,6 +319,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                     for (int j = 0; j < 32; ++j) st[q * 32 + j] = fmaf(e, st[q * 32 + j], v[j]);
                 }
             }
+            fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncthreads();
         }
@@ -289,29 +328,35 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     // ---------------- forward sweep with the outputs ----------------------------------
 #pragma unroll
     for (int p = 0; p < kP; ++p) st[p] = 0.0f;
-    for (int c = 0; c < nc && ok; ++c) {
+    if (tid == 0) {
+        load_x(0, 0);
+        load_c(0, bidir && nc > 1);
+        load_b(0);
+        if (nc > 1) load_x(1, 1);
+    }
+    {
+    float dv = load_dt(0);
+    for (int c = 0; c < nc; ++c) {
         const int c0 = c * kQ;
+        const int xb = c & 1;
         const bool has_s = c > 0;
-        const bool has_r = prm.bidir && (c < nc - 1);
-        if (tid == 0) {
-            uint32_t bytes = NB * kTile * 2 + kTile;
-            if (has_r) bytes += uint32_t(rstride);
-            mbar_arrive_expect_tx(&sm.bar_tma, bytes);
-#pragma unroll
-            for (int r = 0; r < NB; ++r) {
-                tma_load_3d(sm.C[r], &tmC, &sm.bar_tma, r * 64, c0, b);
-                tma_load_3d(sm.B[r], &tmB, &sm.bar_tma, r * 64, c0, b);
-            }
-            tma_load_4d(sm.X, &tmX, &sm.bar_tma, 0, h, c0, b);
-            if (has_r)
-                bulk_load(sm.R, prm.rstate + (size_t(bh) * nc + c) * rstride, uint32_t(rstride),
-                          &sm.bar_tma);
-        }
+        const bool has_r = bidir && (c < nc - 1);
         float tot;
-        tile_cumsum(c0, &tot);
-        ok = mbar_wait_bounded(&sm.bar_tma, ph_tma, &abort_flag, kWaitLimitNs);
-        ph_tma ^= 1;
-        if (__syncthreads_or(!ok)) { ok = false; break; }
+        tile_prep(dv, &tot);
+        if (c + 1 < nc) dv = load_dt(c + 1);
+        {
+            // Column factors for the blocks of the mask below (above) the
+            // diagonal: for s in a 32-column block that ends at row r (starts
+            // at row r') and t past that block,
+            //   exp2(cum_t - cum_s)   = exp2(cum_t - cum_r)   * exp2(cum_r - cum_s),
+            //   exp2(excl_s - excl_t) = exp2(excl_s - excl_r') * exp2(excl_r' - excl_t),
+            // and both factors are <= 1.  Diagonal blocks use the direct form.
+            const int s = tid;
+            sm.csf[s] = ex2(sm.cum[s | 31] - sm.cum[s]) * sm.dtv[s];
+            if (bidir) sm.csr[s] = ex2(sm.excl[s] - sm.excl[s & ~31]) * sm.dtv[s];
+        }
+        SSM_CTA_WAIT(sm.bar_c, ph_c);
+        SSM_CTA_WAIT(sm.bar_b, ph_b);
 
         // MMA group 1: G = C B^T, Zf = C S_in^T, Zr = C R_in^T.
         if (tid == 0) {
@@ -330,35 +375,56 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             mma_commit(&sm.bar_mma);
         }
         // Meanwhile: weighted x rows for this tile's forward chunk state.
-        scale_row(sm.X, sm.Xw, tid, exp2f(tot - sm.cum[tid]) * sm.dtv[tid]);
+        SSM_CTA_WAIT(sm.bar_x[xb], ph_x[xb]);
+        scale_row(sm.X[xb], sm.Xw, tid, ex2(tot - sm.cum[tid]) * sm.dtv[tid]);
         fence_proxy_async_smem();
-        ok = mbar_wait_bounded(&sm.bar_mma, ph_mma, &abort_flag, kWaitLimitNs);
-        ph_mma ^= 1;
-        if (__syncthreads_or(!ok)) { ok = false; break; }
+        SSM_CTA_WAIT(sm.bar_mma, ph_mma);
         tc_fence_after_sync();
+        if (tid == 0 && c + 1 < nc) load_c(c + 1, bidir && (c + 1 < nc - 1));
 
         // Decay mask on row t of G -> bf16 M (K-major, swizzled).
         {
             const int t = tid;
+            const int tb = t >> 5;                 // warp-uniform: warp w owns rows 32w..32w+31
             const float cum_t = sm.cum[t], excl_t = sm.excl[t];
 #pragma unroll 1
             for (int sb = 0; sb < kQ / 32; ++sb) {
-                float g[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kColG + sb * 32, g);
                 uint32_t packed[16];
+                const bool need_f = sb <= tb;
+                const bool need_r = bidir && sb >= tb;
+                if (need_f || need_r) {
+                    float g[32];
+                    tmem_ld_32x32b_x32(tmem + lane_base + kColG + sb * 32, g);
+                    float m[32];
+                    if (sb == tb) {
+                        // diagonal block: direct differences of cumulative sums
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    float m2[2];
+                        for (int j = 0; j < 32; ++j) {
+                            const int s = sb * 32 + j;
+                            const float ds = sm.dtv[s];
+                            float w = (s <= t) ? ex2(cum_t - sm.cum[s]) : 0.0f;
+                            if (bidir && s >= t) w += ex2(sm.excl[s] - excl_t);
+                            m[j] = g[j] * (w * ds);
+                        }
+                    } else {
+                        const bool fwd = sb < tb;
+                        const float e = fwd ? ex2(cum_t - sm.cum[sb * 32 + 31])
+                                            : ex2(sm.excl[sb * 32] - excl_t);
+                        const float4 *f4 = reinterpret_cast<const float4 *>((fwd ? sm.csf : sm.csr) + sb * 32);
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int s = sb * 32 + j + u;
-                        const float ds = sm.dtv[s];
-                        float m = 0.0f;
-                        if (s <= t) m = exp2f(cum_t - sm.cum[s]);
-                        if (prm.bidir && s >= t) m += exp2f(sm.excl[s] - excl_t);
-                        m2[u] = g[j + u] * m * ds;
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 f = f4[j4];
+                            m[4 * j4 + 0] = g[4 * j4 + 0] * (e * f.x);
+                            m[4 * j4 + 1] = g[4 * j4 + 1] * (e * f.y);
+                            m[4 * j4 + 2] = g[4 * j4 + 2] * (e * f.z);
+                            m[4 * j4 + 3] = g[4 * j4 + 3] * (e * f.w);
+                        }
                     }
-                    packed[j >> 1] = pack_bf16(m2[0], m2[1]);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) packed[j] = pack_bf16(m[2 * j], m[2 * j + 1]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) packed[j] = 0u;
                 }
                 uint8_t *reg = sm.M[sb >> 1];
 #pragma unroll
@@ -376,6 +442,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         // MMA group 2: Y = M X, S_c^T = B^T Xw.
         if (tid == 0) {
             tc_fence_after_sync();
+            const uint32_t sX = smem_addr(sm.X[xb]);
 #pragma unroll
             for (int kk = 0; kk < kQ / 16; ++kk) {
                 const uint64_t a = smem_desc(sM + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024, kSwizzle128B);
@@ -385,19 +452,18 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             issue_state_mma();
             mma_commit(&sm.bar_mma);
         }
-        ok = mbar_wait_bounded(&sm.bar_mma, ph_mma, &abort_flag, kWaitLimitNs);
-        ph_mma ^= 1;
-        if (__syncthreads_or(!ok)) { ok = false; break; }
+        SSM_CTA_WAIT(sm.bar_mma, ph_mma);
         tc_fence_after_sync();
+        if (tid == 0 && c + 1 < nc) load_b(c + 1);
 
         // Epilogue: row t of y.
         {
             const int t = tid;
             const int row = c0 + t;
-            const float ef = exp2f(sm.cum[t]);
-            const float er = exp2f(tot - sm.excl[t]);
+            const float ef = ex2(sm.cum[t]);
+            const float er = ex2(tot - sm.excl[t]);
             float *yrow = prm.y + ((int64_t(b) * L + row) * prm.H + h) * kP;
-            const uint4 *xs = reinterpret_cast<const uint4 *>(sm.X + t * 128);
+            const uint4 *xs = reinterpret_cast<const uint4 *>(sm.X[xb] + t * 128);
 #pragma unroll 1
             for (int q = 0; q < kP / 32; ++q) {
                 float xr[32];
@@ -430,7 +496,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         }
         // State passing: column n = tid of S_in.
         if (tid < N) {
-            const float e = exp2f(tot);
+            const float e = ex2(tot);
 #pragma unroll
             for (int q = 0; q < kP / 32; ++q) {
                 float v[32];
@@ -443,15 +509,16 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
+        if (tid == 0 && c + 2 < nc) load_x(c + 2, xb);
+    }
     }
 
+done:
     if (!ok && tid == 0) {
         abort_flag = 1;
         atomicOr(&g_device_error, 1u);
-    }
-    // An MMA still in flight after a timeout: give it a bounded chance to land
-    // before the tensor memory is released.
-    if (!ok && tid == 0) {
+        // Copies or an MMA still in flight after a timeout: give them a
+        // bounded chance to land before the tensor memory is released.
         volatile int never = 0;
         (void)mbar_wait_bounded(&sm.bar_mma, ph_mma, &never, 100000000ull);
     }

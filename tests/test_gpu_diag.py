@@ -61,6 +61,35 @@ def test_diag_matches_oracle(cuda_device, dtype, Bs, L, ED, N):
     _check(y, ref, dtype)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("Bs,L,ED,N", [
+    (1, 4000, 256, 16),   # long sequence, few channels: split into time segments
+    (2, 3000, 128, 7),
+    (3, 700, 96, 12),
+    (1, 600, 128, 16),
+])
+def test_time_split_matches_oracle(cuda_device, dtype, Bs, L, ED, N):
+    inp = workloads.diag_inputs(Bs, L, ED, N, dtype, seed=L + ED)
+    ref = oracle.diag_scan(**inp)
+    y = lrs.ssm_scan_fwd(**_to_dev(inp, cuda_device))
+    torch.cuda.synchronize()
+    _check(y, ref, dtype)
+
+
+def test_time_split_without_monotone_decay(cuda_device):
+    # Some delta < 0 and some A > 0: the carried state's contribution can grow
+    # again, so the second pass must not stop early.
+    inp = workloads.diag_inputs(1, 900, 128, 16, "f32", seed=77)
+    g = torch.Generator().manual_seed(1)
+    inp["delta"] = (inp["delta"] - 0.05 * torch.rand(inp["delta"].shape, generator=g)).contiguous()
+    inp["A"] = (0.1 * inp["A"]).contiguous()
+    inp["A"][:, 0] = 0.002
+    ref = oracle.diag_scan(**inp)
+    y = lrs.ssm_scan_fwd(**_to_dev(inp, cuda_device))
+    torch.cuda.synchronize()
+    _check(y, ref, "f32")
+
+
 def test_cumsum_worked_example_on_gpu(cuda_device):
     # a = 1, b = x = [1..8]: the scan is the page's cumsum, exact in fp32.
     x = torch.arange(1, 9, dtype=torch.float32).reshape(1, 8, 1)
