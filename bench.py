@@ -37,6 +37,8 @@ L2_BYTES = 129 * 1024 * 1024
 METRIC = "scan throughput (Bs·L·ED·N element-steps/s) and HBM GB/s vs roofline, 1 GB300"
 UNIT = "element-steps/s"
 FALLBACK_HBM_GBS = 6800.0
+NUM_SMS = 152
+ALU_ELEM_PER_CLK_SM = 32.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -177,10 +179,15 @@ class ClockSampler:
 # The hot path
 # ---------------------------------------------------------------------------
 
-def kernels_per_call(w) -> int:
-    """Kernels one library call launches (the diagonal scan is one kernel;
-    the chunked scan is one kernel per call in either direction mode)."""
-    return 1
+def kernels_per_call(w, lrs) -> int:
+    """Kernels one library call launches: the chunked scan is one kernel; the
+    diagonal scan is one, or two when the library splits the sequence into
+    time segments (segment pass + carry pass)."""
+    if w.kind != "diag":
+        return 1
+    s = w.shape
+    _, _, k = lrs.ssm_scan_fwd_plan(s["Bs"], s["L"], s["ED"], s["N"], w.dtype == "bf16")
+    return 2 if k > 1 else 1
 
 
 def make_step(w, lrs, bufs):
@@ -312,19 +319,36 @@ def run_ours(args, rank, world, local):
     value = units * args.steps * world / (ms / 1e3)
     e2e_value = units * k_e2e * world / (ms_e2e / 1e3) if k_e2e else None
     peaks = load_peaks()
-    per_launch_s = ms / 1e3 / (args.steps * kernels_per_call(w))
-    achieved = w.algorithmic_bytes / per_launch_s / 1e9
-    roofline = {
-        "bound": "hbm",
-        "achieved": round(achieved, 1),
-        "peak": peaks["hbm_gbs"],
-        "unit": "GB/s",
-        "frac": round(achieved / peaks["hbm_gbs"], 4),
-        "traffic": ncu_traffic(w.name, w.kind),
-        "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-        "algorithmic_bytes_per_launch": w.algorithmic_bytes,
-        "launch_us": round(per_launch_s * 1e6, 3),
-    }
+    launches_per_step = kernels_per_call(w, lrs)
+    per_launch_s = ms / 1e3 / args.steps
+    hbm_achieved = w.algorithmic_bytes / per_launch_s / 1e9
+    if w.kind == "diag":
+        # One exp2 on the special-function unit and four fp32 operations per
+        # element-step; both the MUFU (32 ex2 / clk / SM) and the FMA pipe
+        # (128 lanes / clk / SM) allow 32 element-steps / clk / SM.
+        alu_peak = ALU_ELEM_PER_CLK_SM * NUM_SMS * peaks["sm_max_mhz"] * 1e6 / 1e12
+        achieved = w.element_steps / per_launch_s / 1e12
+        roofline = {
+            "bound": "alu", "achieved": round(achieved, 4), "peak": round(alu_peak, 4),
+            "unit": "T element-steps/s", "frac": round(achieved / alu_peak, 4),
+            "traffic": ncu_traffic(w.name, w.kind),
+            "peak_source": "derived: 152 SMs x 32 ex2/clk/SM (MUFU) x sm_max_mhz of "
+                           "MEASURED_PEAKS.json; 1 ex2 + 4 fp32 ops per element-step",
+            "hbm": {"achieved_gbs": round(hbm_achieved, 1), "peak_gbs": peaks["hbm_gbs"],
+                    "frac": round(hbm_achieved / peaks["hbm_gbs"], 4),
+                    "algorithmic_bytes_per_launch": w.algorithmic_bytes},
+            "launch_us": round(per_launch_s * 1e6, 3),
+        }
+    else:
+        roofline = {
+            "bound": "hbm", "achieved": round(hbm_achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(hbm_achieved / peaks["hbm_gbs"], 4),
+            "traffic": ncu_traffic(w.name, w.kind),
+            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+            "algorithmic_bytes_per_launch": w.algorithmic_bytes,
+            "launch_us": round(per_launch_s * 1e6, 3),
+        }
+    achieved = hbm_achieved
     s = w.shape
     config = {"workload": w.name, **{k: v for k, v in s.items()},
               "input_dtype": w.dtype, "state_dtype": "f32", "output_dtype": "f32",
@@ -342,7 +366,7 @@ def run_ours(args, rank, world, local):
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": k_e2e},
-        "gpu_launches": args.steps * kernels_per_call(w),
+        "gpu_launches": args.steps * launches_per_step,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

@@ -94,6 +94,22 @@ SSM_API ssm_status_t ssm_scan_fwd_bf16(const void *x, const void *delta,
                                void *stream);
 
 /*
+ * How ssm_scan_fwd / ssm_scan_fwd_bf16 (input_bf16 != 0) decompose a shape
+ * on the current device: states held per thread, lanes sharing a channel, and
+ * the number of time segments scanned in parallel.  With time_segments > 1 a
+ * call launches two kernels (the segments, then a pass that carries each
+ * segment's entering state into its first outputs) and takes stream-ordered
+ * scratch of time_segments*Bs*ED*18*4 bytes; otherwise one kernel and no
+ * scratch.  Same argument rules as ssm_scan_fwd; output pointers must be
+ * non-NULL.
+ */
+SSM_API ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED,
+                                       int64_t N, int input_bf16,
+                                       int32_t *states_per_thread,
+                                       int32_t *lanes_per_channel,
+                                       int32_t *time_segments);
+
+/*
  * Chunked scalar-decay (SSD) scan, bf16 x / dt / B / C (raw bfloat16
  * storage), fp32 A_head, D, state and y.
  *   x  : (Bs, L, H, P) bf16        dt : (Bs, L, H) bf16

@@ -28,6 +28,7 @@ import os
 from . import _build
 
 __all__ = ["ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssd_chunk_scan_fwd", "ssm_check_device_errors",
+           "ssm_scan_fwd_plan",
            "SsmError", "library", "build", "status_string", "STATUS"]
 
 STATUS = {
@@ -42,6 +43,8 @@ SIGNATURES = {
     "ssm_scan_fwd": ([_VP] * 7 + [_I64] * 4 + [_VP], ctypes.c_int),
     "ssm_scan_fwd_bf16": ([_VP] * 7 + [_I64] * 4 + [_VP], ctypes.c_int),
     "ssd_chunk_scan_fwd": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP], ctypes.c_int),
+    "ssm_scan_fwd_plan": ([_I64] * 4 + [ctypes.c_int] + [ctypes.POINTER(ctypes.c_int32)] * 3,
+                          ctypes.c_int),
     "ssm_check_device_errors": ([_VP], ctypes.c_int),
     "ssm_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "ssm_version": ([], ctypes.c_int),
@@ -176,6 +179,18 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
     if st != 0:
         raise SsmError("ssd_chunk_scan_fwd", st)
     return y
+
+
+def ssm_scan_fwd_plan(Bs: int, L: int, ED: int, N: int, bf16: bool = True):
+    """(states per thread, lanes per channel, time segments) the diagonal scan
+    uses for this shape on the current device; time segments > 1 means two
+    kernel launches per call."""
+    s, g, k = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    st = library().ssm_scan_fwd_plan(Bs, L, ED, N, int(bool(bf16)), ctypes.byref(s),
+                                     ctypes.byref(g), ctypes.byref(k))
+    if st != 0:
+        raise SsmError("ssm_scan_fwd_plan", st)
+    return s.value, g.value, k.value
 
 
 def ssm_check_device_errors(device=None) -> None:

@@ -14,7 +14,11 @@ template <typename Tin>
 cudaError_t launch(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
                    const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
                    int num_sms, cudaStream_t st);
-}
+struct Plan {
+    int S, G, K, seg_len;
+};
+Plan plan_for(int64_t Bs, int64_t L, int64_t ED, int64_t N, int esz, int num_sms);
+}  // namespace diag
 namespace ssd {
 cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
                    const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
@@ -145,6 +149,24 @@ ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt, const float *A_he
                                       static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
                                       bidirectional != 0, dev.num_sms,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED, int64_t N, int input_bf16,
+                               int32_t *states_per_thread, int32_t *lanes_per_channel,
+                               int32_t *time_segments) {
+    if (!states_per_thread || !lanes_per_channel || !time_segments) return SSM_ERR_INVALID_ARG;
+    if (!sizes_ok({Bs, L, ED}) || !sizes_ok({Bs, L, N}) || !sizes_ok({ED, N}))
+        return SSM_ERR_INVALID_ARG;
+    if (N > 64) return SSM_ERR_UNSUPPORTED;
+    if (L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    ssm_status_t s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    const ssm::diag::Plan p = ssm::diag::plan_for(Bs, L, ED, N, input_bf16 ? 2 : 4, dev.num_sms);
+    *states_per_thread = p.S;
+    *lanes_per_channel = p.G;
+    *time_segments = p.K;
+    return SSM_OK;
 }
 
 ssm_status_t ssm_check_device_errors(void *stream) {

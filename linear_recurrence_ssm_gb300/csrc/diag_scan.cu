@@ -116,7 +116,6 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
     using Sh = Shape<Tin, S, G>;
     constexpr int ET = Sh::ET;
     constexpr int NP = Sh::NP;
-    constexpr int S2 = S / 2;
     static_assert(S % 4 == 0, "states per thread must be a multiple of 4");
 
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -138,15 +137,15 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
     const int e = e0 + ch;
     const bool e_ok = e < ED;
 
-    // State pairs and A * log2(e) pairs, so that the per-step arithmetic runs
-    // as packed fp32x2 multiplies / fused multiply-adds.
-    float2 A2[S2], h[S2];
+    // States and A * log2(e) in registers.  The per-step arithmetic is scalar
+    // fp32: on this part a packed fp32x2 multiply-add occupies the FMA pipe
+    // longer than two scalar ones.
+    float A2[S], h[S];
 #pragma unroll
-    for (int j = 0; j < S2; ++j) {
-        const int n = g * S + 2 * j;
-        A2[j].x = (e_ok && n < N) ? A[int64_t(e) * N + n] * SSM_LOG2E : 0.0f;
-        A2[j].y = (e_ok && n + 1 < N) ? A[int64_t(e) * N + n + 1] * SSM_LOG2E : 0.0f;
-        h[j] = make_float2(0.0f, 0.0f);
+    for (int j = 0; j < S; ++j) {
+        const int n = g * S + j;
+        A2[j] = (e_ok && n < N) ? A[int64_t(e) * N + n] * SSM_LOG2E : 0.0f;
+        h[j] = 0.0f;
     }
     const float Dv = (D != nullptr && e_ok) ? D[e] : 0.0f;
     float dsum = 0.0f, dmin = 3.0e38f;
@@ -199,36 +198,21 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
         // may not move shared loads across a store that could alias them.
         float n_dl = to_f32(ds[0]), n_xv = to_f32(xs[0]);
         float4 n_b[S / 4], n_c[S / 4];
-        float2 n_a[S2];   // next step's decays, exp2(delta * A * log2 e)
 #pragma unroll
         for (int q = 0; q < S / 4; ++q) {
             n_b[q] = reinterpret_cast<const float4 *>(bq)[q];
             n_c[q] = reinterpret_cast<const float4 *>(cq)[q];
         }
-        {
-            const float2 dl2 = make_float2(n_dl, n_dl);
-#pragma unroll
-            for (int j = 0; j < S2; ++j) {
-                const float2 z = __fmul2_rn(dl2, A2[j]);
-                n_a[j] = make_float2(ex2(z.x), ex2(z.y));
-            }
-        }
 #pragma unroll 2
         for (int t = 0; t < kTileT; ++t) {
             const float dl = n_dl, xv = n_xv;
-            float4 cb[S / 4], cc[S / 4];
-            float2 a[S2];
+            float bv[S], cv[S];
 #pragma unroll
             for (int q = 0; q < S / 4; ++q) {
-                cb[q] = n_b[q];
-                cc[q] = n_c[q];
+                bv[4 * q] = n_b[q].x; bv[4 * q + 1] = n_b[q].y; bv[4 * q + 2] = n_b[q].z; bv[4 * q + 3] = n_b[q].w;
+                cv[4 * q] = n_c[q].x; cv[4 * q + 1] = n_c[q].y; cv[4 * q + 2] = n_c[q].z; cv[4 * q + 3] = n_c[q].w;
             }
-#pragma unroll
-            for (int j = 0; j < S2; ++j) a[j] = n_a[j];
             if (t + 1 < kTileT) {
-                // Operands and exponentials of step t+1 come first: the
-                // exponentials keep the MUFU pipe busy while this step's
-                // state update waits on them.
                 n_dl = to_f32(ds[(t + 1) * ET]);
                 n_xv = to_f32(xs[(t + 1) * ET]);
 #pragma unroll
@@ -236,30 +220,20 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
                     n_b[q] = reinterpret_cast<const float4 *>(bq + (t + 1) * NP)[q];
                     n_c[q] = reinterpret_cast<const float4 *>(cq + (t + 1) * NP)[q];
                 }
-                const float2 dl2 = make_float2(n_dl, n_dl);
-#pragma unroll
-                for (int j = 0; j < S2; ++j) {
-                    const float2 z = __fmul2_rn(dl2, A2[j]);
-                    n_a[j] = make_float2(ex2(z.x), ex2(z.y));
-                }
             }
             const float dlx = dl * xv;
             if constexpr (SPLIT) {
                 dsum += dl;
                 dmin = (t < tl) ? fminf(dmin, dl) : dmin;
             }
-            const float2 dlx2 = make_float2(dlx, dlx);
-            float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int q = 0; q < S / 4; ++q) {
-                const float2 u0 = __fmul2_rn(dlx2, make_float2(cb[q].x, cb[q].y));
-                const float2 u1 = __fmul2_rn(dlx2, make_float2(cb[q].z, cb[q].w));
-                h[2 * q] = __ffma2_rn(a[2 * q], h[2 * q], u0);
-                h[2 * q + 1] = __ffma2_rn(a[2 * q + 1], h[2 * q + 1], u1);
-                acc0 = __ffma2_rn(make_float2(cc[q].x, cc[q].y), h[2 * q], acc0);
-                acc1 = __ffma2_rn(make_float2(cc[q].z, cc[q].w), h[2 * q + 1], acc1);
+            for (int n = 0; n < S; ++n) {
+                const float a = ex2(dl * A2[n]);
+                h[n] = fmaf(a, h[n], dlx * bv[n]);
+                acc[n & 3] = fmaf(cv[n], h[n], acc[n & 3]);
             }
-            float yv = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+            float yv = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 #pragma unroll
             for (int o = 1; o < G; o <<= 1) yv += __shfl_xor_sync(0xffffffffu, yv, o);
             if (store_ok && t < tl) yp[int64_t(t) * ED] = fmaf(Dv, xv, yv);
@@ -273,11 +247,7 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
         if (e_ok) {
             const int64_t c = (int64_t(seg) * (gridDim.x / n_etiles) + b) * ED + e;
 #pragma unroll
-            for (int j = 0; j < S2; ++j) {
-                const int n = g * S + 2 * j;
-                summ.h_end[c * 16 + n] = h[j].x;
-                summ.h_end[c * 16 + n + 1] = h[j].y;
-            }
+            for (int j = 0; j < S; ++j) summ.h_end[c * 16 + g * S + j] = h[j];
             if (g == 0) {
                 summ.dsum[c] = dsum;
                 summ.dmin[c] = dmin;
@@ -515,22 +485,23 @@ static Plan choose_plan(int64_t Bs, int64_t L, int64_t ED, int N, int num_sms, i
     return best;
 }
 
+// The decomposition used for a shape: (S, G, K) and the segment length.
+Plan plan_for(int64_t Bs, int64_t L, int64_t ED, int64_t N, int esz, int num_sms) {
+    const int NP = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
+    // CTAs per SM allowed by shared memory (228 KB per SM, 1 KB reserved per
+    // CTA) for the 16-states-per-thread split, capped at 16.
+    const int et = kThreads / (NP / 16);
+    const int smem = (kStages * 2 * kTileT * et + kStages * 2 * kTileT * NP) * esz +
+                     2 * kTileT * NP * 4;
+    return choose_plan(Bs, L, ED, int(N), num_sms, std::min(16, (228 * 1024) / (smem + 1024)));
+}
+
 template <typename Tin>
 cudaError_t launch(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
                    const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
                    int num_sms, cudaStream_t st) {
     const int esz = int(sizeof(Tin));
-    const int NP = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
-    // CTAs per SM allowed by shared memory for each split (228 KB per SM,
-    // 1 KB reserved per CTA), capped by the 16-warp-per-scheduler limit.
-    auto ctas_per_sm = [&](int s) {
-        const int g = NP / s, et = kThreads / g;
-        const int smem = (kStages * 2 * kTileT * et + kStages * 2 * kTileT * NP) * esz +
-                         2 * kTileT * NP * 4;
-        return std::min(16, (228 * 1024) / (smem + 1024));
-    };
-    Plan p = choose_plan(Bs, L, ED, int(N), num_sms, ctas_per_sm(16));
-    (void)ctas_per_sm;
+    Plan p = plan_for(Bs, L, ED, N, esz, num_sms);
     const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(dlt) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(Bm) % 16 == 0) &&

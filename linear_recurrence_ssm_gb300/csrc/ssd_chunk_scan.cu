@@ -126,13 +126,15 @@ __device__ __forceinline__ float cta_inclusive_scan(float v, float *wsum, float 
 }
 
 // Scale row s of the x tile by w into the Xw tile.  Both tiles share the
-// same swizzle, and the scale is uniform along the row, so the 16-byte
-// chunks are processed in their physical order.
+// same swizzle and the scale is uniform along the row, so 16-byte chunks are
+// processed in place; thread s starts at chunk (s % 8) so that the 32 rows a
+// warp touches at once fall in different shared-memory banks.
 __device__ __forceinline__ void scale_row(const uint8_t *X, uint8_t *Xw, int s, float w) {
     const uint4 *src = reinterpret_cast<const uint4 *>(X + s * 128);
     uint4 *dst = reinterpret_cast<uint4 *>(Xw + s * 128);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int jj = 0; jj < 8; ++jj) {
+        const int j = jj ^ (s & 7);
         uint4 v = src[j];
         float2 a = unpack_bf16(v.x), b = unpack_bf16(v.y), c = unpack_bf16(v.z), d = unpack_bf16(v.w);
         v.x = pack_bf16(a.x * w, a.y * w);
