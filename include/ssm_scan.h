@@ -137,6 +137,37 @@ SSM_API ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt,
                                 void *stream);
 
 /*
+ * Same computation, arguments and rules as ssd_chunk_scan_fwd, for callers
+ * that cannot allocate device memory -- code running where cudaMalloc and
+ * stream-ordered allocation are unavailable or forbidden (a custom
+ * allocator owns all device memory, or the call sits in a region that must
+ * not touch the memory pool).  It allocates nothing and calls no
+ * allocating routine: the scratch that bidirectional calls need for the
+ * reverse scan's entering states lives in one fixed array inside the
+ * library, SSM_NOALLOC_SCRATCH_BYTES long, which every GPU that loads the
+ * library holds until the process exits.  The pages have no counterpart to
+ * this entry point; it exists for such callers only.
+ *   - Calls needing more than SSM_NOALLOC_SCRATCH_BYTES of scratch, i.e.
+ *     bidirectional with Bs*H*ceil(L/128)*P*N*2 > SSM_NOALLOC_SCRATCH_BYTES,
+ *     return SSM_ERR_UNSUPPORTED and launch nothing.  Unidirectional calls
+ *     need no scratch.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array: calls that overlap on the GPU (on
+ *     different streams, or from different threads) race and give wrong
+ *     results.  The array keeps the last call's contents; no call depends
+ *     on it starting at zero.
+ */
+#define SSM_NOALLOC_SCRATCH_BYTES (16ull << 20)
+SSM_API ssm_status_t ssd_chunk_scan_fwd_noalloc(const void *x, const void *dt,
+                                        const float *A_head, const void *B,
+                                        const void *C, const float *D, float *y,
+                                        int64_t Bs, int64_t L, int64_t H, int64_t P,
+                                        int64_t N, int64_t chunk, int bidirectional,
+                                        void *stream);
+
+/*
  * Synchronise `stream` and report whether a kernel of this library running on
  * the current device gave up a bounded wait (SSM_ERR_DEVICE_TIMEOUT) since
  * the previous check; the record is cleared by the call.  Kernels never hang

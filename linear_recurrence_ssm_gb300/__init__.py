@@ -43,6 +43,7 @@ SIGNATURES = {
     "ssm_scan_fwd": ([_VP] * 7 + [_I64] * 4 + [_VP], ctypes.c_int),
     "ssm_scan_fwd_bf16": ([_VP] * 7 + [_I64] * 4 + [_VP], ctypes.c_int),
     "ssd_chunk_scan_fwd": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP], ctypes.c_int),
+    "ssd_chunk_scan_fwd_noalloc": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP], ctypes.c_int),
     "ssm_scan_fwd_plan": ([_I64] * 4 + [ctypes.c_int] + [ctypes.POINTER(ctypes.c_int32)] * 3,
                           ctypes.c_int),
     "ssm_check_device_errors": ([_VP], ctypes.c_int),

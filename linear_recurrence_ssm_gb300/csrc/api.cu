@@ -25,6 +25,11 @@ cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float 
                    int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N, int64_t chunk,
                    bool bidirectional, int num_sms, cudaStream_t st);
 cudaError_t take_device_error(unsigned int *out);
+size_t noalloc_scratch_needed(int64_t Bs, int64_t L, int64_t H, int64_t N, bool bidirectional);
+cudaError_t launch_noalloc(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
+                           const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D,
+                           float *y, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                           bool bidirectional, cudaStream_t stream);
 }
 }  // namespace ssm
 
@@ -149,6 +154,32 @@ ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt, const float *A_he
                                       static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
                                       bidirectional != 0, dev.num_sms,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+ssm_status_t ssd_chunk_scan_fwd_noalloc(const void *x, const void *dt, const float *A_head,
+                                        const void *B, const void *C, const float *D, float *y,
+                                        int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                                        int64_t chunk, int bidirectional, void *stream) {
+    if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_INVALID_ARG;
+    if (!sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, N}) || chunk < 1) return SSM_ERR_INVALID_ARG;
+    if (P != 64) return SSM_ERR_UNSUPPORTED;
+    if (N != 64 && N != 128) return SSM_ERR_UNSUPPORTED;
+    if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
+    if (L > INT_MAX || H > 65535 || Bs > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    if (ssm::ssd::noalloc_scratch_needed(Bs, L, H, N, bidirectional != 0) > SSM_NOALLOC_SCRATCH_BYTES)
+        return SSM_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+        !aligned(dt, 2) || !aligned(A_head, 4) || (D && !aligned(D, 4)))
+        return SSM_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    ssm_status_t s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    using bf = __nv_bfloat16;
+    return from_cuda(ssm::ssd::launch_noalloc(static_cast<const bf *>(x), static_cast<const bf *>(dt),
+                                              A_head, static_cast<const bf *>(B),
+                                              static_cast<const bf *>(C), D, y, Bs, L, H, P, N,
+                                              bidirectional != 0,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED, int64_t N, int input_bf16,

@@ -57,6 +57,8 @@ constexpr uint32_t kTile = kQ * 128;      // bytes of a 128-row x 128-byte tile 
 constexpr uint32_t kStateRegion = kP * 128;
 
 __device__ unsigned int g_device_error;   // non-zero once a bounded wait ran out
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB, see launch_noalloc
+static_assert(kNoAllocScratchBytes == SSM_NOALLOC_SCRATCH_BYTES, "header and library disagree");
 
 template <int NB>  // NB = N / 64
 struct __align__(1024) Smem {
@@ -566,7 +568,7 @@ template <int NB>
 static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A,
                              const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D,
                              float *y, int64_t Bs, int64_t L, int64_t H, bool bidir,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, uint8_t *fixed_scratch = nullptr) {
     constexpr int N = NB * 64;
     CUtensorMap tmC, tmB, tmX;
     const cuuint64_t dbc[3] = {cuuint64_t(N), cuuint64_t(L), cuuint64_t(Bs)};
@@ -598,7 +600,9 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
     if (err != cudaSuccess) return err;
 
     void *scratch = nullptr;
-    if (bidir && prm.nc > 1) {
+    if (bidir && prm.nc > 1 && fixed_scratch != nullptr) {
+        prm.rstate = fixed_scratch;   // caller-provided region, sized by the caller
+    } else if (bidir && prm.nc > 1) {
         const size_t bytes = size_t(grid) * prm.nc * NB * kStateRegion;
         err = cudaMallocAsync(&scratch, bytes, stream);
         if (err != cudaSuccess) return err;
@@ -625,6 +629,64 @@ cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float 
     if (N == 128)
         return launch_nb<2>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream);
     return cudaErrorNotSupported;
+}
+
+// ---------------------------------------------------------------------------
+// Variant that allocates nothing
+// ---------------------------------------------------------------------------
+// Callers that may not allocate device memory (for instance code running
+// under an allocator that forbids it, or inside a region that must not touch
+// the memory pool) get the reverse scan's entering states in this fixed
+// module-scope array instead of a cudaMallocAsync buffer.  Every GPU that
+// loads the library holds it until the process exits.  All calls share it:
+// two such calls that overlap on the GPU race.  No part of it needs to start
+// at zero -- every slot a call reads was written earlier by the same call.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDev = 64;
+std::once_flag g_na_once[kMaxDev];
+void *g_na_addr[kMaxDev];
+cudaError_t g_na_err[kMaxDev];
+}  // namespace
+
+size_t noalloc_scratch_needed(int64_t Bs, int64_t L, int64_t H, int64_t N, bool bidirectional) {
+    const int64_t nc = (L + kQ - 1) / kQ;
+    if (!bidirectional || nc <= 1) return 0;
+    return size_t(Bs) * size_t(H) * size_t(nc) * size_t(N / 64) * kStateRegion;
+}
+
+// Device address of the array: looked up once per device (with that device
+// current) on the first call, since the host-side symbol is not a device
+// address.
+static cudaError_t noalloc_scratch_address(uint8_t **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::call_once(g_na_once[dev], [dev]() {
+        void *p = nullptr;
+        g_na_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        g_na_addr[dev] = p;
+    });
+    if (g_na_err[dev] != cudaSuccess) return g_na_err[dev];
+    *out = static_cast<uint8_t *>(g_na_addr[dev]);
+    return cudaSuccess;
+}
+
+cudaError_t launch_noalloc(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
+                           const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D,
+                           float *y, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                           bool bidirectional, cudaStream_t stream) {
+    if (P != kP || (N != 64 && N != 128)) return cudaErrorNotSupported;
+    if (noalloc_scratch_needed(Bs, L, H, N, bidirectional) > kNoAllocScratchBytes)
+        return cudaErrorNotSupported;
+    uint8_t *scratch = nullptr;
+    cudaError_t e = noalloc_scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    if (N == 64)
+        return launch_nb<1>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream, scratch);
+    return launch_nb<2>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream, scratch);
 }
 
 // Read and clear the device error word (host side, synchronous).

@@ -88,6 +88,15 @@ def test_ssd_rejects_bad_arguments():
     assert ssd(ptrs) == 3
 
 
+def test_noalloc_rejects_scratch_beyond_its_fixed_size():
+    lib = lrs.library()
+    # bidirectional, Bs*H*ceil(L/128)*P*N*2 = 1 GiB > SSM_NOALLOC_SCRATCH_BYTES: rejected up front
+    assert lib.ssd_chunk_scan_fwd_noalloc(*([P] * 7), 64, 4096, 32, 64, 128, 256, 1, None) == 2
+    ptrs = [P] * 7
+    ptrs[4] = None
+    assert lib.ssd_chunk_scan_fwd_noalloc(*ptrs, 1, 8, 2, 64, 64, 128, 1, None) == 1
+
+
 def test_valid_call_without_device_reports_no_device():
     import torch
     if torch.cuda.is_available():
@@ -95,3 +104,6 @@ def test_valid_call_without_device_reports_no_device():
     assert diag() == 6
     assert ssd() == 6
     assert lrs.library().ssm_check_device_errors(None) == 6
+    # the same large call without the reverse scan needs no scratch: passes the size check
+    assert lrs.library().ssd_chunk_scan_fwd_noalloc(*([P] * 7), 64, 4096, 32, 64, 128, 256, 0,
+                                                    None) == 6
