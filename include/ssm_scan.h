@@ -24,8 +24,9 @@
  *         H_t = exp(dt_t * A_h) * H_{t-1} + dt_t * x_t (outer) B_t   (P x N)
  *         y_t = H_t C_t + D_h * x_t
  *       With bidirectional != 0 the reversed scan (same x, dt, A, B, C, the
- *       time axis walked from the end) is added, and D x once: "the addition
- *       of two separate SSMs, plus D x(t)" on the same page.
+ *       time axis walked from the end) is added, and D x once: the page
+ *       describes Bi-Mamba2 as the sum of two SSMs with shared weights plus
+ *       the skip term.
  *
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller, dense

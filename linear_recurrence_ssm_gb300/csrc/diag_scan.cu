@@ -196,30 +196,30 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
         // Operands of the next step are read from shared memory before this
         // step's result is stored: y is a generic pointer, and the compiler
         // may not move shared loads across a store that could alias them.
-        float n_dl = to_f32(ds[0]), n_xv = to_f32(xs[0]);
-        float4 n_b[S / 4], n_c[S / 4];
+        // Two register sets hold the operands of consecutive steps; the tile
+        // loop is fully unrolled so that they alternate without copies.
+        float o_dl[2], o_xv[2];
+        float4 o_b[2][S / 4], o_c[2][S / 4];
+        auto fetch = [&](int t, int r) {
+            o_dl[r] = to_f32(ds[t * ET]);
+            o_xv[r] = to_f32(xs[t * ET]);
 #pragma unroll
-        for (int q = 0; q < S / 4; ++q) {
-            n_b[q] = reinterpret_cast<const float4 *>(bq)[q];
-            n_c[q] = reinterpret_cast<const float4 *>(cq)[q];
-        }
-#pragma unroll 2
+            for (int q = 0; q < S / 4; ++q) {
+                o_b[r][q] = reinterpret_cast<const float4 *>(bq + t * NP)[q];
+                o_c[r][q] = reinterpret_cast<const float4 *>(cq + t * NP)[q];
+            }
+        };
+        fetch(0, 0);
+#pragma unroll
         for (int t = 0; t < kTileT; ++t) {
-            const float dl = n_dl, xv = n_xv;
+            const int r = t & 1;
+            if (t + 1 < kTileT) fetch(t + 1, r ^ 1);
+            const float dl = o_dl[r], xv = o_xv[r];
             float bv[S], cv[S];
 #pragma unroll
             for (int q = 0; q < S / 4; ++q) {
-                bv[4 * q] = n_b[q].x; bv[4 * q + 1] = n_b[q].y; bv[4 * q + 2] = n_b[q].z; bv[4 * q + 3] = n_b[q].w;
-                cv[4 * q] = n_c[q].x; cv[4 * q + 1] = n_c[q].y; cv[4 * q + 2] = n_c[q].z; cv[4 * q + 3] = n_c[q].w;
-            }
-            if (t + 1 < kTileT) {
-                n_dl = to_f32(ds[(t + 1) * ET]);
-                n_xv = to_f32(xs[(t + 1) * ET]);
-#pragma unroll
-                for (int q = 0; q < S / 4; ++q) {
-                    n_b[q] = reinterpret_cast<const float4 *>(bq + (t + 1) * NP)[q];
-                    n_c[q] = reinterpret_cast<const float4 *>(cq + (t + 1) * NP)[q];
-                }
+                bv[4 * q] = o_b[r][q].x; bv[4 * q + 1] = o_b[r][q].y; bv[4 * q + 2] = o_b[r][q].z; bv[4 * q + 3] = o_b[r][q].w;
+                cv[4 * q] = o_c[r][q].x; cv[4 * q + 1] = o_c[r][q].y; cv[4 * q + 2] = o_c[r][q].z; cv[4 * q + 3] = o_c[r][q].w;
             }
             const float dlx = dl * xv;
             if constexpr (SPLIT) {

@@ -4,16 +4,18 @@
 // Computes, per batch row b and head h (state H_t in R^{P x N}, H_{-1} = 0),
 //     H_t = exp(dt_t A_h) H_{t-1} + dt_t x_t (outer) B_t,   y_t = H_t C_t + D_h x_t
 // and, when bidirectional, adds the same recurrence run from the end of the
-// sequence (shared x, dt, A, B, C), counting D_h x_t once: "the addition of
-// two separate SSMs, plus D x(t)" with shared weights, from "Some questions of
-// Bi-Mamba2 and Hydra" (Bi-Mamba2 issue 1), whose chunked forward pass names
-// the stages used here (dA cumulative sums per direction, chunk states,
-// state passing, chunk-scan output).
+// sequence (shared x, dt, A, B, C), counting D_h x_t once -- the sum of a
+// forward and a backward SSM with shared weights plus the skip term, as the
+// author describes Bi-Mamba2 in "Some questions of Bi-Mamba2 and Hydra"
+// (Bi-Mamba2 issue 1), whose chunked forward pass names the stages used here
+// (dA cumulative sums per direction, chunk states, state passing, chunk-scan
+// output).
 //
 // Chunked form, for a tile of Q = 128 rows with dA_r = dt_r A_h,
 // cum = inclusive prefix sum of dA in the tile, excl = cum - dA, tot = cum
 // at the tile's end (every exponent below is a difference of cumulative sums
-// and is <= 0 when dt A_h <= 0 -- the subtraction-based "stable segsum"):
+// and is <= 0 when dt A_h <= 0: the segment sums are formed by subtracting
+// cumulative sums, the numerically stable way that page discusses):
 //   G     = C B^T                                   (tensor core, Q x Q)
 //   M[t,s]= G[t,s] dt_s (exp(cum_t - cum_s) [s <= t] + exp(excl_s - excl_t) [s >= t, reverse])
 //   Y     = M X                                     (tensor core, Q x P)
@@ -45,7 +47,7 @@ using namespace ssm::tc;
 
 constexpr int kQ = 128;          // tile rows (MMA M)
 constexpr int kP = 64;           // head dimension
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;         // two warpgroups; both cover the 128 tile rows
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0;    // G: 128 columns
 constexpr uint32_t kColY = 128;  // Y: 64 columns
@@ -106,8 +108,10 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t w) {
     return __bfloat1622float2(v);
 }
 
-// Inclusive prefix sum over the CTA's 128 threads; also returns the total.
-__device__ __forceinline__ float cta_inclusive_scan(float v, float *wsum, float *total) {
+// Inclusive prefix sum of one value per tile row.  Both warpgroups hold the
+// same 128 values (thread and thread + 128 share row tid % 128) and compute
+// the same sums; returns the total too.
+__device__ __forceinline__ float tile_inclusive_scan(float v, float *wsum, float *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -116,26 +120,27 @@ __device__ __forceinline__ float cta_inclusive_scan(float v, float *wsum, float 
     }
     if (lane == 31) wsum[warp] = v;
     __syncthreads();
+    const int w0 = warp & ~3, wr = warp & 3;
     float off = 0.0f, tot = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
-        const float s = wsum[w];
-        off += (w < warp) ? s : 0.0f;
+    for (int w = 0; w < 4; ++w) {
+        const float s = wsum[w0 + w];
+        off += (w < wr) ? s : 0.0f;
         tot += s;
     }
     *total = tot;
     return v + off;
 }
 
-// Scale row s of the x tile by w into the Xw tile.  Both tiles share the
-// same swizzle and the scale is uniform along the row, so 16-byte chunks are
-// processed in place; thread s starts at chunk (s % 8) so that the 32 rows a
-// warp touches at once fall in different shared-memory banks.
-__device__ __forceinline__ void scale_row(const uint8_t *X, uint8_t *Xw, int s, float w) {
+// Scale half `half` (four of the eight 16-byte chunks) of row s of the x tile
+// by w into the Xw tile.  Both tiles share the same swizzle and the scale is
+// uniform along the row, so chunks are processed in place; the XOR with
+// s % 8 makes the 32 rows a warp touches at once fall in different banks.
+__device__ __forceinline__ void scale_row(const uint8_t *X, uint8_t *Xw, int s, float w, int half) {
     const uint4 *src = reinterpret_cast<const uint4 *>(X + s * 128);
     uint4 *dst = reinterpret_cast<uint4 *>(Xw + s * 128);
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
+    for (int jj = 4 * half; jj < 4 * half + 4; ++jj) {
         const int j = jj ^ (s & 7);
         uint4 v = src[j];
         float2 a = unpack_bf16(v.x), b = unpack_bf16(v.y), c = unpack_bf16(v.z), d = unpack_bf16(v.w);
@@ -147,17 +152,17 @@ __device__ __forceinline__ void scale_row(const uint8_t *X, uint8_t *Xw, int s, 
     }
 }
 
-// Store a P-vector state column (thread n owns column n) as bf16 into a
-// K-major state image: row p, K index n.
+// Store rows [p0, p0 + 32) of a state column (thread n owns column n) as
+// bf16 into a K-major state image: row p, K index n.
 template <int NB>
-__device__ __forceinline__ void store_state_bf16(uint8_t (*img)[kStateRegion], int n,
-                                                 const float (&s)[kP]) {
+__device__ __forceinline__ void store_state_bf16(uint8_t (*img)[kStateRegion], int n, int p0,
+                                                 const float (&s)[32]) {
     uint8_t *reg = img[n >> 6];
     const int nc = n & 63;
 #pragma unroll
-    for (int p = 0; p < kP; ++p) {
+    for (int p = 0; p < 32; ++p) {
         __nv_bfloat16 v = __float2bfloat16_rn(s[p]);
-        *reinterpret_cast<__nv_bfloat16 *>(reg + swz(p, nc)) = v;
+        *reinterpret_cast<__nv_bfloat16 *>(reg + swz(p0 + p, nc)) = v;
     }
 }
 
@@ -185,6 +190,8 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
+    const int row = tid & (kQ - 1);      // tile row == TMEM lane of this thread
+    const int wg = tid >> 7;             // warpgroup: which half of the columns it handles
     const int bh = blockIdx.x;
     const int b = bh / prm.H;
     const int h = bh % prm.H;
@@ -193,7 +200,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     const bool bidir = prm.bidir != 0;
     const float Ah = prm.A[h] * SSM_LOG2E;        // decays are exp2 of log2e-scaled sums
     const float Dh = prm.D ? prm.D[h] : 0.0f;
-    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const size_t rstride = size_t(NB) * kStateRegion;
 
     if (tid == 0) {
@@ -252,18 +259,20 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                       &sm.bar_c);
     };
     auto load_dt = [&](int c) {
-        const int row = c * kQ + tid;
-        return row < L ? __bfloat162float(prm.dt[(int64_t(b) * L + row) * prm.H + h]) : 0.0f;
+        const int r = c * kQ + row;
+        return r < L ? __bfloat162float(prm.dt[(int64_t(b) * L + r) * prm.H + h]) : 0.0f;
     };
-    // Per-tile cumulative sums of dt * A (log2 units) and the column factors
-    // of the decay masks.  Rows past L have dt = 0 (no decay, no input).
+    // Per-tile cumulative sums of dt * A (log2 units).  Rows past L have
+    // dt = 0 (no decay, no input).
     auto tile_prep = [&](float dv, float *tot_out) {
         const float dA = dv * Ah;
         float tot;
-        const float cum = cta_inclusive_scan(dA, sm.wsum, &tot);
-        sm.cum[tid] = cum;
-        sm.excl[tid] = cum - dA;
-        sm.dtv[tid] = dv;
+        const float cum = tile_inclusive_scan(dA, sm.wsum, &tot);
+        if (wg == 0) {
+            sm.cum[row] = cum;
+            sm.excl[row] = cum - dA;
+            sm.dtv[row] = dv;
+        }
         *tot_out = tot;
     };
     auto issue_state_mma = [&]() {
@@ -274,13 +283,22 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             mma_bf16_ss(tmem + kColS, a, bd, idS, kk > 0);
         }
     };
+    // State update for column n = row, rows p in [32 wg, 32 wg + 32):
+    // st = e * st + S_c^T[n, p] (TMEM lane n, columns kColS + p).
+    auto state_update = [&](float *st, float e) {
+        uint32_t v[32];
+        tmem_ld32_async(tmem + lane_base + kColS + wg * 32, v);
+        tmem_wait_tie(v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st[j] = fmaf(e, st[j], __uint_as_float(v[j]));
+    };
 
-    float st[kP];   // this thread's state column (n = tid), fp32
+    float st[32];   // rows [32 wg, 32 wg + 32) of this thread's state column (n = row), fp32
 
     // ---------------- reverse sweep: entering states of the reverse scan -------------
     if (bidir) {
 #pragma unroll
-        for (int p = 0; p < kP; ++p) st[p] = 0.0f;
+        for (int p = 0; p < 32; ++p) st[p] = 0.0f;
         if (tid == 0) {
             load_x(nc - 1, (nc - 1) & 1);
             load_b(nc - 1);
@@ -294,7 +312,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             if (c >= 1) dv = load_dt(c - 1);
             // R_in of this tile (state entering from the right) -> scratch.
             if (c < nc - 1) {
-                if (tid < N) store_state_bf16<NB>(sm.R, tid, st);
+                if (row < N) store_state_bf16<NB>(sm.R, row, wg * 32, *reinterpret_cast<float(*)[32]>(st));
                 __syncthreads();
                 uint4 *dst = reinterpret_cast<uint4 *>(prm.rstate + (size_t(bh) * nc + c) * rstride);
                 const uint4 *src = reinterpret_cast<const uint4 *>(sm.R);
@@ -302,7 +320,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                 fence_proxy_async_all();
             }
             SSM_CTA_WAIT(sm.bar_x[xb], ph_x[xb]);
-            scale_row(sm.X[xb], sm.Xw, tid, ex2(sm.excl[tid]) * sm.dtv[tid]);
+            scale_row(sm.X[xb], sm.Xw, row, ex2(sm.excl[row]) * sm.dtv[row], wg);
             fence_proxy_async_smem();
             SSM_CTA_WAIT(sm.bar_b, ph_b);
             if (tid == 0) {
@@ -313,16 +331,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             SSM_CTA_WAIT(sm.bar_mma, ph_mma);
             tc_fence_after_sync();
             if (tid == 0 && c >= 1) load_b(c - 1);
-            if (tid < N) {
-                const float e = ex2(tot);
-#pragma unroll
-                for (int q = 0; q < kP / 32; ++q) {
-                    float v[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + kColS + q * 32, v);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) st[q * 32 + j] = fmaf(e, st[q * 32 + j], v[j]);
-                }
-            }
+            if (row < N) state_update(st, ex2(tot));
             fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncthreads();
@@ -331,7 +340,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
 
     // ---------------- forward sweep with the outputs ----------------------------------
 #pragma unroll
-    for (int p = 0; p < kP; ++p) st[p] = 0.0f;
+    for (int p = 0; p < 32; ++p) st[p] = 0.0f;
     if (tid == 0) {
         load_x(0, 0);
         load_c(0, bidir && nc > 1);
@@ -348,14 +357,14 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         float tot;
         tile_prep(dv, &tot);
         if (c + 1 < nc) dv = load_dt(c + 1);
-        {
+        if (wg == 0) {
             // Column factors for the blocks of the mask below (above) the
             // diagonal: for s in a 32-column block that ends at row r (starts
             // at row r') and t past that block,
             //   exp2(cum_t - cum_s)   = exp2(cum_t - cum_r)   * exp2(cum_r - cum_s),
             //   exp2(excl_s - excl_t) = exp2(excl_s - excl_r') * exp2(excl_r' - excl_t),
             // and both factors are <= 1.  Diagonal blocks use the direct form.
-            const int s = tid;
+            const int s = row;
             sm.csf[s] = ex2(sm.cum[s | 31] - sm.cum[s]) * sm.dtv[s];
             if (bidir) sm.csr[s] = ex2(sm.excl[s] - sm.excl[s & ~31]) * sm.dtv[s];
         }
@@ -380,35 +389,43 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         }
         // Meanwhile: weighted x rows for this tile's forward chunk state.
         SSM_CTA_WAIT(sm.bar_x[xb], ph_x[xb]);
-        scale_row(sm.X[xb], sm.Xw, tid, ex2(tot - sm.cum[tid]) * sm.dtv[tid]);
+        scale_row(sm.X[xb], sm.Xw, row, ex2(tot - sm.cum[row]) * sm.dtv[row], wg);
         fence_proxy_async_smem();
         SSM_CTA_WAIT(sm.bar_mma, ph_mma);
         tc_fence_after_sync();
         if (tid == 0 && c + 1 < nc) load_c(c + 1, bidir && (c + 1 < nc - 1));
 
-        // Decay mask on row t of G -> bf16 M (K-major, swizzled).
+        // Decay mask on row t of G -> bf16 M (K-major, swizzled); this
+        // warpgroup handles column blocks 2 wg and 2 wg + 1.
         {
-            const int t = tid;
-            const int tb = t >> 5;                 // warp-uniform: warp w owns rows 32w..32w+31
+            const int t = row;
+            const int tb = t >> 5;                 // warp-uniform: the warp owns rows 32 tb..
             const float cum_t = sm.cum[t], excl_t = sm.excl[t];
-#pragma unroll 1
-            for (int sb = 0; sb < kQ / 32; ++sb) {
+            const int sb0 = 2 * wg;
+            const bool need0 = (sb0 <= tb) || (bidir && sb0 >= tb);
+            const bool need1 = (sb0 + 1 <= tb) || (bidir && sb0 + 1 >= tb);
+            uint32_t gr[2][32];
+            if (need0) tmem_ld32_async(tmem + lane_base + kColG + sb0 * 32, gr[0]);
+            if (need1) tmem_ld32_async(tmem + lane_base + kColG + (sb0 + 1) * 32, gr[1]);
+            if (need0 || need1) {
+                tmem_wait_tie(gr[0]);
+                reg_tie(gr[1]);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int sb = sb0 + i;
+                const bool need = i == 0 ? need0 : need1;
                 uint32_t packed[16];
-                const bool need_f = sb <= tb;
-                const bool need_r = bidir && sb >= tb;
-                if (need_f || need_r) {
-                    float g[32];
-                    tmem_ld_32x32b_x32(tmem + lane_base + kColG + sb * 32, g);
+                if (need) {
                     float m[32];
                     if (sb == tb) {
                         // diagonal block: direct differences of cumulative sums
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const int s = sb * 32 + j;
-                            const float ds = sm.dtv[s];
                             float w = (s <= t) ? ex2(cum_t - sm.cum[s]) : 0.0f;
                             if (bidir && s >= t) w += ex2(sm.excl[s] - excl_t);
-                            m[j] = g[j] * (w * ds);
+                            m[j] = __uint_as_float(gr[i][j]) * (w * sm.dtv[s]);
                         }
                     } else {
                         const bool fwd = sb < tb;
@@ -418,10 +435,10 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
 #pragma unroll
                         for (int j4 = 0; j4 < 8; ++j4) {
                             const float4 f = f4[j4];
-                            m[4 * j4 + 0] = g[4 * j4 + 0] * (e * f.x);
-                            m[4 * j4 + 1] = g[4 * j4 + 1] * (e * f.y);
-                            m[4 * j4 + 2] = g[4 * j4 + 2] * (e * f.z);
-                            m[4 * j4 + 3] = g[4 * j4 + 3] * (e * f.w);
+                            m[4 * j4 + 0] = __uint_as_float(gr[i][4 * j4 + 0]) * (e * f.x);
+                            m[4 * j4 + 1] = __uint_as_float(gr[i][4 * j4 + 1]) * (e * f.y);
+                            m[4 * j4 + 2] = __uint_as_float(gr[i][4 * j4 + 2]) * (e * f.z);
+                            m[4 * j4 + 3] = __uint_as_float(gr[i][4 * j4 + 3]) * (e * f.w);
                         }
                     }
 #pragma unroll
@@ -460,55 +477,49 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         tc_fence_after_sync();
         if (tid == 0 && c + 1 < nc) load_b(c + 1);
 
-        // Epilogue: row t of y.
+        // Epilogue: row t of y, columns p in [32 wg, 32 wg + 32).
         {
-            const int t = tid;
-            const int row = c0 + t;
+            const int t = row;
+            const int grow = c0 + t;
+            const int q = wg;
+            uint32_t yv[32], zf[32], zr[32];
+            tmem_ld32_async(tmem + lane_base + kColY + q * 32, yv);
+            if (has_s) tmem_ld32_async(tmem + lane_base + kColZf + q * 32, zf);
+            if (has_r) tmem_ld32_async(tmem + lane_base + kColZr + q * 32, zr);
             const float ef = ex2(sm.cum[t]);
             const float er = ex2(tot - sm.excl[t]);
-            float *yrow = prm.y + ((int64_t(b) * L + row) * prm.H + h) * kP;
+            float xr[32];
             const uint4 *xs = reinterpret_cast<const uint4 *>(sm.X[xb] + t * 128);
-#pragma unroll 1
-            for (int q = 0; q < kP / 32; ++q) {
-                float xr[32];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 v = xs[(q * 4 + j) ^ (t & 7)];
-                    const float2 a = unpack_bf16(v.x), bb = unpack_bf16(v.y),
-                                 cc = unpack_bf16(v.z), dd = unpack_bf16(v.w);
-                    xr[8 * j + 0] = a.x; xr[8 * j + 1] = a.y; xr[8 * j + 2] = bb.x; xr[8 * j + 3] = bb.y;
-                    xr[8 * j + 4] = cc.x; xr[8 * j + 5] = cc.y; xr[8 * j + 6] = dd.x; xr[8 * j + 7] = dd.y;
-                }
-                float yv[32], zf[32], zr[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kColY + q * 32, yv);
-                if (has_s) tmem_ld_32x32b_x32(tmem + lane_base + kColZf + q * 32, zf);
-                if (has_r) tmem_ld_32x32b_x32(tmem + lane_base + kColZr + q * 32, zr);
+            for (int j = 0; j < 4; ++j) {
+                const uint4 v = xs[(q * 4 + j) ^ (t & 7)];
+                const float2 a = unpack_bf16(v.x), bb = unpack_bf16(v.y),
+                             cc = unpack_bf16(v.z), dd = unpack_bf16(v.w);
+                xr[8 * j + 0] = a.x; xr[8 * j + 1] = a.y; xr[8 * j + 2] = bb.x; xr[8 * j + 3] = bb.y;
+                xr[8 * j + 4] = cc.x; xr[8 * j + 5] = cc.y; xr[8 * j + 6] = dd.x; xr[8 * j + 7] = dd.y;
+            }
+            tmem_wait_tie(yv);
+            reg_tie(zf);
+            reg_tie(zr);
+            float out[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float v = fmaf(Dh, xr[j], yv[j]);
-                    if (has_s) v = fmaf(ef, zf[j], v);
-                    if (has_r) v = fmaf(er, zr[j], v);
-                    yv[j] = v;
-                }
-                if (row < L) {
+            for (int j = 0; j < 32; ++j) {
+                float v = fmaf(Dh, xr[j], __uint_as_float(yv[j]));
+                if (has_s) v = fmaf(ef, __uint_as_float(zf[j]), v);
+                if (has_r) v = fmaf(er, __uint_as_float(zr[j]), v);
+                out[j] = v;
+            }
+            if (grow < L) {
+                float *yrow = prm.y + ((int64_t(b) * L + grow) * prm.H + h) * kP + q * 32;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(yrow + q * 32 + j) =
-                            make_float4(yv[j], yv[j + 1], yv[j + 2], yv[j + 3]);
-                }
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(yrow + j) = make_float4(out[j], out[j + 1], out[j + 2], out[j + 3]);
             }
         }
-        // State passing: column n = tid of S_in.
-        if (tid < N) {
-            const float e = ex2(tot);
-#pragma unroll
-            for (int q = 0; q < kP / 32; ++q) {
-                float v[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kColS + q * 32, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) st[q * 32 + j] = fmaf(e, st[q * 32 + j], v[j]);
-            }
-            store_state_bf16<NB>(sm.S, tid, st);
+        // State passing: column n = row of S_in, rows [32 wg, 32 wg + 32).
+        if (row < N) {
+            state_update(st, ex2(tot));
+            store_state_bf16<NB>(sm.S, row, wg * 32, *reinterpret_cast<float(*)[32]>(st));
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();

@@ -10,9 +10,9 @@ Contents
     The definition: a strictly sequential fp64 recurrence written in plain C
     (``ssm_oracle.c``), following ``selective_scan_seq`` and the shape API of
     "scan output is different between sequential and parallel versions"
-    (mamba.py issue 26), and the bidirectional reading "the addition of two
-    separate SSMs, plus D x(t)" of "Some questions of Bi-Mamba2 and Hydra"
-    (Bi-Mamba2 issue 1).
+    (mamba.py issue 26), and the bidirectional reading of "Some questions of
+    Bi-Mamba2 and Hydra" (Bi-Mamba2 issue 1): a forward and a backward SSM
+    with shared weights, summed, plus D x once.
 ``forms``
     Second and third forms of the same result (Blelloch up-sweep/down-sweep,
     chunkwise with carry, chunked SSD), used only to cross-check the

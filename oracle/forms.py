@@ -18,8 +18,9 @@ scan and a chunkwise form, and state that their results must agree.
   through those two forms.
 * ``ssd_scan_chunked`` -- the chunked scalar-decay (SSD) form: per-chunk
   cumulative sums of dt*A, the masked C B^T intra-chunk product built from
-  differences of cumulative sums (the "stable segsum" of "Some questions of
-  Bi-Mamba2 and Hydra"), per-chunk states, state passing across chunks and
+  differences of cumulative sums (the numerically stable segment sum that
+  "Some questions of Bi-Mamba2 and Hydra" discusses), per-chunk states,
+  state passing across chunks and
   the inter-chunk output; optionally with the reversed direction computed from
   the same chunks (no flipped copy), as that page describes.
 """

@@ -15,8 +15,8 @@
  *   [P2] "Some questions of Bi-Mamba2 and Hydra" (Hprairie/Bi-Mamba2
  *        issue 1): the chunked scalar-decay scan's argument list
  *        (x, dt, A, B, C, chunk_size, D, ...) and the bidirectional
- *        reading "the addition of two separate SSMs, plus D x(t)" with
- *        weights shared between the two scans.
+ *        reading: a forward and a backward SSM that share their weights,
+ *        summed, plus the skip term D x counted once.
  *
  * The recurrence itself is not printed on the pages; the plainest reading
  * that they support (Mamba zero-order-hold discretisation) is used:
