@@ -226,12 +226,19 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
                 dsum += dl;
                 dmin = (t < tl) ? fminf(dmin, dl) : dmin;
             }
+            // Products with the step's delta and delta*x are formed two states
+            // at a time (packed fp32x2 multiply: one issue slot for two), the
+            // state update and the readout as scalar fused multiply-adds.
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const float2 dl2 = make_float2(dl, dl), dlx2 = make_float2(dlx, dlx);
 #pragma unroll
-            for (int n = 0; n < S; ++n) {
-                const float a = ex2(dl * A2[n]);
-                h[n] = fmaf(a, h[n], dlx * bv[n]);
+            for (int n = 0; n < S; n += 2) {
+                const float2 z = __fmul2_rn(dl2, make_float2(A2[n], A2[n + 1]));
+                const float2 u = __fmul2_rn(dlx2, make_float2(bv[n], bv[n + 1]));
+                h[n] = fmaf(ex2(z.x), h[n], u.x);
+                h[n + 1] = fmaf(ex2(z.y), h[n + 1], u.y);
                 acc[n & 3] = fmaf(cv[n], h[n], acc[n & 3]);
+                acc[(n + 1) & 3] = fmaf(cv[n + 1], h[n + 1], acc[(n + 1) & 3]);
             }
             float yv = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 #pragma unroll
@@ -338,11 +345,20 @@ diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
         const int t0 = tb + k * kTileT;
         stage_rows<Tin, VEC>(s_d[buf], dlt, b, t0, te, L, e0, ED);
         stage_rows<float, VEC>(s_y[buf], y, b, t0, te, L, e0, ED);
+        // C rows t0..t0+rows-1: one contiguous block, zero padded to 16 states
         const int rows = max(0, min(kTileT, te - t0));
         const int64_t base = (b * L + t0) * N;
-        for (int i = tid; i < kTileT * NP; i += kThreads) {
-            const int t = i / NP, n = i % NP;
-            s_c[buf][i] = (t < rows && n < N) ? Cm[base + t * N + n] : Tin(0.0f);
+        if (VEC && N == NP) {
+            constexpr int EPC = 16 / sizeof(Tin);
+            for (int i = tid; i < kTileT * NP / EPC; i += kThreads) {
+                const bool ok = i * EPC < rows * NP;
+                cp_async16(&s_c[buf][i * EPC], Cm + (ok ? base + int64_t(i) * EPC : 0), ok ? 16 : 0);
+            }
+        } else {
+            for (int i = tid; i < kTileT * NP; i += kThreads) {
+                const int t = i / NP, n = i % NP;
+                s_c[buf][i] = (t < rows && n < N) ? Cm[base + t * N + n] : Tin(0.0f);
+            }
         }
     };
     uint32_t live = 0xFu;    // this warp's groups of four states that can still contribute

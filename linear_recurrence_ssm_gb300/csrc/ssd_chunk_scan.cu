@@ -181,7 +181,8 @@ __device__ __forceinline__ void store_state_bf16(uint8_t (*img)[kStateRegion], i
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmX, const Params prm) {
+                      const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                      const Params prm) {
     constexpr int N = NB * 64;
     extern __shared__ uint8_t smem_raw[];
     Smem<NB> &sm = *reinterpret_cast<Smem<NB> *>(
@@ -214,6 +215,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         prefetch_tmap(&tmC);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmX);
+        prefetch_tmap(&tmY);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -391,29 +393,33 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         SSM_CTA_WAIT(sm.bar_x[xb], ph_x[xb]);
         scale_row(sm.X[xb], sm.Xw, row, ex2(tot - sm.cum[row]) * sm.dtv[row], wg);
         fence_proxy_async_smem();
+        // The previous tile's output rows staged in the mask buffer must have
+        // been read by their store before the mask pass below overwrites it.
+        if (tid == 0) bulk_wait_read0();
         SSM_CTA_WAIT(sm.bar_mma, ph_mma);
         tc_fence_after_sync();
         if (tid == 0 && c + 1 < nc) load_c(c + 1, bidir && (c + 1 < nc - 1));
 
-        // Decay mask on row t of G -> bf16 M (K-major, swizzled); this
-        // warpgroup handles column blocks 2 wg and 2 wg + 1.
+        // Decay mask on row t of G -> bf16 M (K-major, swizzled).
         {
             const int t = row;
             const int tb = t >> 5;                 // warp-uniform: the warp owns rows 32 tb..
             const float cum_t = sm.cum[t], excl_t = sm.excl[t];
-            const int sb0 = 2 * wg;
-            const bool need0 = (sb0 <= tb) || (bidir && sb0 >= tb);
-            const bool need1 = (sb0 + 1 <= tb) || (bidir && sb0 + 1 >= tb);
+            // Blocks {0, 3} to warpgroup 0 and {1, 2} to warpgroup 1: the causal
+            // (and diagonal) work of every row warp is then split evenly.
+            const int sbs[2] = {wg == 0 ? 0 : 1, wg == 0 ? 3 : 2};
+            const bool need0 = (sbs[0] <= tb) || (bidir && sbs[0] >= tb);
+            const bool need1 = (sbs[1] <= tb) || (bidir && sbs[1] >= tb);
             uint32_t gr[2][32];
-            if (need0) tmem_ld32_async(tmem + lane_base + kColG + sb0 * 32, gr[0]);
-            if (need1) tmem_ld32_async(tmem + lane_base + kColG + (sb0 + 1) * 32, gr[1]);
+            if (need0) tmem_ld32_async(tmem + lane_base + kColG + sbs[0] * 32, gr[0]);
+            if (need1) tmem_ld32_async(tmem + lane_base + kColG + sbs[1] * 32, gr[1]);
             if (need0 || need1) {
                 tmem_wait_tie(gr[0]);
                 reg_tie(gr[1]);
             }
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const int sb = sb0 + i;
+                const int sb = sbs[i];
                 const bool need = i == 0 ? need0 : need1;
                 uint32_t packed[16];
                 if (need) {
@@ -509,12 +515,15 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                 if (has_r) v = fmaf(er, __uint_as_float(zr[j]), v);
                 out[j] = v;
             }
-            if (grow < L) {
-                float *yrow = prm.y + ((int64_t(b) * L + grow) * prm.H + h) * kP + q * 32;
+            // Stage the row in the (now free) mask buffer as a 128-byte-swizzled
+            // [128 rows][32 fp32] tile per warpgroup; one TMA store per tile
+            // writes it out coalesced (rows past L are clipped by the store).
+            uint8_t *ys = sm.M[wg] + t * 128;
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(yrow + j) = make_float4(out[j], out[j + 1], out[j + 2], out[j + 3]);
-            }
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4 *>(ys + ((j ^ (t & 7)) << 4)) =
+                    make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+            (void)grow;
         }
         // State passing: column n = row of S_in, rows [32 wg, 32 wg + 32).
         if (row < N) {
@@ -524,11 +533,17 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
-        if (tid == 0 && c + 2 < nc) load_x(c + 2, xb);
+        if (tid == 0) {
+            tma_store_4d(&tmY, sm.M[0], 0, h, c0, b);
+            tma_store_4d(&tmY, sm.M[1], 32, h, c0, b);
+            bulk_commit();
+            if (c + 2 < nc) load_x(c + 2, xb);
+        }
     }
     }
 
 done:
+    if (tid == 0) bulk_wait0();
     if (!ok && tid == 0) {
         abort_flag = 1;
         atomicOr(&g_device_error, 1u);
@@ -564,11 +579,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 static bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
-                     const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+                     const cuuint64_t *strides_bytes, const cuuint32_t *box,
+                     CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void *>(base),
+    CUresult r = fn(m, dtype, cuuint32_t(rank), const_cast<void *>(base),
                     dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -581,15 +597,18 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
                              float *y, int64_t Bs, int64_t L, int64_t H, bool bidir,
                              cudaStream_t stream, uint8_t *fixed_scratch = nullptr) {
     constexpr int N = NB * 64;
-    CUtensorMap tmC, tmB, tmX;
+    CUtensorMap tmC, tmB, tmX, tmY;
     const cuuint64_t dbc[3] = {cuuint64_t(N), cuuint64_t(L), cuuint64_t(Bs)};
     const cuuint64_t sbc[2] = {cuuint64_t(N) * 2, cuuint64_t(L) * N * 2};
     const cuuint32_t boxbc[3] = {64, kQ, 1};
     const cuuint64_t dx[4] = {cuuint64_t(kP), cuuint64_t(H), cuuint64_t(L), cuuint64_t(Bs)};
     const cuuint64_t sx[3] = {cuuint64_t(kP) * 2, cuuint64_t(H) * kP * 2, cuuint64_t(L) * H * kP * 2};
     const cuuint32_t boxx[4] = {64, 1, kQ, 1};
+    const cuuint64_t sy[3] = {cuuint64_t(kP) * 4, cuuint64_t(H) * kP * 4, cuuint64_t(L) * H * kP * 4};
+    const cuuint32_t boxy[4] = {32, 1, kQ, 1};
     if (!make_map(&tmC, Cm, 3, dbc, sbc, boxbc) || !make_map(&tmB, Bm, 3, dbc, sbc, boxbc) ||
-        !make_map(&tmX, x, 4, dx, sx, boxx))
+        !make_map(&tmX, x, 4, dx, sx, boxx) ||
+        !make_map(&tmY, y, 4, dx, sy, boxy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return cudaErrorInvalidValue;
 
     Params prm;
@@ -619,7 +638,7 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
         if (err != cudaSuccess) return err;
         prm.rstate = static_cast<uint8_t *>(scratch);
     }
-    kern<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tmC, tmB, tmX, prm);
+    kern<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tmC, tmB, tmX, tmY, prm);
     err = cudaGetLastError();
     if (scratch) {
         cudaError_t e2 = cudaFreeAsync(scratch, stream);
