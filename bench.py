@@ -190,6 +190,23 @@ def kernels_per_call(w, lrs) -> int:
     return 2 if k > 1 else 1
 
 
+def max_over_ranks(values, world: int, device):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest
+    rank defines the step time); identity on one rank."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch of the workload (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
 def make_step(w, lrs, bufs):
     s = w.shape
     if w.kind == "diag":
@@ -227,7 +244,7 @@ def run_ours(args, rank, world, local):
 
     # Resident input/output sets; each rank draws its own batch (weak scaling).
     host = workloads.workload_inputs(
-        workloads.Workload(w.name, w.kind, w.dtype, w.shape, seed=w.seed + 1000 * rank))
+        workloads.Workload(w.name, w.kind, w.dtype, w.shape, seed=shard_seed(w.seed, rank)))
     per_set = w.algorithmic_bytes
     nsets = max(3, -(-3 * L2_BYTES // per_set))
     bufs = []
@@ -310,10 +327,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     ms_e2e = f0.elapsed_time(f1) if k_e2e else float("nan")
 
-    if world > 1:
-        t = torch.tensor([ms, ms_e2e], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], world, dev)
 
     units = w.element_steps
     value = units * args.steps * world / (ms / 1e3)

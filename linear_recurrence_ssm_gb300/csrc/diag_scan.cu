@@ -32,7 +32,7 @@ namespace diag {
 
 constexpr int kThreads = 128;
 constexpr int kTileT = 32;   // time steps per shared-memory tile
-constexpr int kStages = 3;   // tiles in flight (cp.async ring)
+constexpr int kStages = 2;   // tiles in flight (cp.async ring): one ahead hides HBM latency
 
 template <typename Tin, int S, int G>
 struct Shape {
@@ -196,24 +196,24 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
         // Operands of the next step are read from shared memory before this
         // step's result is stored: y is a generic pointer, and the compiler
         // may not move shared loads across a store that could alias them.
-        // Two register sets hold the operands of consecutive steps; the tile
-        // loop is fully unrolled so that they alternate without copies.
+        // Two register sets hold the operands of consecutive steps: the next
+        // step's operands are fetched before the current step's arithmetic.
+        // Eight steps per loop iteration: unrolling the whole tile overflows
+        // the instruction cache once several warps share a scheduler.
+        constexpr int kUnroll = 8;
         float o_dl[2], o_xv[2];
         float4 o_b[2][S / 4], o_c[2][S / 4];
         auto fetch = [&](int t, int r) {
-            o_dl[r] = to_f32(ds[t * ET]);
-            o_xv[r] = to_f32(xs[t * ET]);
+            const int tt = min(t, kTileT - 1);   // past the tile's end: a harmless re-read
+            o_dl[r] = to_f32(ds[tt * ET]);
+            o_xv[r] = to_f32(xs[tt * ET]);
 #pragma unroll
             for (int q = 0; q < S / 4; ++q) {
-                o_b[r][q] = reinterpret_cast<const float4 *>(bq + t * NP)[q];
-                o_c[r][q] = reinterpret_cast<const float4 *>(cq + t * NP)[q];
+                o_b[r][q] = reinterpret_cast<const float4 *>(bq + tt * NP)[q];
+                o_c[r][q] = reinterpret_cast<const float4 *>(cq + tt * NP)[q];
             }
         };
-        fetch(0, 0);
-#pragma unroll
-        for (int t = 0; t < kTileT; ++t) {
-            const int r = t & 1;
-            if (t + 1 < kTileT) fetch(t + 1, r ^ 1);
+        auto step = [&](int t, int r) {
             const float dl = o_dl[r], xv = o_xv[r];
             float bv[S], cv[S];
 #pragma unroll
@@ -244,6 +244,17 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
 #pragma unroll
             for (int o = 1; o < G; o <<= 1) yv += __shfl_xor_sync(0xffffffffu, yv, o);
             if (store_ok && t < tl) yp[int64_t(t) * ED] = fmaf(Dv, xv, yv);
+        };
+        fetch(0, 0);
+#pragma unroll 1
+        for (int t = 0; t < kTileT; t += kUnroll) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; u += 2) {
+                fetch(t + u + 1, 1);
+                step(t + u, 0);
+                fetch(t + u + 2, 0);
+                step(t + u + 1, 1);
+            }
         }
     }
     cp_async_wait<0>();
@@ -263,26 +274,26 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
     }
 }
 
-// Copy rows [t0, t0 + kTileT) x channels [e0, e0 + 128) of a (Bs, L, ED)
-// tensor into shared memory [kTileT][128]; rows >= te and channels >= ED
-// are zero filled.  VEC: 16-byte cp.async chunks (caller checked alignment).
-template <typename T, bool VEC>
+// Copy rows [t0, t0 + kTileT) x channels [e0, e0 + CW) of a (Bs, L, ED)
+// tensor into shared memory [kTileT][CW]; rows >= te and channels >= ED are
+// zero filled.  VEC: 16-byte cp.async chunks (caller checked alignment).
+template <typename T, bool VEC, int CW>
 __device__ __forceinline__ void stage_rows(T *dst, const T *__restrict__ src, int64_t b, int t0,
                                            int te, int L, int e0, int ED) {
     constexpr int EPC = 16 / sizeof(T);
     const int rows = max(0, min(kTileT, te - t0));
     if constexpr (VEC) {
-        constexpr int CPR = 128 / EPC;
+        constexpr int CPR = CW / EPC;
         for (int i = threadIdx.x; i < kTileT * CPR; i += kThreads) {
             const int t = i / CPR, c = i % CPR;
             const int e = e0 + c * EPC;
             const bool ok = (t < rows) && (e < ED);
             const int64_t g = ok ? ((b * L + t0 + t) * ED + e) : 0;
-            cp_async16(dst + t * 128 + c * EPC, src + g, ok ? 16 : 0);
+            cp_async16(dst + t * CW + c * EPC, src + g, ok ? 16 : 0);
         }
     } else {
-        for (int i = threadIdx.x; i < kTileT * 128; i += kThreads) {
-            const int t = i / 128, c = i % 128;
+        for (int i = threadIdx.x; i < kTileT * CW; i += kThreads) {
+            const int t = i / CW, c = i % CW;
             const int e = e0 + c;
             const bool ok = (t < rows) && (e < ED);
             dst[i] = ok ? src[(b * L + t0 + t) * ED + e] : T(0.0f);
@@ -290,52 +301,60 @@ __device__ __forceinline__ void stage_rows(T *dst, const T *__restrict__ src, in
     }
 }
 
-// Second pass of a time-split scan (16 padded states, one channel per
-// thread): for every segment k >= 1, fold the summaries of segments 0..k-1
-// into the state entering segment k, h_in, and add its contribution
+// Second pass of a time-split scan (16 padded states): for every segment
+// k >= 1, fold the summaries of segments 0..k-1 into the state entering
+// segment k, h_in, and add its contribution
 //     y_t += sum_n C_t[n] * exp(A[e,n] * (delta_{tb} + ... + delta_t)) * h_in[n]
 // to the segment's outputs, which the first pass computed from a zero state.
-// exp2 flushes results below 2^-126 to zero, so once A*cumsum + log2|h_in|
-// is below -126 for a group of states the group adds exactly zero, and it
-// stays so while delta >= 0 and A <= 0 (checked per segment and channel):
-// such groups are dropped, and the CTA stops when no warp has one left.
-// delta, C and y are staged through shared memory one tile ahead.
+// A CTA covers 32 channels; warp g takes states 4g..4g+3 of all 32 (lane =
+// channel), so the four groups of states run in parallel and a group's warp
+// stops on its own.  exp2 flushes results below 2^-126 to zero, so once
+// A*cumsum + log2|h_in| is below -126 for all of a warp's states they add
+// exactly zero, and stay so while delta >= 0 and A <= 0 (checked per segment
+// and channel): the warp then drops out, and the CTA stops when all have.
+// delta, C and y are staged through shared memory one tile ahead; the four
+// warps' partial sums meet in shared memory.
+constexpr int kFixCh = 32;
 template <typename Tin, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
                   const Tin *__restrict__ Cm, float *__restrict__ y, int Bs, int L, int ED, int N,
                   int seg_len, SegSummary summ) {
     constexpr int NP = 16;
-    extern __shared__ __align__(16) unsigned char fx_smem[];
-    float (*s_y)[kTileT * 128] = reinterpret_cast<float (*)[kTileT * 128]>(fx_smem);
-    Tin (*s_d)[kTileT * 128] = reinterpret_cast<Tin (*)[kTileT * 128]>(fx_smem + 2 * kTileT * 128 * 4);
-    Tin (*s_c)[kTileT * NP] = reinterpret_cast<Tin (*)[kTileT * NP]>(
-        fx_smem + 2 * kTileT * 128 * (4 + sizeof(Tin)));
+    constexpr int CW = kFixCh;
+    __shared__ __align__(16) Tin s_d[2][kTileT * CW];
+    __shared__ __align__(16) float s_y[2][kTileT * CW];
+    __shared__ __align__(16) Tin s_c[2][kTileT * NP];
+    __shared__ __align__(16) float s_part[4][kTileT * CW];
     const int tid = threadIdx.x;
-    const int e0 = blockIdx.x * kThreads;
-    const int e = e0 + tid;
+    const int lane = tid & 31;
+    const int g = tid >> 5;                 // group of states 4g..4g+3
+    const int e0 = blockIdx.x * CW;
+    const int e = e0 + lane;
     const int64_t b = blockIdx.y;
     const int seg = blockIdx.z + 1;
     const bool e_ok = e < ED;
     const int ec = e_ok ? e : ED - 1;    // lanes past ED mirror a valid channel, store nothing
 
-    float A2[NP], hin[NP], lh[NP];
+    float A2[4], hin[4], lh[4];
     bool mono = true;
 #pragma unroll
-    for (int n = 0; n < NP; ++n) {
-        A2[n] = n < N ? A[int64_t(ec) * N + n] * SSM_LOG2E : 0.0f;
-        mono = mono && (A2[n] <= 0.0f);
-        hin[n] = 0.0f;
+    for (int j = 0; j < 4; ++j) {
+        const int n = 4 * g + j;
+        A2[j] = n < N ? A[int64_t(ec) * N + n] * SSM_LOG2E : 0.0f;
+        mono = mono && (A2[j] <= 0.0f);
+        hin[j] = 0.0f;
     }
-    for (int j = 0; j < seg; ++j) {
-        const int64_t c = (int64_t(j) * Bs + b) * ED + ec;
+    for (int k = 0; k < seg; ++k) {
+        const int64_t c = (int64_t(k) * Bs + b) * ED + ec;
         const float d = summ.dsum[c];
 #pragma unroll
-        for (int n = 0; n < NP; ++n) hin[n] = fmaf(ex2(A2[n] * d), hin[n], summ.h_end[c * 16 + n]);
+        for (int j = 0; j < 4; ++j)
+            hin[j] = fmaf(ex2(A2[j] * d), hin[j], summ.h_end[c * 16 + 4 * g + j]);
     }
     mono = mono && (summ.dmin[(int64_t(seg) * Bs + b) * ED + ec] >= 0.0f);
 #pragma unroll
-    for (int n = 0; n < NP; ++n) lh[n] = __log2f(fabsf(hin[n]));   // -inf for a zero state
+    for (int j = 0; j < 4; ++j) lh[j] = __log2f(fabsf(hin[j]));   // -inf for a zero state
     const bool all_mono = __all_sync(0xffffffffu, mono);
 
     const int tb = seg * seg_len;
@@ -343,8 +362,8 @@ diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
     const int n_tiles = (te - tb + kTileT - 1) / kTileT;
     auto stage = [&](int k, int buf) {
         const int t0 = tb + k * kTileT;
-        stage_rows<Tin, VEC>(s_d[buf], dlt, b, t0, te, L, e0, ED);
-        stage_rows<float, VEC>(s_y[buf], y, b, t0, te, L, e0, ED);
+        stage_rows<Tin, VEC, CW>(s_d[buf], dlt, b, t0, te, L, e0, ED);
+        stage_rows<float, VEC, CW>(s_y[buf], y, b, t0, te, L, e0, ED);
         // C rows t0..t0+rows-1: one contiguous block, zero padded to 16 states
         const int rows = max(0, min(kTileT, te - t0));
         const int64_t base = (b * L + t0) * N;
@@ -361,8 +380,8 @@ diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
             }
         }
     };
-    uint32_t live = 0xFu;    // this warp's groups of four states that can still contribute
-    float cum = 0.0f;
+    bool live = true;          // warp-uniform: this warp's states can still contribute
+    float cum_run = 0.0f;
     stage(0, 0);
     cp_async_commit();
     for (int k = 0; k < n_tiles; ++k) {
@@ -373,33 +392,48 @@ diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
         __syncthreads();
         const int t0 = tb + k * kTileT;
         const int tl = min(kTileT, te - t0);
-#pragma unroll 2
-        for (int t = 0; t < kTileT; ++t) {
-            cum += to_f32(s_d[buf][t * 128 + tid]);
-            float acc = 0.0f;
-            uint32_t alive = 0;
+        bool alive = false;
+        // Eight steps at a time: their running delta sums first, so that the
+        // exponentials of the eight steps are independent of each other.
+#pragma unroll 1
+        for (int t8 = 0; t8 < kTileT; t8 += 8) {
+            float cum[8], acc[8];
 #pragma unroll
-            for (int gi = 0; gi < NP / 4; ++gi) {
-                if (live & (1u << gi)) {
+            for (int t = 0; t < 8; ++t) {
+                cum_run += to_f32(s_d[buf][(t8 + t) * CW + lane]);
+                cum[t] = cum_run;
+                acc[t] = 0.0f;
+            }
+            if (live) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int n = 4 * gi + j;
-                        const float z = fmaf(A2[n], cum, lh[n]);
-                        const float v = copysignf(ex2(z), hin[n]);
-                        acc = fmaf(to_f32(s_c[buf][t * NP + n]), v, acc);
-                        alive |= (z >= -126.0f ? 1u : 0u) << gi;
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const float z = fmaf(A2[j], cum[t], lh[j]);
+                        acc[t] = fmaf(to_f32(s_c[buf][(t8 + t) * NP + 4 * g + j]),
+                                      copysignf(ex2(z), hin[j]), acc[t]);
                     }
                 }
             }
-            if (e_ok && t < tl) y[(b * L + t0 + t) * ED + e] = s_y[buf][t * 128 + tid] + acc;
-            if (all_mono && (t & 7) == 7) {
 #pragma unroll
-                for (int gi = 0; gi < NP / 4; ++gi)
-                    if ((live & (1u << gi)) && !__any_sync(0xffffffffu, (alive >> gi) & 1u))
-                        live &= ~(1u << gi);
+            for (int t = 0; t < 8; ++t) s_part[g][(t8 + t) * CW + lane] = acc[t];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) alive |= fmaf(A2[j], cum_run, lh[j]) >= -126.0f;
+        __syncthreads();
+        // y for this tile: thread (g, lane) finishes steps g, g+4, g+8, ...
+        if (e_ok) {
+#pragma unroll
+            for (int i = 0; i < kTileT / 4; ++i) {
+                const int t = g + 4 * i;
+                const int o = t * CW + lane;
+                if (t < tl)
+                    y[(b * L + t0 + t) * ED + e] =
+                        s_y[buf][o] + ((s_part[0][o] + s_part[1][o]) + (s_part[2][o] + s_part[3][o]));
             }
         }
-        if (!__syncthreads_or(live != 0)) break;   // every warp's carried state has decayed to zero
+        if (all_mono && live && !__any_sync(0xffffffffu, alive)) live = false;
+        if (!__syncthreads_or(live)) break;   // every group's carried state has decayed to zero
     }
     cp_async_wait<0>();
 }
@@ -422,13 +456,14 @@ static cudaError_t launch_one(const Tin *x, const Tin *dlt, const float *A, cons
         x, dlt, A, Bm, Cm, D, y, L, ED, N, n_etiles, seg_len, summ);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || !SPLIT) return err;
-    const dim3 fgrid(unsigned((ED + kThreads - 1) / kThreads), unsigned(Bs), unsigned(K - 1));
+    const dim3 fgrid(unsigned((ED + kFixCh - 1) / kFixCh), unsigned(Bs), unsigned(K - 1));
     const bool yvec = (reinterpret_cast<uintptr_t>(y) % 16 == 0) && (ED % 4 == 0);
-    const int fsmem = 2 * kTileT * 128 * (4 + int(sizeof(Tin))) + 2 * kTileT * 16 * int(sizeof(Tin));
-    auto fk = (VEC && yvec) ? diag_fixup_kernel<Tin, true> : diag_fixup_kernel<Tin, false>;
-    err = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize, fsmem);
-    if (err != cudaSuccess) return err;
-    fk<<<fgrid, dim3(kThreads), fsmem, stream>>>(dlt, A, Cm, y, int(Bs), L, ED, N, seg_len, summ);
+    if (VEC && yvec)
+        diag_fixup_kernel<Tin, true><<<fgrid, dim3(kThreads), 0, stream>>>(dlt, A, Cm, y, int(Bs), L,
+                                                                          ED, N, seg_len, summ);
+    else
+        diag_fixup_kernel<Tin, false><<<fgrid, dim3(kThreads), 0, stream>>>(dlt, A, Cm, y, int(Bs), L,
+                                                                           ED, N, seg_len, summ);
     return cudaGetLastError();
 }
 
@@ -453,49 +488,48 @@ static cudaError_t dispatch_sg(int S, int G, const Tin *x, const Tin *dlt, const
     return cudaErrorInvalidValue;
 }
 
-// Work decomposition.  A warp owns 32/G channels for a time segment; the
-// 152 x 4 schedulers must all get (nearly) the same number of warps.  More
-// lanes per channel (G) or more time segments (K) add warps; G costs a
-// shuffle reduction and less reuse of each step's loads, K costs a second
-// pass over the first steps of each later segment (usually short: it stops
-// once the carried state has decayed to zero).  The estimate below is in
-// issue slots per scheduler.
+// Work decomposition.  A warp owns 32/G channels for a time segment and
+// keeps 16/G states per lane.  Measured on GB300: a single warp per
+// scheduler leaves the MUFU / FMA pipes idle most of the time, two or more
+// keep them busy, and the carry pass of a time split costs about a quarter
+// of a segment pass.  So: 16 states per lane (G = 1) and no split when that
+// already gives >= 1.5 warps per scheduler; otherwise the fewest time
+// segments K (each >= 128 steps) that give >= 1.8 warps per scheduler, and
+// fewer states per lane only if even 8 segments are not enough.  A plan that
+// would need a second wave of CTAs is never chosen.
 struct Plan {
     int S, G, K, seg_len;
 };
 
 static Plan choose_plan(int64_t Bs, int64_t L, int64_t ED, int N, int num_sms, int max_ctas_per_sm) {
     const int NP = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
-    Plan best{16, NP / 16, 1, int(L)};
-    double best_cost = 1e300;
-    for (int s = 16; s >= 4; s /= 2) {
+    const double schedulers = 4.0 * num_sms;
+    auto make = [&](int s, int k) {
+        int64_t seg = (L + k - 1) / k;
+        seg = (seg + kTileT - 1) / kTileT * kTileT;
+        return Plan{s, NP / s, int((L + seg - 1) / seg), int(seg)};
+    };
+    auto warps = [&](int s, int k) {
         const int g = NP / s;
-        if (g > 4) continue;
-        const int et = kThreads / g;
-        const double per_step = 3.0 * s + (s == 16 ? 18.0 : s == 8 ? 15.0 : 13.0);  // issue / lane-step
+        return double((Bs * ED * g + 31) / 32) * k;
+    };
+    auto fits = [&](int s, int k) {
+        const int et = kThreads / (NP / s);
+        const int64_t ctas = (ED + et - 1) / et * Bs * k;
+        return (ctas + num_sms - 1) / num_sms <= max_ctas_per_sm;
+    };
+    if (warps(16, 1) >= 1.5 * schedulers || NP != 16) {
+        // enough channels (or more than 16 states: no split): G = NP / 16
+        return make(16, 1);
+    }
+    Plan best = make(16, 1);
+    for (int s = 16; s >= 4; s /= 2) {
         for (int k = 1; k <= 8; ++k) {
-            if (k > 1 && NP != 16) break;
-            int64_t seg = (L + k - 1) / k;
-            seg = (seg + kTileT - 1) / kTileT * kTileT;
-            const int kk = int((L + seg - 1) / seg);
-            if (kk != k) continue;
-            if (k > 1 && seg < 128) break;
-            const int64_t ctas = (ED + et - 1) / et * Bs * kk;
-            const int64_t per_sm = (ctas + num_sms - 1) / num_sms;   // CTAs on the busiest SM
-            if (per_sm > max_ctas_per_sm) continue;                  // would need a second wave
-            // one warp of each CTA per scheduler; latency hiding improves with warps
-            const double eff = per_sm >= 3 ? 0.95 : per_sm == 2 ? 0.85 : 0.6;
-            double cost = double(per_sm) * double(seg) * per_step / eff;
-            if (kk > 1) {
-                // later segments redo ~min(seg, 96) steps of MUFU-bound work
-                const int64_t fctas = (ED + kThreads - 1) / kThreads * Bs * (kk - 1);
-                const int64_t fper_sm = (fctas + num_sms - 1) / num_sms;
-                cost += double(fper_sm) * double(std::min<int64_t>(seg, 96)) * 16.0 * 4.0 / 4.0;
-            }
-            if (cost < best_cost) {
-                best_cost = cost;
-                best = Plan{s, g, kk, int(seg)};
-            }
+            const Plan p = make(s, k);
+            if (p.K != k || (k > 1 && p.seg_len < 128)) break;
+            if (!fits(s, k)) break;
+            best = p;
+            if (warps(s, k) >= 1.8 * schedulers) return best;
         }
     }
     return best;
