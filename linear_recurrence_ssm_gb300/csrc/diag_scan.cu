@@ -306,15 +306,21 @@ __device__ __forceinline__ void stage_rows(T *dst, const T *__restrict__ src, in
 // segment k, h_in, and add its contribution
 //     y_t += sum_n C_t[n] * exp(A[e,n] * (delta_{tb} + ... + delta_t)) * h_in[n]
 // to the segment's outputs, which the first pass computed from a zero state.
-// A CTA covers 32 channels; warp g takes states 4g..4g+3 of all 32 (lane =
-// channel), so the four groups of states run in parallel and a group's warp
-// stops on its own.  exp2 flushes results below 2^-126 to zero, so once
-// A*cumsum + log2|h_in| is below -126 for all of a warp's states they add
-// exactly zero, and stay so while delta >= 0 and A <= 0 (checked per segment
-// and channel): the warp then drops out, and the CTA stops when all have.
-// delta, C and y are staged through shared memory one tile ahead; the four
-// warps' partial sums meet in shared memory.
+// Every (t, n) term is independent once the running delta sums are known, so
+// the work is spread over time: a CTA covers 32 channels (lane = channel) and
+// its warp w takes rows 8w..8w+7 of each 32-step tile.  A term is evaluated
+// as sign(h_in) * exp2(A log2(e) cumsum + log2|h_in|).  exp2 flushes results
+// below 2^-126 to zero, so once that exponent is below -126 for state n in
+// every channel of the CTA, the state adds exactly zero from then on, as long
+// as delta >= 0 and A <= 0 (checked per segment and channel): such states are
+// skipped (the test is uniform over the CTA, so the skip is a uniform
+// branch), and the CTA stops when all are.  delta and C are staged through a
+// ring of kFixRing tiles in shared memory, so several tiles' copies are in
+// flight at once; each output receives its correction with one atomic add
+// (one add per element, so the result does not depend on ordering).
 constexpr int kFixCh = 32;
+constexpr int kFixRing = 4;
+constexpr int kMaxSeg = 8;     // time segments a split may use
 template <typename Tin, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
@@ -322,13 +328,18 @@ diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
                   int seg_len, SegSummary summ) {
     constexpr int NP = 16;
     constexpr int CW = kFixCh;
-    __shared__ __align__(16) Tin s_d[2][kTileT * CW];
-    __shared__ __align__(16) float s_y[2][kTileT * CW];
-    __shared__ __align__(16) Tin s_c[2][kTileT * NP];
-    __shared__ __align__(16) float s_part[4][kTileT * CW];
+    constexpr int RW = kTileT / 4;           // rows of a tile per warp
+    constexpr int R = kFixRing;
+    __shared__ __align__(16) Tin s_d[R][kTileT * CW];
+    __shared__ __align__(16) Tin s_c[R][kTileT * NP];
+    __shared__ __align__(16) float s_cf[kTileT * NP];
+    __shared__ float s_lh[NP][CW];
+    __shared__ unsigned s_sg[NP][CW];
+    __shared__ float s_psum[4][CW];
+    __shared__ unsigned s_live[4];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
-    const int g = tid >> 5;                 // group of states 4g..4g+3
+    const int w = tid >> 5;
     const int e0 = blockIdx.x * CW;
     const int e = e0 + lane;
     const int64_t b = blockIdx.y;
@@ -336,34 +347,13 @@ diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
     const bool e_ok = e < ED;
     const int ec = e_ok ? e : ED - 1;    // lanes past ED mirror a valid channel, store nothing
 
-    float A2[4], hin[4], lh[4];
-    bool mono = true;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int n = 4 * g + j;
-        A2[j] = n < N ? A[int64_t(ec) * N + n] * SSM_LOG2E : 0.0f;
-        mono = mono && (A2[j] <= 0.0f);
-        hin[j] = 0.0f;
-    }
-    for (int k = 0; k < seg; ++k) {
-        const int64_t c = (int64_t(k) * Bs + b) * ED + ec;
-        const float d = summ.dsum[c];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            hin[j] = fmaf(ex2(A2[j] * d), hin[j], summ.h_end[c * 16 + 4 * g + j]);
-    }
-    mono = mono && (summ.dmin[(int64_t(seg) * Bs + b) * ED + ec] >= 0.0f);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) lh[j] = __log2f(fabsf(hin[j]));   // -inf for a zero state
-    const bool all_mono = __all_sync(0xffffffffu, mono);
-
     const int tb = seg * seg_len;
     const int te = min(L, tb + seg_len);
     const int n_tiles = (te - tb + kTileT - 1) / kTileT;
-    auto stage = [&](int k, int buf) {
+    auto stage = [&](int k) {
         const int t0 = tb + k * kTileT;
-        stage_rows<Tin, VEC, CW>(s_d[buf], dlt, b, t0, te, L, e0, ED);
-        stage_rows<float, VEC, CW>(s_y[buf], y, b, t0, te, L, e0, ED);
+        const int slot = k % R;
+        stage_rows<Tin, VEC, CW>(s_d[slot], dlt, b, t0, te, L, e0, ED);
         // C rows t0..t0+rows-1: one contiguous block, zero padded to 16 states
         const int rows = max(0, min(kTileT, te - t0));
         const int64_t base = (b * L + t0) * N;
@@ -371,69 +361,142 @@ diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
             constexpr int EPC = 16 / sizeof(Tin);
             for (int i = tid; i < kTileT * NP / EPC; i += kThreads) {
                 const bool ok = i * EPC < rows * NP;
-                cp_async16(&s_c[buf][i * EPC], Cm + (ok ? base + int64_t(i) * EPC : 0), ok ? 16 : 0);
+                cp_async16(&s_c[slot][i * EPC], Cm + (ok ? base + int64_t(i) * EPC : 0), ok ? 16 : 0);
             }
         } else {
             for (int i = tid; i < kTileT * NP; i += kThreads) {
                 const int t = i / NP, n = i % NP;
-                s_c[buf][i] = (t < rows && n < N) ? Cm[base + t * N + n] : Tin(0.0f);
+                s_c[slot][i] = (t < rows && n < N) ? Cm[base + t * N + n] : Tin(0.0f);
             }
         }
     };
-    bool live = true;          // warp-uniform: this warp's states can still contribute
-    float cum_run = 0.0f;
-    stage(0, 0);
-    cp_async_commit();
-    for (int k = 0; k < n_tiles; ++k) {
-        const int buf = k & 1;
-        if (k + 1 < n_tiles) stage(k + 1, buf ^ 1);
+    // The first tiles' copies go out before the summaries are read.
+#pragma unroll
+    for (int k = 0; k < R - 1; ++k) {
+        if (k < n_tiles) stage(k);
         cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const int t0 = tb + k * kTileT;
-        const int tl = min(kTileT, te - t0);
-        bool alive = false;
-        // Eight steps at a time: their running delta sums first, so that the
-        // exponentials of the eight steps are independent of each other.
-#pragma unroll 1
-        for (int t8 = 0; t8 < kTileT; t8 += 8) {
-            float cum[8], acc[8];
+    }
+
+    // h_in for states 4w..4w+3 of channel `lane`, shared as log2|h_in| and
+    // sign.  All summary loads are issued before the fold uses them.
+    bool mono = summ.dmin[(int64_t(seg) * Bs + b) * ED + ec] >= 0.0f;
+    {
+        float a2[4], hin[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                cum_run += to_f32(s_d[buf][(t8 + t) * CW + lane]);
-                cum[t] = cum_run;
-                acc[t] = 0.0f;
+        for (int j = 0; j < 4; ++j) {
+            const int n = 4 * w + j;
+            a2[j] = n < N ? A[int64_t(ec) * N + n] * SSM_LOG2E : 0.0f;
+        }
+        float ds[kMaxSeg];
+        float4 he[kMaxSeg];
+#pragma unroll
+        for (int k = 0; k < kMaxSeg; ++k) {
+            if (k < seg) {
+                const int64_t c = (int64_t(k) * Bs + b) * ED + ec;
+                ds[k] = summ.dsum[c];
+                he[k] = reinterpret_cast<const float4 *>(summ.h_end + c * 16)[w];
             }
-            if (live) {
+        }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+        for (int k = 0; k < kMaxSeg; ++k) {
+            if (k < seg) {
+                hin[0] = fmaf(ex2(a2[0] * ds[k]), hin[0], he[k].x);
+                hin[1] = fmaf(ex2(a2[1] * ds[k]), hin[1], he[k].y);
+                hin[2] = fmaf(ex2(a2[2] * ds[k]), hin[2], he[k].z);
+                hin[3] = fmaf(ex2(a2[3] * ds[k]), hin[3], he[k].w);
+            }
+        }
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const float z = fmaf(A2[j], cum[t], lh[j]);
-                        acc[t] = fmaf(to_f32(s_c[buf][(t8 + t) * NP + 4 * g + j]),
-                                      copysignf(ex2(z), hin[j]), acc[t]);
-                    }
+        for (int j = 0; j < 4; ++j) {
+            s_lh[4 * w + j][lane] = __log2f(fabsf(hin[j]));   // -inf for a zero state
+            s_sg[4 * w + j][lane] = __float_as_uint(hin[j]) & 0x80000000u;
+        }
+    }
+    float A2[NP], lh[NP];
+    unsigned sg[NP];
+    __syncthreads();
+#pragma unroll
+    for (int n = 0; n < NP; ++n) {
+        A2[n] = n < N ? A[int64_t(ec) * N + n] * SSM_LOG2E : 0.0f;
+        mono = mono && (A2[n] <= 0.0f);
+        lh[n] = s_lh[n][lane];
+        sg[n] = s_sg[n][lane];
+    }
+    const bool all_mono = __syncthreads_and(mono) != 0;
+
+    float cum_run = 0.0f;      // delta summed over the tiles already done (same in every warp)
+    for (int k = 0; k < n_tiles; ++k) {
+        const int slot = k % R;
+        // The slot refilled here was last read in iteration k - 1, before
+        // its closing barrier.
+        if (k + R - 1 < n_tiles) stage(k + R - 1);
+        cp_async_commit();
+        // States that can still contribute from this tile on.
+        unsigned m = 0xffffu;
+        if (all_mono) {
+            m = 0;
+#pragma unroll
+            for (int n = 0; n < NP; ++n)
+                if (fmaf(A2[n], cum_run, lh[n]) >= -126.0f) m |= 1u << n;
+            m = __reduce_or_sync(0xffffffffu, m);
+        }
+        cp_async_wait<R - 1>();
+        float d[RW], psum = 0.0f;
+        __syncthreads();     // tile k landed everywhere
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            d[r] = to_f32(s_d[slot][(RW * w + r) * CW + lane]);
+            psum += d[r];
+        }
+        s_psum[w][lane] = psum;
+        if (lane == 0) s_live[w] = m;
+        for (int i = 4 * tid; i < kTileT * NP; i += 4 * kThreads)
+            reinterpret_cast<float4 *>(s_cf + i)[0] = to_f32x4(&s_c[slot][i]);
+        __syncthreads();
+        const unsigned live = s_live[0] | s_live[1] | s_live[2] | s_live[3];
+        if (live == 0) break;    // every state's carried part has decayed to zero
+        float cum[RW], acc[RW], tile_sum = 0.0f, run = cum_run;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const float p = s_psum[v][lane];
+            tile_sum += p;
+            run += (v < w) ? p : 0.0f;
+        }
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+            run += d[r];
+            cum[r] = run;
+            acc[r] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (!((live >> (4 * j)) & 0xfu)) continue;
+            float4 c4[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) c4[r] = reinterpret_cast<const float4 *>(s_cf + (RW * w + r) * NP)[j];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int n = 4 * j + q;
+                if (!((live >> n) & 1u)) continue;
+#pragma unroll
+                for (int r = 0; r < RW; ++r) {
+                    const float cv = q == 0 ? c4[r].x : q == 1 ? c4[r].y : q == 2 ? c4[r].z : c4[r].w;
+                    const float z = fmaf(A2[n], cum[r], lh[n]);
+                    acc[r] = fmaf(cv, __uint_as_float(__float_as_uint(ex2(z)) ^ sg[n]), acc[r]);
                 }
             }
-#pragma unroll
-            for (int t = 0; t < 8; ++t) s_part[g][(t8 + t) * CW + lane] = acc[t];
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) alive |= fmaf(A2[j], cum_run, lh[j]) >= -126.0f;
-        __syncthreads();
-        // y for this tile: thread (g, lane) finishes steps g, g+4, g+8, ...
+        const int t0 = tb + k * kTileT;
+        const int tl = min(kTileT, te - t0);
         if (e_ok) {
 #pragma unroll
-            for (int i = 0; i < kTileT / 4; ++i) {
-                const int t = g + 4 * i;
-                const int o = t * CW + lane;
-                if (t < tl)
-                    y[(b * L + t0 + t) * ED + e] =
-                        s_y[buf][o] + ((s_part[0][o] + s_part[1][o]) + (s_part[2][o] + s_part[3][o]));
+            for (int r = 0; r < RW; ++r) {
+                const int t = RW * w + r;
+                if (t < tl && acc[r] != 0.0f) atomicAdd(y + (b * L + t0 + t) * ED + e, acc[r]);
             }
         }
-        if (all_mono && live && !__any_sync(0xffffffffu, alive)) live = false;
-        if (!__syncthreads_or(live)) break;   // every group's carried state has decayed to zero
+        cum_run += tile_sum;
+        __syncthreads();     // every read of this tile's slot and of s_cf is done
     }
     cp_async_wait<0>();
 }
@@ -524,7 +587,7 @@ static Plan choose_plan(int64_t Bs, int64_t L, int64_t ED, int N, int num_sms, i
     }
     Plan best = make(16, 1);
     for (int s = 16; s >= 4; s /= 2) {
-        for (int k = 1; k <= 8; ++k) {
+        for (int k = 1; k <= kMaxSeg; ++k) {
             const Plan p = make(s, k);
             if (p.K != k || (k > 1 && p.seg_len < 128)) break;
             if (!fits(s, k)) break;

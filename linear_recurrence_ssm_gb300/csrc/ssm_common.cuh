@@ -15,6 +15,14 @@ namespace ssm {
 // ---- element conversion ---------------------------------------------------
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+// Four consecutive elements (8-byte aligned for bf16, 16-byte for fp32).
+__device__ __forceinline__ float4 to_f32x4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 to_f32x4(const __nv_bfloat16 *p) {
+    // a bf16 is the high half of the fp32 with the same bits
+    const uint2 w = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
 
 // exp2 on the special-function unit (MUFU.EX2); relative error ~2^-22,
 // subnormal results flushed to zero.
