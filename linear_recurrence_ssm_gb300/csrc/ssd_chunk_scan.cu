@@ -65,22 +65,25 @@ static_assert(kNoAllocScratchBytes == SSM_NOALLOC_SCRATCH_BYTES, "header and lib
 template <int NB>  // NB = N / 64
 struct __align__(1024) Smem {
     uint8_t C[NB][kTile];       // C tile, K-major: row t, 64 n per region (128B swizzle)
-    uint8_t B[2][kTile];        // B tile, rows s; region 1 stays zero when N = 64
+    uint8_t B[2][2][kTile];     // B tiles (double buffered), rows s; region 1 stays zero when N = 64
     uint8_t X[2][kTile];        // x tiles (double buffered), rows s, 64 p (MN-major B operand)
     uint8_t Xw[kTile];          // weighted x rows
-    uint8_t M[2][kTile];        // masked G, K-major: row t, s in two 64-wide regions
+    uint8_t M[2][kTile];        // masked G, K-major: row t, s in two 64-wide regions; then y rows
     uint8_t S[NB][kStateRegion];  // forward entering state (bf16), K-major: row p, n
     uint8_t R[NB][kStateRegion];  // reverse entering state (bf16), same layout
-    float cum[kQ];
-    float excl[kQ];
-    float dtv[kQ];
-    float csf[kQ];              // column factors of the forward decay mask
-    float csr[kQ];              // column factors of the reverse decay mask
+    // per-tile vectors, double buffered by tile parity
+    float cum[2][kQ];
+    float excl[2][kQ];
+    float dtv[2][kQ];
+    float csf[2][kQ];           // column factors of the forward decay mask
+    float csr[2][kQ];           // column factors of the reverse decay mask
     float wsum[kThreads / 32];
     uint64_t bar_x[2];          // x tile landed (one per buffer)
     uint64_t bar_c;             // C tile (and the reverse entering state) landed
-    uint64_t bar_b;             // B tile landed
-    uint64_t bar_mma;           // tensor-core group finished
+    uint64_t bar_b[2];          // B tile landed (one per buffer)
+    uint64_t bar_g;             // G, Zf, Zr of a tile finished
+    uint64_t bar_m2;            // Y and S_c of a tile finished
+    uint64_t bar_fin;           // every MMA issued so far finished (error path)
     uint32_t tmem_base;
 };
 
@@ -209,8 +212,11 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         mbar_init(&sm.bar_x[0], 1);
         mbar_init(&sm.bar_x[1], 1);
         mbar_init(&sm.bar_c, 1);
-        mbar_init(&sm.bar_b, 1);
-        mbar_init(&sm.bar_mma, 1);
+        mbar_init(&sm.bar_b[0], 1);
+        mbar_init(&sm.bar_b[1], 1);
+        mbar_init(&sm.bar_g, 1);
+        mbar_init(&sm.bar_m2, 1);
+        mbar_init(&sm.bar_fin, 1);
         mbar_fence_init();
         prefetch_tmap(&tmC);
         prefetch_tmap(&tmB);
@@ -221,20 +227,23 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    // The second B region (n = 64..127) is read as zero rows when N = 64.
+    // The second B region (n = 64..127) of both buffers is read as zero rows
+    // when N = 64.
     if (NB == 1) {
-        uint4 *z = reinterpret_cast<uint4 *>(sm.B[1]);
-        for (int i = tid; i < int(kTile / 16); i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < int(kTile / 16); i += kThreads) {
+            reinterpret_cast<uint4 *>(sm.B[0][1])[i] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4 *>(sm.B[1][1])[i] = make_uint4(0, 0, 0, 0);
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
-    uint32_t ph_x[2] = {0, 0}, ph_c = 0, ph_b = 0, ph_mma = 0;
+    uint32_t ph_x[2] = {0, 0}, ph_c = 0, ph_b[2] = {0, 0}, ph_g = 0, ph_m2 = 0;
     bool ok = true;
 
-    const uint32_t sC = smem_addr(sm.C), sB = smem_addr(sm.B);
+    const uint32_t sC = smem_addr(sm.C);
     const uint32_t sXw = smem_addr(sm.Xw), sM = smem_addr(sm.M), sS = smem_addr(sm.S);
     const uint32_t sR = smem_addr(sm.R);
     constexpr uint32_t idG = idesc_bf16_f32(128, 128, false, false);
@@ -247,10 +256,11 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         mbar_arrive_expect_tx(&sm.bar_x[buf], kTile);
         tma_load_4d(sm.X[buf], &tmX, &sm.bar_x[buf], 0, h, c * kQ, b);
     };
-    auto load_b = [&](int c) {
-        mbar_arrive_expect_tx(&sm.bar_b, NB * kTile);
+    auto load_b = [&](int c, int buf) {
+        mbar_arrive_expect_tx(&sm.bar_b[buf], NB * kTile);
 #pragma unroll
-        for (int r = 0; r < NB; ++r) tma_load_3d(sm.B[r], &tmB, &sm.bar_b, r * 64, c * kQ, b);
+        for (int r = 0; r < NB; ++r)
+            tma_load_3d(sm.B[buf][r], &tmB, &sm.bar_b[buf], r * 64, c * kQ, b);
     };
     auto load_c = [&](int c, bool with_r) {
         mbar_arrive_expect_tx(&sm.bar_c, NB * kTile + (with_r ? uint32_t(rstride) : 0u));
@@ -264,25 +274,62 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         const int r = c * kQ + row;
         return r < L ? __bfloat162float(prm.dt[(int64_t(b) * L + r) * prm.H + h]) : 0.0f;
     };
-    // Per-tile cumulative sums of dt * A (log2 units).  Rows past L have
-    // dt = 0 (no decay, no input).
-    auto tile_prep = [&](float dv, float *tot_out) {
+    // Per-tile cumulative sums of dt * A (log2 units) into the vectors of
+    // parity p, and the column factors of the decay mask.  Rows past L have
+    // dt = 0 (no decay, no input).  Contains a CTA barrier.
+    auto tile_prep = [&](float dv, int p, float *tot_out) {
         const float dA = dv * Ah;
         float tot;
         const float cum = tile_inclusive_scan(dA, sm.wsum, &tot);
         if (wg == 0) {
-            sm.cum[row] = cum;
-            sm.excl[row] = cum - dA;
-            sm.dtv[row] = dv;
+            sm.cum[p][row] = cum;
+            sm.excl[p][row] = cum - dA;
+            sm.dtv[p][row] = dv;
+            __syncwarp();
+            // Column factors for the blocks of the mask below (above) the
+            // diagonal: for s in a 32-column block that ends at row r (starts
+            // at row r') and t past that block,
+            //   exp2(cum_t - cum_s)   = exp2(cum_t - cum_r)   * exp2(cum_r - cum_s),
+            //   exp2(excl_s - excl_t) = exp2(excl_s - excl_r') * exp2(excl_r' - excl_t),
+            // and both factors are <= 1.  Diagonal blocks use the direct form.
+            // (Rows r, r' are in the same warp as s.)
+            const int s = row;
+            sm.csf[p][s] = ex2(sm.cum[p][s | 31] - cum) * dv;
+            if (bidir) sm.csr[p][s] = ex2(cum - dA - sm.excl[p][s & ~31]) * dv;
         }
         *tot_out = tot;
     };
-    auto issue_state_mma = [&]() {
+    // S_c^T = B^T Xw (tensor core, N x P) from B buffer `bb`.
+    auto issue_state_mma = [&](int bb) {
+        const uint32_t sB = smem_addr(sm.B[bb]);
 #pragma unroll
         for (int kk = 0; kk < kQ / 16; ++kk) {
             const uint64_t a = smem_desc(sB + kk * 2048, kTile, 1024, kSwizzle128B);
             const uint64_t bd = smem_desc(sXw + kk * 2048, kTile, 1024, kSwizzle128B);
             mma_bf16_ss(tmem + kColS, a, bd, idS, kk > 0);
+        }
+    };
+    // G = C B^T from B buffer `bb`.
+    auto issue_g = [&](int bb) {
+        const uint32_t sB = smem_addr(sm.B[bb]);
+#pragma unroll
+        for (int kk = 0; kk < N / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;
+            mma_bf16_ss(tmem + kColG, smem_desc(sC + koff, 16, 1024, kSwizzle128B),
+                        smem_desc(sB + koff, 16, 1024, kSwizzle128B), idG, kk > 0);
+        }
+    };
+    // Zf = C S_in^T, Zr = C R_in^T.
+    auto issue_z = [&](bool has_s, bool has_r) {
+#pragma unroll
+        for (int kk = 0; kk < N / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;
+            const uint64_t a = smem_desc(sC + koff, 16, 1024, kSwizzle128B);
+            const uint32_t soff = (kk >> 2) * kStateRegion + (kk & 3) * 32;
+            if (has_s)
+                mma_bf16_ss(tmem + kColZf, a, smem_desc(sS + soff, 16, 1024, kSwizzle128B), idZ, kk > 0);
+            if (has_r)
+                mma_bf16_ss(tmem + kColZr, a, smem_desc(sR + soff, 16, 1024, kSwizzle128B), idZ, kk > 0);
         }
     };
     // State update for column n = row, rows p in [32 wg, 32 wg + 32):
@@ -303,14 +350,14 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         for (int p = 0; p < 32; ++p) st[p] = 0.0f;
         if (tid == 0) {
             load_x(nc - 1, (nc - 1) & 1);
-            load_b(nc - 1);
+            load_b(nc - 1, 0);
         }
         float dv = load_dt(nc - 1);
         for (int c = nc - 1; c >= 0; --c) {
             const int xb = c & 1;
             if (tid == 0 && c >= 1) load_x(c - 1, xb ^ 1);
             float tot;
-            tile_prep(dv, &tot);
+            tile_prep(dv, 0, &tot);
             if (c >= 1) dv = load_dt(c - 1);
             // R_in of this tile (state entering from the right) -> scratch.
             if (c < nc - 1) {
@@ -322,17 +369,17 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                 fence_proxy_async_all();
             }
             SSM_CTA_WAIT(sm.bar_x[xb], ph_x[xb]);
-            scale_row(sm.X[xb], sm.Xw, row, ex2(sm.excl[row]) * sm.dtv[row], wg);
+            scale_row(sm.X[xb], sm.Xw, row, ex2(sm.excl[0][row]) * sm.dtv[0][row], wg);
             fence_proxy_async_smem();
-            SSM_CTA_WAIT(sm.bar_b, ph_b);
+            SSM_CTA_WAIT(sm.bar_b[0], ph_b[0]);
             if (tid == 0) {
                 tc_fence_after_sync();
-                issue_state_mma();
-                mma_commit(&sm.bar_mma);
+                issue_state_mma(0);
+                mma_commit(&sm.bar_m2);
             }
-            SSM_CTA_WAIT(sm.bar_mma, ph_mma);
+            SSM_CTA_WAIT(sm.bar_m2, ph_m2);
             tc_fence_after_sync();
-            if (tid == 0 && c >= 1) load_b(c - 1);
+            if (tid == 0 && c >= 1) load_b(c - 1, 0);
             if (row < N) state_update(st, ex2(tot));
             fence_proxy_async_smem();
             tc_fence_before_sync();
@@ -341,70 +388,58 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     }
 
     // ---------------- forward sweep with the outputs ----------------------------------
+    // Software pipeline over the tiles: while the mask of tile c is built, the
+    // copies of tile c + 1 land; G of tile c + 1 runs on the tensor core behind
+    // Y and S_c of tile c, and Zf, Zr of tile c + 1 right after the state
+    // update, so that the mask pass of tile c + 1 can start at once.
 #pragma unroll
     for (int p = 0; p < 32; ++p) st[p] = 0.0f;
     if (tid == 0) {
         load_x(0, 0);
         load_c(0, bidir && nc > 1);
-        load_b(0);
-        if (nc > 1) load_x(1, 1);
+        load_b(0, 0);
+        if (nc > 1) {
+            load_b(1, 1);
+            load_x(1, 1);
+        }
     }
     {
     float dv = load_dt(0);
+    float tot_cur, tot_nxt = 0.0f;
+    tile_prep(dv, 0, &tot_cur);
+    if (nc > 1) dv = load_dt(1);
+    SSM_CTA_WAIT(sm.bar_x[0], ph_x[0]);
+    scale_row(sm.X[0], sm.Xw, row, ex2(tot_cur - sm.cum[0][row]) * sm.dtv[0][row], wg);
+    fence_proxy_async_smem();
+    SSM_CTA_WAIT(sm.bar_c, ph_c);
+    SSM_CTA_WAIT(sm.bar_b[0], ph_b[0]);
+    if (tid == 0) {
+        tc_fence_after_sync();
+        issue_g(0);
+        issue_z(false, bidir && nc > 1);
+        mma_commit(&sm.bar_g);
+    }
     for (int c = 0; c < nc; ++c) {
         const int c0 = c * kQ;
-        const int xb = c & 1;
+        const int par = c & 1;      // buffers and per-tile vectors of tile c
+        const bool more = c + 1 < nc;
         const bool has_s = c > 0;
         const bool has_r = bidir && (c < nc - 1);
-        float tot;
-        tile_prep(dv, &tot);
-        if (c + 1 < nc) dv = load_dt(c + 1);
-        if (wg == 0) {
-            // Column factors for the blocks of the mask below (above) the
-            // diagonal: for s in a 32-column block that ends at row r (starts
-            // at row r') and t past that block,
-            //   exp2(cum_t - cum_s)   = exp2(cum_t - cum_r)   * exp2(cum_r - cum_s),
-            //   exp2(excl_s - excl_t) = exp2(excl_s - excl_r') * exp2(excl_r' - excl_t),
-            // and both factors are <= 1.  Diagonal blocks use the direct form.
-            const int s = row;
-            sm.csf[s] = ex2(sm.cum[s | 31] - sm.cum[s]) * sm.dtv[s];
-            if (bidir) sm.csr[s] = ex2(sm.excl[s] - sm.excl[s & ~31]) * sm.dtv[s];
-        }
-        SSM_CTA_WAIT(sm.bar_c, ph_c);
-        SSM_CTA_WAIT(sm.bar_b, ph_b);
-
-        // MMA group 1: G = C B^T, Zf = C S_in^T, Zr = C R_in^T.
-        if (tid == 0) {
-            tc_fence_after_sync();
-#pragma unroll
-            for (int kk = 0; kk < N / 16; ++kk) {
-                const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;
-                const uint64_t a = smem_desc(sC + koff, 16, 1024, kSwizzle128B);
-                mma_bf16_ss(tmem + kColG, a, smem_desc(sB + koff, 16, 1024, kSwizzle128B), idG, kk > 0);
-                const uint32_t soff = (kk >> 2) * kStateRegion + (kk & 3) * 32;
-                if (has_s)
-                    mma_bf16_ss(tmem + kColZf, a, smem_desc(sS + soff, 16, 1024, kSwizzle128B), idZ, kk > 0);
-                if (has_r)
-                    mma_bf16_ss(tmem + kColZr, a, smem_desc(sR + soff, 16, 1024, kSwizzle128B), idZ, kk > 0);
-            }
-            mma_commit(&sm.bar_mma);
-        }
-        // Meanwhile: weighted x rows for this tile's forward chunk state.
-        SSM_CTA_WAIT(sm.bar_x[xb], ph_x[xb]);
-        scale_row(sm.X[xb], sm.Xw, row, ex2(tot - sm.cum[row]) * sm.dtv[row], wg);
-        fence_proxy_async_smem();
         // The previous tile's output rows staged in the mask buffer must have
-        // been read by their store before the mask pass below overwrites it.
+        // been read by their store before the mask pass overwrites it.
         if (tid == 0) bulk_wait_read0();
-        SSM_CTA_WAIT(sm.bar_mma, ph_mma);
+        SSM_CTA_WAIT(sm.bar_g, ph_g);          // G, Zf, Zr of tile c; C and R buffers free
         tc_fence_after_sync();
-        if (tid == 0 && c + 1 < nc) load_c(c + 1, bidir && (c + 1 < nc - 1));
+        if (tid == 0 && more) load_c(c + 1, bidir && (c + 1 < nc - 1));
 
         // Decay mask on row t of G -> bf16 M (K-major, swizzled).
         {
             const int t = row;
             const int tb = t >> 5;                 // warp-uniform: the warp owns rows 32 tb..
-            const float cum_t = sm.cum[t], excl_t = sm.excl[t];
+            const float *cum = sm.cum[par];
+            const float *excl = sm.excl[par];
+            const float *dtv = sm.dtv[par];
+            const float cum_t = cum[t], excl_t = excl[t];
             // Blocks {0, 3} to warpgroup 0 and {1, 2} to warpgroup 1: the causal
             // (and diagonal) work of every row warp is then split evenly.
             const int sbs[2] = {wg == 0 ? 0 : 1, wg == 0 ? 3 : 2};
@@ -426,18 +461,29 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                     float m[32];
                     if (sb == tb) {
                         // diagonal block: direct differences of cumulative sums
+                        const float4 *c4 = reinterpret_cast<const float4 *>(cum + sb * 32);
+                        const float4 *e4 = reinterpret_cast<const float4 *>(excl + sb * 32);
+                        const float4 *d4 = reinterpret_cast<const float4 *>(dtv + sb * 32);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int s = sb * 32 + j;
-                            float w = (s <= t) ? ex2(cum_t - sm.cum[s]) : 0.0f;
-                            if (bidir && s >= t) w += ex2(sm.excl[s] - excl_t);
-                            m[j] = __uint_as_float(gr[i][j]) * (w * sm.dtv[s]);
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 cs = c4[j4], ds = d4[j4];
+                            const float4 es = bidir ? e4[j4] : cs;
+                            const float csv[4] = {cs.x, cs.y, cs.z, cs.w};
+                            const float esv[4] = {es.x, es.y, es.z, es.w};
+                            const float dsv[4] = {ds.x, ds.y, ds.z, ds.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int s = sb * 32 + 4 * j4 + q;
+                                float w = (s <= t) ? ex2(cum_t - csv[q]) : 0.0f;
+                                if (bidir && s >= t) w += ex2(esv[q] - excl_t);
+                                m[4 * j4 + q] = __uint_as_float(gr[i][4 * j4 + q]) * (w * dsv[q]);
+                            }
                         }
                     } else {
                         const bool fwd = sb < tb;
-                        const float e = fwd ? ex2(cum_t - sm.cum[sb * 32 + 31])
-                                            : ex2(sm.excl[sb * 32] - excl_t);
-                        const float4 *f4 = reinterpret_cast<const float4 *>((fwd ? sm.csf : sm.csr) + sb * 32);
+                        const float e = fwd ? ex2(cum_t - cum[sb * 32 + 31])
+                                            : ex2(excl[sb * 32] - excl_t);
+                        const float4 *f4 = reinterpret_cast<const float4 *>((fwd ? sm.csf[par] : sm.csr[par]) + sb * 32);
 #pragma unroll
                         for (int j4 = 0; j4 < 8; ++j4) {
                             const float4 f = f4[j4];
@@ -466,36 +512,46 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         tc_fence_before_sync();
         __syncthreads();
 
-        // MMA group 2: Y = M X, S_c^T = B^T Xw.
+        // Y = M X and S_c^T = B^T Xw of tile c.
         if (tid == 0) {
             tc_fence_after_sync();
-            const uint32_t sX = smem_addr(sm.X[xb]);
+            const uint32_t sX = smem_addr(sm.X[par]);
 #pragma unroll
             for (int kk = 0; kk < kQ / 16; ++kk) {
                 const uint64_t a = smem_desc(sM + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024, kSwizzle128B);
                 const uint64_t bd = smem_desc(sX + kk * 2048, kTile, 1024, kSwizzle128B);
                 mma_bf16_ss(tmem + kColY, a, bd, idY, kk > 0);
             }
-            issue_state_mma();
-            mma_commit(&sm.bar_mma);
+            issue_state_mma(par);
+            mma_commit(&sm.bar_m2);
         }
-        SSM_CTA_WAIT(sm.bar_mma, ph_mma);
+        // Meanwhile: vectors of tile c + 1, then its G behind them.
+        if (more) {
+            tile_prep(dv, par ^ 1, &tot_nxt);
+            if (c + 2 < nc) dv = load_dt(c + 2);
+            SSM_CTA_WAIT(sm.bar_c, ph_c);
+            SSM_CTA_WAIT(sm.bar_b[par ^ 1], ph_b[par ^ 1]);
+            if (tid == 0) {
+                tc_fence_after_sync();
+                issue_g(par ^ 1);
+            }
+        }
+        SSM_CTA_WAIT(sm.bar_m2, ph_m2);
         tc_fence_after_sync();
-        if (tid == 0 && c + 1 < nc) load_b(c + 1);
+        if (tid == 0 && c + 2 < nc) load_b(c + 2, par);
 
         // Epilogue: row t of y, columns p in [32 wg, 32 wg + 32).
         {
             const int t = row;
-            const int grow = c0 + t;
             const int q = wg;
             uint32_t yv[32], zf[32], zr[32];
             tmem_ld32_async(tmem + lane_base + kColY + q * 32, yv);
             if (has_s) tmem_ld32_async(tmem + lane_base + kColZf + q * 32, zf);
             if (has_r) tmem_ld32_async(tmem + lane_base + kColZr + q * 32, zr);
-            const float ef = ex2(sm.cum[t]);
-            const float er = ex2(tot - sm.excl[t]);
+            const float ef = ex2(sm.cum[par][t]);
+            const float er = ex2(tot_cur - sm.excl[par][t]);
             float xr[32];
-            const uint4 *xs = reinterpret_cast<const uint4 *>(sm.X[xb] + t * 128);
+            const uint4 *xs = reinterpret_cast<const uint4 *>(sm.X[par] + t * 128);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint4 v = xs[(q * 4 + j) ^ (t & 7)];
@@ -523,12 +579,17 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             for (int j = 0; j < 8; ++j)
                 *reinterpret_cast<float4 *>(ys + ((j ^ (t & 7)) << 4)) =
                     make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-            (void)grow;
         }
         // State passing: column n = row of S_in, rows [32 wg, 32 wg + 32).
         if (row < N) {
-            state_update(st, ex2(tot));
+            state_update(st, ex2(tot_cur));
             store_state_bf16<NB>(sm.S, row, wg * 32, *reinterpret_cast<float(*)[32]>(st));
+        }
+        // Weighted x rows of tile c + 1 (its S_c reads them).
+        if (more) {
+            SSM_CTA_WAIT(sm.bar_x[par ^ 1], ph_x[par ^ 1]);
+            scale_row(sm.X[par ^ 1], sm.Xw, row,
+                      ex2(tot_nxt - sm.cum[par ^ 1][row]) * sm.dtv[par ^ 1][row], wg);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -537,8 +598,14 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             tma_store_4d(&tmY, sm.M[0], 0, h, c0, b);
             tma_store_4d(&tmY, sm.M[1], 32, h, c0, b);
             bulk_commit();
-            if (c + 2 < nc) load_x(c + 2, xb);
+            if (c + 2 < nc) load_x(c + 2, par);
+            if (more) {
+                tc_fence_after_sync();
+                issue_z(true, bidir && (c + 1 < nc - 1));
+                mma_commit(&sm.bar_g);
+            }
         }
+        tot_cur = tot_nxt;
     }
     }
 
@@ -547,10 +614,11 @@ done:
     if (!ok && tid == 0) {
         abort_flag = 1;
         atomicOr(&g_device_error, 1u);
-        // Copies or an MMA still in flight after a timeout: give them a
-        // bounded chance to land before the tensor memory is released.
+        // MMAs still in flight after a timeout: give them a bounded chance
+        // to finish before the tensor memory is released.
+        mma_commit(&sm.bar_fin);
         volatile int never = 0;
-        (void)mbar_wait_bounded(&sm.bar_mma, ph_mma, &never, 100000000ull);
+        (void)mbar_wait_bounded(&sm.bar_fin, 0, &never, 100000000ull);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -625,6 +693,7 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
     const size_t smem = sizeof(Smem<NB>) + 1024;
+    static_assert(sizeof(Smem<NB>) + 1024 <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
     auto kern = ssd_chunk_scan_kernel<NB>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (err != cudaSuccess) return err;
