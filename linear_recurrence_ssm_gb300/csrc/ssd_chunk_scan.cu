@@ -69,7 +69,7 @@ struct __align__(1024) Smem {
     uint8_t X[2][kTile];        // x tiles (double buffered), rows s, 64 p (MN-major B operand)
     uint8_t Xw[kTile];          // weighted x rows
     uint8_t M[2][kTile];        // masked G, K-major: row t, s in two 64-wide regions; then y rows
-    uint8_t S[NB][kStateRegion];  // forward entering state (bf16), K-major: row p, n
+    uint8_t S[NB][kStateRegion];  // forward entering state (bf16), MN-major: row n, 64 p
     uint8_t R[NB][kStateRegion];  // reverse entering state (bf16), same layout
     // per-tile vectors, double buffered by tile parity
     float cum[2][kQ];
@@ -155,17 +155,20 @@ __device__ __forceinline__ void scale_row(const uint8_t *X, uint8_t *Xw, int s, 
     }
 }
 
-// Store rows [p0, p0 + 32) of a state column (thread n owns column n) as
-// bf16 into a K-major state image: row p, K index n.
+// Store entries [p0, p0 + 32) of state row n (thread n holds them, fp32)
+// as bf16 into an MN-major state image: 128-byte rows n of 64 p, 128-byte
+// swizzle (the 16-byte chunk index XORed with n % 8) -- the layout of a TMA
+// x tile, so the image is the B operand of Zf = C S_in^T directly.
 template <int NB>
 __device__ __forceinline__ void store_state_bf16(uint8_t (*img)[kStateRegion], int n, int p0,
                                                  const float (&s)[32]) {
-    uint8_t *reg = img[n >> 6];
-    const int nc = n & 63;
+    uint8_t *rowp = &img[0][0] + n * 128;
 #pragma unroll
-    for (int p = 0; p < 32; ++p) {
-        __nv_bfloat16 v = __float2bfloat16_rn(s[p]);
-        *reinterpret_cast<__nv_bfloat16 *>(reg + swz(p0 + p, nc)) = v;
+    for (int j = 0; j < 4; ++j) {
+        const int chunk = (p0 >> 3) + j;
+        *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (n & 7)) << 4)) =
+            make_uint4(pack_bf16(s[8 * j], s[8 * j + 1]), pack_bf16(s[8 * j + 2], s[8 * j + 3]),
+                       pack_bf16(s[8 * j + 4], s[8 * j + 5]), pack_bf16(s[8 * j + 6], s[8 * j + 7]));
     }
 }
 
@@ -247,7 +250,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     const uint32_t sXw = smem_addr(sm.Xw), sM = smem_addr(sm.M), sS = smem_addr(sm.S);
     const uint32_t sR = smem_addr(sm.R);
     constexpr uint32_t idG = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t idZ = idesc_bf16_f32(128, 64, false, false);
+    constexpr uint32_t idZ = idesc_bf16_f32(128, 64, false, true);
     constexpr uint32_t idY = idesc_bf16_f32(128, 64, false, true);
     constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);
 
@@ -325,11 +328,11 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         for (int kk = 0; kk < N / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;
             const uint64_t a = smem_desc(sC + koff, 16, 1024, kSwizzle128B);
-            const uint32_t soff = (kk >> 2) * kStateRegion + (kk & 3) * 32;
+            // state images: 16 rows of n per K step
             if (has_s)
-                mma_bf16_ss(tmem + kColZf, a, smem_desc(sS + soff, 16, 1024, kSwizzle128B), idZ, kk > 0);
+                mma_bf16_ss(tmem + kColZf, a, smem_desc(sS + kk * 2048, kTile, 1024, kSwizzle128B), idZ, kk > 0);
             if (has_r)
-                mma_bf16_ss(tmem + kColZr, a, smem_desc(sR + soff, 16, 1024, kSwizzle128B), idZ, kk > 0);
+                mma_bf16_ss(tmem + kColZr, a, smem_desc(sR + kk * 2048, kTile, 1024, kSwizzle128B), idZ, kk > 0);
         }
     };
     // State update for column n = row, rows p in [32 wg, 32 wg + 32):
