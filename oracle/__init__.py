@@ -63,6 +63,14 @@ def _load(path: str | None = None):
         lib.oracle_diag_scan_range.restype = None
         lib.oracle_ssd_scan_range.argtypes = [dp] * 7 + [i64] * 5 + [ctypes.c_int, i64, i64, ctypes.c_int]
         lib.oracle_ssd_scan_range.restype = None
+        dbl = ctypes.c_double
+        lib.oracle_diag_scan_ex_range.argtypes = ([dp] * 7 + [i64] * 4 + [dp, ctypes.c_int, ctypes.c_int,
+                                                  dbl, dbl, dp, dp, dp, i64, i64, ctypes.c_int])
+        lib.oracle_diag_scan_ex_range.restype = None
+        lib.oracle_ssd_scan_ex_range.argtypes = ([dp] * 7 + [i64] * 5 + [ctypes.c_int, dp, ctypes.c_int,
+                                                 ctypes.c_int, dbl, dbl, dp, dp, dp, i64, i64,
+                                                 ctypes.c_int])
+        lib.oracle_ssd_scan_ex_range.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _libs[key] = lib
@@ -88,7 +96,16 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def diag_scan(x, delta, A, B, C, D=None, nthreads: int = 0, channels=None, library=None):
+def _limit(dt_limit):
+    if dt_limit is None:
+        return 0, 0.0, 0.0
+    lo, hi = dt_limit
+    return 1, float(lo), float(hi)
+
+
+def diag_scan(x, delta, A, B, C, D=None, nthreads: int = 0, channels=None, library=None,
+              dt_bias=None, dt_softplus: bool = False, dt_limit=None, z=None, h0=None,
+              return_final_state: bool = False):
     """Sequential diagonal selective scan in fp64.
 
     x, delta: (Bs, L, ED); A: (ED, N); B, C: (Bs, L, N); D: (ED) or None.
@@ -96,30 +113,48 @@ def diag_scan(x, delta, A, B, C, D=None, nthreads: int = 0, channels=None, libra
     flattened (b, e) channels in [c0, c1) (the rest of y is NaN); used to time
     a bounded sample.  ``library`` selects another compiled copy of the oracle
     (the tests use it to show that planted mistakes are caught).
+
+    Options (argument list of the chunked scan in "Some questions of
+    Bi-Mamba2 and Hydra"): ``dt_bias`` (ED) is added to delta, then
+    ``dt_softplus`` applies log(1 + exp(.)), then ``dt_limit=(lo, hi)`` clamps;
+    ``z`` (Bs, L, ED) gates the output with silu(z); ``h0`` (Bs, ED, N) is the
+    initial state; ``return_final_state`` also returns h_{L-1} (Bs, ED, N).
     """
-    x, delta, A, B, C, D = map(_f64, (x, delta, A, B, C, D))
+    x, delta, A, B, C, D, dt_bias, z, h0 = map(_f64, (x, delta, A, B, C, D, dt_bias, z, h0))
     Bs, L, ED = x.shape
     N = A.shape[1]
     assert delta.shape == x.shape and A.shape == (ED, N)
     assert B.shape == (Bs, L, N) and C.shape == (Bs, L, N)
     assert D is None or D.shape == (ED,)
+    assert dt_bias is None or dt_bias.shape == (ED,)
+    assert z is None or z.shape == x.shape
+    assert h0 is None or h0.shape == (Bs, ED, N)
     y = np.full((Bs, L, ED), np.nan) if channels else np.zeros((Bs, L, ED))
+    hf = np.zeros((Bs, ED, N)) if return_final_state else None
     c0, c1 = channels if channels else (0, Bs * ED)
-    _load(library).oracle_diag_scan_range(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                                   _ptr(y), Bs, L, ED, N, c0, c1, nthreads)
-    return y
+    lim, lo, hi = _limit(dt_limit)
+    _load(library).oracle_diag_scan_ex_range(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y), Bs, L, ED, N,
+        _ptr(dt_bias), int(bool(dt_softplus)), lim, lo, hi, _ptr(z), _ptr(h0), _ptr(hf), c0, c1,
+        nthreads)
+    return (y, hf) if return_final_state else y
 
 
 def ssd_scan(x, dt, A_head, B, C, D=None, bidirectional: bool = False,
-             nthreads: int = 0, units=None, library=None):
+             nthreads: int = 0, units=None, library=None, dt_bias=None,
+             dt_softplus: bool = False, dt_limit=None, z=None, h0=None,
+             return_final_state: bool = False):
     """Sequential scalar-per-head (SSD) scan in fp64, optionally bidirectional.
 
     x: (Bs, L, H, P); dt: (Bs, L, H); A_head: (H); B, C: (Bs, L, N) or
     (Bs, L, 1, N) (one group shared by all heads); D: (H) or None.
     Returns y: (Bs, L, H, P) fp64.  ``units=(u0, u1)`` computes only the
     flattened (b, h) pairs in [u0, u1) (the rest of y is NaN).
+    Options as in ``diag_scan``, per head: ``dt_bias`` (H), ``z`` (Bs, L, H, P),
+    ``h0`` and the final state (Bs, H, P, N) -- state I/O for a single
+    direction only.
     """
-    x, dt, A_head, B, C, D = map(_f64, (x, dt, A_head, B, C, D))
+    x, dt, A_head, B, C, D, dt_bias, z, h0 = map(_f64, (x, dt, A_head, B, C, D, dt_bias, z, h0))
     Bs, L, H, P = x.shape
     if B.ndim == 4:
         assert B.shape[2] == 1 and C.shape[2] == 1, "one group of B, C shared by all heads"
@@ -129,8 +164,17 @@ def ssd_scan(x, dt, A_head, B, C, D=None, bidirectional: bool = False,
     assert dt.shape == (Bs, L, H) and A_head.shape == (H,)
     assert B.shape == (Bs, L, N) and C.shape == (Bs, L, N)
     assert D is None or D.shape == (H,)
+    assert dt_bias is None or dt_bias.shape == (H,)
+    assert z is None or z.shape == x.shape
+    assert h0 is None or h0.shape == (Bs, H, P, N)
+    if bidirectional and (h0 is not None or return_final_state):
+        raise ValueError("state input/output is defined for a single direction only")
     y = np.full((Bs, L, H, P), np.nan) if units else np.zeros((Bs, L, H, P))
+    hf = np.zeros((Bs, H, P, N)) if return_final_state else None
     u0, u1 = units if units else (0, Bs * H)
-    _load(library).oracle_ssd_scan_range(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D),
-                                  _ptr(y), Bs, L, H, P, N, int(bool(bidirectional)), u0, u1, nthreads)
-    return y
+    lim, lo, hi = _limit(dt_limit)
+    _load(library).oracle_ssd_scan_ex_range(
+        _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D), _ptr(y), Bs, L, H, P, N,
+        int(bool(bidirectional)), _ptr(dt_bias), int(bool(dt_softplus)), lim, lo, hi, _ptr(z),
+        _ptr(h0), _ptr(hf), u0, u1, nthreads)
+    return (y, hf) if return_final_state else y

@@ -33,6 +33,16 @@
  *   recurrence above without the D term and flip reverses the time axis
  *   of x, dt, B and C together.  D x is added once.
  *
+ * Options of the chunked scan's argument list in [P2] (dt_bias,
+ * dt_softplus, dt_limit, z, initial and final states), applied to both
+ * scans with their plainest reading (the Mamba convention):
+ *   delta <- delta + dt_bias[channel or head]          (if a bias is given)
+ *   delta <- log(1 + exp(delta))                        (if dt_softplus)
+ *   delta <- min(max(delta, dt_min), dt_max)            (if dt_limit)
+ *   y     <- y * z / (1 + exp(-z))   (silu gate, after D x; if z is given)
+ *   h_{-1} = h0 instead of 0; h_final = h_{L-1}        (if given / asked)
+ * State I/O is defined for the single-direction scans only.
+ *
  * All arrays are dense row-major (last index fastest) fp64.
  */
 #include <math.h>
@@ -59,37 +69,67 @@ int oracle_max_threads(void) {
 #endif
 }
 
+/* The delta (dt) seen by the recurrence, after the optional preprocessing. */
+static double prep_delta(double d, const double *bias, int64_t k, int softplus, int limit,
+                         double dmin, double dmax) {
+    if (bias) d += bias[k];
+    if (softplus) d = log1p(exp(d));
+    if (limit) d = fmin(fmax(d, dmin), dmax);
+    return d;
+}
+
+/* silu gate: z * sigmoid(z). */
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
 /*
  * Diagonal selective scan, sequential over t for every (b, e) channel.
- * x, delta, y: (Bs, L, ED); A: (ED, N); B, C: (Bs, L, N); D: (ED) or NULL.
+ * x, delta, y, z: (Bs, L, ED); A: (ED, N); B, C: (Bs, L, N); D, dt_bias:
+ * (ED) or NULL; h0, h_final: (Bs, ED, N) or NULL.
  * Channels listed in [c_begin, c_end) of the flattened (b, e) index are
  * computed; the rest of y is left untouched (lets a caller time a sample).
  */
-void oracle_diag_scan_range(const double *x, const double *delta,
-                            const double *A, const double *B, const double *C,
-                            const double *D, double *y, int64_t Bs, int64_t L,
-                            int64_t ED, int64_t N, int64_t c_begin,
-                            int64_t c_end, int nthreads) {
+void oracle_diag_scan_ex_range(const double *x, const double *delta, const double *A,
+                               const double *B, const double *C, const double *D,
+                               double *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
+                               const double *dt_bias, int dt_softplus, int dt_limit,
+                               double dt_min, double dt_max, const double *z,
+                               const double *h0, double *h_final, int64_t c_begin,
+                               int64_t c_end, int nthreads) {
     set_threads(nthreads);
     if (c_end > Bs * ED) c_end = Bs * ED;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t c = c_begin; c < c_end; ++c) {
         const int64_t b = c / ED, e = c % ED;
         double *h = (double *)calloc((size_t)N, sizeof(double));
+        if (h0)
+            for (int64_t n = 0; n < N; ++n) h[n] = h0[(b * ED + e) * N + n];
         for (int64_t t = 0; t < L; ++t) {
             const int64_t i = (b * L + t) * ED + e;   /* x, delta, y */
             const int64_t r = (b * L + t) * N;        /* B, C row     */
-            const double dl = delta[i], xv = x[i];
+            const double dl = prep_delta(delta[i], dt_bias, e, dt_softplus, dt_limit, dt_min,
+                                         dt_max);
+            const double xv = x[i];
             double acc = 0.0;
             for (int64_t n = 0; n < N; ++n) {
                 const double a = exp(dl * A[e * N + n]);
                 h[n] = a * h[n] + dl * B[r + n] * xv;
                 acc += C[r + n] * h[n];
             }
-            y[i] = acc + (D ? D[e] * xv : 0.0);
+            const double out = acc + (D ? D[e] * xv : 0.0);
+            y[i] = z ? out * silu(z[i]) : out;
         }
+        if (h_final)
+            for (int64_t n = 0; n < N; ++n) h_final[(b * ED + e) * N + n] = h[n];
         free(h);
     }
+}
+
+void oracle_diag_scan_range(const double *x, const double *delta, const double *A,
+                            const double *B, const double *C, const double *D, double *y,
+                            int64_t Bs, int64_t L, int64_t ED, int64_t N, int64_t c_begin,
+                            int64_t c_end, int nthreads) {
+    oracle_diag_scan_ex_range(x, delta, A, B, C, D, y, Bs, L, ED, N, NULL, 0, 0, 0.0, 0.0, NULL,
+                              NULL, NULL, c_begin, c_end, nthreads);
 }
 
 void oracle_diag_scan(const double *x, const double *delta, const double *A,
@@ -104,17 +144,17 @@ void oracle_diag_scan(const double *x, const double *delta, const double *A,
  * One direction of the SSD recurrence for a single (b, h), written into
  * y (accumulating).  `rev` = 0 walks t = 0..L-1; `rev` = 1 walks the
  * flipped sequence, i.e. t = L-1..0, which is F applied to flip(inputs)
- * and flipped back.
- * x, y: (Bs, L, H, P); dt: (Bs, L, H); B, C: (Bs, L, N).
+ * and flipped back.  `dth` is this head's preprocessed dt, (L).
+ * x, y: (Bs, L, H, P); B, C: (Bs, L, N).  `state` (P x N) holds the
+ * entering state on entry and the final state on return.
  */
-static void ssd_one_direction(const double *x, const double *dt, double Ah,
+static void ssd_one_direction(const double *x, const double *dth, double Ah,
                               const double *B, const double *C, double *y,
                               int64_t b, int64_t h, int64_t L, int64_t H,
                               int64_t P, int64_t N, int rev, double *state) {
-    memset(state, 0, (size_t)(P * N) * sizeof(double));
     for (int64_t k = 0; k < L; ++k) {
         const int64_t t = rev ? (L - 1 - k) : k;
-        const double d = dt[(b * L + t) * H + h];
+        const double d = dth[t];
         const double a = exp(d * Ah);
         const double *xt = x + ((b * L + t) * H + h) * P;
         const double *Bt = B + (b * L + t) * N;
@@ -135,33 +175,61 @@ static void ssd_one_direction(const double *x, const double *dt, double Ah,
 /*
  * Scalar-per-head (SSD) scan, optionally bidirectional, for the (b, h)
  * pairs in [u_begin, u_end) of the flattened index u = b * H + h.
- * x, y: (Bs, L, H, P); dt: (Bs, L, H); A_head: (H); B, C: (Bs, L, N)
- * (one group shared by all heads); D: (H) or NULL.
+ * x, y, z: (Bs, L, H, P); dt: (Bs, L, H); A_head, D, dt_bias: (H) (D and
+ * dt_bias may be NULL); B, C: (Bs, L, N) (one group shared by all heads);
+ * h0, h_final: (Bs, H, P, N) or NULL (single direction only).
  */
+void oracle_ssd_scan_ex_range(const double *x, const double *dt, const double *A_head,
+                              const double *B, const double *C, const double *D, double *y,
+                              int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                              int bidirectional, const double *dt_bias, int dt_softplus,
+                              int dt_limit, double dt_min, double dt_max, const double *z,
+                              const double *h0, double *h_final, int64_t u_begin,
+                              int64_t u_end, int nthreads) {
+    set_threads(nthreads);
+    if (u_end > Bs * H) u_end = Bs * H;
+    if (bidirectional && (h0 || h_final)) return;   /* not defined */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = u_begin; u < u_end; ++u) {
+        const int64_t b = u / H, h = u % H;
+        double *state = (double *)malloc((size_t)(P * N) * sizeof(double));
+        /* this head's preprocessed dt */
+        double *dtp = (double *)malloc((size_t)L * sizeof(double));
+        for (int64_t t = 0; t < L; ++t)
+            dtp[t] = prep_delta(dt[(b * L + t) * H + h], dt_bias, h, dt_softplus, dt_limit, dt_min,
+                                dt_max);
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t o = ((b * L + t) * H + h) * P;
+            for (int64_t p = 0; p < P; ++p)
+                y[o + p] = D ? D[h] * x[o + p] : 0.0;
+        }
+        for (int64_t i = 0; i < P * N; ++i) state[i] = h0 ? h0[u * P * N + i] : 0.0;
+        ssd_one_direction(x, dtp, A_head[h], B, C, y, b, h, L, H, P, N, 0, state);
+        if (h_final)
+            for (int64_t i = 0; i < P * N; ++i) h_final[u * P * N + i] = state[i];
+        if (bidirectional) {
+            memset(state, 0, (size_t)(P * N) * sizeof(double));
+            ssd_one_direction(x, dtp, A_head[h], B, C, y, b, h, L, H, P, N, 1, state);
+        }
+        if (z) {
+            for (int64_t t = 0; t < L; ++t) {
+                const int64_t o = ((b * L + t) * H + h) * P;
+                for (int64_t p = 0; p < P; ++p) y[o + p] *= silu(z[o + p]);
+            }
+        }
+        free(dtp);
+        free(state);
+    }
+}
+
 void oracle_ssd_scan_range(const double *x, const double *dt,
                            const double *A_head, const double *B,
                            const double *C, const double *D, double *y,
                            int64_t Bs, int64_t L, int64_t H, int64_t P,
                            int64_t N, int bidirectional, int64_t u_begin,
                            int64_t u_end, int nthreads) {
-    set_threads(nthreads);
-    if (u_end > Bs * H) u_end = Bs * H;
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t u = u_begin; u < u_end; ++u) {
-        const int64_t b = u / H, h = u % H;
-        double *state = (double *)malloc((size_t)(P * N) * sizeof(double));
-        for (int64_t t = 0; t < L; ++t) {
-            const int64_t o = ((b * L + t) * H + h) * P;
-            for (int64_t p = 0; p < P; ++p)
-                y[o + p] = D ? D[h] * x[o + p] : 0.0;
-        }
-        ssd_one_direction(x, dt, A_head[h], B, C, y, b, h, L, H, P, N, 0,
-                          state);
-        if (bidirectional)
-            ssd_one_direction(x, dt, A_head[h], B, C, y, b, h, L, H, P, N, 1,
-                              state);
-        free(state);
-    }
+    oracle_ssd_scan_ex_range(x, dt, A_head, B, C, D, y, Bs, L, H, P, N, bidirectional, NULL, 0, 0,
+                             0.0, 0.0, NULL, NULL, NULL, u_begin, u_end, nthreads);
 }
 
 void oracle_ssd_scan(const double *x, const double *dt, const double *A_head,

@@ -23,9 +23,9 @@ MUTANTS = {
     "input_drops_delta": ("diag", "h[n] = a * h[n] + dl * B[r + n] * xv;",
                           "h[n] = a * h[n] + B[r + n] * xv;"),
     "readout_uses_B": ("diag", "acc += C[r + n] * h[n];", "acc += B[r + n] * h[n];"),
-    "drops_D": ("diag", "y[i] = acc + (D ? D[e] * xv : 0.0);", "y[i] = acc;"),
-    "decay_uses_previous_delta": ("diag", "const double dl = delta[i], xv = x[i];",
-                                  "const double dl = delta[t > 0 ? i - ED : i], xv = x[i];"),
+    "drops_D": ("diag", "const double out = acc + (D ? D[e] * xv : 0.0);", "const double out = acc;"),
+    "decay_uses_previous_delta": ("diag", "prep_delta(delta[i], dt_bias",
+                                  "prep_delta(delta[t > 0 ? i - ED : i], dt_bias"),
     # SSD / bidirectional
     "ssd_no_decay": ("ssd", "*s = a * (*s) + d * xt[p] * Bt[n];", "*s = (*s) + d * xt[p] * Bt[n];"),
     "ssd_readout_uses_B": ("ssd", "acc += (*s) * Ct[n];", "acc += (*s) * Bt[n];"),
