@@ -18,7 +18,8 @@
  *       argument subset (x, dt, A, B, C, chunk_size, D) of the chunked scan
  *       in "Some questions of Bi-Mamba2 and Hydra" (Bi-Mamba2 issue 1, the
  *       MambaChunkScanCombinedFn.forward signature), with z, dt_bias and
- *       dt_softplus off and one group of B, C shared by all heads.
+ *       dt_softplus off and one group of B, C shared by all heads (the
+ *       _ex entry points below add those options and state I/O).
  *       x (Bs, L, H, P); dt (Bs, L, H); A_head (H); B, C (Bs, L, N) -- the
  *       same memory as (Bs, L, 1, N); D (H); y (Bs, L, H, P).  Per (b, h):
  *         H_t = exp(dt_t * A_h) * H_{t-1} + dt_t * x_t (outer) B_t   (P x N)
@@ -167,6 +168,62 @@ SSM_API ssm_status_t ssd_chunk_scan_fwd_noalloc(const void *x, const void *dt,
                                         int64_t Bs, int64_t L, int64_t H, int64_t P,
                                         int64_t N, int64_t chunk, int bidirectional,
                                         void *stream);
+
+/*
+ * Options of the scans: the remaining arguments of the chunked scan's
+ * argument list in "Some questions of Bi-Mamba2 and Hydra" (Bi-Mamba2
+ * issue 1, MambaChunkScanCombinedFn.forward: dt_bias, dt_softplus,
+ * dt_limit, z, initial and returned final states), read the Mamba way.
+ * A zero-initialised structure means no option.  Applied in this order:
+ *   delta <- delta + dt_bias[channel]          if dt_bias != NULL
+ *   delta <- log(1 + exp(delta))               if dt_softplus != 0
+ *   delta <- min(max(delta, dt_min), dt_max)   if dt_limit != 0
+ *   (the scan, from h_{-1} = h0 when h0 != NULL, else 0)
+ *   y     <- (scan + D x) * z / (1 + exp(-z))  if z != NULL   (silu gate)
+ *   h_final <- the state after the last step   if h_final != NULL
+ * "channel" is e for the diagonal scan and the head h for SSD.
+ *   dt_bias : fp32, (ED) or (H)
+ *   z       : same shape and element type as x (fp32 or bf16)
+ *   h0, h_final : fp32 device arrays, (Bs, ED, N) for the diagonal scan,
+ *             (Bs, H, P, N) for SSD (state matrix per head: row p, column
+ *             n); caller-owned; h_final is fully written.
+ * State input/output belongs to a single direction: ssd_chunk_scan_fwd_ex
+ * with bidirectional != 0 and h0 or h_final set returns
+ * SSM_ERR_UNSUPPORTED.
+ */
+typedef struct ssm_scan_options {
+    const float *dt_bias;
+    int32_t dt_softplus;
+    int32_t dt_limit;
+    float dt_min;
+    float dt_max;
+    const void *z;
+    const float *h0;
+    float *h_final;
+} ssm_scan_options_t;
+
+/*
+ * ssm_scan_fwd / ssm_scan_fwd_bf16 with options.  input_bf16 selects the
+ * element type of x, delta, B, C and z (0 = fp32, else bf16); `opts` may be
+ * NULL (no option).  Alignment: x, delta, B, C, z to their element size;
+ * dt_bias, h0, h_final to 4 bytes (SSM_ERR_ALIGNMENT otherwise).
+ */
+SSM_API ssm_status_t ssm_scan_fwd_ex(const void *x, const void *delta, const float *A,
+                                     const void *B, const void *C, const float *D,
+                                     float *y, int64_t Bs, int64_t L, int64_t ED,
+                                     int64_t N, int input_bf16,
+                                     const ssm_scan_options_t *opts, void *stream);
+
+/*
+ * ssd_chunk_scan_fwd with options (same arguments, support and scratch
+ * rules; z is bf16 and 16-byte aligned; `opts` may be NULL).
+ */
+SSM_API ssm_status_t ssd_chunk_scan_fwd_ex(const void *x, const void *dt,
+                                           const float *A_head, const void *B,
+                                           const void *C, const float *D, float *y,
+                                           int64_t Bs, int64_t L, int64_t H, int64_t P,
+                                           int64_t N, int64_t chunk, int bidirectional,
+                                           const ssm_scan_options_t *opts, void *stream);
 
 /*
  * Synchronise `stream` and report whether a kernel of this library running on

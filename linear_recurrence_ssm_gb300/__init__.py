@@ -8,17 +8,23 @@ the library is missing or fails to load, importing a function raises.
 
 Functions
 ---------
-ssm_scan_fwd(x, delta, A, B, C, D=None, y=None)
+ssm_scan_fwd(x, delta, A, B, C, D=None, y=None, **options)
     Diagonal-A selective scan (shape API of selective_scan in "scan output is
     different between sequential and parallel versions", mamba.py issue 26).
     x, delta: (Bs, L, ED); A: (ED, N) fp32; B, C: (Bs, L, N); D: (ED) fp32.
     fp32 inputs call the C ``ssm_scan_fwd``; bf16 inputs call
     ``ssm_scan_fwd_bf16``.  Returns y (Bs, L, ED) fp32.
-ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, bidirectional=False, y=None)
+ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, bidirectional=False, y=None, **options)
     Chunked scalar-decay scan ("Some questions of Bi-Mamba2 and Hydra",
     Bi-Mamba2 issue 1).  x: (Bs, L, H, P) bf16; dt: (Bs, L, H) bf16;
     A_head: (H) fp32; B, C: (Bs, L, N) or (Bs, L, 1, N) bf16; D: (H) fp32.
     Returns y (Bs, L, H, P) fp32.
+
+Options (either function; any of them selects the ``*_ex`` C entry point):
+``dt_bias`` (ED or H, fp32), ``dt_softplus``, ``dt_limit=(lo, hi)``, ``z``
+(shaped and typed like x), ``h0`` (fp32 initial state, (Bs, ED, N) or
+(Bs, H, P, N)) and ``return_final_state`` (the call then returns
+``(y, h_final)``).
 """
 from __future__ import annotations
 
@@ -28,7 +34,7 @@ import os
 from . import _build
 
 __all__ = ["ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssd_chunk_scan_fwd", "ssm_check_device_errors",
-           "ssm_scan_fwd_plan",
+           "ssm_scan_fwd_plan", "ScanOptions",
            "SsmError", "library", "build", "status_string", "STATUS"]
 
 STATUS = {
@@ -46,12 +52,59 @@ SIGNATURES = {
     "ssd_chunk_scan_fwd_noalloc": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP], ctypes.c_int),
     "ssm_scan_fwd_plan": ([_I64] * 4 + [ctypes.c_int] + [ctypes.POINTER(ctypes.c_int32)] * 3,
                           ctypes.c_int),
+    "ssm_scan_fwd_ex": ([_VP] * 7 + [_I64] * 4 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
+    "ssd_chunk_scan_fwd_ex": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
     "ssm_check_device_errors": ([_VP], ctypes.c_int),
     "ssm_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "ssm_version": ([], ctypes.c_int),
 }
 
 _lib = None
+
+
+class ScanOptions(ctypes.Structure):
+    """ssm_scan_options_t of include/ssm_scan.h."""
+    _fields_ = [("dt_bias", _VP), ("dt_softplus", ctypes.c_int32), ("dt_limit", ctypes.c_int32),
+                ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float), ("z", _VP),
+                ("h0", _VP), ("h_final", _VP)]
+
+
+_OPTION_KEYS = ("dt_bias", "dt_softplus", "dt_limit", "z", "h0", "return_final_state")
+
+
+def _options(x, channels, state_shape, dev, dt_bias=None, dt_softplus=False, dt_limit=None,
+             z=None, h0=None, return_final_state=False):
+    """Validate the options and build (ScanOptions, h_final tensor or None, keep-alive list)."""
+    import torch
+    o = ScanOptions()
+    keep = []
+    if dt_bias is not None:
+        _check(dt_bias, "dt_bias", (torch.float32,), dev, (1,))
+        if dt_bias.shape[0] != channels:
+            raise ValueError("dt_bias must have %d entries" % channels)
+        o.dt_bias = dt_bias.data_ptr()
+        keep.append(dt_bias)
+    o.dt_softplus = 1 if dt_softplus else 0
+    if dt_limit is not None:
+        o.dt_limit = 1
+        o.dt_min, o.dt_max = float(dt_limit[0]), float(dt_limit[1])
+    if z is not None:
+        _check(z, "z", (x.dtype,), dev)
+        if z.shape != x.shape:
+            raise ValueError("z must have the shape of x")
+        o.z = z.data_ptr()
+        keep.append(z)
+    if h0 is not None:
+        _check(h0, "h0", (torch.float32,), dev)
+        if tuple(h0.shape) != tuple(state_shape):
+            raise ValueError("h0 must have shape %s" % (tuple(state_shape),))
+        o.h0 = h0.data_ptr()
+        keep.append(h0)
+    hf = None
+    if return_final_state:
+        hf = torch.empty(state_shape, dtype=torch.float32, device=dev)
+        o.h_final = hf.data_ptr()
+    return o, hf, keep
 
 
 class SsmError(RuntimeError):
@@ -112,8 +165,9 @@ def _check(t, name, dtypes, dev, ndim=None):
         raise ValueError("%s must have %s dims, got %d" % (name, ndim, t.dim()))
 
 
-def ssm_scan_fwd(x, delta, A, B, C, D=None, y=None):
-    """Diagonal selective scan on the current CUDA stream; returns y (fp32)."""
+def ssm_scan_fwd(x, delta, A, B, C, D=None, y=None, **options):
+    """Diagonal selective scan on the current CUDA stream; returns y (fp32),
+    or (y, h_final) with ``return_final_state=True``."""
     import torch
     dev = x.device
     if dev.type != "cuda":
@@ -131,6 +185,17 @@ def ssm_scan_fwd(x, delta, A, B, C, D=None, y=None):
     if y is None:
         y = torch.empty((Bs, L, ED), dtype=torch.float32, device=dev)
     _check(y, "y", (torch.float32,), dev, (3,))
+    bad = set(options) - set(_OPTION_KEYS)
+    if bad:
+        raise TypeError("unknown options: %s" % sorted(bad))
+    if options:
+        o, hf, keep = _options(x, ED, (Bs, ED, N), dev, **options)
+        st = library().ssm_scan_fwd_ex(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                       _ptr(y), Bs, L, ED, N, int(x.dtype == torch.bfloat16),
+                                       ctypes.byref(o), _stream(dev))
+        if st != 0:
+            raise SsmError("ssm_scan_fwd_ex", st)
+        return (y, hf) if options.get("return_final_state") else y
     name = "ssm_scan_fwd" if x.dtype == torch.float32 else "ssm_scan_fwd_bf16"
     fn = getattr(library(), name)
     st = fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y),
@@ -140,17 +205,18 @@ def ssm_scan_fwd(x, delta, A, B, C, D=None, y=None):
     return y
 
 
-def ssm_scan_fwd_bf16(x, delta, A, B, C, D=None, y=None):
+def ssm_scan_fwd_bf16(x, delta, A, B, C, D=None, y=None, **options):
     """Same as ``ssm_scan_fwd`` but requires bf16 x, delta, B, C."""
     import torch
     if x.dtype != torch.bfloat16:
         raise TypeError("ssm_scan_fwd_bf16 takes bf16 x, delta, B, C")
-    return ssm_scan_fwd(x, delta, A, B, C, D, y)
+    return ssm_scan_fwd(x, delta, A, B, C, D, y, **options)
 
 
 def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
-                       bidirectional: bool = False, y=None):
-    """Chunked scalar-decay scan on the current CUDA stream; returns y (fp32)."""
+                       bidirectional: bool = False, y=None, **options):
+    """Chunked scalar-decay scan on the current CUDA stream; returns y (fp32),
+    or (y, h_final) with ``return_final_state=True``."""
     import torch
     dev = x.device
     if dev.type != "cuda":
@@ -174,6 +240,18 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
     if y is None:
         y = torch.empty((Bs, L, H, P), dtype=torch.float32, device=dev)
     _check(y, "y", (torch.float32,), dev, (4,))
+    bad = set(options) - set(_OPTION_KEYS)
+    if bad:
+        raise TypeError("unknown options: %s" % sorted(bad))
+    if options:
+        o, hf, keep = _options(x, H, (Bs, H, P, N), dev, **options)
+        st = library().ssd_chunk_scan_fwd_ex(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C),
+                                             _ptr(D), _ptr(y), Bs, L, H, P, N, int(chunk),
+                                             int(bool(bidirectional)), ctypes.byref(o),
+                                             _stream(dev))
+        if st != 0:
+            raise SsmError("ssd_chunk_scan_fwd_ex", st)
+        return (y, hf) if options.get("return_final_state") else y
     st = library().ssd_chunk_scan_fwd(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D),
                                       _ptr(y), Bs, L, H, P, N, int(chunk), int(bool(bidirectional)),
                                       _stream(dev))

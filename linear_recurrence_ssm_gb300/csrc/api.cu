@@ -14,6 +14,10 @@ template <typename Tin>
 cudaError_t launch(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
                    const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
                    int num_sms, cudaStream_t st);
+template <typename Tin>
+cudaError_t launch_ext(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
+                       const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
+                       int num_sms, const ScanOpts &ex, cudaStream_t st);
 struct Plan {
     int S, G, K, seg_len;
 };
@@ -23,7 +27,7 @@ namespace ssd {
 cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
                    const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
                    int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N, int64_t chunk,
-                   bool bidirectional, int num_sms, cudaStream_t st);
+                   bool bidirectional, int num_sms, cudaStream_t st, const ScanOpts *opt);
 cudaError_t take_device_error(unsigned int *out);
 size_t noalloc_scratch_needed(int64_t Bs, int64_t L, int64_t H, int64_t N, bool bidirectional);
 cudaError_t launch_noalloc(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
@@ -93,10 +97,19 @@ ssm_status_t from_cuda(cudaError_t e) {
     return SSM_ERR_CUDA;
 }
 
+// Options present, and their pointers aligned to `zsize` (z) / 4 bytes.
+ssm_status_t check_options(const ssm_scan_options_t *o, size_t zsize) {
+    if (!o) return SSM_OK;
+    if ((o->z && !aligned(o->z, zsize)) || (o->dt_bias && !aligned(o->dt_bias, 4)) ||
+        (o->h0 && !aligned(o->h0, 4)) || (o->h_final && !aligned(o->h_final, 4)))
+        return SSM_ERR_ALIGNMENT;
+    return SSM_OK;
+}
+
 template <typename Tin>
 ssm_status_t diag_entry(const Tin *x, const Tin *delta, const float *A, const Tin *B, const Tin *C,
                         const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
-                        void *stream) {
+                        void *stream, const ssm_scan_options_t *opts = nullptr) {
     if (!x || !delta || !A || !B || !C || !y) return SSM_ERR_INVALID_ARG;
     if (!sizes_ok({Bs, L, ED}) || !sizes_ok({Bs, L, N}) || !sizes_ok({ED, N}))
         return SSM_ERR_INVALID_ARG;
@@ -106,9 +119,18 @@ ssm_status_t diag_entry(const Tin *x, const Tin *delta, const float *A, const Ti
     if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
         !aligned(A, 4) || !aligned(y, 4) || (D && !aligned(D, 4)))
         return SSM_ERR_ALIGNMENT;
-    DeviceInfo dev;
-    ssm_status_t s = current_device(&dev);
+    ssm_status_t s = check_options(opts, es);
     if (s != SSM_OK) return s;
+    DeviceInfo dev;
+    s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    if (opts) {
+        const ssm::ScanOpts ex{opts->dt_bias, opts->z, opts->h0, opts->h_final,
+                               opts->dt_min, opts->dt_max, opts->dt_softplus, opts->dt_limit};
+        return from_cuda(ssm::diag::launch_ext<Tin>(x, delta, A, B, C, D, y, Bs, L, ED, N,
+                                                    dev.num_sms, ex,
+                                                    static_cast<cudaStream_t>(stream)));
+    }
     return from_cuda(ssm::diag::launch<Tin>(x, delta, A, B, C, D, y, Bs, L, ED, N, dev.num_sms,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -153,7 +175,7 @@ ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt, const float *A_he
                                       A_head, static_cast<const bf *>(B),
                                       static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
                                       bidirectional != 0, dev.num_sms,
-                                      static_cast<cudaStream_t>(stream)));
+                                      static_cast<cudaStream_t>(stream), nullptr));
 }
 
 ssm_status_t ssd_chunk_scan_fwd_noalloc(const void *x, const void *dt, const float *A_head,
@@ -180,6 +202,53 @@ ssm_status_t ssd_chunk_scan_fwd_noalloc(const void *x, const void *dt, const flo
                                               static_cast<const bf *>(C), D, y, Bs, L, H, P, N,
                                               bidirectional != 0,
                                               static_cast<cudaStream_t>(stream)));
+}
+
+ssm_status_t ssm_scan_fwd_ex(const void *x, const void *delta, const float *A, const void *B,
+                             const void *C, const float *D, float *y, int64_t Bs, int64_t L,
+                             int64_t ED, int64_t N, int input_bf16,
+                             const ssm_scan_options_t *opts, void *stream) {
+    using bf = __nv_bfloat16;
+    if (input_bf16)
+        return diag_entry<bf>(static_cast<const bf *>(x), static_cast<const bf *>(delta), A,
+                              static_cast<const bf *>(B), static_cast<const bf *>(C), D, y, Bs, L,
+                              ED, N, stream, opts);
+    return diag_entry<float>(static_cast<const float *>(x), static_cast<const float *>(delta), A,
+                             static_cast<const float *>(B), static_cast<const float *>(C), D, y, Bs,
+                             L, ED, N, stream, opts);
+}
+
+ssm_status_t ssd_chunk_scan_fwd_ex(const void *x, const void *dt, const float *A_head,
+                                   const void *B, const void *C, const float *D, float *y,
+                                   int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                                   int64_t chunk, int bidirectional,
+                                   const ssm_scan_options_t *opts, void *stream) {
+    if (!opts)
+        return ssd_chunk_scan_fwd(x, dt, A_head, B, C, D, y, Bs, L, H, P, N, chunk, bidirectional,
+                                  stream);
+    if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_INVALID_ARG;
+    if (!sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, N}) || chunk < 1) return SSM_ERR_INVALID_ARG;
+    if (P != 64) return SSM_ERR_UNSUPPORTED;
+    if (N != 64 && N != 128) return SSM_ERR_UNSUPPORTED;
+    if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
+    if (L > INT_MAX || H > 65535 || Bs > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    if (bidirectional && (opts->h0 || opts->h_final)) return SSM_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+        !aligned(dt, 2) || !aligned(A_head, 4) || (D && !aligned(D, 4)))
+        return SSM_ERR_ALIGNMENT;
+    ssm_status_t s = check_options(opts, 16);
+    if (s != SSM_OK) return s;
+    DeviceInfo dev;
+    s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    using bf = __nv_bfloat16;
+    const ssm::ScanOpts o{opts->dt_bias, opts->z, opts->h0, opts->h_final,
+                          opts->dt_min, opts->dt_max, opts->dt_softplus, opts->dt_limit};
+    return from_cuda(ssm::ssd::launch(static_cast<const bf *>(x), static_cast<const bf *>(dt),
+                                      A_head, static_cast<const bf *>(B),
+                                      static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
+                                      bidirectional != 0, dev.num_sms,
+                                      static_cast<cudaStream_t>(stream), &o));
 }
 
 ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED, int64_t N, int input_bf16,

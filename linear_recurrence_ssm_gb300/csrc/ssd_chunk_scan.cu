@@ -94,7 +94,18 @@ struct Params {
     float *y;
     uint8_t *rstate;   // reverse entering states, [Bs*H][nc][NB * kStateRegion] (bidirectional)
     int L, H, nc, bidir;
+    // options (kernels built with them only): dt <- clamp(softplus(dt + bias)),
+    // y <- y * silu(z), initial / final state (Bs, H, P, N) fp32
+    const float *dt_bias;
+    const __nv_bfloat16 *z;
+    const float *h0;
+    float *h_final;
+    float dt_min, dt_max;
+    int dt_softplus, dt_limit;
 };
+
+// Scan options: see ScanOpts (z is bf16 here; states are (Bs, H, P, N)).
+using Options = ScanOpts;
 
 // Byte offset of element (row, col) of a 128-byte-swizzled tile whose rows
 // are 128 bytes (64 bf16): the 16-byte chunk index is XORed with row % 8.
@@ -184,7 +195,7 @@ __device__ __forceinline__ void store_state_bf16(uint8_t (*img)[kStateRegion], i
         }                                                                                 \
     } while (0)
 
-template <int NB>
+template <int NB, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
@@ -209,6 +220,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     const float Dh = prm.D ? prm.D[h] : 0.0f;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const size_t rstride = size_t(NB) * kStateRegion;
+    const bool has_h0 = EXT && prm.h0 != nullptr;
 
     if (tid == 0) {
         abort_flag = 0;
@@ -273,9 +285,18 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             bulk_load(sm.R, prm.rstate + (size_t(bh) * nc + c) * rstride, uint32_t(rstride),
                       &sm.bar_c);
     };
+    const float dbias = (EXT && prm.dt_bias) ? prm.dt_bias[h] : 0.0f;
     auto load_dt = [&](int c) {
         const int r = c * kQ + row;
-        return r < L ? __bfloat162float(prm.dt[(int64_t(b) * L + r) * prm.H + h]) : 0.0f;
+        if (r >= L) return 0.0f;   // rows past L: no decay, no input
+        float d = __bfloat162float(prm.dt[(int64_t(b) * L + r) * prm.H + h]);
+        if (EXT) {
+            d += dbias;
+            // log(1 + e^d); above 20 the correction is below fp32 resolution
+            if (prm.dt_softplus) d = d > 20.0f ? d : log1pf(__expf(d));
+            if (prm.dt_limit) d = fminf(fmaxf(d, prm.dt_min), prm.dt_max);
+        }
+        return d;
     };
     // Per-tile cumulative sums of dt * A (log2 units) into the vectors of
     // parity p, and the column factors of the decay mask.  Rows past L have
@@ -397,6 +418,14 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     // update, so that the mask pass of tile c + 1 can start at once.
 #pragma unroll
     for (int p = 0; p < 32; ++p) st[p] = 0.0f;
+    if (has_h0 && row < N) {
+        // initial state, rows [32 wg, 32 wg + 32) of column n = row
+        const float *src = prm.h0 + (size_t(bh) * kP + wg * 32) * N + row;
+#pragma unroll
+        for (int p = 0; p < 32; ++p) st[p] = src[size_t(p) * N];
+        store_state_bf16<NB>(sm.S, row, wg * 32, *reinterpret_cast<float(*)[32]>(st));
+    }
+    fence_proxy_async_smem();
     if (tid == 0) {
         load_x(0, 0);
         load_c(0, bidir && nc > 1);
@@ -419,14 +448,14 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     if (tid == 0) {
         tc_fence_after_sync();
         issue_g(0);
-        issue_z(false, bidir && nc > 1);
+        issue_z(has_h0, bidir && nc > 1);
         mma_commit(&sm.bar_g);
     }
     for (int c = 0; c < nc; ++c) {
         const int c0 = c * kQ;
         const int par = c & 1;      // buffers and per-tile vectors of tile c
         const bool more = c + 1 < nc;
-        const bool has_s = c > 0;
+        const bool has_s = c > 0 || has_h0;
         const bool has_r = bidir && (c < nc - 1);
         // The previous tile's output rows staged in the mask buffer must have
         // been read by their store before the mask pass overwrites it.
@@ -528,6 +557,16 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             issue_state_mma(par);
             mma_commit(&sm.bar_m2);
         }
+        // The gate's row for the epilogue (optional), loaded while the MMAs run.
+        uint4 zq[4];
+        const bool gate = EXT && prm.z != nullptr;
+        if (gate) {
+            const int r = c0 + row;
+            const uint4 *zp = reinterpret_cast<const uint4 *>(
+                prm.z + ((int64_t(b) * L + (r < L ? r : L - 1)) * prm.H + h) * kP + wg * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) zq[j] = zp[j];
+        }
         // Meanwhile: vectors of tile c + 1, then its G behind them.
         if (more) {
             tile_prep(dv, par ^ 1, &tot_nxt);
@@ -574,6 +613,18 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                 if (has_r) v = fmaf(er, __uint_as_float(zr[j]), v);
                 out[j] = v;
             }
+            if (gate) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t w4[4] = {zq[j].x, zq[j].y, zq[j].z, zq[j].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 zz = unpack_bf16(w4[k]);
+                        out[8 * j + 2 * k] *= zz.x / (1.0f + __expf(-zz.x));
+                        out[8 * j + 2 * k + 1] *= zz.y / (1.0f + __expf(-zz.y));
+                    }
+                }
+            }
             // Stage the row in the (now free) mask buffer as a 128-byte-swizzled
             // [128 rows][32 fp32] tile per warpgroup; one TMA store per tile
             // writes it out coalesced (rows past L are clipped by the store).
@@ -609,6 +660,13 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             }
         }
         tot_cur = tot_nxt;
+    }
+    // Final state: after the last tile st holds the state after row L - 1
+    // (rows past L have dt = 0 and leave it unchanged).
+    if (EXT && prm.h_final != nullptr && row < N) {
+        float *dst = prm.h_final + (size_t(bh) * kP + wg * 32) * N + row;
+#pragma unroll
+        for (int p = 0; p < 32; ++p) dst[size_t(p) * N] = st[p];
     }
     }
 
@@ -666,7 +724,8 @@ template <int NB>
 static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A,
                              const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D,
                              float *y, int64_t Bs, int64_t L, int64_t H, bool bidir,
-                             cudaStream_t stream, uint8_t *fixed_scratch = nullptr) {
+                             cudaStream_t stream, uint8_t *fixed_scratch = nullptr,
+                             const Options *opt = nullptr) {
     constexpr int N = NB * 64;
     CUtensorMap tmC, tmB, tmX, tmY;
     const cuuint64_t dbc[3] = {cuuint64_t(N), cuuint64_t(L), cuuint64_t(Bs)};
@@ -692,12 +751,22 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
     prm.H = int(H);
     prm.nc = int((L + kQ - 1) / kQ);
     prm.bidir = bidir ? 1 : 0;
+    const Options none{};
+    const Options &o = opt ? *opt : none;
+    prm.dt_bias = o.dt_bias;
+    prm.z = static_cast<const __nv_bfloat16 *>(o.z);
+    prm.h0 = o.h0;
+    prm.h_final = o.h_final;
+    prm.dt_min = o.dt_min;
+    prm.dt_max = o.dt_max;
+    prm.dt_softplus = o.dt_softplus;
+    prm.dt_limit = o.dt_limit;
     const int64_t grid = Bs * H;
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
     const size_t smem = sizeof(Smem<NB>) + 1024;
     static_assert(sizeof(Smem<NB>) + 1024 <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
-    auto kern = ssd_chunk_scan_kernel<NB>;
+    auto kern = opt ? ssd_chunk_scan_kernel<NB, true> : ssd_chunk_scan_kernel<NB, false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (err != cudaSuccess) return err;
 
@@ -722,14 +791,14 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
 cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
                    const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
                    int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N, int64_t chunk,
-                   bool bidirectional, int num_sms, cudaStream_t stream) {
+                   bool bidirectional, int num_sms, cudaStream_t stream, const Options *opt) {
     (void)num_sms;
     (void)chunk;
     if (P != kP) return cudaErrorNotSupported;
     if (N == 64)
-        return launch_nb<1>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream);
+        return launch_nb<1>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream, nullptr, opt);
     if (N == 128)
-        return launch_nb<2>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream);
+        return launch_nb<2>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream, nullptr, opt);
     return cudaErrorNotSupported;
 }
 

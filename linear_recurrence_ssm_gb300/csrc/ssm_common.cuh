@@ -12,6 +12,19 @@
 
 namespace ssm {
 
+// ---- options of the scans (host and device) -------------------------------
+// delta <- clamp(softplus(delta + dt_bias)), y <- y * silu(z), initial and
+// final states; null pointers / zero flags mean "not used".  The public
+// ssm_scan_options_t is copied into this form by the entry points.
+struct ScanOpts {
+    const float *dt_bias;   // (ED) diagonal / (H) SSD
+    const void *z;          // x-shaped gate, element type of x
+    const float *h0;        // initial state, fp32
+    float *h_final;         // final state out, fp32
+    float dt_min, dt_max;
+    int dt_softplus, dt_limit;
+};
+
 // ---- element conversion ---------------------------------------------------
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }

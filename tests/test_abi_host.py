@@ -107,3 +107,42 @@ def test_valid_call_without_device_reports_no_device():
     # the same large call without the reverse scan needs no scratch: passes the size check
     assert lrs.library().ssd_chunk_scan_fwd_noalloc(*([P] * 7), 64, 4096, 32, 64, 128, 256, 0,
                                                     None) == 6
+
+
+def _opts(**kw):
+    o = lrs.ScanOptions()
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+def test_option_entry_points_reject_bad_arguments():
+    lib = lrs.library()
+    ptrs = [P] * 7
+    ptrs[1] = None
+    assert lib.ssm_scan_fwd_ex(*ptrs, 1, 8, 8, 4, 1, ctypes.byref(_opts()), None) == 1
+    # misaligned option pointers
+    assert lib.ssm_scan_fwd_ex(*([P] * 7), 1, 8, 8, 4, 1, ctypes.byref(_opts(z=P_ODD)), None) == 3
+    assert lib.ssm_scan_fwd_ex(*([P] * 7), 1, 8, 8, 4, 0,
+                               ctypes.byref(_opts(h_final=0x10002)), None) == 3
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 0,
+                                     ctypes.byref(_opts(z=0x10008)), None) == 3
+    # state input/output is defined for a single direction only
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1,
+                                     ctypes.byref(_opts(h0=P)), None) == 2
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1,
+                                     ctypes.byref(_opts(h_final=P)), None) == 2
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 32, 64, 128, 0,
+                                     ctypes.byref(_opts()), None) == 2
+
+
+def test_option_calls_without_device_report_no_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    lib = lrs.library()
+    o = _opts(dt_softplus=1, z=P, h0=P, h_final=P)
+    assert lib.ssm_scan_fwd_ex(*([P] * 7), 1, 8, 8, 4, 1, ctypes.byref(o), None) == 6
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 0, ctypes.byref(o), None) == 6
+    # a NULL options pointer is the plain call
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1, None, None) == 6

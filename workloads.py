@@ -110,6 +110,23 @@ def ssd_inputs(Bs: int, L: int, H: int, P: int, N: int, dtype: str = "bf16", see
                 B=_cast(B, dtype), C=_cast(C, dtype), D=D.contiguous() if with_D else None)
 
 
+def option_inputs(x_shape, delta_shape, channels: int, state_shape, dtype: str = "bf16",
+                  seed: int = 0):
+    """Seeded inputs of the scan options on the CPU: dict(delta_raw, dt_bias, z, h0).
+
+    delta_raw ~ N(0, 1) - 1 (delta / dt before the optional bias, softplus and
+    clamp), shaped ``delta_shape``; dt_bias ~ 0.5 N(0, 1) per channel (ED or H);
+    z ~ N(0, 1) shaped like x; h0 ~ 0.5 N(0, 1), fp32, shaped ``state_shape``.
+    """
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    delta_raw = torch.randn(*delta_shape, generator=g) - 1.0
+    dt_bias = 0.5 * torch.randn(channels, generator=g)
+    z = torch.randn(*x_shape, generator=g)
+    h0 = 0.5 * torch.randn(*state_shape, generator=g)
+    return dict(delta_raw=_cast(delta_raw, dtype), dt_bias=dt_bias.contiguous(),
+                z=_cast(z, dtype), h0=h0.contiguous())
+
+
 def workload_inputs(w: Workload):
     s = w.shape
     if w.kind == "diag":
