@@ -60,41 +60,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
-// Plain arrival (count 1) on an mbarrier.
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// ---- per-warpgroup register budgets ----------------------------------------------
-// Every thread of a warpgroup executes these; the new count is a multiple of 8.
-template <uint32_t R>
-__device__ __forceinline__ void regs_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
-}
-template <uint32_t R>
-__device__ __forceinline__ void regs_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
-}
-
-// ---- named barriers among a subset of the CTA's warps -------------------------
-// Barrier `id` (1..15) over the first `n` threads (whole warps) that use it.
-__device__ __forceinline__ void named_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-// The same, returning whether any participating thread passed `pred` true.
-__device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred p, q;\n"
-        " setp.ne.u32 p, %1, 0;\n"
-        " bar.red.or.pred q, %2, %3, p;\n"
-        " selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"(uint32_t(pred)), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
-}
-
 // ---- proxy / tcgen05 fences -----------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tensor core) before a barrier that precedes their use.
