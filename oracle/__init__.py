@@ -67,7 +67,7 @@ def _load(path: str | None = None):
         lib.oracle_diag_scan_ex_range.argtypes = ([dp] * 7 + [i64] * 4 + [dp, ctypes.c_int, ctypes.c_int,
                                                   dbl, dbl, dp, dp, dp, i64, i64, ctypes.c_int])
         lib.oracle_diag_scan_ex_range.restype = None
-        lib.oracle_ssd_scan_ex_range.argtypes = ([dp] * 7 + [i64] * 5 + [ctypes.c_int, dp, ctypes.c_int,
+        lib.oracle_ssd_scan_ex_range.argtypes = ([dp] * 7 + [i64] * 6 + [ctypes.c_int, dp, ctypes.c_int,
                                                  ctypes.c_int, dbl, dbl, dp, dp, dp, i64, i64,
                                                  ctypes.c_int])
         lib.oracle_ssd_scan_ex_range.restype = None
@@ -146,8 +146,9 @@ def ssd_scan(x, dt, A_head, B, C, D=None, bidirectional: bool = False,
              return_final_state: bool = False):
     """Sequential scalar-per-head (SSD) scan in fp64, optionally bidirectional.
 
-    x: (Bs, L, H, P); dt: (Bs, L, H); A_head: (H); B, C: (Bs, L, N) or
-    (Bs, L, 1, N) (one group shared by all heads); D: (H) or None.
+    x: (Bs, L, H, P); dt: (Bs, L, H); A_head: (H); B, C: (Bs, L, N) (one
+    group shared by all heads) or (Bs, L, G, N) with G dividing H (head h
+    reads group h // (H // G)); D: (H) or None.
     Returns y: (Bs, L, H, P) fp64.  ``units=(u0, u1)`` computes only the
     flattened (b, h) pairs in [u0, u1) (the rest of y is NaN).
     Options as in ``diag_scan``, per head: ``dt_bias`` (H), ``z`` (Bs, L, H, P),
@@ -156,13 +157,13 @@ def ssd_scan(x, dt, A_head, B, C, D=None, bidirectional: bool = False,
     """
     x, dt, A_head, B, C, D, dt_bias, z, h0 = map(_f64, (x, dt, A_head, B, C, D, dt_bias, z, h0))
     Bs, L, H, P = x.shape
-    if B.ndim == 4:
-        assert B.shape[2] == 1 and C.shape[2] == 1, "one group of B, C shared by all heads"
-        B = np.ascontiguousarray(B[:, :, 0, :])
-        C = np.ascontiguousarray(C[:, :, 0, :])
-    N = B.shape[-1]
+    if B.ndim == 3:
+        B, C = B[:, :, None, :], C[:, :, None, :]
+    G, N = B.shape[2], B.shape[3]
+    assert G >= 1 and H % G == 0, "heads must split evenly into the groups of B, C"
     assert dt.shape == (Bs, L, H) and A_head.shape == (H,)
-    assert B.shape == (Bs, L, N) and C.shape == (Bs, L, N)
+    assert B.shape == (Bs, L, G, N) and C.shape == (Bs, L, G, N)
+    B, C = np.ascontiguousarray(B), np.ascontiguousarray(C)
     assert D is None or D.shape == (H,)
     assert dt_bias is None or dt_bias.shape == (H,)
     assert z is None or z.shape == x.shape
@@ -174,7 +175,7 @@ def ssd_scan(x, dt, A_head, B, C, D=None, bidirectional: bool = False,
     u0, u1 = units if units else (0, Bs * H)
     lim, lo, hi = _limit(dt_limit)
     _load(library).oracle_ssd_scan_ex_range(
-        _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D), _ptr(y), Bs, L, H, P, N,
+        _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D), _ptr(y), Bs, L, H, P, N, G,
         int(bool(bidirectional)), _ptr(dt_bias), int(bool(dt_softplus)), lim, lo, hi, _ptr(z),
         _ptr(h0), _ptr(hf), u0, u1, nthreads)
     return (y, hf) if return_final_state else y

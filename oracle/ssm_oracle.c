@@ -43,6 +43,10 @@
  *   h_{-1} = h0 instead of 0; h_final = h_{L-1}        (if given / asked)
  * State I/O is defined for the single-direction scans only.
  *
+ * Groups of B, C (ngroups in the chunked scan's interface): B, C have shape
+ * (Bs, L, G, N) and head h reads group h / (H / G); G = 1 is one group
+ * shared by all heads.
+ *
  * All arrays are dense row-major (last index fastest) fp64.
  */
 #include <math.h>
@@ -145,20 +149,21 @@ void oracle_diag_scan(const double *x, const double *delta, const double *A,
  * y (accumulating).  `rev` = 0 walks t = 0..L-1; `rev` = 1 walks the
  * flipped sequence, i.e. t = L-1..0, which is F applied to flip(inputs)
  * and flipped back.  `dth` is this head's preprocessed dt, (L).
- * x, y: (Bs, L, H, P); B, C: (Bs, L, N).  `state` (P x N) holds the
+ * x, y: (Bs, L, H, P); B, C: (Bs, L, G, N), group g.  `state` (P x N) holds the
  * entering state on entry and the final state on return.
  */
 static void ssd_one_direction(const double *x, const double *dth, double Ah,
                               const double *B, const double *C, double *y,
                               int64_t b, int64_t h, int64_t L, int64_t H,
-                              int64_t P, int64_t N, int rev, double *state) {
+                              int64_t P, int64_t N, int64_t G, int64_t g, int rev,
+                              double *state) {
     for (int64_t k = 0; k < L; ++k) {
         const int64_t t = rev ? (L - 1 - k) : k;
         const double d = dth[t];
         const double a = exp(d * Ah);
         const double *xt = x + ((b * L + t) * H + h) * P;
-        const double *Bt = B + (b * L + t) * N;
-        const double *Ct = C + (b * L + t) * N;
+        const double *Bt = B + ((b * L + t) * G + g) * N;
+        const double *Ct = C + ((b * L + t) * G + g) * N;
         double *yt = y + ((b * L + t) * H + h) * P;
         for (int64_t p = 0; p < P; ++p) {
             double acc = 0.0;
@@ -176,22 +181,24 @@ static void ssd_one_direction(const double *x, const double *dth, double Ah,
  * Scalar-per-head (SSD) scan, optionally bidirectional, for the (b, h)
  * pairs in [u_begin, u_end) of the flattened index u = b * H + h.
  * x, y, z: (Bs, L, H, P); dt: (Bs, L, H); A_head, D, dt_bias: (H) (D and
- * dt_bias may be NULL); B, C: (Bs, L, N) (one group shared by all heads);
+ * dt_bias may be NULL); B, C: (Bs, L, G, N), G dividing H;
  * h0, h_final: (Bs, H, P, N) or NULL (single direction only).
  */
 void oracle_ssd_scan_ex_range(const double *x, const double *dt, const double *A_head,
                               const double *B, const double *C, const double *D, double *y,
                               int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
-                              int bidirectional, const double *dt_bias, int dt_softplus,
+                              int64_t G, int bidirectional, const double *dt_bias, int dt_softplus,
                               int dt_limit, double dt_min, double dt_max, const double *z,
                               const double *h0, double *h_final, int64_t u_begin,
                               int64_t u_end, int nthreads) {
     set_threads(nthreads);
     if (u_end > Bs * H) u_end = Bs * H;
     if (bidirectional && (h0 || h_final)) return;   /* not defined */
+    if (G < 1 || H % G != 0) return;                 /* heads split evenly into groups */
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t u = u_begin; u < u_end; ++u) {
         const int64_t b = u / H, h = u % H;
+        const int64_t g = h / (H / G);   /* this head's group of B, C */
         double *state = (double *)malloc((size_t)(P * N) * sizeof(double));
         /* this head's preprocessed dt */
         double *dtp = (double *)malloc((size_t)L * sizeof(double));
@@ -204,12 +211,12 @@ void oracle_ssd_scan_ex_range(const double *x, const double *dt, const double *A
                 y[o + p] = D ? D[h] * x[o + p] : 0.0;
         }
         for (int64_t i = 0; i < P * N; ++i) state[i] = h0 ? h0[u * P * N + i] : 0.0;
-        ssd_one_direction(x, dtp, A_head[h], B, C, y, b, h, L, H, P, N, 0, state);
+        ssd_one_direction(x, dtp, A_head[h], B, C, y, b, h, L, H, P, N, G, g, 0, state);
         if (h_final)
             for (int64_t i = 0; i < P * N; ++i) h_final[u * P * N + i] = state[i];
         if (bidirectional) {
             memset(state, 0, (size_t)(P * N) * sizeof(double));
-            ssd_one_direction(x, dtp, A_head[h], B, C, y, b, h, L, H, P, N, 1, state);
+            ssd_one_direction(x, dtp, A_head[h], B, C, y, b, h, L, H, P, N, G, g, 1, state);
         }
         if (z) {
             for (int64_t t = 0; t < L; ++t) {
@@ -228,7 +235,7 @@ void oracle_ssd_scan_range(const double *x, const double *dt,
                            int64_t Bs, int64_t L, int64_t H, int64_t P,
                            int64_t N, int bidirectional, int64_t u_begin,
                            int64_t u_end, int nthreads) {
-    oracle_ssd_scan_ex_range(x, dt, A_head, B, C, D, y, Bs, L, H, P, N, bidirectional, NULL, 0, 0,
+    oracle_ssd_scan_ex_range(x, dt, A_head, B, C, D, y, Bs, L, H, P, N, 1, bidirectional, NULL, 0, 0,
                              0.0, 0.0, NULL, NULL, NULL, u_begin, u_end, nthreads);
 }
 
