@@ -187,6 +187,10 @@ SSM_API ssm_status_t ssd_chunk_scan_fwd_noalloc(const void *x, const void *dt,
  *   h0, h_final : fp32 device arrays, (Bs, ED, N) for the diagonal scan,
  *             (Bs, H, P, N) for SSD (state matrix per head: row p, column
  *             n); caller-owned; h_final is fully written.
+ *   ngroups : SSD only -- B and C have shape (Bs, L, ngroups, N) and head h
+ *             reads group h / (H / ngroups) (ngroups must divide H, else
+ *             SSM_ERR_INVALID_ARG); 0 or 1 = one group shared by all heads.
+ *             The diagonal scan returns SSM_ERR_UNSUPPORTED for ngroups > 1.
  * State input/output belongs to a single direction: ssd_chunk_scan_fwd_ex
  * with bidirectional != 0 and h0 or h_final set returns
  * SSM_ERR_UNSUPPORTED.
@@ -200,6 +204,7 @@ typedef struct ssm_scan_options {
     const void *z;
     const float *h0;
     float *h_final;
+    int32_t ngroups;
 } ssm_scan_options_t;
 
 /*

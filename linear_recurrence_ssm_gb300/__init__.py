@@ -17,8 +17,8 @@ ssm_scan_fwd(x, delta, A, B, C, D=None, y=None, **options)
 ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, bidirectional=False, y=None, **options)
     Chunked scalar-decay scan ("Some questions of Bi-Mamba2 and Hydra",
     Bi-Mamba2 issue 1).  x: (Bs, L, H, P) bf16; dt: (Bs, L, H) bf16;
-    A_head: (H) fp32; B, C: (Bs, L, N) or (Bs, L, 1, N) bf16; D: (H) fp32.
-    Returns y (Bs, L, H, P) fp32.
+    A_head: (H) fp32; B, C: (Bs, L, N) or (Bs, L, G, N) bf16 (head h reads
+    group h // (H // G)); D: (H) fp32.  Returns y (Bs, L, H, P) fp32.
 
 Options (either function; any of them selects the ``*_ex`` C entry point):
 ``dt_bias`` (ED or H, fp32), ``dt_softplus``, ``dt_limit=(lo, hi)``, ``z``
@@ -66,14 +66,14 @@ class ScanOptions(ctypes.Structure):
     """ssm_scan_options_t of include/ssm_scan.h."""
     _fields_ = [("dt_bias", _VP), ("dt_softplus", ctypes.c_int32), ("dt_limit", ctypes.c_int32),
                 ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float), ("z", _VP),
-                ("h0", _VP), ("h_final", _VP)]
+                ("h0", _VP), ("h_final", _VP), ("ngroups", ctypes.c_int32)]
 
 
 _OPTION_KEYS = ("dt_bias", "dt_softplus", "dt_limit", "z", "h0", "return_final_state")
 
 
 def _options(x, channels, state_shape, dev, dt_bias=None, dt_softplus=False, dt_limit=None,
-             z=None, h0=None, return_final_state=False):
+             z=None, h0=None, return_final_state=False, ngroups=1):
     """Validate the options and build (ScanOptions, h_final tensor or None, keep-alive list)."""
     import torch
     o = ScanOptions()
@@ -100,6 +100,7 @@ def _options(x, channels, state_shape, dev, dt_bias=None, dt_softplus=False, dt_
             raise ValueError("h0 must have shape %s" % (tuple(state_shape),))
         o.h0 = h0.data_ptr()
         keep.append(h0)
+    o.ngroups = int(ngroups)
     hf = None
     if return_final_state:
         hf = torch.empty(state_shape, dtype=torch.float32, device=dev)
@@ -229,20 +230,22 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
     _check(A_head, "A_head", (torch.float32,), dev, (1,))
     _check(D, "D", (torch.float32,), dev, (1,))
     Bs, L, H, P = x.shape
-    if B.dim() == 4:
-        if B.shape[2] != 1 or C.dim() != 4 or C.shape[2] != 1:
-            raise ValueError("B, C must have one group: (Bs, L, 1, N)")
+    G = B.shape[2] if B.dim() == 4 else 1
+    if B.dim() == 4 and (C.dim() != 4 or C.shape[2] != G or H % G != 0):
+        raise ValueError("B, C must be (Bs, L, G, N) with G dividing H")
     N = B.shape[-1]
     if tuple(dt.shape) != (Bs, L, H) or tuple(A_head.shape) != (H,) \
             or B.shape[0] != Bs or B.shape[1] != L or tuple(C.shape) != tuple(B.shape) \
             or (D is not None and tuple(D.shape) != (H,)):
-        raise ValueError("shape mismatch: x (Bs,L,H,P); dt (Bs,L,H); A_head (H); B, C (Bs,L,[1,]N)")
+        raise ValueError("shape mismatch: x (Bs,L,H,P); dt (Bs,L,H); A_head (H); B, C (Bs,L,[G,]N)")
     if y is None:
         y = torch.empty((Bs, L, H, P), dtype=torch.float32, device=dev)
     _check(y, "y", (torch.float32,), dev, (4,))
     bad = set(options) - set(_OPTION_KEYS)
     if bad:
         raise TypeError("unknown options: %s" % sorted(bad))
+    if G > 1:
+        options = dict(options, ngroups=G)
     if options:
         o, hf, keep = _options(x, H, (Bs, H, P, N), dev, **options)
         st = library().ssd_chunk_scan_fwd_ex(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C),

@@ -119,6 +119,7 @@ ssm_status_t diag_entry(const Tin *x, const Tin *delta, const float *A, const Ti
     if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
         !aligned(A, 4) || !aligned(y, 4) || (D && !aligned(D, 4)))
         return SSM_ERR_ALIGNMENT;
+    if (opts && opts->ngroups > 1) return SSM_ERR_UNSUPPORTED;   // groups: SSD only
     ssm_status_t s = check_options(opts, es);
     if (s != SSM_OK) return s;
     DeviceInfo dev;
@@ -126,7 +127,7 @@ ssm_status_t diag_entry(const Tin *x, const Tin *delta, const float *A, const Ti
     if (s != SSM_OK) return s;
     if (opts) {
         const ssm::ScanOpts ex{opts->dt_bias, opts->z, opts->h0, opts->h_final,
-                               opts->dt_min, opts->dt_max, opts->dt_softplus, opts->dt_limit};
+                               opts->dt_min, opts->dt_max, opts->dt_softplus, opts->dt_limit, 1};
         return from_cuda(ssm::diag::launch_ext<Tin>(x, delta, A, B, C, D, y, Bs, L, ED, N,
                                                     dev.num_sms, ex,
                                                     static_cast<cudaStream_t>(stream)));
@@ -233,6 +234,9 @@ ssm_status_t ssd_chunk_scan_fwd_ex(const void *x, const void *dt, const float *A
     if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
     if (L > INT_MAX || H > 65535 || Bs > INT_MAX) return SSM_ERR_UNSUPPORTED;
     if (bidirectional && (opts->h0 || opts->h_final)) return SSM_ERR_UNSUPPORTED;
+    if (opts->ngroups < 0 || (opts->ngroups > 1 && H % opts->ngroups != 0))
+        return SSM_ERR_INVALID_ARG;
+    if (opts->ngroups > 1 && !sizes_ok({Bs, L, opts->ngroups, N})) return SSM_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
         !aligned(dt, 2) || !aligned(A_head, 4) || (D && !aligned(D, 4)))
         return SSM_ERR_ALIGNMENT;
@@ -243,7 +247,8 @@ ssm_status_t ssd_chunk_scan_fwd_ex(const void *x, const void *dt, const float *A
     if (s != SSM_OK) return s;
     using bf = __nv_bfloat16;
     const ssm::ScanOpts o{opts->dt_bias, opts->z, opts->h0, opts->h_final,
-                          opts->dt_min, opts->dt_max, opts->dt_softplus, opts->dt_limit};
+                          opts->dt_min, opts->dt_max, opts->dt_softplus, opts->dt_limit,
+                          opts->ngroups};
     return from_cuda(ssm::ssd::launch(static_cast<const bf *>(x), static_cast<const bf *>(dt),
                                       A_head, static_cast<const bf *>(B),
                                       static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,

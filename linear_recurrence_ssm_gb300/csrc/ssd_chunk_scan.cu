@@ -102,6 +102,7 @@ struct Params {
     float *h_final;
     float dt_min, dt_max;
     int dt_softplus, dt_limit;
+    int G;             // groups of B, C; head h reads group h / (H / G)
 };
 
 // Scan options: see ScanOpts (z is bf16 here; states are (Bs, H, P, N)).
@@ -216,6 +217,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     const int L = prm.L;
     const int nc = prm.nc;
     const bool bidir = prm.bidir != 0;
+    const int grp = h / (prm.H / prm.G);          // this head's group of B, C
     const float Ah = prm.A[h] * SSM_LOG2E;        // decays are exp2 of log2e-scaled sums
     const float Dh = prm.D ? prm.D[h] : 0.0f;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
@@ -275,12 +277,12 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         mbar_arrive_expect_tx(&sm.bar_b[buf], NB * kTile);
 #pragma unroll
         for (int r = 0; r < NB; ++r)
-            tma_load_3d(sm.B[buf][r], &tmB, &sm.bar_b[buf], r * 64, c * kQ, b);
+            tma_load_4d(sm.B[buf][r], &tmB, &sm.bar_b[buf], r * 64, grp, c * kQ, b);
     };
     auto load_c = [&](int c, bool with_r) {
         mbar_arrive_expect_tx(&sm.bar_c, NB * kTile + (with_r ? uint32_t(rstride) : 0u));
 #pragma unroll
-        for (int r = 0; r < NB; ++r) tma_load_3d(sm.C[r], &tmC, &sm.bar_c, r * 64, c * kQ, b);
+        for (int r = 0; r < NB; ++r) tma_load_4d(sm.C[r], &tmC, &sm.bar_c, r * 64, grp, c * kQ, b);
         if (with_r)
             bulk_load(sm.R, prm.rstate + (size_t(bh) * nc + c) * rstride, uint32_t(rstride),
                       &sm.bar_c);
@@ -728,15 +730,17 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
                              const Options *opt = nullptr) {
     constexpr int N = NB * 64;
     CUtensorMap tmC, tmB, tmX, tmY;
-    const cuuint64_t dbc[3] = {cuuint64_t(N), cuuint64_t(L), cuuint64_t(Bs)};
-    const cuuint64_t sbc[2] = {cuuint64_t(N) * 2, cuuint64_t(L) * N * 2};
-    const cuuint32_t boxbc[3] = {64, kQ, 1};
+    const int64_t G = (opt && opt->ngroups > 1) ? opt->ngroups : 1;
+    // B, C: (Bs, L, G, N); one box is 64 n x 128 rows of one group
+    const cuuint64_t dbc[4] = {cuuint64_t(N), cuuint64_t(G), cuuint64_t(L), cuuint64_t(Bs)};
+    const cuuint64_t sbc[3] = {cuuint64_t(N) * 2, cuuint64_t(G) * N * 2, cuuint64_t(L) * G * N * 2};
+    const cuuint32_t boxbc[4] = {64, 1, kQ, 1};
     const cuuint64_t dx[4] = {cuuint64_t(kP), cuuint64_t(H), cuuint64_t(L), cuuint64_t(Bs)};
     const cuuint64_t sx[3] = {cuuint64_t(kP) * 2, cuuint64_t(H) * kP * 2, cuuint64_t(L) * H * kP * 2};
     const cuuint32_t boxx[4] = {64, 1, kQ, 1};
     const cuuint64_t sy[3] = {cuuint64_t(kP) * 4, cuuint64_t(H) * kP * 4, cuuint64_t(L) * H * kP * 4};
     const cuuint32_t boxy[4] = {32, 1, kQ, 1};
-    if (!make_map(&tmC, Cm, 3, dbc, sbc, boxbc) || !make_map(&tmB, Bm, 3, dbc, sbc, boxbc) ||
+    if (!make_map(&tmC, Cm, 4, dbc, sbc, boxbc) || !make_map(&tmB, Bm, 4, dbc, sbc, boxbc) ||
         !make_map(&tmX, x, 4, dx, sx, boxx) ||
         !make_map(&tmY, y, 4, dx, sy, boxy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
         return cudaErrorInvalidValue;
@@ -761,6 +765,7 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
     prm.dt_max = o.dt_max;
     prm.dt_softplus = o.dt_softplus;
     prm.dt_limit = o.dt_limit;
+    prm.G = int(G);
     const int64_t grid = Bs * H;
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
 

@@ -23,6 +23,7 @@ struct ScanOpts {
     float *h_final;         // final state out, fp32
     float dt_min, dt_max;
     int dt_softplus, dt_limit;
+    int ngroups;            // SSD: groups of B, C (0 or 1 = one group)
 };
 
 // ---- element conversion ---------------------------------------------------

@@ -146,3 +146,14 @@ def test_option_calls_without_device_report_no_device():
     assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 0, ctypes.byref(o), None) == 6
     # a NULL options pointer is the plain call
     assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1, None, None) == 6
+
+
+def test_groups_are_validated():
+    lib = lrs.library()
+    # ngroups must divide H
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 6, 64, 64, 128, 0,
+                                     ctypes.byref(_opts(ngroups=4)), None) == 1
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 6, 64, 64, 128, 0,
+                                     ctypes.byref(_opts(ngroups=-1)), None) == 1
+    # groups belong to the SSD scan only
+    assert lib.ssm_scan_fwd_ex(*([P] * 7), 1, 8, 8, 4, 1, ctypes.byref(_opts(ngroups=2)), None) == 2

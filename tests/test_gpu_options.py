@@ -177,3 +177,33 @@ def test_plain_entry_points_unchanged_by_empty_options(cuda_device):
     torch.cuda.synchronize()
     for a, b in ((y0, y1), (z0, z1)):
         assert float((a - b).abs().max()) <= 1e-6 * float(a.abs().max())
+
+
+@pytest.mark.parametrize("Bs,L,H,N,G,bidir", [
+    (2, 300, 4, 64, 2, False),
+    (1, 700, 6, 128, 3, False),
+    (2, 260, 4, 64, 4, True),     # one group per head
+    (1, 400, 8, 128, 2, True),
+])
+def test_ssd_groups_of_B_C(cuda_device, Bs, L, H, N, G, bidir):
+    inp = workloads.ssd_inputs(Bs, L, H, 64, N, "bf16", seed=L + G, groups=G)
+    ref = oracle.ssd_scan(**inp, bidirectional=bidir)
+    y = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=128, bidirectional=bidir)
+    torch.cuda.synchronize()
+    _close(y, ref, "bf16", "y")
+
+
+def test_ssd_groups_with_options(cuda_device):
+    Bs, L, H, N, G = 2, 333, 4, 64, 2
+    inp = workloads.ssd_inputs(Bs, L, H, 64, N, "bf16", seed=61, groups=G)
+    opt = workloads.option_inputs((Bs, L, H, 64), (Bs, L, H), H, (Bs, H, 64, N), "bf16", 62)
+    inp["dt"] = opt["delta_raw"]
+    ref, href = oracle.ssd_scan(**inp, dt_bias=opt["dt_bias"], dt_softplus=True, z=opt["z"],
+                                h0=opt["h0"], return_final_state=True)
+    y, hf = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=128,
+                                   dt_bias=opt["dt_bias"].to(cuda_device), dt_softplus=True,
+                                   z=opt["z"].to(cuda_device), h0=opt["h0"].to(cuda_device),
+                                   return_final_state=True)
+    torch.cuda.synchronize()
+    _close(y, ref, "bf16", "y")
+    _close(hf, href, "bf16", "h_final")

@@ -94,17 +94,18 @@ def diag_inputs(Bs: int, L: int, ED: int, N: int, dtype: str = "f32", seed: int 
 
 
 def ssd_inputs(Bs: int, L: int, H: int, P: int, N: int, dtype: str = "bf16", seed: int = 0,
-               with_D: bool = True):
+               with_D: bool = True, groups: int = 1):
     """Inputs of the chunked scalar-decay scan on the CPU: dict(x, dt, A_head, B, C, D).
 
-    B and C have shape (Bs, L, 1, N): one group shared by all heads.
+    B and C have shape (Bs, L, groups, N); one group (the default) is shared
+    by all heads.
     """
     g = torch.Generator(device="cpu").manual_seed(seed)
     x = torch.randn(Bs, L, H, P, generator=g)
     dt = F.softplus(torch.randn(Bs, L, H, generator=g) - 2.0)
     A_head = -torch.exp(torch.rand(H, generator=g) * math.log(16.0))
-    B = torch.randn(Bs, L, 1, N, generator=g) / math.sqrt(N)
-    C = torch.randn(Bs, L, 1, N, generator=g) / math.sqrt(N)
+    B = torch.randn(Bs, L, groups, N, generator=g) / math.sqrt(N)
+    C = torch.randn(Bs, L, groups, N, generator=g) / math.sqrt(N)
     D = torch.randn(H, generator=g)
     return dict(x=_cast(x, dtype), dt=_cast(dt, dtype), A_head=A_head.contiguous(),
                 B=_cast(B, dtype), C=_cast(C, dtype), D=D.contiguous() if with_D else None)
