@@ -71,6 +71,8 @@ def _load(path: str | None = None):
                                                  ctypes.c_int, dbl, dbl, dp, dp, dp, i64, i64,
                                                  ctypes.c_int])
         lib.oracle_ssd_scan_ex_range.restype = None
+        lib.oracle_diag_scan_bwd_range.argtypes = [dp] * 13 + [i64] * 6 + [ctypes.c_int]
+        lib.oracle_diag_scan_bwd_range.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _libs[key] = lib
@@ -138,6 +140,28 @@ def diag_scan(x, delta, A, B, C, D=None, nthreads: int = 0, channels=None, libra
         _ptr(dt_bias), int(bool(dt_softplus)), lim, lo, hi, _ptr(z), _ptr(h0), _ptr(hf), c0, c1,
         nthreads)
     return (y, hf) if return_final_state else y
+
+
+def diag_scan_bwd(x, delta, A, B, C, D, dy, nthreads: int = 0, library=None):
+    """Gradients of the diagonal scan in fp64 (reverse mode written out by hand).
+
+    Same inputs as ``diag_scan`` plus dy (Bs, L, ED), the gradient of the loss
+    with respect to y.  Returns dict(dx, ddelta, dA, dB, dC, dD) shaped like
+    x, delta, A, B, C, D (dD is None when D is None).
+    """
+    x, delta, A, B, C, D, dy = map(_f64, (x, delta, A, B, C, D, dy))
+    Bs, L, ED = x.shape
+    N = A.shape[1]
+    assert delta.shape == x.shape and dy.shape == x.shape and A.shape == (ED, N)
+    assert B.shape == (Bs, L, N) and C.shape == (Bs, L, N)
+    out = dict(dx=np.zeros((Bs, L, ED)), ddelta=np.zeros((Bs, L, ED)), dA=np.zeros((ED, N)),
+               dB=np.zeros((Bs, L, N)), dC=np.zeros((Bs, L, N)),
+               dD=None if D is None else np.zeros(ED))
+    _load(library).oracle_diag_scan_bwd_range(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(out["dx"]),
+        _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+        Bs, L, ED, N, 0, Bs * ED, nthreads)
+    return out
 
 
 def ssd_scan(x, dt, A_head, B, C, D=None, bidirectional: bool = False,

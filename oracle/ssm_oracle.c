@@ -246,3 +246,80 @@ void oracle_ssd_scan(const double *x, const double *dt, const double *A_head,
     oracle_ssd_scan_range(x, dt, A_head, B, C, D, y, Bs, L, H, P, N,
                           bidirectional, 0, Bs * H, nthreads);
 }
+
+/*
+ * Gradients of the diagonal scan (reverse mode, written out by hand) for the
+ * channels in [c_begin, c_end) of the flattened (b, e) index, given dy,
+ * the gradient of the loss with respect to y.  With a_t[n] = exp(delta_t A[e,n])
+ * the adjoint of the state obeys the reverse-time recurrence
+ *   g_t[n] = dy_t C_t[n] + a_{t+1}[n] g_{t+1}[n],   g_L = 0,
+ * and, with h_{t-1} the state entering step t,
+ *   dx_t     = sum_n g_t[n] delta_t B_t[n] + D[e] dy_t
+ *   ddelta_t = sum_n g_t[n] (A[e,n] a_t[n] h_{t-1}[n] + B_t[n] x_t)
+ *   dA[e,n]  = sum_{b,t} g_t[n] delta_t a_t[n] h_{t-1}[n]
+ *   dB_t[n]  = sum_e g_t[n] delta_t x_t,    dC_t[n] = sum_e dy_t h_t[n]
+ *   dD[e]    = sum_{b,t} dy_t x_t.
+ * dx, ddelta: (Bs, L, ED) overwritten for the channels done; dA (ED, N),
+ * dB, dC (Bs, L, N) and dD (ED) are ACCUMULATED into (the caller zeroes
+ * them); dD may be NULL.
+ */
+void oracle_diag_scan_bwd_range(const double *x, const double *delta, const double *A,
+                                const double *B, const double *C, const double *D,
+                                const double *dy, double *dx, double *ddelta, double *dA,
+                                double *dB, double *dC, double *dD, int64_t Bs, int64_t L,
+                                int64_t ED, int64_t N, int64_t c_begin, int64_t c_end,
+                                int nthreads) {
+    set_threads(nthreads);
+    if (c_end > Bs * ED) c_end = Bs * ED;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t c = c_begin; c < c_end; ++c) {
+        const int64_t b = c / ED, e = c % ED;
+        /* forward: the states h_t (t = -1 .. L-1), row t + 1 of hist */
+        double *hist = (double *)calloc((size_t)((L + 1) * N), sizeof(double));
+        double *g = (double *)calloc((size_t)N, sizeof(double));
+        double *lA = (double *)calloc((size_t)N, sizeof(double));
+        double *lB = (double *)calloc((size_t)(L * N), sizeof(double));
+        double *lC = (double *)calloc((size_t)(L * N), sizeof(double));
+        double lD = 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t i = (b * L + t) * ED + e, r = (b * L + t) * N;
+            for (int64_t n = 0; n < N; ++n)
+                hist[(t + 1) * N + n] = exp(delta[i] * A[e * N + n]) * hist[t * N + n] +
+                                        delta[i] * B[r + n] * x[i];
+        }
+        /* reverse */
+        for (int64_t t = L - 1; t >= 0; --t) {
+            const int64_t i = (b * L + t) * ED + e, r = (b * L + t) * N;
+            const double dl = delta[i], xv = x[i], gy = dy[i];
+            double sdx = 0.0, sdd = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double a = exp(dl * A[e * N + n]);
+                const double hprev = hist[t * N + n];
+                g[n] += gy * C[r + n];                 /* g now holds g_t[n] */
+                sdx += g[n] * dl * B[r + n];
+                sdd += g[n] * (A[e * N + n] * a * hprev + B[r + n] * xv);
+                lA[n] += g[n] * dl * a * hprev;
+                lB[t * N + n] += g[n] * dl * xv;
+                lC[t * N + n] += gy * hist[(t + 1) * N + n];
+                g[n] *= a;                             /* a_t g_t, carried to step t - 1 */
+            }
+            dx[i] = sdx + (D ? D[e] * gy : 0.0);
+            ddelta[i] = sdd;
+            lD += gy * xv;
+        }
+#pragma omp critical
+        {
+            for (int64_t n = 0; n < N; ++n) dA[e * N + n] += lA[n];
+            for (int64_t k = 0; k < L * N; ++k) {
+                dB[b * L * N + k] += lB[k];
+                dC[b * L * N + k] += lC[k];
+            }
+            if (dD) dD[e] += lD;
+        }
+        free(hist);
+        free(g);
+        free(lA);
+        free(lB);
+        free(lC);
+    }
+}
