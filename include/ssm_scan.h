@@ -231,6 +231,30 @@ SSM_API ssm_status_t ssd_chunk_scan_fwd_ex(const void *x, const void *dt,
                                            const ssm_scan_options_t *opts, void *stream);
 
 /*
+ * Gradients of the diagonal scan (ssm_scan_fwd without options): given dy,
+ * the gradient of a loss with respect to y, writes the gradients with
+ * respect to every input (the backward pass of the chunked scan's function
+ * in "Some questions of Bi-Mamba2 and Hydra", Bi-Mamba2 issue 1, for the
+ * diagonal form):
+ *   dx, ddelta : (Bs, L, ED) fp32, overwritten
+ *   dA         : (ED, N) fp32,  dB, dC : (Bs, L, N) fp32,  dD : (ED) fp32
+ *                (zeroed by the call, then accumulated; dD may be NULL)
+ * x, delta, B, C are fp32 (input_bf16 == 0) or bf16; A, D, dy are fp32.
+ * Supported: N <= 16 (SSM_ERR_UNSUPPORTED otherwise), Bs <= 65535.  dx and
+ * ddelta are deterministic; dA, dB, dC, dD are sums formed with atomic
+ * additions, so their last bits may differ between runs.  Takes a
+ * stream-ordered scratch buffer of ceil(L/16)*Bs*ED*64 bytes for the
+ * re-computation checkpoints.
+ * Alignment: every pointer to its element size; dy, dx, ddelta, dA, dB, dC,
+ * dD to 4 bytes.
+ */
+SSM_API ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float *A,
+                                  const void *B, const void *C, const float *D,
+                                  const float *dy, float *dx, float *ddelta, float *dA,
+                                  float *dB, float *dC, float *dD, int64_t Bs, int64_t L,
+                                  int64_t ED, int64_t N, int input_bf16, void *stream);
+
+/*
  * Synchronise `stream` and report whether a kernel of this library running on
  * the current device gave up a bounded wait (SSM_ERR_DEVICE_TIMEOUT) since
  * the previous check; the record is cleared by the call.  Kernels never hang

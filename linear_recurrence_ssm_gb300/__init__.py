@@ -34,7 +34,7 @@ import os
 from . import _build
 
 __all__ = ["ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssd_chunk_scan_fwd", "ssm_check_device_errors",
-           "ssm_scan_fwd_plan", "ScanOptions",
+           "ssm_scan_fwd_plan", "ssm_scan_bwd", "ScanOptions",
            "SsmError", "library", "build", "status_string", "STATUS"]
 
 STATUS = {
@@ -53,6 +53,7 @@ SIGNATURES = {
     "ssm_scan_fwd_plan": ([_I64] * 4 + [ctypes.c_int] + [ctypes.POINTER(ctypes.c_int32)] * 3,
                           ctypes.c_int),
     "ssm_scan_fwd_ex": ([_VP] * 7 + [_I64] * 4 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
+    "ssm_scan_bwd": ([_VP] * 13 + [_I64] * 4 + [ctypes.c_int, _VP], ctypes.c_int),
     "ssd_chunk_scan_fwd_ex": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
     "ssm_check_device_errors": ([_VP], ctypes.c_int),
     "ssm_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -261,6 +262,38 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
     if st != 0:
         raise SsmError("ssd_chunk_scan_fwd", st)
     return y
+
+
+def ssm_scan_bwd(x, delta, A, B, C, D, dy):
+    """Gradients of the diagonal scan for the upstream gradient dy (fp32,
+    shaped like y): dict(dx, ddelta, dA, dB, dC, dD) as fp32 tensors (dD is
+    None when D is None)."""
+    import torch
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    ins = (torch.float32, torch.bfloat16)
+    for t, n in ((x, "x"), (delta, "delta"), (B, "B"), (C, "C")):
+        _check(t, n, (x.dtype,) if x.dtype in ins else ins, dev, (3,))
+    _check(A, "A", (torch.float32,), dev, (2,))
+    _check(D, "D", (torch.float32,), dev, (1,))
+    _check(dy, "dy", (torch.float32,), dev, (3,))
+    Bs, L, ED = x.shape
+    N = A.shape[1]
+    if delta.shape != x.shape or dy.shape != x.shape or tuple(A.shape) != (ED, N) \
+            or tuple(B.shape) != (Bs, L, N) or tuple(C.shape) != (Bs, L, N):
+        raise ValueError("shape mismatch: x, delta, dy (Bs,L,ED); A (ED,N); B, C (Bs,L,N)")
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(dx=torch.empty((Bs, L, ED), **f32), ddelta=torch.empty((Bs, L, ED), **f32),
+             dA=torch.empty((ED, N), **f32), dB=torch.empty((Bs, L, N), **f32),
+             dC=torch.empty((Bs, L, N), **f32), dD=None if D is None else torch.empty(ED, **f32))
+    st = library().ssm_scan_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dy),
+                                _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]),
+                                _ptr(g["dC"]), _ptr(g["dD"]), Bs, L, ED, N,
+                                int(x.dtype == torch.bfloat16), _stream(dev))
+    if st != 0:
+        raise SsmError("ssm_scan_bwd", st)
+    return g
 
 
 def ssm_scan_fwd_plan(Bs: int, L: int, ED: int, N: int, bf16: bool = True):

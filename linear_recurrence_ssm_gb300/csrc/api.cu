@@ -23,6 +23,13 @@ struct Plan {
 };
 Plan plan_for(int64_t Bs, int64_t L, int64_t ED, int64_t N, int esz, int num_sms);
 }  // namespace diag
+namespace diag_bwd {
+template <typename Tin>
+cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
+                       const float *D, const float *dy, float *dx, float *ddelta, float *dA,
+                       float *dB, float *dC, float *dD, int64_t Bs, int64_t L, int64_t ED,
+                       int64_t N, cudaStream_t st);
+}
 namespace ssd {
 cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
                    const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
@@ -254,6 +261,37 @@ ssm_status_t ssd_chunk_scan_fwd_ex(const void *x, const void *dt, const float *A
                                       static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
                                       bidirectional != 0, dev.num_sms,
                                       static_cast<cudaStream_t>(stream), &o));
+}
+
+ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float *A, const void *B,
+                          const void *C, const float *D, const float *dy, float *dx,
+                          float *ddelta, float *dA, float *dB, float *dC, float *dD, int64_t Bs,
+                          int64_t L, int64_t ED, int64_t N, int input_bf16, void *stream) {
+    if (!x || !delta || !A || !B || !C || !dy || !dx || !ddelta || !dA || !dB || !dC)
+        return SSM_ERR_INVALID_ARG;
+    if (!sizes_ok({Bs, L, ED}) || !sizes_ok({Bs, L, N}) || !sizes_ok({ED, N}))
+        return SSM_ERR_INVALID_ARG;
+    if (N > 16 || Bs > 65535 || L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    const size_t es = input_bf16 ? 2 : 4;
+    if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
+        !aligned(A, 4) || (D && !aligned(D, 4)) || !aligned(dy, 4) || !aligned(dx, 4) ||
+        !aligned(ddelta, 4) || !aligned(dA, 4) || !aligned(dB, 4) || !aligned(dC, 4) ||
+        (dD && !aligned(dD, 4)))
+        return SSM_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    ssm_status_t s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    using bf = __nv_bfloat16;
+    if (input_bf16)
+        return from_cuda(ssm::diag_bwd::launch_bwd<bf>(
+            static_cast<const bf *>(x), static_cast<const bf *>(delta), A,
+            static_cast<const bf *>(B), static_cast<const bf *>(C), D, dy, dx, ddelta, dA, dB, dC,
+            dD, Bs, L, ED, N, st));
+    return from_cuda(ssm::diag_bwd::launch_bwd<float>(
+        static_cast<const float *>(x), static_cast<const float *>(delta), A,
+        static_cast<const float *>(B), static_cast<const float *>(C), D, dy, dx, ddelta, dA, dB,
+        dC, dD, Bs, L, ED, N, st));
 }
 
 ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED, int64_t N, int input_bf16,

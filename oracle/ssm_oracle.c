@@ -293,7 +293,7 @@ void oracle_diag_scan_bwd_range(const double *x, const double *delta, const doub
             const double dl = delta[i], xv = x[i], gy = dy[i];
             double sdx = 0.0, sdd = 0.0;
             for (int64_t n = 0; n < N; ++n) {
-                const double a = exp(dl * A[e * N + n]);
+                const double a = exp(A[e * N + n] * dl);
                 const double hprev = hist[t * N + n];
                 g[n] += gy * C[r + n];                 /* g now holds g_t[n] */
                 sdx += g[n] * dl * B[r + n];

@@ -157,3 +157,15 @@ def test_groups_are_validated():
                                      ctypes.byref(_opts(ngroups=-1)), None) == 1
     # groups belong to the SSD scan only
     assert lib.ssm_scan_fwd_ex(*([P] * 7), 1, 8, 8, 4, 1, ctypes.byref(_opts(ngroups=2)), None) == 2
+
+
+def test_backward_rejects_bad_arguments():
+    lib = lrs.library()
+    p13 = [P] * 13
+    assert lib.ssm_scan_bwd(*p13, 1, 8, 8, 17, 0, None) == 2       # N > 16
+    bad = list(p13)
+    bad[6] = None                                                  # dy
+    assert lib.ssm_scan_bwd(*bad, 1, 8, 8, 4, 0, None) == 1
+    bad = list(p13)
+    bad[8] = P_ODD                                                 # ddelta misaligned
+    assert lib.ssm_scan_bwd(*bad, 1, 8, 8, 4, 0, None) == 3

@@ -128,6 +128,12 @@ def option_inputs(x_shape, delta_shape, channels: int, state_shape, dtype: str =
                 z=_cast(z, dtype), h0=h0.contiguous())
 
 
+def grad_output(shape, seed: int = 0):
+    """A seeded upstream gradient dy ~ N(0, 1), fp32, of the given shape (CPU)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    return torch.randn(*shape, generator=g)
+
+
 def workload_inputs(w: Workload):
     s = w.shape
     if w.kind == "diag":
