@@ -56,6 +56,10 @@ def parse_args():
                         "(used for profiler runs)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target wall time of the CPU oracle sample")
+    p.add_argument("--mode", choices=["fwd", "options", "bwd"], default="fwd",
+                   help="fwd: the plain forward scan (the headline); options: the forward scan "
+                        "with every option on (delta bias + softplus + clamp, silu gate, initial "
+                        "and final state); bwd: the diagonal scan's gradients")
     return p.parse_args()
 
 
@@ -84,10 +88,10 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 
 def kernel_source_hash(kind: str) -> str:
-    src = os.path.join(ROOT, "linear_recurrence_ssm_gb300", "csrc",
-                       "diag_scan.cu" if kind == "diag" else "ssd_chunk_scan.cu")
+    csrc = os.path.join(ROOT, "linear_recurrence_ssm_gb300", "csrc")
+    srcs = ["diag_scan.cuh", "diag_scan.cu"] if kind == "diag" else ["ssd_chunk_scan.cu"]
     h = hashlib.sha256()
-    for p in (src, os.path.join(ROOT, "linear_recurrence_ssm_gb300", "csrc", "ssm_common.cuh")):
+    for p in [os.path.join(csrc, f) for f in srcs] + [os.path.join(csrc, "ssm_common.cuh")]:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -207,18 +211,73 @@ def shard_seed(base_seed: int, rank: int) -> int:
     return base_seed + 1000 * rank
 
 
-def make_step(w, lrs, bufs):
+OPTION_LIMIT = (1e-4, 100.0)
+
+
+def option_host_inputs(w, seed):
+    """Seeded option inputs for the workload (delta / dt before activation,
+    bias, gate z, initial state)."""
     s = w.shape
     if w.kind == "diag":
+        return workloads.option_inputs((s["Bs"], s["L"], s["ED"]), (s["Bs"], s["L"], s["ED"]),
+                                       s["ED"], (s["Bs"], s["ED"], s["N"]), w.dtype, seed + 7)
+    state = None if s["bidirectional"] else (s["Bs"], s["H"], s["P"], s["N"])
+    o = workloads.option_inputs((s["Bs"], s["L"], s["H"], s["P"]), (s["Bs"], s["L"], s["H"]),
+                                s["H"], state or (1,), w.dtype, seed + 7)
+    if state is None:
+        o["h0"] = None
+    return o
+
+
+def make_step(w, lrs, bufs, mode="fwd"):
+    s = w.shape
+    if mode == "bwd":
         def step(i):
             b = bufs[i % len(bufs)]
-            lrs.ssm_scan_fwd(b["x"], b["delta"], b["A"], b["B"], b["C"], b["D"], y=b["y"])
+            lrs.ssm_scan_bwd(b["x"], b["delta"], b["A"], b["B"], b["C"], b["D"], b["dy"])
+    elif w.kind == "diag":
+        def step(i):
+            b = bufs[i % len(bufs)]
+            if mode == "options":
+                lrs.ssm_scan_fwd(b["x"], b["delta_raw"], b["A"], b["B"], b["C"], b["D"], y=b["y"],
+                                 dt_bias=b["dt_bias"], dt_softplus=True, dt_limit=OPTION_LIMIT,
+                                 z=b["z"], h0=b["h0"], return_final_state=True)
+            else:
+                lrs.ssm_scan_fwd(b["x"], b["delta"], b["A"], b["B"], b["C"], b["D"], y=b["y"])
     else:
         def step(i):
             b = bufs[i % len(bufs)]
-            lrs.ssd_chunk_scan_fwd(b["x"], b["dt"], b["A_head"], b["B"], b["C"], b["D"],
-                                   chunk=s["chunk"], bidirectional=s["bidirectional"], y=b["y"])
+            if mode == "options":
+                st = {} if s["bidirectional"] else dict(h0=b["h0"], return_final_state=True)
+                lrs.ssd_chunk_scan_fwd(b["x"], b["delta_raw"], b["A_head"], b["B"], b["C"], b["D"],
+                                       chunk=s["chunk"], bidirectional=s["bidirectional"],
+                                       y=b["y"], dt_bias=b["dt_bias"], dt_softplus=True,
+                                       dt_limit=OPTION_LIMIT, z=b["z"], **st)
+            else:
+                lrs.ssd_chunk_scan_fwd(b["x"], b["dt"], b["A_head"], b["B"], b["C"], b["D"],
+                                       chunk=s["chunk"], bidirectional=s["bidirectional"],
+                                       y=b["y"])
     return step
+
+
+def mode_bytes(w, mode) -> int:
+    """Algorithmic bytes of one call in the given mode (inputs read once,
+    outputs written once)."""
+    s = w.shape
+    esz = 2 if w.dtype == "bf16" else 4
+    if mode == "fwd":
+        return w.algorithmic_bytes
+    if mode == "options":
+        if w.kind == "diag":
+            xs, state = s["Bs"] * s["L"] * s["ED"], s["Bs"] * s["ED"] * s["N"]
+            return w.algorithmic_bytes + xs * esz + 2 * state * 4 + s["ED"] * 4
+        xs = s["Bs"] * s["L"] * s["H"] * s["P"]
+        state = 0 if s["bidirectional"] else s["Bs"] * s["H"] * s["P"] * s["N"]
+        return w.algorithmic_bytes + xs * esz + 2 * state * 4 + s["H"] * 4
+    # backward of the diagonal scan: x, delta, B, C, A, D, dy in; dx, ddelta, dA, dB, dC, dD out
+    xs, bc = s["Bs"] * s["L"] * s["ED"], s["Bs"] * s["L"] * s["N"]
+    return (2 * xs * esz + 2 * bc * esz + xs * 4 + 2 * xs * 4 + 2 * bc * 4
+            + 2 * s["ED"] * s["N"] * 4 + 2 * s["ED"] * 4)
 
 
 def out_shape(w):
@@ -240,19 +299,25 @@ def run_ours(args, rank, world, local):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     w = workloads.BY_NAME[args.workload]
+    if args.mode == "bwd" and w.kind != "diag":
+        raise SystemExit("bench.py: --mode bwd exists for the diagonal scan only")
     lrs.library()
 
     # Resident input/output sets; each rank draws its own batch (weak scaling).
     host = workloads.workload_inputs(
         workloads.Workload(w.name, w.kind, w.dtype, w.shape, seed=shard_seed(w.seed, rank)))
-    per_set = w.algorithmic_bytes
+    if args.mode == "options":
+        host.update(option_host_inputs(w, shard_seed(w.seed, rank)))
+    if args.mode == "bwd":
+        host["dy"] = workloads.grad_output(out_shape(w), seed=shard_seed(w.seed, rank) + 11)
+    per_set = mode_bytes(w, args.mode)
     nsets = max(3, -(-3 * L2_BYTES // per_set))
     bufs = []
     for k in range(nsets):
         b = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
         b["y"] = torch.empty(out_shape(w), dtype=torch.float32, device=dev)
         bufs.append(b)
-    step = make_step(w, lrs, bufs)
+    step = make_step(w, lrs, bufs, args.mode)
     stream = torch.cuda.current_stream(dev)
 
     for i in range(max(3, args.warmup)):
@@ -304,7 +369,7 @@ def run_ours(args, rank, world, local):
     dbuf = bufs[0]
     h2d = sum(t.numel() * t.element_size() for t in pinned.values() if t is not None)
     d2h = y_host.numel() * 4
-    k_e2e = 0 if args.quick else max(1, min(args.steps, 200))
+    k_e2e = 0 if (args.quick or args.mode == "bwd") else max(1, min(args.steps, 200))
     for _ in range(0 if args.quick else 2):
         for n, t in pinned.items():
             if t is not None:
@@ -333,9 +398,10 @@ def run_ours(args, rank, world, local):
     value = units * args.steps * world / (ms / 1e3)
     e2e_value = units * k_e2e * world / (ms_e2e / 1e3) if k_e2e else None
     peaks = load_peaks()
-    launches_per_step = kernels_per_call(w, lrs)
+    launches_per_step = 2 if args.mode == "bwd" else kernels_per_call(w, lrs)
     per_launch_s = ms / 1e3 / args.steps
-    hbm_achieved = w.algorithmic_bytes / per_launch_s / 1e9
+    call_bytes = mode_bytes(w, args.mode)
+    hbm_achieved = call_bytes / per_launch_s / 1e9
     if w.kind == "diag":
         # One exp2 on the special-function unit and four fp32 operations per
         # element-step; both the MUFU (32 ex2 / clk / SM) and the FMA pipe
@@ -345,26 +411,29 @@ def run_ours(args, rank, world, local):
         roofline = {
             "bound": "alu", "achieved": round(achieved, 4), "peak": round(alu_peak, 4),
             "unit": "T element-steps/s", "frac": round(achieved / alu_peak, 4),
-            "traffic": ncu_traffic(w.name, w.kind),
+            "traffic": ncu_traffic(w.name, w.kind) if args.mode == "fwd" else None,
             "peak_source": "derived: 152 SMs x 32 ex2/clk/SM (MUFU) x sm_max_mhz of "
-                           "MEASURED_PEAKS.json; 1 ex2 + 4 fp32 ops per element-step",
+                           "MEASURED_PEAKS.json; 1 ex2 + 4 fp32 ops per element-step"
+                           + ("" if args.mode != "bwd" else
+                              " of the forward scan (the gradients re-run the forward twice "
+                              "and do about twice its work on the way back)"),
             "hbm": {"achieved_gbs": round(hbm_achieved, 1), "peak_gbs": peaks["hbm_gbs"],
                     "frac": round(hbm_achieved / peaks["hbm_gbs"], 4),
-                    "algorithmic_bytes_per_launch": w.algorithmic_bytes},
+                    "algorithmic_bytes_per_launch": call_bytes},
             "launch_us": round(per_launch_s * 1e6, 3),
         }
     else:
         roofline = {
             "bound": "hbm", "achieved": round(hbm_achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(hbm_achieved / peaks["hbm_gbs"], 4),
-            "traffic": ncu_traffic(w.name, w.kind),
+            "traffic": ncu_traffic(w.name, w.kind) if args.mode == "fwd" else None,
             "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-            "algorithmic_bytes_per_launch": w.algorithmic_bytes,
+            "algorithmic_bytes_per_launch": call_bytes,
             "launch_us": round(per_launch_s * 1e6, 3),
         }
     achieved = hbm_achieved
     s = w.shape
-    config = {"workload": w.name, **{k: v for k, v in s.items()},
+    config = {"workload": w.name, **{k: v for k, v in s.items()}, "mode": args.mode,
               "input_dtype": w.dtype, "state_dtype": "f32", "output_dtype": "f32",
               "l2": "inputs rotate over %d resident sets (%.0f MB each, > 2x L2 between reuses)"
                     % (nsets, per_set / 1e6),
@@ -382,7 +451,7 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h, "steps": k_e2e},
         "gpu_launches": args.steps * launches_per_step,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.mode == "fwd":
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if world > 1:
         dist.destroy_process_group()
@@ -433,12 +502,15 @@ def cpu_baseline(w, seconds: float):
     fn()
     rate = units / max(1e-6, time.perf_counter() - t0)
     fn, units, desc = _oracle_sample(w, host, rate * seconds)
+    # The sample is capped at the whole workload; repeat it to fill the time budget.
+    reps = max(1, min(200, int(seconds * rate / max(1.0, units))))
     t0 = time.perf_counter()
-    fn()
+    for _ in range(reps):
+        fn()
     dt = time.perf_counter() - t0
-    return {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "%s; %.3g element-steps in %.2f s (fp64 sequential C, OpenMP)"
-                      % (desc, units, dt)}
+    return {"value": units * reps / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%s, %d pass(es); %.3g element-steps in %.2f s (fp64 sequential C, OpenMP)"
+                      % (desc, reps, units * reps, dt)}
 
 
 def run_reference(args, rank, world):
