@@ -502,8 +502,12 @@ def cpu_baseline(w, seconds: float):
     fn()
     rate = units / max(1e-6, time.perf_counter() - t0)
     fn, units, desc = _oracle_sample(w, host, rate * seconds)
-    # The sample is capped at the whole workload; repeat it to fill the time budget.
-    reps = max(1, min(200, int(seconds * rate / max(1.0, units))))
+    # The sample is capped at the whole workload: time one pass, then repeat
+    # it until the time budget is filled.
+    t0 = time.perf_counter()
+    fn()
+    t_one = time.perf_counter() - t0
+    reps = max(1, min(500, int(round(seconds / max(t_one, 1e-3)))))
     t0 = time.perf_counter()
     for _ in range(reps):
         fn()
