@@ -28,7 +28,7 @@ template <typename Tin>
 cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
                        const float *D, const float *dy, float *dx, float *ddelta, float *dA,
                        float *dB, float *dC, float *dD, int64_t Bs, int64_t L, int64_t ED,
-                       int64_t N, cudaStream_t st);
+                       int64_t N, int num_sms, cudaStream_t st);
 }
 namespace ssd {
 cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
@@ -287,11 +287,11 @@ ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float *A, cons
         return from_cuda(ssm::diag_bwd::launch_bwd<bf>(
             static_cast<const bf *>(x), static_cast<const bf *>(delta), A,
             static_cast<const bf *>(B), static_cast<const bf *>(C), D, dy, dx, ddelta, dA, dB, dC,
-            dD, Bs, L, ED, N, st));
+            dD, Bs, L, ED, N, dev.num_sms, st));
     return from_cuda(ssm::diag_bwd::launch_bwd<float>(
         static_cast<const float *>(x), static_cast<const float *>(delta), A,
         static_cast<const float *>(B), static_cast<const float *>(C), D, dy, dx, ddelta, dA, dB,
-        dC, dD, Bs, L, ED, N, st));
+        dC, dD, Bs, L, ED, N, dev.num_sms, st));
 }
 
 ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED, int64_t N, int input_bf16,

@@ -124,14 +124,13 @@ using Ext = ScanOpts;
 // The delta the recurrence sees, from the stored one and the channel's bias.
 __device__ __forceinline__ float prep_delta(float d, float bias, const Ext &ex) {
     d += bias;
-    // log(1 + e^d); above 20 the correction term is below fp32 resolution
-    if (ex.dt_softplus) d = d > 20.0f ? d : log1pf(__expf(d));
+    if (ex.dt_softplus) d = softplus_fast(d);
     if (ex.dt_limit) d = fminf(fmaxf(d, ex.dt_min), ex.dt_max);
     return d;
 }
 
 // silu(z) = z * sigmoid(z)
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+__device__ __forceinline__ float silu(float z) { return silu_fast(z); }
 
 template <typename Tin, int S, int G, bool VEC, bool SPLIT, bool EXT>
 __global__ void __launch_bounds__(kThreads)
@@ -226,7 +225,7 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
         const float *bq = fB + g * S;
         const float *cq = fC + g * S;
         float *yp = y + (b * L + t0) * ED + e;
-        const bool store_ok = (g == 0) && e_ok;
+        const bool store_ok = (g == 0) && e_ok && !(EXT && ex.no_y);
         // Operands of the next step are read from shared memory before this
         // step's result is stored: y is a generic pointer, and the compiler
         // may not move shared loads across a store that could alias them.
@@ -287,6 +286,15 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
         fetch(0, 0);
 #pragma unroll 1
         for (int t = 0; t < kTileT; t += kUnroll) {
+            if (EXT && ex.ckpt && (t & 15) == 0 && e_ok && t0 + t < te) {
+                // state entering steps t0 + t .. t0 + t + 15 (one segment, K = 1)
+                float4 *dst = reinterpret_cast<float4 *>(
+                    ex.ckpt + ((int64_t((t0 + t) >> 4) * (gridDim.x / n_etiles) + b) * ED + e) * 16 +
+                    g * S);
+#pragma unroll
+                for (int q = 0; q < S / 4; ++q)
+                    dst[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+            }
 #pragma unroll
             for (int u = 0; u < kUnroll; u += 2) {
                 fetch(t + u + 1, 1);
@@ -634,7 +642,8 @@ cudaError_t launch_impl(const Tin *x, const Tin *dlt, const float *A, const Tin 
                         const Tin *Cm, const float *D, float *y, int64_t Bs, int64_t L,
                         int64_t ED, int64_t N, int num_sms, const Ext &ex, cudaStream_t st) {
     const int esz = int(sizeof(Tin));
-    Plan p = plan_for(Bs, L, ED, N, esz, num_sms);
+    // checkpointing for the gradients needs the true state at every step: one segment
+    Plan p = (EXT && ex.ckpt) ? Plan{16, 1, 1, int(L)} : plan_for(Bs, L, ED, N, esz, num_sms);
     const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(dlt) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(Bm) % 16 == 0) &&

@@ -7,163 +7,258 @@
 // and every input gradient is a sum over (t, n) of g_t with quantities of
 // the forward pass (h_{t-1}, a_t): see the formulas at diag_bwd_kernel.
 //
-// Two passes.  The first re-runs the forward recurrence and keeps the state
-// entering every kSeg-step segment (checkpoints).  The second walks the
+// Two passes.  The first is the forward scan itself (its kernel run as one
+// time segment, y not written), keeping the state entering every kSeg-step
+// segment (checkpoints).  The second walks the
 // segments from the last to the first: it re-runs a segment forward from its
 // checkpoint into shared memory (the entering state of each step), then
-// walks the segment backwards carrying g.  Gradients of the per-channel
-// parameters (A, D) are summed in registers and added once per thread;
-// gradients of B and C are sums over the channels of one batch row: each
-// warp reduces its 32 channels through shared memory and adds one value per
-// (t, n) to global memory with an atomic add.
+// walks the segment backwards carrying g.  Four lanes share a channel, each
+// with four of the 16 (padded) states, so a CTA of 256 threads covers 64
+// channels of one batch row.  The segment's inputs are staged into shared
+// memory one segment ahead.  Gradients of the per-channel parameters (A, D)
+// are summed in registers and added once per thread; gradients of B and C
+// are sums over channels: each warp reduces its 8 channels with shuffles,
+// the CTA sums its 8 warps once per segment and adds one value per (t, n)
+// with an atomic add.
 #include "ssm_common.cuh"
 
 namespace ssm {
+namespace diag {
+template <typename Tin>
+cudaError_t launch_ext(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
+                       const float *D, float *y, int64_t Bs, int64_t L, int64_t ED, int64_t N,
+                       int num_sms, const ScanOpts &ex, cudaStream_t st);
+}  // namespace diag
+
 namespace diag_bwd {
 
-constexpr int kNP = 16;       // states (padded)
-constexpr int kSeg = 16;      // steps per checkpointed segment
-constexpr int kCh = 64;       // channels per CTA (two warps)
+constexpr int kNP = 16;               // states (padded)
+constexpr int kLanes = 4;             // lanes per channel
+constexpr int kSpl = kNP / kLanes;    // states per lane
+constexpr int kSeg = 16;              // steps per checkpointed segment (the forward kernel's)
+constexpr int kThreads = 256;
+constexpr int kCh = kThreads / kLanes;    // channels per CTA
+constexpr int kWarps = kThreads / 32;
 
-// State entering segment k of channel c: ckpt[(k * nch + c) * 16 + n].
+// Inputs of one segment, staged in shared memory.
 template <typename Tin>
-__global__ void __launch_bounds__(kCh)
-diag_ckpt_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
-                 const float *__restrict__ A, const Tin *__restrict__ Bm, float *__restrict__ ckpt,
-                 int Bs, int L, int ED, int N) {
-    const int64_t b = blockIdx.y;
-    const int e = blockIdx.x * kCh + threadIdx.x;
-    if (e >= ED) return;
-    const int64_t c = b * ED + e;
-    const int64_t nch = int64_t(Bs) * ED;
-    float A2[kNP], h[kNP];
-#pragma unroll
-    for (int n = 0; n < kNP; ++n) {
-        A2[n] = n < N ? A[int64_t(e) * N + n] * SSM_LOG2E : 0.0f;
-        h[n] = 0.0f;
-    }
-    for (int t = 0; t < L; ++t) {
-        if (t % kSeg == 0) {
-            float4 *dst = reinterpret_cast<float4 *>(ckpt + ((int64_t(t / kSeg) * nch + c) * kNP));
-#pragma unroll
-            for (int q = 0; q < kNP / 4; ++q)
-                dst[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+struct Stage {
+    Tin x[kSeg][kCh];
+    Tin d[kSeg][kCh];
+    float dy[kSeg][kCh];
+    Tin B[kSeg][kNP];
+    Tin C[kSeg][kNP];
+};
+
+template <typename Tin>
+struct Shared {
+    float hist[kSeg][kNP][kCh];           // state entering each step of the segment
+    float red[kWarps][kSeg][2 * kNP];     // per-warp sums of dB_t, dC_t over the warp's channels
+    Stage<Tin> st[2];
+};
+
+// Stage rows [t0, t0 + kSeg) of the segment (rows past L and channels past
+// ED zero filled).  VEC: 16-byte cp.async copies (the caller checked that
+// every row start is 16-byte aligned).
+template <typename Tin, bool VEC>
+__device__ __forceinline__ void stage_segment(Stage<Tin> &s, const Tin *__restrict__ x,
+                                              const Tin *__restrict__ dlt,
+                                              const float *__restrict__ dy,
+                                              const Tin *__restrict__ Bm, const Tin *__restrict__ Cm,
+                                              int64_t b, int t0, int L, int e0, int ED, int N) {
+    const int tid = threadIdx.x;
+    const int rows = min(kSeg, L - t0);
+    if constexpr (VEC) {
+        constexpr int EPC = 16 / sizeof(Tin);
+        constexpr int CPR = kCh / EPC;                 // chunks per x row
+        for (int i = tid; i < kSeg * CPR; i += kThreads) {
+            const int t = i / CPR, cc = i % CPR;
+            const int e = e0 + cc * EPC;
+            const bool ok = t < rows && e < ED;
+            const int64_t g = ok ? (b * L + t0 + t) * ED + e : 0;
+            cp_async16(&s.x[t][cc * EPC], x + g, ok ? 16 : 0);
+            cp_async16(&s.d[t][cc * EPC], dlt + g, ok ? 16 : 0);
         }
-        const int64_t i = (b * L + t) * ED + e;
-        const float dl = to_f32(dlt[i]), dlx = dl * to_f32(x[i]);
-        const Tin *br = Bm + (b * L + t) * N;
-#pragma unroll
-        for (int n = 0; n < kNP; ++n) {
-            const float bv = n < N ? to_f32(br[n]) : 0.0f;
-            h[n] = fmaf(ex2(dl * A2[n]), h[n], dlx * bv);
+        constexpr int CPRY = kCh / 4;
+        for (int i = tid; i < kSeg * CPRY; i += kThreads) {
+            const int t = i / CPRY, cc = i % CPRY;
+            const int e = e0 + cc * 4;
+            const bool ok = t < rows && e < ED;
+            cp_async16(&s.dy[t][cc * 4], dy + (ok ? (b * L + t0 + t) * ED + e : 0), ok ? 16 : 0);
+        }
+        // B, C rows: N == 16 here, one contiguous block of rows * 16 values
+        const int nchunk = kSeg * kNP / EPC;
+        const int64_t base = (b * L + t0) * kNP;
+        for (int i = tid; i < nchunk; i += kThreads) {
+            const bool ok = i * EPC < rows * kNP;
+            const int64_t g = ok ? base + int64_t(i) * EPC : 0;
+            cp_async16(&s.B[0][0] + i * EPC, Bm + g, ok ? 16 : 0);
+            cp_async16(&s.C[0][0] + i * EPC, Cm + g, ok ? 16 : 0);
+        }
+    } else {
+        for (int i = tid; i < kSeg * kCh; i += kThreads) {
+            const int t = i / kCh, cc = i % kCh;
+            const int e = e0 + cc;
+            const bool ok = t < rows && e < ED;
+            const int64_t g = (b * L + t0 + t) * ED + e;
+            s.x[t][cc] = ok ? x[g] : Tin(0.0f);
+            s.d[t][cc] = ok ? dlt[g] : Tin(0.0f);
+            s.dy[t][cc] = ok ? dy[g] : 0.0f;
+        }
+        for (int i = tid; i < kSeg * kNP; i += kThreads) {
+            const int t = i / kNP, n = i % kNP;
+            const bool ok = t < rows && n < N;
+            const int64_t g = (b * L + t0 + t) * N + n;
+            s.B[t][n] = ok ? Bm[g] : Tin(0.0f);
+            s.C[t][n] = ok ? Cm[g] : Tin(0.0f);
         }
     }
 }
 
-// Reverse pass.  Per step t (thread = channel e of batch row b), with
-// hp = h_{t-1} and g = g_t:
+// Reverse pass.  Per step t (channel e of batch row b), with hp = h_{t-1}
+// and g = g_t:
 //   dx_t     = sum_n g[n] delta_t B_t[n] + D[e] dy_t
 //   ddelta_t = sum_n g[n] (A[e,n] a_t[n] hp[n] + B_t[n] x_t)
 //   dA[e,n] += g[n] delta_t a_t[n] hp[n]
 //   dB_t[n] += g[n] delta_t x_t        (summed over the channels e)
 //   dC_t[n] += dy_t h_t[n]             (summed over the channels e)
 //   dD[e]   += dy_t x_t
-template <typename Tin>
-__global__ void __launch_bounds__(kCh)
+template <typename Tin, bool VEC>
+__global__ void __launch_bounds__(kThreads)
 diag_bwd_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt, const float *__restrict__ A,
                 const Tin *__restrict__ Bm, const Tin *__restrict__ Cm, const float *__restrict__ D,
                 const float *__restrict__ dy, const float *__restrict__ ckpt,
                 float *__restrict__ dx, float *__restrict__ ddelta, float *__restrict__ dA,
                 float *__restrict__ dB, float *__restrict__ dC, float *__restrict__ dD, int Bs,
                 int L, int ED, int N) {
-    extern __shared__ float smem[];
-    float *hist = smem;                                  // [kSeg][kNP][kCh]: h_{t-1} per step
-    float *red = smem + kSeg * kNP * kCh;                // [2 warps][32 lanes][2 * kNP + 1]
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Shared<Tin> &sm = *reinterpret_cast<Shared<Tin> *>(smem_raw);
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int q = tid % kLanes;                      // states q*4 .. q*4+3
+    const int cl = tid / kLanes;                     // channel within the CTA
     const int64_t b = blockIdx.y;
-    const int e = blockIdx.x * kCh + threadIdx.x;
+    const int e0 = blockIdx.x * kCh;
+    const int e = e0 + cl;
     const bool e_ok = e < ED;
-    const int ec = e_ok ? e : ED - 1;                    // lanes past ED mirror a channel, add zero
+    const int ec = e_ok ? e : ED - 1;                // lanes past ED mirror a channel, add zero
     const int64_t c = b * ED + ec;
     const int64_t nch = int64_t(Bs) * ED;
-    float A2[kNP], An[kNP], g[kNP], lA[kNP];
+    float A2[kSpl], An[kSpl], g[kSpl], lA[kSpl];
 #pragma unroll
-    for (int n = 0; n < kNP; ++n) {
-        An[n] = n < N ? A[int64_t(ec) * N + n] : 0.0f;
-        A2[n] = An[n] * SSM_LOG2E;
-        g[n] = 0.0f;
-        lA[n] = 0.0f;
+    for (int i = 0; i < kSpl; ++i) {
+        const int n = q * kSpl + i;
+        An[i] = n < N ? A[int64_t(ec) * N + n] : 0.0f;
+        A2[i] = An[i] * SSM_LOG2E;
+        g[i] = 0.0f;
+        lA[i] = 0.0f;
     }
     const float Dv = D ? D[ec] : 0.0f;
     float lD = 0.0f;
-    float *myred = red + (warp * 32 + lane) * (2 * kNP + 1);
     const int nseg = (L + kSeg - 1) / kSeg;
+
+    stage_segment<Tin, VEC>(sm.st[(nseg - 1) & 1], x, dlt, dy, Bm, Cm, b, (nseg - 1) * kSeg, L, e0,
+                            ED, N);
+    cp_async_commit();
     for (int k = nseg - 1; k >= 0; --k) {
+        Stage<Tin> &s = sm.st[k & 1];
+        if (k > 0)
+            stage_segment<Tin, VEC>(sm.st[(k - 1) & 1], x, dlt, dy, Bm, Cm, b, (k - 1) * kSeg, L,
+                                    e0, ED, N);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();                              // segment k staged everywhere
         const int t0 = k * kSeg;
         const int tl = min(kSeg, L - t0);
-        float h[kNP];
+        float h[kSpl];
         {
-            const float4 *src = reinterpret_cast<const float4 *>(ckpt + (int64_t(k) * nch + c) * kNP);
-#pragma unroll
-            for (int q = 0; q < kNP / 4; ++q) {
-                const float4 v = src[q];
-                h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
-            }
+            const float4 v = *reinterpret_cast<const float4 *>(ckpt + (int64_t(k) * nch + c) * kNP +
+                                                               q * kSpl);
+            h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
         }
         // forward over the segment: keep the entering state of every step
         for (int j = 0; j < tl; ++j) {
-            const int64_t i = (b * L + t0 + j) * ED + ec;
-            const float dl = to_f32(dlt[i]), dlx = dl * to_f32(x[i]);
-            const Tin *br = Bm + (b * L + t0 + j) * N;
+            const float dl = to_f32(s.d[j][cl]), dlx = dl * to_f32(s.x[j][cl]);
 #pragma unroll
-            for (int n = 0; n < kNP; ++n) {
-                hist[(j * kNP + n) * kCh + threadIdx.x] = h[n];
-                const float bv = n < N ? to_f32(br[n]) : 0.0f;
-                h[n] = fmaf(ex2(dl * A2[n]), h[n], dlx * bv);
+            for (int i = 0; i < kSpl; ++i) {
+                const int n = q * kSpl + i;
+                sm.hist[j][n][cl] = h[i];
+                h[i] = fmaf(ex2(dl * A2[i]), h[i], dlx * to_f32(s.B[j][n]));
             }
         }
         // backward over the segment
         for (int j = tl - 1; j >= 0; --j) {
-            const int t = t0 + j;
-            const int64_t i = (b * L + t) * ED + ec;
-            const float dl = to_f32(dlt[i]), xv = to_f32(x[i]);
-            const float gy = e_ok ? dy[i] : 0.0f;
-            const Tin *br = Bm + (b * L + t) * N;
-            const Tin *cr = Cm + (b * L + t) * N;
-            float sdx = 0.0f, sdd = 0.0f;
+            const float dl = to_f32(s.d[j][cl]), xv = to_f32(s.x[j][cl]);
+            const float gy = s.dy[j][cl];                 // zero past ED
+            float sdx = 0.0f, sdd = 0.0f, vb[kSpl], vc[kSpl];
 #pragma unroll
-            for (int n = 0; n < kNP; ++n) {
-                const float bv = n < N ? to_f32(br[n]) : 0.0f;
-                const float cv = n < N ? to_f32(cr[n]) : 0.0f;
-                const float a = ex2(dl * A2[n]);
-                const float hp = hist[(j * kNP + n) * kCh + threadIdx.x];
-                g[n] = fmaf(gy, cv, g[n]);                      // g_t
-                sdx = fmaf(g[n] * dl, bv, sdx);
-                sdd = fmaf(g[n], fmaf(An[n] * a, hp, bv * xv), sdd);
-                lA[n] = fmaf(g[n] * dl * a, hp, lA[n]);
-                myred[n] = e_ok ? g[n] * dl * xv : 0.0f;        // this channel's share of dB_t[n]
-                myred[kNP + n] = gy * fmaf(a, hp, dl * bv * xv);  // share of dC_t[n] (dy_t h_t[n])
-                g[n] *= a;                                      // a_t g_t, for step t - 1
+            for (int i = 0; i < kSpl; ++i) {
+                const int n = q * kSpl + i;
+                const float bv = to_f32(s.B[j][n]), cv = to_f32(s.C[j][n]);
+                const float a = ex2(dl * A2[i]);
+                const float hp = sm.hist[j][n][cl];
+                g[i] = fmaf(gy, cv, g[i]);                      // g_t
+                sdx = fmaf(g[i] * dl, bv, sdx);
+                sdd = fmaf(g[i], fmaf(An[i] * a, hp, bv * xv), sdd);
+                lA[i] = fmaf(g[i] * dl * a, hp, lA[i]);
+                vb[i] = e_ok ? g[i] * dl * xv : 0.0f;           // share of dB_t[n]
+                vc[i] = gy * fmaf(a, hp, dl * bv * xv);         // share of dC_t[n] (dy_t h_t[n])
+                g[i] *= a;                                      // a_t g_t, for step t - 1
             }
-            if (e_ok) {
+            // the channel's four lanes hold disjoint states: sum their parts
+            sdx += __shfl_xor_sync(0xffffffffu, sdx, 1);
+            sdd += __shfl_xor_sync(0xffffffffu, sdd, 1);
+            sdx += __shfl_xor_sync(0xffffffffu, sdx, 2);
+            sdd += __shfl_xor_sync(0xffffffffu, sdd, 2);
+            if (q == 0 && e_ok) {
+                const int64_t i = (b * L + t0 + j) * ED + e;
                 dx[i] = fmaf(Dv, gy, sdx);
                 ddelta[i] = sdd;
                 lD = fmaf(gy, xv, lD);
             }
-            __syncwarp();
-            // lane l sums column l (l < 16: dB_t[l]; l >= 16: dC_t[l - 16]) over the warp
-            float s = 0.0f;
-            for (int r = 0; r < 32; ++r) s += red[(warp * 32 + r) * (2 * kNP + 1) + lane];
-            const int n = lane & (kNP - 1);
-            if (n < N) atomicAdd((lane < kNP ? dB : dC) + (b * L + t) * N + n, s);
-            __syncwarp();
+            // Sum the 8 values (dB, dC shares of this lane's states) over the
+            // warp's 8 channels (lane = 4 * channel + q) by halving exchanges:
+            // at each level a lane keeps half of its values, adds the partner's
+            // copy of that half and hands over the other half; after three
+            // levels lane (channel c, q) holds the warp sum of value c.
+            float v[8] = {vb[0], vb[1], vb[2], vb[3], vc[0], vc[1], vc[2], vc[3]};
+#pragma unroll
+            for (int lvl = 0, half = 4; lvl < 3; ++lvl, half >>= 1) {
+                const bool hi = (lane >> (4 - lvl)) & 1;     // channel bit 2 - lvl
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float keep = hi ? v[i + half] : v[i];
+                    const float give = hi ? v[i] : v[i + half];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, give, 16 >> lvl);
+                }
+            }
+            {
+                const int o = lane >> 2;                       // value index 0..7
+                sm.red[warp][j][(o < 4 ? 0 : kNP) + q * kSpl + (o & 3)] = v[0];
+            }
         }
+        __syncthreads();                              // per-warp sums of the segment are in place
+        // one atomic add per (t, n) for B and C
+        for (int o = tid; o < tl * 2 * kNP; o += kThreads) {
+            const int j = o / (2 * kNP), r = o % (2 * kNP);
+            const int n = r % kNP;
+            if (n >= N) continue;
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) sum += sm.red[w][j][r];
+            atomicAdd((r < kNP ? dB : dC) + (b * L + t0 + j) * N + n, sum);
+        }
+        // the next iteration's staging (issued above) and this one's reads of
+        // s, hist and red are ordered by the barrier at its top
     }
+    cp_async_wait<0>();
     if (e_ok) {
 #pragma unroll
-        for (int n = 0; n < kNP; ++n)
-            if (n < N) atomicAdd(dA + int64_t(e) * N + n, lA[n]);
-        if (dD) atomicAdd(dD + e, lD);
+        for (int i = 0; i < kSpl; ++i) {
+            const int n = q * kSpl + i;
+            if (n < N) atomicAdd(dA + int64_t(e) * N + n, lA[i]);
+        }
+        if (dD && q == 0) atomicAdd(dD + e, lD);
     }
 }
 
@@ -171,7 +266,7 @@ template <typename Tin>
 cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
                        const float *D, const float *dy, float *dx, float *ddelta, float *dA,
                        float *dB, float *dC, float *dD, int64_t Bs, int64_t L, int64_t ED,
-                       int64_t N, cudaStream_t st) {
+                       int64_t N, int num_sms, cudaStream_t st) {
     if (N > kNP) return cudaErrorNotSupported;
     if (Bs > 65535) return cudaErrorInvalidConfiguration;
     // parameter gradients are sums: start from zero
@@ -186,16 +281,25 @@ cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *
     if (err != cudaSuccess) return err;
     float *ckpt = static_cast<float *>(scratch);
     const dim3 grid(unsigned((ED + kCh - 1) / kCh), unsigned(Bs));
-    diag_ckpt_kernel<Tin><<<grid, kCh, 0, st>>>(x, dlt, A, Bm, ckpt, int(Bs), int(L), int(ED), int(N));
-    err = cudaGetLastError();
+    // forward pass for the checkpoints (dx stands in for y, which is not written)
+    ScanOpts fw{};
+    fw.ckpt = ckpt;
+    fw.no_y = 1;
+    err = diag::launch_ext<Tin>(x, dlt, A, Bm, Cm, D, dx, Bs, L, ED, N, num_sms, fw, st);
     if (err == cudaSuccess) {
-        const int smem = int((kSeg * kNP * kCh + 2 * 32 * (2 * kNP + 1)) * sizeof(float));
-        err = cudaFuncSetAttribute(diag_bwd_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem);
+        const size_t esz = sizeof(Tin);
+        const bool vec = N == kNP && (ED * esz) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(dlt) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(dy) % 16 == 0 && ED % 4 == 0 &&
+                         reinterpret_cast<uintptr_t>(Bm) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(Cm) % 16 == 0;
+        const int smem = int(sizeof(Shared<Tin>));
+        auto kern = vec ? diag_bwd_kernel<Tin, true> : diag_bwd_kernel<Tin, false>;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (err == cudaSuccess) {
-            diag_bwd_kernel<Tin><<<grid, kCh, smem, st>>>(x, dlt, A, Bm, Cm, D, dy, ckpt, dx, ddelta,
-                                                          dA, dB, dC, dD, int(Bs), int(L), int(ED),
-                                                          int(N));
+            kern<<<grid, kThreads, smem, st>>>(x, dlt, A, Bm, Cm, D, dy, ckpt, dx, ddelta, dA, dB,
+                                               dC, dD, int(Bs), int(L), int(ED), int(N));
             err = cudaGetLastError();
         }
     }
@@ -206,12 +310,12 @@ cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *
 template cudaError_t launch_bwd<float>(const float *, const float *, const float *, const float *,
                                        const float *, const float *, const float *, float *,
                                        float *, float *, float *, float *, float *, int64_t,
-                                       int64_t, int64_t, int64_t, cudaStream_t);
+                                       int64_t, int64_t, int64_t, int, cudaStream_t);
 template cudaError_t launch_bwd<__nv_bfloat16>(const __nv_bfloat16 *, const __nv_bfloat16 *,
                                                const float *, const __nv_bfloat16 *,
                                                const __nv_bfloat16 *, const float *, const float *,
                                                float *, float *, float *, float *, float *,
-                                               float *, int64_t, int64_t, int64_t, int64_t,
+                                               float *, int64_t, int64_t, int64_t, int64_t, int,
                                                cudaStream_t);
 
 }  // namespace diag_bwd

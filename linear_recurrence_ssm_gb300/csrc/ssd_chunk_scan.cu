@@ -294,8 +294,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
         float d = __bfloat162float(prm.dt[(int64_t(b) * L + r) * prm.H + h]);
         if (EXT) {
             d += dbias;
-            // log(1 + e^d); above 20 the correction is below fp32 resolution
-            if (prm.dt_softplus) d = d > 20.0f ? d : log1pf(__expf(d));
+            if (prm.dt_softplus) d = softplus_fast(d);
             if (prm.dt_limit) d = fminf(fmaxf(d, prm.dt_min), prm.dt_max);
         }
         return d;
@@ -622,8 +621,8 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const float2 zz = unpack_bf16(w4[k]);
-                        out[8 * j + 2 * k] *= zz.x / (1.0f + __expf(-zz.x));
-                        out[8 * j + 2 * k + 1] *= zz.y / (1.0f + __expf(-zz.y));
+                        out[8 * j + 2 * k] *= silu_fast(zz.x);
+                        out[8 * j + 2 * k + 1] *= silu_fast(zz.y);
                     }
                 }
             }

@@ -24,6 +24,11 @@ struct ScanOpts {
     float dt_min, dt_max;
     int dt_softplus, dt_limit;
     int ngroups;            // SSD: groups of B, C (0 or 1 = one group)
+    // internal (gradients of the diagonal scan): the forward pass keeps the
+    // state entering every 16-step segment, ckpt[(k * Bs * ED + c) * 16 + n],
+    // and may skip writing y
+    float *ckpt;
+    int no_y;
 };
 
 // ---- element conversion ---------------------------------------------------
@@ -45,6 +50,17 @@ __device__ __forceinline__ float ex2(float v) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
     return r;
 }
+
+// softplus(d) = log(1 + e^d) on the special-function unit.  Above 20 the
+// correction term is below fp32 resolution; far below 0 the result (~e^d)
+// may flush to 0, an absolute error under 1e-8.
+__device__ __forceinline__ float softplus_fast(float d) {
+    return d > 20.0f ? d : __logf(1.0f + __expf(d));
+}
+
+// silu(z) = z * sigmoid(z) = z / (1 + e^-z); the fast division returns 0 once
+// the denominator is huge (z -> -inf), the function's limit.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // ---- cp.async (Ampere-style asynchronous global -> shared copies) ---------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
