@@ -264,6 +264,16 @@ SSM_API ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float 
  */
 SSM_API ssm_status_t ssm_check_device_errors(void *stream);
 
+/*
+ * Self-test of the timeout path: enqueues on `stream` a one-thread kernel
+ * whose bounded mbarrier wait (the kernels' own wait, 20 ms limit) cannot
+ * complete; it gives up and records the timeout, so the next
+ * ssm_check_device_errors on that stream returns SSM_ERR_DEVICE_TIMEOUT (and
+ * the one after it SSM_OK).  No fault, trap or hang is involved; the context
+ * stays usable.
+ */
+SSM_API ssm_status_t ssm_selftest_wait_timeout(void *stream);
+
 /* Static, human-readable name of a status code. */
 SSM_API const char *ssm_status_string(ssm_status_t status);
 

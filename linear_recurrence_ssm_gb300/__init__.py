@@ -56,6 +56,7 @@ SIGNATURES = {
     "ssm_scan_bwd": ([_VP] * 13 + [_I64] * 4 + [ctypes.c_int, _VP], ctypes.c_int),
     "ssd_chunk_scan_fwd_ex": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
     "ssm_check_device_errors": ([_VP], ctypes.c_int),
+    "ssm_selftest_wait_timeout": ([_VP], ctypes.c_int),
     "ssm_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "ssm_version": ([], ctypes.c_int),
 }

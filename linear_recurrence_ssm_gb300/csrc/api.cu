@@ -36,6 +36,7 @@ cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float 
                    int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N, int64_t chunk,
                    bool bidirectional, int num_sms, cudaStream_t st, const ScanOpts *opt);
 cudaError_t take_device_error(unsigned int *out);
+cudaError_t probe_wait_timeout(cudaStream_t st);
 size_t noalloc_scratch_needed(int64_t Bs, int64_t L, int64_t H, int64_t N, bool bidirectional);
 cudaError_t launch_noalloc(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
                            const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D,
@@ -320,6 +321,13 @@ ssm_status_t ssm_check_device_errors(void *stream) {
     unsigned int flag = 0;
     if (ssm::ssd::take_device_error(&flag) != cudaSuccess) return SSM_ERR_CUDA;
     return flag ? SSM_ERR_DEVICE_TIMEOUT : SSM_OK;
+}
+
+ssm_status_t ssm_selftest_wait_timeout(void *stream) {
+    DeviceInfo dev;
+    ssm_status_t s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    return from_cuda(ssm::ssd::probe_wait_timeout(static_cast<cudaStream_t>(stream)));
 }
 
 const char *ssm_status_string(ssm_status_t status) {

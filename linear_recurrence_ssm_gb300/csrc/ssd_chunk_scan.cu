@@ -864,6 +864,22 @@ cudaError_t launch_noalloc(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, cons
     return launch_nb<2>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream, scratch);
 }
 
+// Self-test of the timeout path: one thread waits on an mbarrier that
+// nothing ever arrives on, with the kernels' bounded wait and a short limit,
+// and reports through the same error word when the wait runs out.
+__global__ void wait_timeout_probe_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    volatile int never = 0;
+    if (!mbar_wait_bounded(&bar, 0, &never, limit_ns)) atomicOr(&g_device_error, 1u);
+}
+
+cudaError_t probe_wait_timeout(cudaStream_t st) {
+    wait_timeout_probe_kernel<<<1, 1, 0, st>>>(20000000ull);   // 20 ms
+    return cudaGetLastError();
+}
+
 // Read and clear the device error word (host side, synchronous).
 cudaError_t take_device_error(unsigned int *out) {
     unsigned int v = 0;

@@ -4,6 +4,8 @@ against the fp64 oracle on the same bf16-rounded inputs.
 Tolerance: max|y - y_ref| <= 2e-2 * max|y_ref| (bf16 inputs, bf16 tensor-core
 operands with fp32 accumulation and fp32 state).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -115,3 +117,18 @@ def test_runs_on_caller_stream(cuda_device):
         y = lrs.ssd_chunk_scan_fwd(**inp, chunk=128, bidirectional=True)
     s.synchronize()
     assert torch.equal(y, ref)
+
+
+def test_bounded_wait_reports_timeout(cuda_device):
+    """A bounded wait that cannot complete gives up, the error word records it,
+    the check reports it once and the context stays usable."""
+    lib = lrs.library()
+    stream = ctypes.c_void_p(torch.cuda.current_stream(cuda_device).cuda_stream)
+    assert lib.ssm_check_device_errors(stream) == 0
+    assert lib.ssm_selftest_wait_timeout(stream) == 0
+    assert lib.ssm_check_device_errors(stream) == 5      # SSM_ERR_DEVICE_TIMEOUT
+    assert lib.ssm_check_device_errors(stream) == 0      # cleared
+    inp = workloads.ssd_inputs(1, 200, 2, 64, 64, "bf16", seed=3)
+    y = lrs.ssd_chunk_scan_fwd(**{k: v.to(cuda_device) for k, v in inp.items()})
+    torch.cuda.synchronize()
+    _check(y, oracle.ssd_scan(**inp))
