@@ -119,17 +119,21 @@ SSM_API ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED,
  *   D  : (H) fp32 or NULL          y  : (Bs, L, H, P) fp32 output
  *   chunk : time-chunk length Q of the chunked algorithm.
  *   bidirectional : 0 = forward scan; != 0 = forward + reversed scan + D x.
- * Supported: P == 64; N in {64, 128}; chunk in {64, 128, 256}; any
- * Bs, L, H >= 1 (L need not be a multiple of chunk).  x, B, C and y must be
- * 16-byte aligned, dt 2-byte aligned (SSM_ERR_ALIGNMENT otherwise).
+ * Supported: P in {16, 32, 64, 128}, N in {32, 64, 128, 256} with
+ * P * N <= 16384; chunk in {64, 128, 256}; any Bs, L, H >= 1 (L need not be
+ * a multiple of chunk).  x, B, C and y must be 16-byte aligned, dt aligned
+ * to its element size (SSM_ERR_ALIGNMENT otherwise).  bf16 inputs with
+ * P == 64 and N in {64, 128} run on the tensor cores (tcgen05); every other
+ * supported shape, and fp32 inputs (ssd_chunk_scan_fwd_ex), on CUDA cores.
  * The chunked result equals the recurrence for every chunk length (up to
- * rounding).  The kernel passes the state between 128-row tiles -- the
- * tensor-core tile height -- so a chunk of 256 rows is computed as two
- * 128-row tiles and a chunk of 64 as half of one; `chunk` is validated and
- * does not change the result beyond rounding.
- * Bidirectional calls with L > 128 take a stream-ordered scratch buffer of
- * Bs*H*ceil(L/128)*P*N*2 bytes (cudaMallocAsync / cudaFreeAsync on
- * `stream`) for the reverse scan's entering states.
+ * rounding).  The tensor-core kernel passes the state between 128-row tiles
+ * -- the tensor-core tile height -- so a chunk of 256 rows is computed as
+ * two 128-row tiles and a chunk of 64 as half of one; `chunk` is validated
+ * and does not change the result beyond rounding.
+ * Bidirectional calls of the tensor-core kernel with L > 128 take a
+ * stream-ordered scratch buffer of Bs*H*ceil(L/128)*P*N*2 bytes
+ * (cudaMallocAsync / cudaFreeAsync on `stream`) for the reverse scan's
+ * entering states; the CUDA-core kernel needs none.
  */
 SSM_API ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt,
                                 const float *A_head, const void *B,
@@ -220,15 +224,18 @@ SSM_API ssm_status_t ssm_scan_fwd_ex(const void *x, const void *delta, const flo
                                      const ssm_scan_options_t *opts, void *stream);
 
 /*
- * ssd_chunk_scan_fwd with options (same arguments, support and scratch
- * rules; z is bf16 and 16-byte aligned; `opts` may be NULL).
+ * ssd_chunk_scan_fwd with options and a choice of input type: input_bf16
+ * selects the element type of x, dt, B, C and z (0 = fp32, else bf16).
+ * Same arguments, support and scratch rules otherwise; z is 16-byte aligned;
+ * `opts` may be NULL.
  */
 SSM_API ssm_status_t ssd_chunk_scan_fwd_ex(const void *x, const void *dt,
                                            const float *A_head, const void *B,
                                            const void *C, const float *D, float *y,
                                            int64_t Bs, int64_t L, int64_t H, int64_t P,
                                            int64_t N, int64_t chunk, int bidirectional,
-                                           const ssm_scan_options_t *opts, void *stream);
+                                           int input_bf16, const ssm_scan_options_t *opts,
+                                           void *stream);
 
 /*
  * Gradients of the diagonal scan (ssm_scan_fwd without options): given dy,

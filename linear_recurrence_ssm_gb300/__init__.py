@@ -16,7 +16,7 @@ ssm_scan_fwd(x, delta, A, B, C, D=None, y=None, **options)
     ``ssm_scan_fwd_bf16``.  Returns y (Bs, L, ED) fp32.
 ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk=256, bidirectional=False, y=None, **options)
     Chunked scalar-decay scan ("Some questions of Bi-Mamba2 and Hydra",
-    Bi-Mamba2 issue 1).  x: (Bs, L, H, P) bf16; dt: (Bs, L, H) bf16;
+    Bi-Mamba2 issue 1).  x: (Bs, L, H, P) bf16 or fp32; dt: (Bs, L, H), same type;
     A_head: (H) fp32; B, C: (Bs, L, N) or (Bs, L, G, N) bf16 (head h reads
     group h // (H // G)); D: (H) fp32.  Returns y (Bs, L, H, P) fp32.
 
@@ -54,7 +54,8 @@ SIGNATURES = {
                           ctypes.c_int),
     "ssm_scan_fwd_ex": ([_VP] * 7 + [_I64] * 4 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
     "ssm_scan_bwd": ([_VP] * 13 + [_I64] * 4 + [ctypes.c_int, _VP], ctypes.c_int),
-    "ssd_chunk_scan_fwd_ex": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
+    "ssd_chunk_scan_fwd_ex": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, ctypes.c_int, _VP, _VP],
+                              ctypes.c_int),
     "ssm_check_device_errors": ([_VP], ctypes.c_int),
     "ssm_selftest_wait_timeout": ([_VP], ctypes.c_int),
     "ssm_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -224,7 +225,9 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
     dev = x.device
     if dev.type != "cuda":
         raise ValueError("inputs must be CUDA tensors")
-    bf = (torch.bfloat16,)
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("x must be bf16 or fp32")
+    bf = (x.dtype,)
     _check(x, "x", bf, dev, (4,))
     _check(dt, "dt", bf, dev, (3,))
     _check(B, "B", bf, dev, (3, 4))
@@ -248,11 +251,12 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
         raise TypeError("unknown options: %s" % sorted(bad))
     if G > 1:
         options = dict(options, ngroups=G)
-    if options:
+    if options or x.dtype != torch.bfloat16:
         o, hf, keep = _options(x, H, (Bs, H, P, N), dev, **options)
         st = library().ssd_chunk_scan_fwd_ex(_ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C),
                                              _ptr(D), _ptr(y), Bs, L, H, P, N, int(chunk),
-                                             int(bool(bidirectional)), ctypes.byref(o),
+                                             int(bool(bidirectional)),
+                                             int(x.dtype == torch.bfloat16), ctypes.byref(o),
                                              _stream(dev))
         if st != 0:
             raise SsmError("ssd_chunk_scan_fwd_ex", st)

@@ -30,6 +30,13 @@ cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *
                        float *dB, float *dC, float *dD, int64_t Bs, int64_t L, int64_t ED,
                        int64_t N, int num_sms, cudaStream_t st);
 }
+namespace ssd_general {
+bool supported(int64_t P, int64_t N);
+template <typename Tin>
+cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *Bm, const Tin *Cm,
+                   const float *D, float *y, int64_t Bs, int64_t L, int64_t H, int64_t P,
+                   int64_t N, bool bidir, const ScanOpts *opt, cudaStream_t st);
+}
 namespace ssd {
 cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
                    const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
@@ -144,6 +151,67 @@ ssm_status_t diag_entry(const Tin *x, const Tin *delta, const float *A, const Ti
                                             static_cast<cudaStream_t>(stream)));
 }
 
+
+// The chunked scan: validation, then the tensor-core kernel (bf16, P = 64,
+// N in {64, 128}) or the CUDA-core kernel (every other supported shape and
+// fp32 inputs).  `noalloc`: the reverse states' scratch comes from the fixed
+// module array (the CUDA-core kernel needs none).
+ssm_status_t ssd_entry(const void *x, const void *dt, const float *A_head, const void *B,
+                       const void *C, const float *D, float *y, int64_t Bs, int64_t L, int64_t H,
+                       int64_t P, int64_t N, int64_t chunk, int bidirectional, int input_bf16,
+                       const ssm_scan_options_t *opts, void *stream, bool noalloc) {
+    if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_INVALID_ARG;
+    if (!sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, N}) || chunk < 1) return SSM_ERR_INVALID_ARG;
+    const bool tc = input_bf16 && P == 64 && (N == 64 || N == 128);
+    if (!tc && !ssm::ssd_general::supported(P, N)) return SSM_ERR_UNSUPPORTED;
+    if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
+    if (L > INT_MAX || H > 65535 || Bs > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    if (opts) {
+        if (bidirectional && (opts->h0 || opts->h_final)) return SSM_ERR_UNSUPPORTED;
+        if (opts->ngroups < 0 || (opts->ngroups > 1 && H % opts->ngroups != 0))
+            return SSM_ERR_INVALID_ARG;
+        if (opts->ngroups > 1 && !sizes_ok({Bs, L, opts->ngroups, N})) return SSM_ERR_INVALID_ARG;
+    }
+    if (tc && noalloc &&
+        ssm::ssd::noalloc_scratch_needed(Bs, L, H, N, bidirectional != 0) > SSM_NOALLOC_SCRATCH_BYTES)
+        return SSM_ERR_UNSUPPORTED;
+    const size_t es = input_bf16 ? 2 : 4;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+        !aligned(dt, es) || !aligned(A_head, 4) || (D && !aligned(D, 4)))
+        return SSM_ERR_ALIGNMENT;
+    ssm_status_t s = check_options(opts, 16);
+    if (s != SSM_OK) return s;
+    DeviceInfo dev;
+    s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    using bf = __nv_bfloat16;
+    ssm::ScanOpts o{};
+    if (opts)
+        o = ssm::ScanOpts{opts->dt_bias, opts->z, opts->h0, opts->h_final, opts->dt_min,
+                          opts->dt_max, opts->dt_softplus, opts->dt_limit, opts->ngroups};
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!tc) {
+        if (input_bf16)
+            return from_cuda(ssm::ssd_general::launch<bf>(
+                static_cast<const bf *>(x), static_cast<const bf *>(dt), A_head,
+                static_cast<const bf *>(B), static_cast<const bf *>(C), D, y, Bs, L, H, P, N,
+                bidirectional != 0, opts ? &o : nullptr, st));
+        return from_cuda(ssm::ssd_general::launch<float>(
+            static_cast<const float *>(x), static_cast<const float *>(dt), A_head,
+            static_cast<const float *>(B), static_cast<const float *>(C), D, y, Bs, L, H, P, N,
+            bidirectional != 0, opts ? &o : nullptr, st));
+    }
+    if (noalloc)
+        return from_cuda(ssm::ssd::launch_noalloc(static_cast<const bf *>(x),
+                                                  static_cast<const bf *>(dt), A_head,
+                                                  static_cast<const bf *>(B),
+                                                  static_cast<const bf *>(C), D, y, Bs, L, H, P, N,
+                                                  bidirectional != 0, st));
+    return from_cuda(ssm::ssd::launch(static_cast<const bf *>(x), static_cast<const bf *>(dt),
+                                      A_head, static_cast<const bf *>(B),
+                                      static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
+                                      bidirectional != 0, dev.num_sms, st, opts ? &o : nullptr));
+}
 }  // namespace
 
 extern "C" {
@@ -167,50 +235,16 @@ ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt, const float *A_he
                                 const void *C, const float *D, float *y, int64_t Bs, int64_t L,
                                 int64_t H, int64_t P, int64_t N, int64_t chunk, int bidirectional,
                                 void *stream) {
-    if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_INVALID_ARG;
-    if (!sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, N}) || chunk < 1) return SSM_ERR_INVALID_ARG;
-    if (P != 64) return SSM_ERR_UNSUPPORTED;
-    if (N != 64 && N != 128) return SSM_ERR_UNSUPPORTED;
-    if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
-    if (L > INT_MAX || H > 65535 || Bs > INT_MAX) return SSM_ERR_UNSUPPORTED;
-    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
-        !aligned(dt, 2) || !aligned(A_head, 4) || (D && !aligned(D, 4)))
-        return SSM_ERR_ALIGNMENT;
-    DeviceInfo dev;
-    ssm_status_t s = current_device(&dev);
-    if (s != SSM_OK) return s;
-    using bf = __nv_bfloat16;
-    return from_cuda(ssm::ssd::launch(static_cast<const bf *>(x), static_cast<const bf *>(dt),
-                                      A_head, static_cast<const bf *>(B),
-                                      static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
-                                      bidirectional != 0, dev.num_sms,
-                                      static_cast<cudaStream_t>(stream), nullptr));
+    return ssd_entry(x, dt, A_head, B, C, D, y, Bs, L, H, P, N, chunk, bidirectional, 1, nullptr,
+                     stream, false);
 }
 
 ssm_status_t ssd_chunk_scan_fwd_noalloc(const void *x, const void *dt, const float *A_head,
                                         const void *B, const void *C, const float *D, float *y,
                                         int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
                                         int64_t chunk, int bidirectional, void *stream) {
-    if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_INVALID_ARG;
-    if (!sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, N}) || chunk < 1) return SSM_ERR_INVALID_ARG;
-    if (P != 64) return SSM_ERR_UNSUPPORTED;
-    if (N != 64 && N != 128) return SSM_ERR_UNSUPPORTED;
-    if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
-    if (L > INT_MAX || H > 65535 || Bs > INT_MAX) return SSM_ERR_UNSUPPORTED;
-    if (ssm::ssd::noalloc_scratch_needed(Bs, L, H, N, bidirectional != 0) > SSM_NOALLOC_SCRATCH_BYTES)
-        return SSM_ERR_UNSUPPORTED;
-    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
-        !aligned(dt, 2) || !aligned(A_head, 4) || (D && !aligned(D, 4)))
-        return SSM_ERR_ALIGNMENT;
-    DeviceInfo dev;
-    ssm_status_t s = current_device(&dev);
-    if (s != SSM_OK) return s;
-    using bf = __nv_bfloat16;
-    return from_cuda(ssm::ssd::launch_noalloc(static_cast<const bf *>(x), static_cast<const bf *>(dt),
-                                              A_head, static_cast<const bf *>(B),
-                                              static_cast<const bf *>(C), D, y, Bs, L, H, P, N,
-                                              bidirectional != 0,
-                                              static_cast<cudaStream_t>(stream)));
+    return ssd_entry(x, dt, A_head, B, C, D, y, Bs, L, H, P, N, chunk, bidirectional, 1, nullptr,
+                     stream, true);
 }
 
 ssm_status_t ssm_scan_fwd_ex(const void *x, const void *delta, const float *A, const void *B,
@@ -230,38 +264,10 @@ ssm_status_t ssm_scan_fwd_ex(const void *x, const void *delta, const float *A, c
 ssm_status_t ssd_chunk_scan_fwd_ex(const void *x, const void *dt, const float *A_head,
                                    const void *B, const void *C, const float *D, float *y,
                                    int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
-                                   int64_t chunk, int bidirectional,
+                                   int64_t chunk, int bidirectional, int input_bf16,
                                    const ssm_scan_options_t *opts, void *stream) {
-    if (!opts)
-        return ssd_chunk_scan_fwd(x, dt, A_head, B, C, D, y, Bs, L, H, P, N, chunk, bidirectional,
-                                  stream);
-    if (!x || !dt || !A_head || !B || !C || !y) return SSM_ERR_INVALID_ARG;
-    if (!sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, N}) || chunk < 1) return SSM_ERR_INVALID_ARG;
-    if (P != 64) return SSM_ERR_UNSUPPORTED;
-    if (N != 64 && N != 128) return SSM_ERR_UNSUPPORTED;
-    if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
-    if (L > INT_MAX || H > 65535 || Bs > INT_MAX) return SSM_ERR_UNSUPPORTED;
-    if (bidirectional && (opts->h0 || opts->h_final)) return SSM_ERR_UNSUPPORTED;
-    if (opts->ngroups < 0 || (opts->ngroups > 1 && H % opts->ngroups != 0))
-        return SSM_ERR_INVALID_ARG;
-    if (opts->ngroups > 1 && !sizes_ok({Bs, L, opts->ngroups, N})) return SSM_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
-        !aligned(dt, 2) || !aligned(A_head, 4) || (D && !aligned(D, 4)))
-        return SSM_ERR_ALIGNMENT;
-    ssm_status_t s = check_options(opts, 16);
-    if (s != SSM_OK) return s;
-    DeviceInfo dev;
-    s = current_device(&dev);
-    if (s != SSM_OK) return s;
-    using bf = __nv_bfloat16;
-    const ssm::ScanOpts o{opts->dt_bias, opts->z, opts->h0, opts->h_final,
-                          opts->dt_min, opts->dt_max, opts->dt_softplus, opts->dt_limit,
-                          opts->ngroups};
-    return from_cuda(ssm::ssd::launch(static_cast<const bf *>(x), static_cast<const bf *>(dt),
-                                      A_head, static_cast<const bf *>(B),
-                                      static_cast<const bf *>(C), D, y, Bs, L, H, P, N, chunk,
-                                      bidirectional != 0, dev.num_sms,
-                                      static_cast<cudaStream_t>(stream), &o));
+    return ssd_entry(x, dt, A_head, B, C, D, y, Bs, L, H, P, N, chunk, bidirectional, input_bf16,
+                     opts, stream, false);
 }
 
 ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float *A, const void *B,

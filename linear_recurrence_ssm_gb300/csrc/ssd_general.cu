@@ -1,0 +1,253 @@
+// ssd_general.cu -- the chunked scalar-decay ("SSD") scan on CUDA cores, for
+// the shapes and input types the tensor-core kernel (ssd_chunk_scan.cu: bf16,
+// P = 64, N in {64, 128}) does not take: fp32 inputs, P in {16, 32, 64, 128},
+// N in {32, 64, 128, 256}.
+//
+// Per (b, h), with H_t the P x N state,
+//     H_t = exp(dt_t A_h) H_{t-1} + dt_t x_t (outer) B_t,   y_t = H_t C_t + D_h x_t,
+// walked sequentially over t with the state in registers: a CTA of 256
+// threads owns one (b, h); warp w holds rows p = w, w + 8, ... and lane l
+// columns n = l, l + 32, ... of the state.  y_t[p] is a sum over n: the
+// warp's lanes reduce it with shuffles each step.  The inputs of kT steps
+// are staged in shared memory one tile ahead.  The bidirectional scan runs
+// a second pass from the last step that adds its part to y.  The scan
+// options (dt bias / softplus / clamp, silu gate, initial and final state,
+// groups of B and C) are applied as in the tensor-core kernel.
+#include "ssm_common.cuh"
+
+namespace ssm {
+namespace ssd_general {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kT = 16;            // steps per staged tile
+
+struct Args {
+    const void *x, *dt, *B, *C, *z;
+    const float *A, *D, *dt_bias, *h0;
+    float *y, *h_final;
+    int L, H, P, N, G;
+    float dt_min, dt_max;
+    int dt_softplus, dt_limit;
+};
+
+template <typename Tin>
+struct Tile {
+    Tin x[kT][128];
+    Tin B[kT][256];
+    Tin C[kT][256];
+    float dt[kT];
+};
+
+// Stage the x, B, C rows of steps [t0, t0 + kT) (in walk order: `rev`
+// walks backwards) of one (b, h) with 16-byte asynchronous copies (rows are
+// multiples of 16 bytes; the entry points require 16-byte aligned x, B, C).
+// Rows outside [0, L) are zero filled.
+template <typename Tin>
+__device__ __forceinline__ void stage_rows(Tile<Tin> &s, const Args &a, int64_t b, int h, int g,
+                                           int t0, bool rev) {
+    constexpr int EPC = 16 / sizeof(Tin);
+    const Tin *x = static_cast<const Tin *>(a.x);
+    const Tin *Bm = static_cast<const Tin *>(a.B);
+    const Tin *Cm = static_cast<const Tin *>(a.C);
+    const int cpx = a.P / EPC, cpn = a.N / EPC;
+    for (int i = threadIdx.x; i < kT * cpx; i += kThreads) {
+        const int k = i / cpx, c = i % cpx;
+        const int t = rev ? a.L - 1 - (t0 + k) : t0 + k;
+        const bool ok = t0 + k < a.L;
+        cp_async16(&s.x[k][c * EPC], x + (ok ? ((b * a.L + t) * a.H + h) * a.P + c * EPC : 0),
+                   ok ? 16 : 0);
+    }
+    for (int i = threadIdx.x; i < kT * cpn; i += kThreads) {
+        const int k = i / cpn, c = i % cpn;
+        const int t = rev ? a.L - 1 - (t0 + k) : t0 + k;
+        const bool ok = t0 + k < a.L;
+        const int64_t o = ok ? ((b * a.L + t) * a.G + g) * a.N + c * EPC : 0;
+        cp_async16(&s.B[k][c * EPC], Bm + o, ok ? 16 : 0);
+        cp_async16(&s.C[k][c * EPC], Cm + o, ok ? 16 : 0);
+    }
+}
+
+// The preprocessed dt of step t0 + k (walk order) for k = threadIdx.x < kT;
+// 0 outside [0, L).
+template <typename Tin>
+__device__ __forceinline__ float load_dt(const Args &a, int64_t b, int h, int t0, bool rev,
+                                         float dbias) {
+    const int k = threadIdx.x;
+    if (k >= kT || t0 + k >= a.L) return 0.0f;
+    const int t = rev ? a.L - 1 - (t0 + k) : t0 + k;
+    float d = to_f32(static_cast<const Tin *>(a.dt)[(b * a.L + t) * a.H + h]) + dbias;
+    if (a.dt_softplus) d = softplus_fast(d);
+    if (a.dt_limit) d = fminf(fmaxf(d, a.dt_min), a.dt_max);
+    return d;
+}
+
+// One direction.  pass 0: forward, writes y (= scan + D x, gated unless a
+// reverse pass follows); pass 1: reverse, adds its scan to y and gates.
+template <typename Tin, int PW, int NL>
+__global__ void __launch_bounds__(kThreads)
+ssd_general_kernel(Args a, int pass, int gate_now) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Tile<Tin> *tiles = reinterpret_cast<Tile<Tin> *>(smem_raw);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int bh = blockIdx.x;
+    const int64_t b = bh / a.H;
+    const int h = bh % a.H;
+    const int g = h / (a.H / a.G);
+    const bool rev = pass == 1;
+    const float A2 = a.A[h] * SSM_LOG2E;
+    const float Dh = (a.D && !rev) ? a.D[h] : 0.0f;
+    const float dbias = a.dt_bias ? a.dt_bias[h] : 0.0f;
+    const Tin *zg = static_cast<const Tin *>(a.z);
+
+    float st[PW][NL];
+#pragma unroll
+    for (int i = 0; i < PW; ++i)
+#pragma unroll
+        for (int j = 0; j < NL; ++j) {
+            const int p = w + kWarps * i, n = lane + 32 * j;
+            st[i][j] = (a.h0 && !rev) ? a.h0[((int64_t(bh) * a.P) + p) * a.N + n] : 0.0f;
+        }
+
+    const int ntiles = (a.L + kT - 1) / kT;
+    stage_rows<Tin>(tiles[0], a, b, h, g, 0, rev);
+    cp_async_commit();
+    if (threadIdx.x < kT) tiles[0].dt[threadIdx.x] = load_dt<Tin>(a, b, h, 0, rev, dbias);
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int k = 0; k < ntiles; ++k) {
+        Tile<Tin> &s = tiles[k & 1];
+        // the next tile's copies run while this one is used
+        float dnext = 0.0f;
+        if (k + 1 < ntiles) {
+            stage_rows<Tin>(tiles[(k + 1) & 1], a, b, h, g, (k + 1) * kT, rev);
+            dnext = load_dt<Tin>(a, b, h, (k + 1) * kT, rev, dbias);
+        }
+        cp_async_commit();
+        const int steps = min(kT, a.L - k * kT);
+        for (int j = 0; j < steps; ++j) {
+            const float d = s.dt[j];
+            const float dec = ex2(d * A2);
+            float bv[NL], cv[NL];
+#pragma unroll
+            for (int q = 0; q < NL; ++q) {
+                bv[q] = to_f32(s.B[j][lane + 32 * q]);
+                cv[q] = to_f32(s.C[j][lane + 32 * q]);
+            }
+            float yp[PW];
+#pragma unroll
+            for (int i = 0; i < PW; ++i) {
+                const float dx = d * to_f32(s.x[j][w + kWarps * i]);
+                float acc = 0.0f;
+#pragma unroll
+                for (int q = 0; q < NL; ++q) {
+                    st[i][q] = fmaf(dec, st[i][q], dx * bv[q]);
+                    acc = fmaf(st[i][q], cv[q], acc);
+                }
+                yp[i] = acc;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < PW; ++i) yp[i] += __shfl_xor_sync(0xffffffffu, yp[i], o);
+            // lane i of the warp writes row p = w + 8 i
+            const int t = rev ? a.L - 1 - (k * kT + j) : k * kT + j;
+#pragma unroll
+            for (int i = 0; i < PW; ++i) {
+                if (lane == i) {
+                    const int p = w + kWarps * i;
+                    const int64_t o = ((b * a.L + t) * a.H + h) * a.P + p;
+                    float v = yp[i];
+                    if (rev) v += a.y[o];                       // forward part, written by pass 0
+                    else v = fmaf(Dh, to_f32(s.x[j][p]), v);
+                    if (gate_now && zg) v *= silu_fast(to_f32(zg[o]));
+                    a.y[o] = v;
+                }
+            }
+        }
+        cp_async_wait<0>();
+        if (k + 1 < ntiles && threadIdx.x < kT) tiles[(k + 1) & 1].dt[threadIdx.x] = dnext;
+        __syncthreads();    // the next tile is staged; this one's reads are done
+    }
+    if (a.h_final && !rev) {
+#pragma unroll
+        for (int i = 0; i < PW; ++i)
+#pragma unroll
+            for (int j = 0; j < NL; ++j) {
+                const int p = w + kWarps * i, n = lane + 32 * j;
+                a.h_final[((int64_t(bh) * a.P) + p) * a.N + n] = st[i][j];
+            }
+    }
+}
+
+template <typename Tin, int PW, int NL>
+static cudaError_t run(const Args &a, int64_t grid, bool bidir, cudaStream_t st) {
+    const int smem = int(2 * sizeof(Tile<Tin>));
+    auto kern = ssd_general_kernel<Tin, PW, NL>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kern<<<unsigned(grid), kThreads, smem, st>>>(a, 0, bidir ? 0 : 1);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || !bidir) return err;
+    kern<<<unsigned(grid), kThreads, smem, st>>>(a, 1, 1);
+    return cudaGetLastError();
+}
+
+template <typename Tin, int PW>
+static cudaError_t run_pw(const Args &a, int64_t grid, bool bidir, cudaStream_t st) {
+    switch (a.N) {
+        case 32: return run<Tin, PW, 1>(a, grid, bidir, st);
+        case 64: return run<Tin, PW, 2>(a, grid, bidir, st);
+        case 128: return run<Tin, PW, 4>(a, grid, bidir, st);
+        case 256:
+            if constexpr (PW <= 8) return run<Tin, PW, 8>(a, grid, bidir, st);
+            return cudaErrorNotSupported;
+    }
+    return cudaErrorNotSupported;
+}
+
+// Shapes this path takes: P in {16, 32, 64, 128}, N in {32, 64, 128, 256},
+// P * N <= 16384.
+bool supported(int64_t P, int64_t N) {
+    const bool p_ok = P == 16 || P == 32 || P == 64 || P == 128;
+    const bool n_ok = N == 32 || N == 64 || N == 128 || N == 256;
+    return p_ok && n_ok && P * N <= 16384;
+}
+
+template <typename Tin>
+cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *Bm, const Tin *Cm,
+                   const float *D, float *y, int64_t Bs, int64_t L, int64_t H, int64_t P,
+                   int64_t N, bool bidir, const ScanOpts *opt, cudaStream_t st) {
+    if (!supported(P, N)) return cudaErrorNotSupported;
+    const int64_t grid = Bs * H;
+    if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const ScanOpts none{};
+    const ScanOpts &o = opt ? *opt : none;
+    Args a;
+    a.x = x; a.dt = dt; a.B = Bm; a.C = Cm; a.z = o.z;
+    a.A = A_head; a.D = D; a.dt_bias = o.dt_bias; a.h0 = o.h0;
+    a.y = y; a.h_final = o.h_final;
+    a.L = int(L); a.H = int(H); a.P = int(P); a.N = int(N);
+    a.G = o.ngroups > 1 ? o.ngroups : 1;
+    a.dt_min = o.dt_min; a.dt_max = o.dt_max;
+    a.dt_softplus = o.dt_softplus; a.dt_limit = o.dt_limit;
+    switch (P) {
+        case 16: return run_pw<Tin, 2>(a, grid, bidir, st);
+        case 32: return run_pw<Tin, 4>(a, grid, bidir, st);
+        case 64: return run_pw<Tin, 8>(a, grid, bidir, st);
+        case 128: return run_pw<Tin, 16>(a, grid, bidir, st);
+    }
+    return cudaErrorNotSupported;
+}
+
+template cudaError_t launch<float>(const float *, const float *, const float *, const float *,
+                                   const float *, const float *, float *, int64_t, int64_t, int64_t,
+                                   int64_t, int64_t, bool, const ScanOpts *, cudaStream_t);
+template cudaError_t launch<__nv_bfloat16>(const __nv_bfloat16 *, const __nv_bfloat16 *,
+                                           const float *, const __nv_bfloat16 *,
+                                           const __nv_bfloat16 *, const float *, float *, int64_t,
+                                           int64_t, int64_t, int64_t, int64_t, bool,
+                                           const ScanOpts *, cudaStream_t);
+
+}  // namespace ssd_general
+}  // namespace ssm

@@ -79,9 +79,11 @@ def test_ssd_rejects_bad_arguments():
     assert ssd(ptrs) == 1
     assert ssd(L=0) == 1
     assert ssd(chunk=0) == 1
-    assert ssd(P_=32) == 2
+    assert ssd(P_=48) == 2
+    assert ssd(P_=256) == 2
     assert ssd(N=48) == 2
-    assert ssd(N=32) == 2
+    assert ssd(N=16) == 2
+    assert ssd(P_=128, N=256) == 2        # P * N above 16384
     assert ssd(chunk=96) == 2
     ptrs = [P] * 7
     ptrs[3] = P_ODD                       # B not 16-byte aligned
@@ -125,14 +127,14 @@ def test_option_entry_points_reject_bad_arguments():
     assert lib.ssm_scan_fwd_ex(*([P] * 7), 1, 8, 8, 4, 1, ctypes.byref(_opts(z=P_ODD)), None) == 3
     assert lib.ssm_scan_fwd_ex(*([P] * 7), 1, 8, 8, 4, 0,
                                ctypes.byref(_opts(h_final=0x10002)), None) == 3
-    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 0,
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 0, 1,
                                      ctypes.byref(_opts(z=0x10008)), None) == 3
     # state input/output is defined for a single direction only
-    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1,
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1, 1,
                                      ctypes.byref(_opts(h0=P)), None) == 2
-    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1,
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1, 1,
                                      ctypes.byref(_opts(h_final=P)), None) == 2
-    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 32, 64, 128, 0,
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 48, 64, 128, 0, 1,
                                      ctypes.byref(_opts()), None) == 2
 
 
@@ -143,17 +145,17 @@ def test_option_calls_without_device_report_no_device():
     lib = lrs.library()
     o = _opts(dt_softplus=1, z=P, h0=P, h_final=P)
     assert lib.ssm_scan_fwd_ex(*([P] * 7), 1, 8, 8, 4, 1, ctypes.byref(o), None) == 6
-    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 0, ctypes.byref(o), None) == 6
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 0, 1, ctypes.byref(o), None) == 6
     # a NULL options pointer is the plain call
-    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1, None, None) == 6
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 2, 64, 64, 128, 1, 1, None, None) == 6
 
 
 def test_groups_are_validated():
     lib = lrs.library()
     # ngroups must divide H
-    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 6, 64, 64, 128, 0,
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 6, 64, 64, 128, 0, 1,
                                      ctypes.byref(_opts(ngroups=4)), None) == 1
-    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 6, 64, 64, 128, 0,
+    assert lib.ssd_chunk_scan_fwd_ex(*([P] * 7), 1, 8, 6, 64, 64, 128, 0, 1,
                                      ctypes.byref(_opts(ngroups=-1)), None) == 1
     # groups belong to the SSD scan only
     assert lib.ssm_scan_fwd_ex(*([P] * 7), 1, 8, 8, 4, 1, ctypes.byref(_opts(ngroups=2)), None) == 2
