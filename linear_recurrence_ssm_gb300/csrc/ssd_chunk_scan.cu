@@ -88,6 +88,7 @@ struct __align__(1024) Smem {
 };
 
 struct Params {
+    const __nv_bfloat16 *x;    // read by the warp-specialised kernel's epilogue (D x)
     const __nv_bfloat16 *dt;
     const float *A;
     const float *D;
@@ -691,6 +692,659 @@ done:
 }
 
 // ---------------------------------------------------------------------------
+// Warp-specialised kernel (unidirectional)
+// ---------------------------------------------------------------------------
+// The same computation as ssd_chunk_scan_kernel for the forward scan, with
+// the work of a tile split between roles that run up to a tile apart and
+// meet only at mbarriers, so that the mask of one tile, the outputs of the
+// previous one and the tensor-core products overlap instead of taking turns:
+//   warpgroup 0 (rows t = 0..127): the per-tile vectors (dt, cumulative sums,
+//     column factors) a tile ahead, then the decay mask of each tile from G;
+//   warpgroup 1 (rows t = 0..127 / state columns n): the fp32 state update
+//     and its bf16 image, the weighted x rows of the next tile, then the
+//     output rows y = Y + e^{cum} Zf + D x (stored straight from registers);
+//   warp 8, one thread: every tcgen05.mma, as soon as its inputs are ready;
+//   warp 9, one thread: every TMA copy, as soon as its buffer is free.
+// Y and Zf have two accumulators each (by tile parity): the products of tile
+// c + 1 run while warpgroup 1 reads the outputs of tile c.
+namespace ws {
+
+constexpr int kThreads = 384;
+// Registers: the CTA is launched with 168 per thread (65536 / 384 rounded
+// down to a multiple of 8); the issuing warpgroup gives some back and the
+// two math warpgroups take them (setmaxnreg).
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kIssuerRegs = 56;
+constexpr uint32_t kMathRegs = 224;
+static_assert(128 * kIssuerRegs + 256 * kMathRegs <= kThreads * kLaunchRegs,
+              "the register split must fit in what the CTA is launched with");
+constexpr int kSlots = 3;        // per-tile vectors in flight (tile c uses slot c % 3)
+
+// Tensor-memory columns.
+constexpr uint32_t kWsG = 0, kWsY0 = 128, kWsY1 = 192, kWsZ0 = 256, kWsZ1 = 320, kWsS = 384;
+
+template <int NB>
+struct __align__(1024) Smem {
+    uint8_t C[2][NB][kTile];    // C tiles (double buffered), K-major rows t
+    uint8_t B[2][2][kTile];     // B tiles (double buffered); region 1 zero when N = 64
+    uint8_t X[kTile];           // x tile (MN-major B operand of Y)
+    uint8_t Xw[kTile];          // weighted x rows (operand of S_c)
+    uint8_t M[2][kTile];        // masked G (K-major, two 64-wide regions of s)
+    uint8_t S[NB][kStateRegion];    // entering state image
+    float cum[kSlots][kQ];
+    float excl[kSlots][kQ];
+    float dtv[kSlots][kQ];
+    float csf[kSlots][kQ];
+    float tot[kSlots];
+    float wsum[kSlots][4];      // warp sums of warpgroup 0's scans
+    uint64_t bar_c[2], bar_b[2], bar_x;              // TMA copies landed
+    uint64_t bar_g, bar_z[2], bar_m2;                // products finished (bar_z by tile parity)
+    uint64_t bar_gfree, bar_mfull, bar_xw, bar_st;   // hand-offs between roles
+    uint64_t bar_vec[kSlots], bar_vfree[kSlots], bar_sync, bar_fin;
+    uint32_t tmem_base;
+};
+
+// Non-blocking test of whether the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Row n of an MN-major bf16 state image (64 p, 128-byte swizzle) from the 64
+// fp32 values a thread holds.
+__device__ __forceinline__ void put_state_row(uint8_t *img, int n, const float (&s)[64]) {
+    uint8_t *rowp = img + n * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4 *>(rowp + ((j ^ (n & 7)) << 4)) =
+            make_uint4(pack_bf16(s[8 * j], s[8 * j + 1]), pack_bf16(s[8 * j + 2], s[8 * j + 3]),
+                       pack_bf16(s[8 * j + 4], s[8 * j + 5]), pack_bf16(s[8 * j + 6], s[8 * j + 7]));
+}
+
+template <int NB>
+struct Ctx {
+    Smem<NB> &sm;
+    const Params &prm;
+    int b, h, grp, bh, L, nc;
+    float Ah, Dh, dbias;
+    uint32_t tmem;
+    volatile int *abort;
+};
+
+#define WS_WAIT(bar, ph)                                                                  \
+    do {                                                                                  \
+        if (!mbar_wait_bounded(&(bar), (ph), cx.abort, kWaitLimitNs)) return false;       \
+        (ph) ^= 1u;                                                                       \
+    } while (0)
+
+// ---- the issuing thread -------------------------------------------------------------
+template <int NB, bool EXT>
+__device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
+    constexpr int N = NB * 64;
+    auto &sm = cx.sm;
+    const int nc = cx.nc;
+    const uint32_t tmem = cx.tmem;
+    constexpr uint32_t idG = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idZ = idesc_bf16_f32(128, 64, false, true);
+    constexpr uint32_t idY = idesc_bf16_f32(128, 64, false, true);
+    constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);
+    uint32_t ph_c[2] = {0, 0}, ph_b[2] = {0, 0}, ph_x = 0;
+    uint32_t ph_gfree = 0, ph_mfull = 0, ph_xw = 0, ph_st = 0;
+
+    // S_c^T = B^T (w x): A = B tile read MN-major (128 n rows), B = the weighted x rows.
+    auto issue_s = [&](int bb) {
+        const uint32_t sB = smem_addr(sm.B[bb]), sXw = smem_addr(sm.Xw);
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk)
+            mma_bf16_ss(tmem + kWsS, smem_desc(sB + kk * 2048, kTile, 1024, kSwizzle128B),
+                        smem_desc(sXw + kk * 2048, kTile, 1024, kSwizzle128B), idS, kk > 0);
+    };
+    auto issue_g = [&](int buf) {
+        const uint32_t sC = smem_addr(sm.C[buf]), sB = smem_addr(sm.B[buf]);
+#pragma unroll
+        for (int kk = 0; kk < N / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;
+            mma_bf16_ss(tmem + kWsG, smem_desc(sC + koff, 16, 1024, kSwizzle128B),
+                        smem_desc(sB + koff, 16, 1024, kSwizzle128B), idG, kk > 0);
+        }
+    };
+    auto issue_z = [&](int buf) {    // Zf of the tile whose parity is buf
+        const uint32_t sC = smem_addr(sm.C[buf]), sS = smem_addr(sm.S);
+        const uint32_t zcol = buf ? kWsZ1 : kWsZ0;
+#pragma unroll
+        for (int kk = 0; kk < N / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kTile + (kk & 3) * 32;
+            mma_bf16_ss(tmem + zcol, smem_desc(sC + koff, 16, 1024, kSwizzle128B),
+                        smem_desc(sS + kk * 2048, kTile, 1024, kSwizzle128B), idZ, kk > 0);
+        }
+    };
+    auto issue_y = [&](int c) {
+        const uint32_t sM = smem_addr(sm.M), sX = smem_addr(sm.X);
+        const uint32_t dcol = (c & 1) ? kWsY1 : kWsY0;
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk)
+            mma_bf16_ss(tmem + dcol, smem_desc(sM + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024, kSwizzle128B),
+                        smem_desc(sX + kk * 2048, kTile, 1024, kSwizzle128B), idY, kk > 0);
+    };
+
+    WS_WAIT(sm.bar_c[0], ph_c[0]);
+    WS_WAIT(sm.bar_b[0], ph_b[0]);
+    tc_fence_after_sync();
+    issue_g(0);
+    mma_commit(&sm.bar_g);
+    WS_WAIT(sm.bar_st, ph_st);                  // the initial state image (if any)
+    if (has_h0) {
+        tc_fence_after_sync();
+        issue_z(0);
+    }
+    mma_commit(&sm.bar_z[0]);
+    // Three streams of products, each issued as soon as its inputs are ready
+    // (non-blocking polls, so that a late input of one stream does not hold
+    // up another):
+    //   Y(c), S_c(c): mask(c) and weighted rows(c) written, x(c) landed, and
+    //                 G(c), Zf(c) issued before them -- so that the end of
+    //                 Y(c), S_c(c) also means the end of everything of tile c;
+    //   G(c):         G(c - 1) read by warpgroup 0, C(c) and B(c) landed;
+    //   Zf(c):        state image of tile c written (C(c) landed: G(c) issued).
+    // (The copies are another thread's: issuing them can hold a thread for
+    // thousands of cycles.)
+    int y_next = 0, g_next = 1, z_next = 1;
+    uint64_t t_idle = 0;
+    while (y_next < nc) {
+        bool progress = false;
+        if (g_next > y_next && z_next > y_next && mbar_test_wait(&sm.bar_mfull, ph_mfull) &&
+            mbar_test_wait(&sm.bar_xw, ph_xw) && mbar_test_wait(&sm.bar_x, ph_x)) {
+            ph_mfull ^= 1u;
+            ph_xw ^= 1u;
+            ph_x ^= 1u;
+            tc_fence_after_sync();
+            issue_y(y_next);
+            issue_s(y_next & 1);
+            mma_commit(&sm.bar_m2);
+            ++y_next;
+            progress = true;
+        }
+        if (g_next < nc && mbar_test_wait(&sm.bar_gfree, ph_gfree) &&
+            mbar_test_wait(&sm.bar_c[g_next & 1], ph_c[g_next & 1]) &&
+            mbar_test_wait(&sm.bar_b[g_next & 1], ph_b[g_next & 1])) {
+            ph_gfree ^= 1u;
+            ph_c[g_next & 1] ^= 1u;
+            ph_b[g_next & 1] ^= 1u;
+            tc_fence_after_sync();
+            issue_g(g_next & 1);
+            mma_commit(&sm.bar_g);
+            ++g_next;
+            progress = true;
+        }
+        if (z_next < nc && g_next > z_next && mbar_test_wait(&sm.bar_st, ph_st)) {
+            ph_st ^= 1u;
+            tc_fence_after_sync();
+            issue_z(z_next & 1);
+            mma_commit(&sm.bar_z[z_next & 1]);
+            ++z_next;
+            progress = true;
+        }
+        if (progress) {
+            t_idle = 0;
+        } else {
+            // (reading the clock on every idle pass also paces the polls,
+            // which otherwise take issue slots from the math warps)
+            const uint64_t now = globaltimer_ns();
+            if (t_idle == 0) t_idle = now;
+            else if (now - t_idle > kWaitLimitNs || *cx.abort) return false;
+        }
+    }
+    return true;
+}
+
+// ---- the copying thread --------------------------------------------------------------
+// Every TMA copy, each into a buffer whose previous contents have been used:
+// the end of Y(c), S_c(c) means the end of every product of tile c (the
+// issuing thread orders G(c) and Zf(c) before them).
+template <int NB, bool EXT>
+__device__ __forceinline__ bool loader_role(Ctx<NB> &cx, const CUtensorMap *tmC, const CUtensorMap *tmB,
+                                            const CUtensorMap *tmX) {
+    auto &sm = cx.sm;
+    const int nc = cx.nc, b = cx.b, h = cx.h, grp = cx.grp;
+    uint32_t ph_m2 = 0;
+    auto load_b = [&](int c, int buf) {
+        mbar_arrive_expect_tx(&sm.bar_b[buf], NB * kTile);
+#pragma unroll
+        for (int r = 0; r < NB; ++r)
+            tma_load_4d(sm.B[buf][r], tmB, &sm.bar_b[buf], r * 64, grp, c * kQ, b);
+    };
+    auto load_c = [&](int c, int buf) {
+        mbar_arrive_expect_tx(&sm.bar_c[buf], NB * kTile);
+#pragma unroll
+        for (int r = 0; r < NB; ++r) tma_load_4d(sm.C[buf][r], tmC, &sm.bar_c[buf], r * 64, grp, c * kQ, b);
+    };
+    auto load_x = [&](int c) {
+        mbar_arrive_expect_tx(&sm.bar_x, kTile);
+        tma_load_4d(sm.X, tmX, &sm.bar_x, 0, h, c * kQ, b);
+    };
+    load_c(0, 0);
+    load_b(0, 0);
+    load_x(0);
+    if (nc > 1) {
+        load_c(1, 1);
+        load_b(1, 1);
+    }
+    for (int c = 0; c < nc; ++c) {
+        WS_WAIT(sm.bar_m2, ph_m2);
+        if (c + 1 < nc) load_x(c + 1);
+        if (c + 2 < nc) {
+            load_c(c + 2, c & 1);
+            load_b(c + 2, c & 1);
+        }
+    }
+    return true;
+}
+
+// ---- warpgroup 0: vectors and decay mask --------------------------------------------
+template <int NB, bool EXT>
+__device__ __forceinline__ bool mask_role(Ctx<NB> &cx) {
+    auto &sm = cx.sm;
+    const int t = threadIdx.x;          // 0..127: tile row, TMEM lane
+    const int warp = t >> 5;
+    const int tb = warp;                // the warp's 32-row block
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    const int nc = cx.nc, L = cx.L;
+    const __nv_bfloat16 *dtp = cx.prm.dt + (int64_t(cx.b) * L) * cx.prm.H + cx.h;
+    uint32_t ph_g = 0, ph_m2 = 0, ph_vfree[kSlots] = {0, 0, 0}, ph_sync = 0;
+    // raw dt of row c * kQ + t (loaded a tile ahead); rows past L: 0
+    auto load_dt = [&](int c) {
+        const int r = c * kQ + t;
+        return r < L ? dtp[int64_t(r) * cx.prm.H] : __float2bfloat16(0.0f);
+    };
+    // vectors of tile c into slot c % 3
+    auto tile_prep = [&](int c, __nv_bfloat16 raw) -> bool {
+        const int p = c % kSlots;
+        float dv = 0.0f;
+        if (c * kQ + t < L) {
+            dv = __bfloat162float(raw);
+            if (EXT) {
+                dv += cx.dbias;
+                if (cx.prm.dt_softplus) dv = softplus_fast(dv);
+                if (cx.prm.dt_limit) dv = fminf(fmaxf(dv, cx.prm.dt_min), cx.prm.dt_max);
+            }
+        }
+        const float dA = dv * cx.Ah;
+        // inclusive prefix sum over the 128 rows: warp scan, then the warp totals
+        const int lane = t & 31;
+        float v = dA;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += n;
+        }
+        if (lane == 31) sm.wsum[p][warp] = v;
+        mbar_arrive(&sm.bar_sync);
+        WS_WAIT(sm.bar_sync, ph_sync);
+        float off = 0.0f, tot = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float s = sm.wsum[p][w];
+            off += (w < warp) ? s : 0.0f;
+            tot += s;
+        }
+        const float cum = v + off;
+        sm.cum[p][t] = cum;
+        sm.excl[p][t] = cum - dA;
+        sm.dtv[p][t] = dv;
+        if (t == 0) sm.tot[p] = tot;
+        __syncwarp();
+        // column factors of the off-diagonal blocks (row s | 31 is in this warp)
+        sm.csf[p][t] = ex2(sm.cum[p][t | 31] - cum) * dv;
+        mbar_arrive(&sm.bar_sync);              // the mask reads other rows' vectors
+        WS_WAIT(sm.bar_sync, ph_sync);
+        mbar_arrive(&sm.bar_vec[p]);
+        return true;
+    };
+
+    __nv_bfloat16 raw_next = load_dt(0);
+    if (!tile_prep(0, raw_next)) return false;
+    if (nc > 1) raw_next = load_dt(1);
+    for (int c = 0; c < nc; ++c) {
+        const int p = c % kSlots;
+        const float *cum = sm.cum[p];
+        const float *dtv = sm.dtv[p];
+        const float cum_t = cum[t];
+        WS_WAIT(sm.bar_g, ph_g);
+        tc_fence_after_sync();
+        uint32_t packed[4][16];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t gr[2][32];
+            bool need[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int sb = 2 * half + i;
+                need[i] = sb <= tb;
+                if (need[i]) tmem_ld32_async(cx.tmem + lane_base + kWsG + sb * 32, gr[i]);
+            }
+            if (need[0] || need[1]) {
+                tmem_wait_tie(gr[0]);
+                reg_tie(gr[1]);
+            }
+            if (half == 1) {
+                tc_fence_before_sync();
+                mbar_arrive(&sm.bar_gfree);     // G may be overwritten now
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int sb = 2 * half + i;
+                if (!need[i]) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) packed[sb][j] = 0u;
+                    continue;
+                }
+                float m[32];
+                if (sb == tb) {
+                    // diagonal block: direct differences of cumulative sums
+                    const float4 *c4 = reinterpret_cast<const float4 *>(cum + sb * 32);
+                    const float4 *d4 = reinterpret_cast<const float4 *>(dtv + sb * 32);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 cs = c4[j4], ds = d4[j4];
+                        const float csv[4] = {cs.x, cs.y, cs.z, cs.w};
+                        const float dsv[4] = {ds.x, ds.y, ds.z, ds.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int s = sb * 32 + 4 * j4 + q;
+                            const float w = (s <= t) ? ex2(cum_t - csv[q]) : 0.0f;
+                            m[4 * j4 + q] = __uint_as_float(gr[i][4 * j4 + q]) * (w * dsv[q]);
+                        }
+                    }
+                } else {
+                    const float e = ex2(cum_t - cum[sb * 32 + 31]);
+                    const float4 *f4 = reinterpret_cast<const float4 *>(sm.csf[p] + sb * 32);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 f = f4[j4];
+                        m[4 * j4 + 0] = __uint_as_float(gr[i][4 * j4 + 0]) * (e * f.x);
+                        m[4 * j4 + 1] = __uint_as_float(gr[i][4 * j4 + 1]) * (e * f.y);
+                        m[4 * j4 + 2] = __uint_as_float(gr[i][4 * j4 + 2]) * (e * f.z);
+                        m[4 * j4 + 3] = __uint_as_float(gr[i][4 * j4 + 3]) * (e * f.w);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) packed[sb][j] = pack_bf16(m[2 * j], m[2 * j + 1]);
+            }
+        }
+        if (c >= 1) WS_WAIT(sm.bar_m2, ph_m2);  // Y(c - 1) has read the mask buffer
+#pragma unroll
+        for (int sb = 0; sb < 4; ++sb) {
+            uint8_t *reg = sm.M[sb >> 1];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int col = (sb & 1) * 32 + q * 8;
+                *reinterpret_cast<uint4 *>(reg + swz(t, col)) =
+                    make_uint4(packed[sb][4 * q], packed[sb][4 * q + 1], packed[sb][4 * q + 2],
+                               packed[sb][4 * q + 3]);
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.bar_mfull);
+        if (c + 1 < nc) {
+            const int pn = (c + 1) % kSlots;
+            if (c + 1 >= kSlots) WS_WAIT(sm.bar_vfree[pn], ph_vfree[pn]);   // tile c - 2 is done with them
+            if (!tile_prep(c + 1, raw_next)) return false;
+            if (c + 2 < nc) raw_next = load_dt(c + 2);
+        }
+    }
+    return true;
+}
+
+// ---- warpgroup 1: state, weighted rows, outputs ---------------------------------------
+template <int NB, bool EXT>
+__device__ __forceinline__ bool output_role(Ctx<NB> &cx, bool has_h0) {
+    constexpr int N = NB * 64;
+    auto &sm = cx.sm;
+    const int r = threadIdx.x - 128;    // 0..127: tile row t, state column n, TMEM lane
+    const int warp = r >> 5;
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    const int nc = cx.nc, L = cx.L, b = cx.b, h = cx.h, H = cx.prm.H;
+    uint32_t ph_x = 0, ph_m2 = 0, ph_z[2] = {0, 0}, ph_vec[kSlots] = {0, 0, 0};
+    const bool is_state = r < N;        // warp-uniform: N is 64 or 128
+    float st[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) st[j] = 0.0f;
+
+    if (has_h0 && is_state) {
+        // column n = r of the initial state (Bs, H, P, N)
+        const float *src = cx.prm.h0 + size_t(cx.bh) * kP * N + r;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) st[j] = src[size_t(j) * N];
+        put_state_row(&sm.S[0][0], r, st);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&sm.bar_st);
+
+    auto weigh = [&](int c) -> bool {   // weighted x rows of tile c
+        const int p = c % kSlots;
+        WS_WAIT(sm.bar_vec[p], ph_vec[p]);
+        WS_WAIT(sm.bar_x, ph_x);
+        const float w = ex2(sm.tot[p] - sm.cum[p][r]) * sm.dtv[p][r];
+        scale_row(sm.X, sm.Xw, r, w, 0);
+        scale_row(sm.X, sm.Xw, r, w, 1);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.bar_xw);
+        return true;
+    };
+    const bool gate = EXT && cx.prm.z != nullptr;
+    // x and z rows of tile c (bf16, 64 values each), loaded a step early
+    uint4 xq[8], zq[8];
+    auto prefetch_rows = [&](int c) {
+        const int row = c * kQ + r;
+        if (row >= L) return;
+        const size_t off = ((size_t(b) * L + row) * H + h) * kP;
+        const uint4 *xp = reinterpret_cast<const uint4 *>(cx.prm.x + off);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xq[j] = __ldg(xp + j);
+        if (gate) {
+            const uint4 *zp = reinterpret_cast<const uint4 *>(cx.prm.z + off);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) zq[j] = __ldg(zp + j);
+        }
+    };
+    // y rows of tile c from its accumulators and the prefetched rows.
+    auto epilogue = [&](int c) -> bool {
+        const int p = c % kSlots;
+        const int row = c * kQ + r;
+        const bool valid = row < L;
+        const bool has_s = c > 0 || has_h0;
+        const float ef = ex2(sm.cum[p][r]);
+        WS_WAIT(sm.bar_z[c & 1], ph_z[c & 1]);
+        tc_fence_after_sync();
+        float *yrow = cx.prm.y + ((size_t(b) * L + (valid ? row : 0)) * H + h) * kP;
+        const uint32_t ycol = (c & 1) ? kWsY1 : kWsY0, zcol = (c & 1) ? kWsZ1 : kWsZ0;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            uint32_t yv[32], zf[32];
+            tmem_ld32_async(cx.tmem + lane_base + ycol + q * 32, yv);
+            if (has_s) tmem_ld32_async(cx.tmem + lane_base + zcol + q * 32, zf);
+            tmem_wait_tie(yv);
+            reg_tie(zf);
+            if (!valid) continue;
+            float out[32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 xv = xq[4 * q + j];
+                const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 xx = unpack_bf16(w4[k]);
+                    out[8 * j + 2 * k] = fmaf(cx.Dh, xx.x, __uint_as_float(yv[8 * j + 2 * k]));
+                    out[8 * j + 2 * k + 1] = fmaf(cx.Dh, xx.y, __uint_as_float(yv[8 * j + 2 * k + 1]));
+                }
+            }
+            if (has_s) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) out[j] = fmaf(ef, __uint_as_float(zf[j]), out[j]);
+            }
+            if (gate) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 zv = zq[4 * q + j];
+                    const uint32_t w4[4] = {zv.x, zv.y, zv.z, zv.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 zz = unpack_bf16(w4[k]);
+                        out[8 * j + 2 * k] *= silu_fast(zz.x);
+                        out[8 * j + 2 * k + 1] *= silu_fast(zz.y);
+                    }
+                }
+            }
+            float4 *yp = reinterpret_cast<float4 *>(yrow + q * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                yp[j] = make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+        }
+        return true;
+    };
+
+    if (!weigh(0)) return false;
+    prefetch_rows(0);
+    for (int c = 0; c < nc; ++c) {
+        WS_WAIT(sm.bar_m2, ph_m2);              // Y(c), S_c(c) done
+        tc_fence_after_sync();
+        // state passing: column n = r of S_in, then the image of the state
+        // entering tile c + 1 for Zf(c + 1)
+        if (is_state) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32_async(cx.tmem + lane_base + kWsS, v0);
+            tmem_ld32_async(cx.tmem + lane_base + kWsS + 32, v1);
+            tmem_wait_tie(v0);
+            reg_tie(v1);
+            const float e = ex2(sm.tot[c % kSlots]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                st[j] = fmaf(e, st[j], __uint_as_float(v0[j]));
+                st[32 + j] = fmaf(e, st[32 + j], __uint_as_float(v1[j]));
+            }
+            if (c + 1 < nc) put_state_row(&sm.S[0][0], r, st);
+        }
+        if (c + 1 < nc) {
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(&sm.bar_st);
+            if (!weigh(c + 1)) return false;    // the products of tile c + 1 can start
+        }
+        if (!epilogue(c)) return false;
+        mbar_arrive(&sm.bar_vfree[c % kSlots]);
+        if (c + 1 < nc) prefetch_rows(c + 1);
+    }
+    if (EXT && cx.prm.h_final != nullptr && is_state) {
+        float *dst = cx.prm.h_final + size_t(cx.bh) * kP * N + r;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) dst[size_t(j) * N] = st[j];
+    }
+    return true;
+}
+
+template <int NB, bool EXT>
+__global__ void __launch_bounds__(kThreads, 1)
+ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Params prm) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem<NB> &sm = *reinterpret_cast<Smem<NB> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ volatile int abort_flag;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int bh = blockIdx.x;
+
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.bar_c[i], 1);
+            mbar_init(&sm.bar_b[i], 1);
+            mbar_init(&sm.bar_z[i], 1);
+        }
+        mbar_init(&sm.bar_x, 1);
+        mbar_init(&sm.bar_g, 1);
+        mbar_init(&sm.bar_m2, 1);
+        mbar_init(&sm.bar_fin, 1);
+        mbar_init(&sm.bar_gfree, 128);
+        mbar_init(&sm.bar_mfull, 128);
+        mbar_init(&sm.bar_xw, 128);
+        mbar_init(&sm.bar_st, 128);
+        mbar_init(&sm.bar_sync, 128);
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&sm.bar_vec[i], 128);
+            mbar_init(&sm.bar_vfree[i], 128);
+        }
+        mbar_fence_init();
+        prefetch_tmap(&tmC);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (NB == 1) {   // the n = 64..127 rows that S_c's A operand spans read as zeros
+        for (int i = tid; i < int(kTile / 16); i += kThreads) {
+            reinterpret_cast<uint4 *>(sm.B[0][1])[i] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4 *>(sm.B[1][1])[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+
+    Ctx<NB> cx{sm, prm, bh / prm.H, bh % prm.H, 0, bh, prm.L, prm.nc, 0.0f, 0.0f, 0.0f,
+               sm.tmem_base, &abort_flag};
+    cx.grp = cx.h / (prm.H / prm.G);
+    cx.Ah = prm.A[cx.h] * SSM_LOG2E;
+    cx.Dh = prm.D ? prm.D[cx.h] : 0.0f;
+    cx.dbias = (EXT && prm.dt_bias) ? prm.dt_bias[cx.h] : 0.0f;
+    const bool has_h0 = EXT && prm.h0 != nullptr;
+
+    bool ok = true;
+    if (warp >= 8) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kIssuerRegs));
+        if (tid == 256) ok = issuer_role<NB, EXT>(cx, has_h0);
+        if (tid == 288) ok = loader_role<NB, EXT>(cx, &tmC, &tmB, &tmX);
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kMathRegs));
+        ok = warp < 4 ? mask_role<NB, EXT>(cx) : output_role<NB, EXT>(cx, has_h0);
+    }
+    if (!ok) {
+        abort_flag = 1;
+        atomicOr(&g_device_error, 1u);
+    }
+    if (!ok && tid == 256) {
+        // products still in flight after a timeout: give them a bounded
+        // chance to finish before the tensor memory is released
+        mma_commit(&sm.bar_fin);
+        volatile int never = 0;
+        (void)mbar_wait_bounded(&sm.bar_fin, 0, &never, 100000000ull);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(sm.tmem_base, kTmemCols);
+    }
+}
+#undef WS_WAIT
+
+}  // namespace ws
+
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -745,6 +1399,7 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
         return cudaErrorInvalidValue;
 
     Params prm;
+    prm.x = x;
     prm.dt = dt;
     prm.A = A;
     prm.D = D;
@@ -768,11 +1423,32 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
     const int64_t grid = Bs * H;
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
 
-    const size_t smem = sizeof(Smem<NB>) + 1024;
+    // The warp-specialised kernel takes the unidirectional scan.
+    const bool use_ws = !bidir;
+    size_t smem = sizeof(Smem<NB>) + 1024;
     static_assert(sizeof(Smem<NB>) + 1024 <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
+    static_assert(sizeof(ws::Smem<NB>) + 1024 <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
     auto kern = opt ? ssd_chunk_scan_kernel<NB, true> : ssd_chunk_scan_kernel<NB, false>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (err != cudaSuccess) return err;
+    using WsKern = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);
+    WsKern wkern = nullptr;
+    if (use_ws) {
+        wkern = opt ? ws::ssd_ws_kernel<NB, true> : ws::ssd_ws_kernel<NB, false>;
+        smem = sizeof(ws::Smem<NB>) + 1024;
+    }
+    cudaError_t err;
+    if (wkern) {
+        err = cudaFuncSetAttribute(wkern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (err != cudaSuccess) return err;
+        // setmaxnreg re-divides the registers the CTA was launched with; had
+        // it been launched with fewer, the larger share could never be granted.
+        cudaFuncAttributes fa;
+        err = cudaFuncGetAttributes(&fa, wkern);
+        if (err != cudaSuccess) return err;
+        if (fa.numRegs < int(ws::kLaunchRegs)) return cudaErrorNotSupported;
+    } else {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (err != cudaSuccess) return err;
+    }
 
     void *scratch = nullptr;
     if (bidir && prm.nc > 1 && fixed_scratch != nullptr) {
@@ -783,7 +1459,10 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
         if (err != cudaSuccess) return err;
         prm.rstate = static_cast<uint8_t *>(scratch);
     }
-    kern<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tmC, tmB, tmX, tmY, prm);
+    if (wkern)
+        wkern<<<dim3(unsigned(grid)), dim3(ws::kThreads), smem, stream>>>(tmC, tmB, tmX, prm);
+    else
+        kern<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tmC, tmB, tmX, tmY, prm);
     err = cudaGetLastError();
     if (scratch) {
         cudaError_t e2 = cudaFreeAsync(scratch, stream);
