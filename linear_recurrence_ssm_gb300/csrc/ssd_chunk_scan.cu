@@ -702,7 +702,8 @@ done:
 //     column factors) a tile ahead, then the decay mask of each tile from G;
 //   warpgroup 1 (rows t = 0..127 / state columns n): the fp32 state update
 //     and its bf16 image, the weighted x rows of the next tile, then the
-//     output rows y = Y + e^{cum} Zf + D x (stored straight from registers);
+//     output rows y = Y + e^{cum} Zf (stored straight from registers; D x
+//     is part of Y: warpgroup 0 adds D_h to the diagonal of the mask);
 //   warp 8, one thread: every tcgen05.mma, as soon as its inputs are ready;
 //   warp 9, one thread: every TMA copy, as soon as its buffer is free.
 // Y and Zf have two accumulators each (by tile parity): the products of tile
@@ -959,6 +960,7 @@ __device__ __forceinline__ bool mask_role(Ctx<NB> &cx) {
     const int tb = warp;                // the warp's 32-row block
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
     const int nc = cx.nc, L = cx.L;
+    const float Dh = cx.Dh;
     const __nv_bfloat16 *dtp = cx.prm.dt + (int64_t(cx.b) * L) * cx.prm.H + cx.h;
     uint32_t ph_g = 0, ph_m2 = 0, ph_vfree[kSlots] = {0, 0, 0}, ph_sync = 0;
     // raw dt of row c * kQ + t (loaded a tile ahead); rows past L: 0
@@ -1093,6 +1095,10 @@ __device__ __forceinline__ bool mask_role(Ctx<NB> &cx) {
                                packed[sb][4 * q + 3]);
             }
         }
+        {   // the skip term rides on the diagonal: Y = (M + D_h I) X
+            __nv_bfloat16 *d = reinterpret_cast<__nv_bfloat16 *>(sm.M[t >> 6] + swz(t, t & 63));
+            *d = __float2bfloat16(__bfloat162float(*d) + Dh);
+        }
         fence_proxy_async_smem();
         mbar_arrive(&sm.bar_mfull);
         if (c + 1 < nc) {
@@ -1142,22 +1148,16 @@ __device__ __forceinline__ bool output_role(Ctx<NB> &cx, bool has_h0) {
         return true;
     };
     const bool gate = EXT && cx.prm.z != nullptr;
-    // x and z rows of tile c (bf16, 64 values each), loaded a step early
-    uint4 xq[8], zq[8];
+    // gate rows of tile c (bf16, 64 values), loaded a step early
+    uint4 zq[8];
     auto prefetch_rows = [&](int c) {
         const int row = c * kQ + r;
-        if (row >= L) return;
-        const size_t off = ((size_t(b) * L + row) * H + h) * kP;
-        const uint4 *xp = reinterpret_cast<const uint4 *>(cx.prm.x + off);
+        if (!gate || row >= L) return;
+        const uint4 *zp = reinterpret_cast<const uint4 *>(cx.prm.z + ((size_t(b) * L + row) * H + h) * kP);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) xq[j] = __ldg(xp + j);
-        if (gate) {
-            const uint4 *zp = reinterpret_cast<const uint4 *>(cx.prm.z + off);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) zq[j] = __ldg(zp + j);
-        }
+        for (int j = 0; j < 8; ++j) zq[j] = __ldg(zp + j);
     };
-    // y rows of tile c from its accumulators and the prefetched rows.
+    // y rows of tile c from its accumulators (Y already holds D x).
     auto epilogue = [&](int c) -> bool {
         const int p = c % kSlots;
         const int row = c * kQ + r;
@@ -1178,16 +1178,7 @@ __device__ __forceinline__ bool output_role(Ctx<NB> &cx, bool has_h0) {
             if (!valid) continue;
             float out[32];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 xv = xq[4 * q + j];
-                const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 xx = unpack_bf16(w4[k]);
-                    out[8 * j + 2 * k] = fmaf(cx.Dh, xx.x, __uint_as_float(yv[8 * j + 2 * k]));
-                    out[8 * j + 2 * k + 1] = fmaf(cx.Dh, xx.y, __uint_as_float(yv[8 * j + 2 * k + 1]));
-                }
-            }
+            for (int j = 0; j < 32; ++j) out[j] = __uint_as_float(yv[j]);
             if (has_s) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) out[j] = fmaf(ef, __uint_as_float(zf[j]), out[j]);
