@@ -89,7 +89,7 @@ def load_peaks():
 
 def kernel_source_hash(kind: str) -> str:
     csrc = os.path.join(ROOT, "linear_recurrence_ssm_gb300", "csrc")
-    srcs = ["diag_scan.cuh", "diag_scan.cu"] if kind == "diag" else ["ssd_chunk_scan.cu"]
+    srcs = ["diag_scan.cuh", "diag_scan.cu"] if kind == "diag" else ["ssd_chunk_scan.cu", "tc_ptx.cuh"]
     h = hashlib.sha256()
     for p in [os.path.join(csrc, f) for f in srcs] + [os.path.join(csrc, "ssm_common.cuh")]:
         with open(p, "rb") as f:
