@@ -732,6 +732,7 @@ struct __align__(1024) Smem {
     uint8_t Xw[kTile];          // weighted x rows (operand of S_c)
     uint8_t M[2][kTile];        // masked G (K-major, two 64-wide regions of s)
     uint8_t S[NB][kStateRegion];    // entering state image
+    float ystage[4][32 * 16];       // per output warp: 32 rows x 16 columns of y on their way out
     float cum[kSlots][kQ];
     float excl[kSlots][kQ];
     float dtv[kSlots][kQ];
@@ -1118,6 +1119,7 @@ __device__ __forceinline__ bool output_role(Ctx<NB> &cx, bool has_h0) {
     auto &sm = cx.sm;
     const int r = threadIdx.x - 128;    // 0..127: tile row t, state column n, TMEM lane
     const int warp = r >> 5;
+    const int lane = r & 31;
     const uint32_t lane_base = uint32_t(warp * 32) << 16;
     const int nc = cx.nc, L = cx.L, b = cx.b, h = cx.h, H = cx.prm.H;
     uint32_t ph_x = 0, ph_m2 = 0, ph_z[2] = {0, 0}, ph_vec[kSlots] = {0, 0, 0};
@@ -1166,7 +1168,6 @@ __device__ __forceinline__ bool output_role(Ctx<NB> &cx, bool has_h0) {
         const float ef = ex2(sm.cum[p][r]);
         WS_WAIT(sm.bar_z[c & 1], ph_z[c & 1]);
         tc_fence_after_sync();
-        float *yrow = cx.prm.y + ((size_t(b) * L + (valid ? row : 0)) * H + h) * kP;
         const uint32_t ycol = (c & 1) ? kWsY1 : kWsY0, zcol = (c & 1) ? kWsZ1 : kWsZ0;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -1175,7 +1176,6 @@ __device__ __forceinline__ bool output_role(Ctx<NB> &cx, bool has_h0) {
             if (has_s) tmem_ld32_async(cx.tmem + lane_base + zcol + q * 32, zf);
             tmem_wait_tie(yv);
             reg_tie(zf);
-            if (!valid) continue;
             float out[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) out[j] = __uint_as_float(yv[j]);
@@ -1183,7 +1183,7 @@ __device__ __forceinline__ bool output_role(Ctx<NB> &cx, bool has_h0) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) out[j] = fmaf(ef, __uint_as_float(zf[j]), out[j]);
             }
-            if (gate) {
+            if (gate && valid) {   // (rows past L are computed but not stored)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint4 zv = zq[4 * q + j];
@@ -1196,10 +1196,31 @@ __device__ __forceinline__ bool output_role(Ctx<NB> &cx, bool has_h0) {
                     }
                 }
             }
-            float4 *yp = reinterpret_cast<float4 *>(yrow + q * 32);
+            // Out through a per-warp staging tile, 16 columns at a time, so
+            // that each store instruction covers 8 rows x 64 contiguous bytes
+            // instead of 32 rows x 16 bytes.  The 16-byte chunks of a row are
+            // XOR-permuted by (row / 2) % 4: conflict-free in both directions.
+            float *stg = sm.ystage[warp];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                yp[j] = make_float4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+            for (int hh = 0; hh < 2; ++hh) {
+                const int sw = (lane >> 1) & 3;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    reinterpret_cast<float4 *>(stg + lane * 16)[j ^ sw] =
+                        make_float4(out[16 * hh + 4 * j], out[16 * hh + 4 * j + 1],
+                                    out[16 * hh + 4 * j + 2], out[16 * hh + 4 * j + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int rr = 8 * k + (lane >> 2), ch = lane & 3;
+                    const float4 v = reinterpret_cast<const float4 *>(stg + rr * 16)[ch ^ ((rr >> 1) & 3)];
+                    const int trow = c * kQ + warp * 32 + rr;
+                    if (trow < L)
+                        *reinterpret_cast<float4 *>(cx.prm.y + ((size_t(b) * L + trow) * H + h) * kP +
+                                                    q * 32 + hh * 16 + ch * 4) = v;
+                }
+                __syncwarp();
+            }
         }
         return true;
     };
