@@ -88,7 +88,6 @@ struct __align__(1024) Smem {
 };
 
 struct Params {
-    const __nv_bfloat16 *x;    // read by the warp-specialised kernel's epilogue (D x)
     const __nv_bfloat16 *dt;
     const float *A;
     const float *D;
@@ -702,8 +701,9 @@ done:
 //     column factors) a tile ahead, then the decay mask of each tile from G;
 //   warpgroup 1 (rows t = 0..127 / state columns n): the fp32 state update
 //     and its bf16 image, the weighted x rows of the next tile, then the
-//     output rows y = Y + e^{cum} Zf (stored straight from registers; D x
-//     is part of Y: warpgroup 0 adds D_h to the diagonal of the mask);
+//     output rows y = Y + e^{cum} Zf (out through a per-warp shared-memory
+//     staging tile; D x is part of Y: warpgroup 0 adds D_h to the diagonal
+//     of the mask);
 //   warp 8, one thread: every tcgen05.mma, as soon as its inputs are ready;
 //   warp 9, one thread: every TMA copy, as soon as its buffer is free.
 // Y and Zf have two accumulators each (by tile parity): the products of tile
@@ -1411,7 +1411,6 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
         return cudaErrorInvalidValue;
 
     Params prm;
-    prm.x = x;
     prm.dt = dt;
     prm.A = A;
     prm.D = D;
