@@ -73,6 +73,8 @@ def _load(path: str | None = None):
         lib.oracle_ssd_scan_ex_range.restype = None
         lib.oracle_diag_scan_bwd_range.argtypes = [dp] * 13 + [i64] * 6 + [ctypes.c_int]
         lib.oracle_diag_scan_bwd_range.restype = None
+        lib.oracle_ssd_scan_bwd.argtypes = [dp] * 13 + [i64] * 6 + [ctypes.c_int, ctypes.c_int]
+        lib.oracle_ssd_scan_bwd.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _libs[key] = lib
@@ -203,3 +205,35 @@ def ssd_scan(x, dt, A_head, B, C, D=None, bidirectional: bool = False,
         int(bool(bidirectional)), _ptr(dt_bias), int(bool(dt_softplus)), lim, lo, hi, _ptr(z),
         _ptr(h0), _ptr(hf), u0, u1, nthreads)
     return (y, hf) if return_final_state else y
+
+
+def ssd_scan_bwd(x, dt, A_head, B, C, D, dy, bidirectional: bool = False, nthreads: int = 0,
+                 library=None):
+    """Gradients of the SSD scan in fp64 (reverse mode written out by hand).
+
+    Same inputs as ``ssd_scan`` (no options) plus dy (Bs, L, H, P), the
+    gradient of the loss with respect to y.  Returns dict(dx, ddt, dA, dB, dC,
+    dD) shaped like x, dt, A_head, B, C (as given: (Bs, L, N) or
+    (Bs, L, G, N)), D (dD is None when D is None).
+    """
+    x, dt, A_head, B, C, D, dy = map(_f64, (x, dt, A_head, B, C, D, dy))
+    Bs, L, H, P = x.shape
+    shape_bc = B.shape
+    if B.ndim == 3:
+        B, C = B[:, :, None, :], C[:, :, None, :]
+    G, N = B.shape[2], B.shape[3]
+    assert G >= 1 and H % G == 0, "heads must split evenly into the groups of B, C"
+    assert dt.shape == (Bs, L, H) and A_head.shape == (H,) and dy.shape == x.shape
+    assert B.shape == (Bs, L, G, N) and C.shape == (Bs, L, G, N)
+    B, C = np.ascontiguousarray(B), np.ascontiguousarray(C)
+    assert D is None or D.shape == (H,)
+    out = dict(dx=np.zeros((Bs, L, H, P)), ddt=np.zeros((Bs, L, H)), dA=np.zeros(H),
+               dB=np.zeros((Bs, L, G, N)), dC=np.zeros((Bs, L, G, N)),
+               dD=None if D is None else np.zeros(H))
+    _load(library).oracle_ssd_scan_bwd(
+        _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(out["dx"]),
+        _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+        Bs, L, H, P, N, G, int(bool(bidirectional)), nthreads)
+    out["dB"] = out["dB"].reshape(shape_bc)
+    out["dC"] = out["dC"].reshape(shape_bc)
+    return out

@@ -323,3 +323,114 @@ void oracle_diag_scan_bwd_range(const double *x, const double *delta, const doub
         free(lC);
     }
 }
+
+/* Gradients of the chunked scalar-decay scan (the SSD form above) for an
+ * upstream gradient dy of y, written out by hand in reverse mode -- the
+ * quantities the chunked backward pass named in "Some questions of Bi-Mamba2
+ * and Hydra" (Bi-Mamba2 issue 1) returns: dx, ddt, dA, dB, dC, dD.  Per
+ * (b, h) and direction, walking k = 0 .. L-1 over t = k (forward) or
+ * t = L-1-k (reversed), with H_k the P x N state after walk step k and
+ * a_k = exp(dt_t A_h):
+ *   H_k = a_k H_{k-1} + dt_t x_t B_t^T,   y_t += H_k C_t   (+ D_h x_t once)
+ * the adjoint of H_k is
+ *   Gb_k = dy_t C_t^T + a_{k+1} Gb_{k+1},   Gb_L = 0,
+ * and
+ *   dx_t[p]   += dt_t sum_n Gb_k[p,n] B_t[n]          (+ D_h dy_t[p] once)
+ *   dB_t[n]   += dt_t sum_p Gb_k[p,n] x_t[p]          (summed over the heads of a group)
+ *   dC_t[n]   += sum_p dy_t[p] H_k[p,n]               (likewise)
+ *   ddt_t     += sum_{p,n} Gb_k[p,n] (x_t[p] B_t[n] + A_h a_k H_{k-1}[p,n])
+ *   dA_h      += sum_k dt_t a_k sum_{p,n} Gb_k[p,n] H_{k-1}[p,n]
+ *   dD_h      += sum_t dy_t . x_t                      (once).
+ * B, C, dB, dC: (Bs, L, G, N), head h reads group h / (H / G).  All outputs
+ * are ACCUMULATED into (the caller zeroes them); dD may be NULL.  The loop
+ * over batch rows is the parallel one (a batch row's heads share its dB, dC).
+ */
+static void ssd_bwd_one_direction(const double *x, const double *dt, double Ah,
+                                  const double *B, const double *C, const double *dy,
+                                  double *dx, double *ddt, double *dAh, double *dB, double *dC,
+                                  int64_t b, int64_t h, int64_t L, int64_t H, int64_t P,
+                                  int64_t N, int64_t G, int64_t g, int rev, double *hist,
+                                  double *gb) {
+    const int64_t PN = P * N;
+    /* forward: hist row k + 1 holds H_k; row 0 is the zero initial state */
+    for (int64_t i = 0; i < PN; ++i) hist[i] = 0.0;
+    for (int64_t k = 0; k < L; ++k) {
+        const int64_t t = rev ? (L - 1 - k) : k;
+        const double dtv = dt[(b * L + t) * H + h], a = exp(dtv * Ah);
+        const double *xr = x + ((b * L + t) * H + h) * P;
+        const double *br = B + ((b * L + t) * G + g) * N;
+        for (int64_t p = 0; p < P; ++p)
+            for (int64_t n = 0; n < N; ++n)
+                hist[(k + 1) * PN + p * N + n] = a * hist[k * PN + p * N + n] + dtv * xr[p] * br[n];
+    }
+    /* reverse */
+    for (int64_t i = 0; i < PN; ++i) gb[i] = 0.0;
+    for (int64_t k = L - 1; k >= 0; --k) {
+        const int64_t t = rev ? (L - 1 - k) : k;
+        const double dtv = dt[(b * L + t) * H + h], a = exp(dtv * Ah);
+        const double *xr = x + ((b * L + t) * H + h) * P;
+        const double *gy = dy + ((b * L + t) * H + h) * P;
+        const double *br = B + ((b * L + t) * G + g) * N;
+        const double *cr = C + ((b * L + t) * G + g) * N;
+        double *dxr = dx + ((b * L + t) * H + h) * P;
+        double *dbr = dB + ((b * L + t) * G + g) * N;
+        double *dcr = dC + ((b * L + t) * G + g) * N;
+        const double *hk = hist + (k + 1) * PN, *hprev = hist + k * PN;
+        double sdt = 0.0, sda = 0.0;
+        for (int64_t p = 0; p < P; ++p) {
+            double sx = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double *gpn = gb + p * N + n;
+                *gpn += gy[p] * cr[n];                 /* Gb_k */
+                sx += *gpn * br[n];
+                dbr[n] += dtv * *gpn * xr[p];
+                dcr[n] += gy[p] * hk[p * N + n];
+                sdt += *gpn * xr[p] * br[n];
+                sda += *gpn * hprev[p * N + n];
+                *gpn *= a;                             /* a_k Gb_k, carried to step k - 1 */
+            }
+            dxr[p] += dtv * sx;
+        }
+        ddt[(b * L + t) * H + h] += sdt + Ah * a * sda;
+        *dAh += dtv * a * sda;
+    }
+}
+
+void oracle_ssd_scan_bwd(const double *x, const double *dt, const double *A_head,
+                         const double *B, const double *C, const double *D, const double *dy,
+                         double *dx, double *ddt, double *dA, double *dB, double *dC,
+                         double *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                         int64_t G, int bidirectional, int nthreads) {
+    set_threads(nthreads);
+    if (G < 1 || H % G != 0) return;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t b = 0; b < Bs; ++b) {
+        double *hist = (double *)malloc((size_t)((L + 1) * P * N) * sizeof(double));
+        double *gb = (double *)malloc((size_t)(P * N) * sizeof(double));
+        double *lA = (double *)calloc((size_t)H, sizeof(double));
+        double *lD = (double *)calloc((size_t)H, sizeof(double));
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t g = h / (H / G);
+            for (int dir = 0; dir < (bidirectional ? 2 : 1); ++dir)
+                ssd_bwd_one_direction(x, dt, A_head[h], B, C, dy, dx, ddt, &lA[h], dB, dC, b, h,
+                                      L, H, P, N, G, g, dir, hist, gb);
+            for (int64_t t = 0; t < L; ++t)
+                for (int64_t p = 0; p < P; ++p) {
+                    const int64_t i = ((b * L + t) * H + h) * P + p;
+                    if (D) dx[i] += D[h] * dy[i];
+                    lD[h] += dy[i] * x[i];
+                }
+        }
+#pragma omp critical
+        {
+            for (int64_t h = 0; h < H; ++h) {
+                dA[h] += lA[h];
+                if (dD) dD[h] += lD[h];
+            }
+        }
+        free(hist);
+        free(gb);
+        free(lA);
+        free(lD);
+    }
+}

@@ -1,0 +1,135 @@
+"""Pins of the oracle's gradients of the SSD scan (CPU only).
+
+Reverse mode is written out by hand in the oracle; every gradient entry is
+checked here against central finite differences of the oracle's forward
+scan (fp64, step 1e-6: truncation error ~1e-12), on tiny random inputs --
+unidirectional, bidirectional, with groups of B, C, and without D.  Planted
+mistakes in the adjoint code are caught by the same check.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from test_oracle import _rand_ssd, _rng
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
+EPS = 1e-6
+
+
+def _case(seed, Bs, L, H, P, N, G=1, bidir=False):
+    rng = _rng(seed)
+    x, dt, A, B, C, D = _rand_ssd(rng, Bs, L, H, P, N)
+    if G > 1:
+        B = rng.standard_normal((Bs, L, G, N)) / np.sqrt(N)
+        C = rng.standard_normal((Bs, L, G, N)) / np.sqrt(N)
+    dy = rng.standard_normal(x.shape)
+    return dict(x=x, dt=dt, A_head=A, B=B, C=C, D=D), dy, bidir
+
+
+def _fd_grads(args, dy, bidir):
+    """d(sum(dy * y)) / d(each input) by central differences of the forward oracle."""
+    out = {}
+    for name in ("x", "dt", "A_head", "B", "C", "D"):
+        base = args[name]
+        if base is None:
+            continue
+        g = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            plus, minus = dict(args), dict(args)
+            p, m = base.copy(), base.copy()
+            p[idx] += EPS
+            m[idx] -= EPS
+            plus[name], minus[name] = p, m
+            lp = float(np.sum(dy * oracle.ssd_scan(**plus, bidirectional=bidir)))
+            lm = float(np.sum(dy * oracle.ssd_scan(**minus, bidirectional=bidir)))
+            g[idx] = (lp - lm) / (2 * EPS)
+        out[{"A_head": "dA"}.get(name, "d" + name)] = g
+    return out
+
+
+def _worst(an, fd):
+    return max(float(np.max(np.abs(an[k] - fd[k]))) / max(1.0, float(np.max(np.abs(fd[k]))))
+               for k in fd)
+
+
+CASES = [
+    # seed, Bs, L, H, P, N, G, bidirectional
+    (1, 1, 5, 2, 2, 3, 1, False),
+    (2, 2, 4, 1, 3, 2, 1, False),
+    (3, 1, 6, 2, 2, 3, 1, True),
+    (4, 1, 4, 4, 2, 2, 2, False),    # groups of B, C: dB, dC sum over a group's heads
+    (5, 1, 5, 2, 2, 2, 2, True),     # one group per head, both directions
+    (6, 1, 1, 1, 2, 2, 1, True),     # L = 1
+]
+
+
+@pytest.mark.parametrize("seed,Bs,L,H,P,N,G,bidir", CASES)
+def test_gradients_match_finite_differences(seed, Bs, L, H, P, N, G, bidir):
+    args, dy, bidir = _case(seed, Bs, L, H, P, N, G, bidir)
+    an = oracle.ssd_scan_bwd(**args, dy=dy, bidirectional=bidir)
+    fd = _fd_grads(args, dy, bidir)
+    assert set(an) == set(fd)
+    assert _worst(an, fd) < 1e-7
+
+
+def test_gradients_without_D():
+    args, dy, _ = _case(7, 1, 5, 2, 2, 3)
+    args["D"] = None
+    g = oracle.ssd_scan_bwd(**args, dy=dy)
+    assert g["dD"] is None
+    fd = _fd_grads(args, dy, False)
+    assert _worst({k: g[k] for k in fd}, fd) < 1e-7
+
+
+def test_single_head_width_one_equals_diagonal_gradients():
+    """With P = 1 and one head the SSD scan is the diagonal scan with ED = 1,
+    N states sharing one decay: the two oracles' gradients agree."""
+    rng = _rng(8)
+    Bs, L, N = 2, 6, 3
+    x = rng.standard_normal((Bs, L, 1, 1))
+    dt = np.log1p(np.exp(rng.standard_normal((Bs, L, 1)) - 1.0))
+    Ah = np.array([-1.7])
+    B = rng.standard_normal((Bs, L, N))
+    C = rng.standard_normal((Bs, L, N))
+    D = rng.standard_normal(1)
+    dy = rng.standard_normal((Bs, L, 1, 1))
+    s = oracle.ssd_scan_bwd(x, dt, Ah, B, C, D, dy)
+    d = oracle.diag_scan_bwd(x[:, :, :, 0], dt, np.full((1, N), Ah[0]), B, C, D, dy[:, :, :, 0])
+    assert np.allclose(s["dx"][:, :, :, 0], d["dx"], rtol=1e-12, atol=1e-12)
+    assert np.allclose(s["ddt"], d["ddelta"], rtol=1e-12, atol=1e-12)
+    assert np.allclose(s["dA"], d["dA"].sum(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(s["dB"], d["dB"], rtol=1e-12, atol=1e-12)
+    assert np.allclose(s["dC"], d["dC"], rtol=1e-12, atol=1e-12)
+    assert np.allclose(s["dD"], d["dD"], rtol=1e-12, atol=1e-12)
+
+
+SSD_BWD_MUTANTS = {
+    "adjoint_not_decayed": ("*gpn *= a;                             /* a_k Gb_k, carried to step k - 1 */",
+                            "*gpn *= 1.0;                           /* a_k Gb_k, carried to step k - 1 */"),
+    "dC_uses_entering_state": ("dcr[n] += gy[p] * hk[p * N + n];",
+                               "dcr[n] += gy[p] * hprev[p * N + n];"),
+    "ddt_decay_sign": ("ddt[(b * L + t) * H + h] += sdt + Ah * a * sda;",
+                       "ddt[(b * L + t) * H + h] += sdt - Ah * a * sda;"),
+    "dA_misses_dt": ("*dAh += dtv * a * sda;", "*dAh += a * sda;"),
+    "dB_misses_dt": ("dbr[n] += dtv * *gpn * xr[p];", "dbr[n] += *gpn * xr[p];"),
+    "dx_drops_D": ("if (D) dx[i] += D[h] * dy[i];", "if (D) dx[i] += 0.0 * dy[i];"),
+    "reverse_direction_skipped": ("for (int dir = 0; dir < (bidirectional ? 2 : 1); ++dir)",
+                                  "for (int dir = 0; dir < 1; ++dir)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SSD_BWD_MUTANTS))
+def test_planted_gradient_mistake_is_caught(name, tmp_path):
+    old, new = SSD_BWD_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation site not found: " + old
+    path = str(tmp_path / (name + ".c"))
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.compile_source(path, str(tmp_path / (name + ".so")))
+    args, dy, bidir = _case(9, 1, 5, 2, 2, 2, 2, True)
+    an = oracle.ssd_scan_bwd(**args, dy=dy, bidirectional=bidir, library=lib)
+    fd = _fd_grads(args, dy, bidir)    # the real forward oracle
+    assert _worst(an, fd) > 1e-6, "planted mistake %s was not caught" % name
