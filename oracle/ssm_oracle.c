@@ -355,7 +355,7 @@ static void ssd_bwd_one_direction(const double *x, const double *dt, double Ah,
     /* forward: hist row k + 1 holds H_k; row 0 is the zero initial state */
     for (int64_t i = 0; i < PN; ++i) hist[i] = 0.0;
     for (int64_t k = 0; k < L; ++k) {
-        const int64_t t = rev ? (L - 1 - k) : k;
+        const int64_t t = rev ? L - 1 - k : k;
         const double dtv = dt[(b * L + t) * H + h], a = exp(dtv * Ah);
         const double *xr = x + ((b * L + t) * H + h) * P;
         const double *br = B + ((b * L + t) * G + g) * N;
@@ -366,7 +366,7 @@ static void ssd_bwd_one_direction(const double *x, const double *dt, double Ah,
     /* reverse */
     for (int64_t i = 0; i < PN; ++i) gb[i] = 0.0;
     for (int64_t k = L - 1; k >= 0; --k) {
-        const int64_t t = rev ? (L - 1 - k) : k;
+        const int64_t t = rev ? L - 1 - k : k;
         const double dtv = dt[(b * L + t) * H + h], a = exp(dtv * Ah);
         const double *xr = x + ((b * L + t) * H + h) * P;
         const double *gy = dy + ((b * L + t) * H + h) * P;
@@ -410,10 +410,10 @@ void oracle_ssd_scan_bwd(const double *x, const double *dt, const double *A_head
         double *lA = (double *)calloc((size_t)H, sizeof(double));
         double *lD = (double *)calloc((size_t)H, sizeof(double));
         for (int64_t h = 0; h < H; ++h) {
-            const int64_t g = h / (H / G);
+            const int64_t hg = h / (H / G);   /* the head's group of B, C */
             for (int dir = 0; dir < (bidirectional ? 2 : 1); ++dir)
                 ssd_bwd_one_direction(x, dt, A_head[h], B, C, dy, dx, ddt, &lA[h], dB, dC, b, h,
-                                      L, H, P, N, G, g, dir, hist, gb);
+                                      L, H, P, N, G, hg, dir, hist, gb);
             for (int64_t t = 0; t < L; ++t)
                 for (int64_t p = 0; p < P; ++p) {
                     const int64_t i = ((b * L + t) * H + h) * P + p;
