@@ -262,6 +262,32 @@ SSM_API ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float 
                                   int64_t ED, int64_t N, int input_bf16, void *stream);
 
 /*
+ * Gradients of the chunked scalar-decay scan (ssd_chunk_scan_fwd_ex without
+ * options; unidirectional or bidirectional, groups of B, C): given dy, the
+ * gradient of a loss with respect to y, writes the gradients with respect to
+ * every input -- the outputs of the chunked backward pass named in "Some
+ * questions of Bi-Mamba2 and Hydra" (Bi-Mamba2 issue 1):
+ *   dx      : (Bs, L, H, P) fp32,  ddt : (Bs, L, H) fp32, overwritten
+ *   dA_head : (H) fp32,  dB, dC : (Bs, L, G, N) fp32,  dD : (H) fp32
+ *             (zeroed by the call, then accumulated; dD may be NULL)
+ * x, dt, B, C are fp32 (input_bf16 == 0) or bf16; A_head, D, dy are fp32;
+ * B, C are (Bs, L, G, N) with G = ngroups dividing H (head h reads group
+ * h / (H / G)).  Supported (SSM_ERR_UNSUPPORTED otherwise): P in {16, 32,
+ * 64, 128}, N in {32, 64, 128, 256}, P * N <= 8192.  Computed on CUDA cores
+ * from the recurrence step by step (a correctness path, not tuned): takes a
+ * stream-ordered scratch buffer of Bs*H*L*P*N*4 bytes (every state of one
+ * direction).  dx and ddt are deterministic; dA_head, dB, dC, dD are sums
+ * formed with atomic additions, so their last bits may differ between runs.
+ * Alignment: every pointer to its element size.
+ */
+SSM_API ssm_status_t ssd_chunk_scan_bwd(const void *x, const void *dt, const float *A_head,
+                                        const void *B, const void *C, const float *D,
+                                        const float *dy, float *dx, float *ddt, float *dA_head,
+                                        float *dB, float *dC, float *dD, int64_t Bs, int64_t L,
+                                        int64_t H, int64_t P, int64_t N, int64_t ngroups,
+                                        int bidirectional, int input_bf16, void *stream);
+
+/*
  * Synchronise `stream` and report whether a kernel of this library running on
  * the current device gave up a bounded wait (SSM_ERR_DEVICE_TIMEOUT) since
  * the previous check; the record is cleared by the call.  Kernels never hang

@@ -34,7 +34,7 @@ import os
 from . import _build
 
 __all__ = ["ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssd_chunk_scan_fwd", "ssm_check_device_errors",
-           "ssm_scan_fwd_plan", "ssm_scan_bwd", "ScanOptions",
+           "ssm_scan_fwd_plan", "ssm_scan_bwd", "ssd_chunk_scan_bwd", "ScanOptions",
            "SsmError", "library", "build", "status_string", "STATUS"]
 
 STATUS = {
@@ -54,6 +54,7 @@ SIGNATURES = {
                           ctypes.c_int),
     "ssm_scan_fwd_ex": ([_VP] * 7 + [_I64] * 4 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
     "ssm_scan_bwd": ([_VP] * 13 + [_I64] * 4 + [ctypes.c_int, _VP], ctypes.c_int),
+    "ssd_chunk_scan_bwd": ([_VP] * 13 + [_I64] * 6 + [ctypes.c_int, ctypes.c_int, _VP], ctypes.c_int),
     "ssd_chunk_scan_fwd_ex": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, ctypes.c_int, _VP, _VP],
                               ctypes.c_int),
     "ssm_check_device_errors": ([_VP], ctypes.c_int),
@@ -298,6 +299,43 @@ def ssm_scan_bwd(x, delta, A, B, C, D, dy):
                                 int(x.dtype == torch.bfloat16), _stream(dev))
     if st != 0:
         raise SsmError("ssm_scan_bwd", st)
+    return g
+
+
+def ssd_chunk_scan_bwd(x, dt, A_head, B, C, D, dy, bidirectional: bool = False):
+    """Gradients of the chunked scan (no options) for the upstream gradient
+    dy (fp32, shaped like y): dict(dx, ddt, dA, dB, dC, dD) as fp32 tensors
+    (dB, dC shaped like B, C; dD is None when D is None)."""
+    import torch
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    ins = (torch.float32, torch.bfloat16)
+    _check(x, "x", ins, dev, (4,))
+    _check(dt, "dt", (x.dtype,), dev, (3,))
+    _check(B, "B", (x.dtype,), dev, (3, 4))
+    _check(C, "C", (x.dtype,), dev, (3, 4))
+    _check(A_head, "A_head", (torch.float32,), dev, (1,))
+    _check(D, "D", (torch.float32,), dev, (1,))
+    _check(dy, "dy", (torch.float32,), dev, (4,))
+    Bs, L, H, P = x.shape
+    G = 1 if B.dim() == 3 else B.shape[2]
+    N = B.shape[-1]
+    bc = (Bs, L, N) if B.dim() == 3 else (Bs, L, G, N)
+    if tuple(dt.shape) != (Bs, L, H) or tuple(A_head.shape) != (H,) or dy.shape != x.shape \
+            or tuple(B.shape) != bc or tuple(C.shape) != bc:
+        raise ValueError("shape mismatch: x, dy (Bs,L,H,P); dt (Bs,L,H); A_head (H); "
+                         "B, C (Bs,L,N) or (Bs,L,G,N)")
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(dx=torch.empty((Bs, L, H, P), **f32), ddt=torch.empty((Bs, L, H), **f32),
+             dA=torch.empty(H, **f32), dB=torch.empty(bc, **f32), dC=torch.empty(bc, **f32),
+             dD=None if D is None else torch.empty(H, **f32))
+    st = library().ssd_chunk_scan_bwd(
+        _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(g["dx"]),
+        _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+        Bs, L, H, P, N, G, int(bool(bidirectional)), int(x.dtype == torch.bfloat16), _stream(dev))
+    if st != 0:
+        raise SsmError("ssd_chunk_scan_bwd", st)
     return g
 
 

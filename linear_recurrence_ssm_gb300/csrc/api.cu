@@ -30,6 +30,14 @@ cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *
                        float *dB, float *dC, float *dD, int64_t Bs, int64_t L, int64_t ED,
                        int64_t N, int num_sms, cudaStream_t st);
 }
+namespace ssd_bwd {
+bool supported(int64_t P, int64_t N);
+template <typename Tin>
+cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *Bm, const Tin *Cm,
+                   const float *D, const float *dy, float *dx, float *ddt, float *dA, float *dB,
+                   float *dC, float *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                   int64_t G, bool bidir, cudaStream_t st);
+}
 namespace ssd_general {
 bool supported(int64_t P, int64_t N);
 template <typename Tin>
@@ -299,6 +307,40 @@ ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float *A, cons
         static_cast<const float *>(x), static_cast<const float *>(delta), A,
         static_cast<const float *>(B), static_cast<const float *>(C), D, dy, dx, ddelta, dA, dB,
         dC, dD, Bs, L, ED, N, dev.num_sms, st));
+}
+
+ssm_status_t ssd_chunk_scan_bwd(const void *x, const void *dt, const float *A_head, const void *B,
+                                const void *C, const float *D, const float *dy, float *dx,
+                                float *ddt, float *dA_head, float *dB, float *dC, float *dD,
+                                int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                                int64_t ngroups, int bidirectional, int input_bf16, void *stream) {
+    if (!x || !dt || !A_head || !B || !C || !dy || !dx || !ddt || !dA_head || !dB || !dC)
+        return SSM_ERR_INVALID_ARG;
+    if (ngroups < 1 || !sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, ngroups, N}) ||
+        !sizes_ok({Bs, H, L, P, N}))
+        return SSM_ERR_INVALID_ARG;
+    if (!ssm::ssd_bwd::supported(P, N) || H % ngroups != 0 || Bs * H > INT_MAX || L > INT_MAX)
+        return SSM_ERR_UNSUPPORTED;
+    const size_t es = input_bf16 ? 2 : 4;
+    if (!aligned(x, es) || !aligned(dt, es) || !aligned(B, es) || !aligned(C, es) ||
+        !aligned(A_head, 4) || (D && !aligned(D, 4)) || !aligned(dy, 4) || !aligned(dx, 4) ||
+        !aligned(ddt, 4) || !aligned(dA_head, 4) || !aligned(dB, 4) || !aligned(dC, 4) ||
+        (dD && !aligned(dD, 4)))
+        return SSM_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    ssm_status_t s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    using bf = __nv_bfloat16;
+    if (input_bf16)
+        return from_cuda(ssm::ssd_bwd::launch<bf>(
+            static_cast<const bf *>(x), static_cast<const bf *>(dt), A_head,
+            static_cast<const bf *>(B), static_cast<const bf *>(C), D, dy, dx, ddt, dA_head, dB,
+            dC, dD, Bs, L, H, P, N, ngroups, bidirectional != 0, st));
+    return from_cuda(ssm::ssd_bwd::launch<float>(
+        static_cast<const float *>(x), static_cast<const float *>(dt), A_head,
+        static_cast<const float *>(B), static_cast<const float *>(C), D, dy, dx, ddt, dA_head, dB,
+        dC, dD, Bs, L, H, P, N, ngroups, bidirectional != 0, st));
 }
 
 ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED, int64_t N, int input_bf16,

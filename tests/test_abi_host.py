@@ -171,3 +171,23 @@ def test_backward_rejects_bad_arguments():
     bad = list(p13)
     bad[8] = P_ODD                                                 # ddelta misaligned
     assert lib.ssm_scan_bwd(*bad, 1, 8, 8, 4, 0, None) == 3
+
+
+def test_ssd_backward_rejects_bad_arguments():
+    lib = lrs.library()
+    p13 = [P] * 13
+    # (Bs, L, H, P, N, ngroups, bidirectional, input_bf16)
+    assert lib.ssd_chunk_scan_bwd(*p13, 1, 8, 2, 48, 64, 1, 0, 1, None) == 2     # P = 48
+    assert lib.ssd_chunk_scan_bwd(*p13, 1, 8, 2, 64, 16, 1, 0, 1, None) == 2     # N = 16
+    assert lib.ssd_chunk_scan_bwd(*p13, 1, 8, 2, 128, 128, 1, 0, 1, None) == 2   # P * N > 8192
+    assert lib.ssd_chunk_scan_bwd(*p13, 1, 8, 3, 64, 64, 2, 0, 1, None) == 2     # H % G != 0
+    assert lib.ssd_chunk_scan_bwd(*p13, 1, 8, 2, 64, 64, 0, 0, 1, None) == 1     # no groups
+    assert lib.ssd_chunk_scan_bwd(*p13, 0, 8, 2, 64, 64, 1, 0, 1, None) == 1     # Bs = 0
+    bad = list(p13)
+    bad[6] = None                                                                 # dy
+    assert lib.ssd_chunk_scan_bwd(*bad, 1, 8, 2, 64, 64, 1, 0, 1, None) == 1
+    bad = list(p13)
+    bad[8] = P_ODD                                                                # ddt misaligned
+    assert lib.ssd_chunk_scan_bwd(*bad, 1, 8, 2, 64, 64, 1, 0, 1, None) == 3
+    # a valid call reaches the device check (no GPU here, or a real launch there)
+    assert lib.ssd_chunk_scan_bwd(*([None] * 13), 1, 8, 2, 64, 64, 1, 0, 1, None) == 1
