@@ -59,7 +59,8 @@ def parse_args():
     p.add_argument("--mode", choices=["fwd", "options", "bwd"], default="fwd",
                    help="fwd: the plain forward scan (the headline); options: the forward scan "
                         "with every option on (delta bias + softplus + clamp, silu gate, initial "
-                        "and final state); bwd: the diagonal scan's gradients")
+                        "and final state); bwd: the gradients (diagonal scan, or the chunked "
+                        "scan's CUDA-core correctness path)")
     return p.parse_args()
 
 
@@ -231,10 +232,15 @@ def option_host_inputs(w, seed):
 
 def make_step(w, lrs, bufs, mode="fwd"):
     s = w.shape
-    if mode == "bwd":
+    if mode == "bwd" and w.kind == "diag":
         def step(i):
             b = bufs[i % len(bufs)]
             lrs.ssm_scan_bwd(b["x"], b["delta"], b["A"], b["B"], b["C"], b["D"], b["dy"])
+    elif mode == "bwd":
+        def step(i):
+            b = bufs[i % len(bufs)]
+            lrs.ssd_chunk_scan_bwd(b["x"], b["dt"], b["A_head"], b["B"], b["C"], b["D"], b["dy"],
+                                   bidirectional=s["bidirectional"])
     elif w.kind == "diag":
         def step(i):
             b = bufs[i % len(bufs)]
@@ -274,6 +280,11 @@ def mode_bytes(w, mode) -> int:
         xs = s["Bs"] * s["L"] * s["H"] * s["P"]
         state = 0 if s["bidirectional"] else s["Bs"] * s["H"] * s["P"] * s["N"]
         return w.algorithmic_bytes + xs * esz + 2 * state * 4 + s["H"] * 4
+    if w.kind != "diag":
+        # backward of the chunked scan: x, dt, B, C, A, D, dy in; dx, ddt, dA, dB, dC, dD out
+        xs, dts, bc = s["Bs"] * s["L"] * s["H"] * s["P"], s["Bs"] * s["L"] * s["H"], s["Bs"] * s["L"] * s["N"]
+        return (xs * esz + dts * esz + 2 * bc * esz + xs * 4 + xs * 4 + dts * 4 + 2 * bc * 4
+                + 4 * s["H"] * 4)
     # backward of the diagonal scan: x, delta, B, C, A, D, dy in; dx, ddelta, dA, dB, dC, dD out
     xs, bc = s["Bs"] * s["L"] * s["ED"], s["Bs"] * s["L"] * s["N"]
     return (2 * xs * esz + 2 * bc * esz + xs * 4 + 2 * xs * 4 + 2 * bc * 4
@@ -299,8 +310,6 @@ def run_ours(args, rank, world, local):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     w = workloads.BY_NAME[args.workload]
-    if args.mode == "bwd" and w.kind != "diag":
-        raise SystemExit("bench.py: --mode bwd exists for the diagonal scan only")
     lrs.library()
 
     # Resident input/output sets; each rank draws its own batch (weak scaling).
@@ -398,7 +407,12 @@ def run_ours(args, rank, world, local):
     value = units * args.steps * world / (ms / 1e3)
     e2e_value = units * k_e2e * world / (ms_e2e / 1e3) if k_e2e else None
     peaks = load_peaks()
-    launches_per_step = 2 if args.mode == "bwd" else kernels_per_call(w, lrs)
+    if args.mode == "bwd":
+        # diagonal: checkpointing forward + reverse pass; chunked: state pass +
+        # reverse pass per direction
+        launches_per_step = 2 if w.kind == "diag" else 2 * (2 if w.shape["bidirectional"] else 1)
+    else:
+        launches_per_step = kernels_per_call(w, lrs)
     per_launch_s = ms / 1e3 / args.steps
     call_bytes = mode_bytes(w, args.mode)
     hbm_achieved = call_bytes / per_launch_s / 1e9
