@@ -23,6 +23,9 @@ scan and a chunkwise form, and state that their results must agree.
   state passing across chunks and
   the inter-chunk output; optionally with the reversed direction computed from
   the same chunks (no flipped copy), as that page describes.
+* ``ssd_scan_bwd_chunked`` -- the gradients of the SSD scan in the same
+  chunked shape (the chunked backward pass that page names): transposed chunk
+  products and a state gradient passed from the last chunk to the first.
 """
 from __future__ import annotations
 
@@ -232,3 +235,102 @@ def ssd_scan_chunked(x, dt, A_head, B, C, D=None, chunk: int = 64, bidirectional
     if D is not None:
         y = y + D[None, None, :, None] * x
     return y
+
+
+# ---------------------------------------------------------------------------
+# Chunked form of the SSD gradients
+# ---------------------------------------------------------------------------
+
+def _ssd_bwd_chunked_one_direction(x, dt, A_head, B, C, dy, chunk):
+    """Gradients of the forward-direction chunked scan (no D term).
+
+    B, C: (Bs, L, G, N).  Per (b, h) the forward chunk recursion is run to get
+    the state S_in entering each chunk; then, from the last chunk to the first,
+    with dS the gradient of the state leaving the chunk (0 after the last):
+
+      du_s   = sum_{t>=s} G[t,s] e^{cum_t-cum_s} dY_t + e^{tot-cum_s} dS B_s
+      dG     = Lf o (dY u^T)  ->  dC += dG B,  dB += dG^T C
+      dC_t  += e^{cum_t} dY_t S_in,      dB_s += e^{tot-cum_s} dS^T u_s
+      dcum_t = sum_s W[t,s] - sum_s W[s,t] + e^{cum_t} dY_t . (S_in C_t)
+               - e^{tot-cum_t} u_t . (dS B_t),     W = G o dG
+      dtot   = <dS, S_out>
+      d(dt_r A_h) = sum_{i>=r} dcum_i + dtot
+      dS_in  = e^{tot} dS + sum_t e^{cum_t} dY_t (x) C_t
+
+    with u_s = dt_s x_s, so dx_s = dt_s du_s, ddt_s = x_s . du_s + A_h d(dA_s)
+    and dA_h = sum_r dt_r d(dA_r).
+    """
+    Bs, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    hpg = H // G
+    out = dict(dx=np.zeros_like(x), ddt=np.zeros_like(dt), dA=np.zeros(H),
+               dB=np.zeros_like(B), dC=np.zeros_like(C))
+    bounds = [(c0, min(L, c0 + chunk)) for c0 in range(0, L, chunk)]
+    for b in range(Bs):
+        for h in range(H):
+            g = h // hpg
+            Ah = A_head[h]
+            pieces = []
+            S = np.zeros((P, N))
+            for (c0, c1) in bounds:          # forward: the state entering each chunk
+                dA = dt[b, c0:c1, h] * Ah
+                cum = np.cumsum(dA)
+                tot = cum[-1]
+                u = dt[b, c0:c1, h, None] * x[b, c0:c1, h]
+                S_out = np.exp(tot) * S + (np.exp(tot - cum)[:, None] * u).T @ B[b, c0:c1, g]
+                pieces.append((c0, c1, cum, tot, u, S, S_out))
+                S = S_out
+            dS = np.zeros((P, N))
+            for (c0, c1, cum, tot, u, S_in, S_out) in reversed(pieces):
+                Bc, Cc, dY = B[b, c0:c1, g], C[b, c0:c1, g], dy[b, c0:c1, h]
+                Gm = Cc @ Bc.T
+                q = c1 - c0
+                tt, ss = np.meshgrid(np.arange(q), np.arange(q), indexing="ij")
+                with np.errstate(over="ignore", invalid="ignore"):
+                    Lf = np.where(ss <= tt, np.exp(cum[:, None] - cum[None, :]), 0.0)
+                dSB = Bc @ dS.T                                   # (Q, P): dS B_s
+                du = (Gm * Lf).T @ dY + np.exp(tot - cum)[:, None] * dSB
+                dG = Lf * (dY @ u.T)
+                out["dC"][b, c0:c1, g] += dG @ Bc + np.exp(cum)[:, None] * (dY @ S_in)
+                out["dB"][b, c0:c1, g] += dG.T @ Cc + np.exp(tot - cum)[:, None] * (u @ dS)
+                W = Gm * dG
+                dcum = (W.sum(axis=1) - W.sum(axis=0)
+                        + np.exp(cum) * np.sum(dY * (Cc @ S_in.T), axis=1)
+                        - np.exp(tot - cum) * np.sum(u * dSB, axis=1))
+                dtot = float(np.sum(dS * S_out))
+                d_dA = np.cumsum(dcum[::-1])[::-1] + dtot
+                out["dx"][b, c0:c1, h] += dt[b, c0:c1, h, None] * du
+                out["ddt"][b, c0:c1, h] += np.sum(x[b, c0:c1, h] * du, axis=1) + Ah * d_dA
+                out["dA"][h] += float(np.sum(dt[b, c0:c1, h] * d_dA))
+                dS = np.exp(tot) * dS + (np.exp(cum)[:, None] * dY).T @ Cc
+    return out
+
+
+def ssd_scan_bwd_chunked(x, dt, A_head, B, C, D, dy, chunk: int = 64, bidirectional: bool = False):
+    """Gradients (dx, ddt, dA, dB, dC, dD) of sum(dy * y) for the SSD scan,
+    chunk by chunk: the transposed products of the chunked pipeline and the
+    state gradient passed from the last chunk to the first.
+
+    B, C: (Bs, L, N) or (Bs, L, G, N) (groups of heads sharing B, C; dB, dC
+    are summed over a group's heads).  The reversed direction of the
+    bidirectional scan is the forward direction's gradient on time-reversed
+    inputs and upstream gradient, reversed back; D x enters once.
+    """
+    x, dt, A_head, B, C, D, dy = map(_f64, (x, dt, A_head, B, C, D, dy))
+    grouped = B.ndim == 4
+    if not grouped:
+        B, C = B[:, :, None, :], C[:, :, None, :]
+    out = _ssd_bwd_chunked_one_direction(x, dt, A_head, B, C, dy, chunk)
+    if bidirectional:
+        rev = lambda a: a[:, ::-1]
+        r = _ssd_bwd_chunked_one_direction(rev(x), rev(dt), A_head, rev(B), rev(C), rev(dy), chunk)
+        for k in ("dx", "ddt", "dB", "dC"):
+            out[k] = out[k] + rev(r[k])
+        out["dA"] = out["dA"] + r["dA"]
+    out["dD"] = None
+    if D is not None:
+        out["dx"] = out["dx"] + D[None, None, :, None] * dy
+        out["dD"] = np.sum(dy * x, axis=(0, 1, 3))
+    if not grouped:
+        out["dB"], out["dC"] = out["dB"][:, :, 0], out["dC"][:, :, 0]
+    return out

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
+from oracle import forms
 from test_oracle import _rand_ssd, _rng
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
@@ -103,6 +104,33 @@ def test_single_head_width_one_equals_diagonal_gradients():
     assert np.allclose(s["dB"], d["dB"], rtol=1e-12, atol=1e-12)
     assert np.allclose(s["dC"], d["dC"], rtol=1e-12, atol=1e-12)
     assert np.allclose(s["dD"], d["dD"], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed,Bs,L,H,P,N,G,bidir,chunk", [
+    (11, 1, 9, 2, 3, 4, 1, False, 4),      # ragged last chunk
+    (12, 2, 13, 2, 2, 3, 1, True, 5),
+    (13, 1, 17, 4, 3, 2, 2, False, 1),     # one step per chunk: the recurrence itself
+    (14, 1, 11, 2, 2, 3, 2, True, 11),     # one chunk: the quadratic masked form
+    (15, 1, 20, 2, 3, 4, 1, True, 64),     # chunk longer than L
+    (16, 1, 24, 1, 2, 2, 1, False, 8),     # whole chunks only
+])
+def test_chunked_gradient_form_matches_sequential(seed, Bs, L, H, P, N, G, bidir, chunk):
+    """The chunked form of the gradients (transposed chunk products, state
+    gradient passed from the last chunk back) reaches the sequential
+    reverse-mode result for every chunk size, to rounding."""
+    rng = _rng(seed)
+    x, dt, A, B, C, D = _rand_ssd(rng, Bs, L, H, P, N)
+    if G > 1:
+        B = rng.standard_normal((Bs, L, G, N)) / np.sqrt(N)
+        C = rng.standard_normal((Bs, L, G, N)) / np.sqrt(N)
+    dy = rng.standard_normal(x.shape)
+    ref = oracle.ssd_scan_bwd(x, dt, A, B, C, D, dy, bidirectional=bidir)
+    got = forms.ssd_scan_bwd_chunked(x, dt, A, B, C, D, dy, chunk=chunk, bidirectional=bidir)
+    assert set(got) == set(ref)
+    for k in ref:
+        assert got[k].shape == ref[k].shape, k
+        scale = max(1.0, float(np.max(np.abs(ref[k]))))
+        assert float(np.max(np.abs(got[k] - ref[k]))) <= 1e-12 * scale, k
 
 
 SSD_BWD_MUTANTS = {
