@@ -1,5 +1,6 @@
 """Parity at the benchmark sizes for the widened paths: every scan option
-on (the benchmark's option mode) and the diagonal scan's gradients.
+on (the benchmark's option mode), the diagonal scan's gradients and the
+chunked scan's gradients.
 
 The GPU runs the whole workload in the launch configuration the benchmark
 times; the fp64 oracle recomputes a spread-out sample of channels / heads
@@ -7,7 +8,8 @@ one by one (the option inputs follow the benchmark's recipe: seed + 7,
 dt_limit = (1e-4, 100)).  For the gradients the sample is whole channels e
 over all batch rows, so that the per-channel sums dA[e, :] and dD[e] are
 complete; dB and dC (sums over all channels) are covered at small sizes in
-test_gpu_backward.  Tolerance: 2e-2 * max|ref| of each compared quantity
+test_gpu_backward.  The chunked scan's gradients are compared whole: the
+oracle computes every head (seconds at these sizes).  Tolerance: 2e-2 * max|ref| of each compared quantity
 (bf16 inputs).
 """
 import numpy as np
@@ -117,3 +119,22 @@ def test_gradients_at_benchmark_size(cuda_device):
         _close(got["ddelta"][:, :, e], ref["ddelta"][:, :, 0], "ddelta (e=%d)" % e)
         _close(got["dA"][e], ref["dA"][0], "dA (e=%d)" % e)
         _close(got["dD"][e:e + 1], ref["dD"], "dD (e=%d)" % e)
+
+
+@pytest.mark.parametrize("name", ["ssd_bf16_Bs4_L4096_H32_P64_N128_Q256",
+                                  "bissd_bf16_Bs32_L400_H8_P64_N64_Q128"])
+def test_ssd_gradients_at_benchmark_size(cuda_device, name):
+    w = workloads.BY_NAME[name]
+    s = w.shape
+    bidir = s["bidirectional"]
+    inp = workloads.workload_inputs(w)
+    dy = workloads.grad_output((s["Bs"], s["L"], s["H"], s["P"]), seed=w.seed + 11)
+    got = lrs.ssd_chunk_scan_bwd(**{k: v.to(cuda_device) for k, v in inp.items()},
+                                 dy=dy.to(cuda_device), bidirectional=bidir)
+    torch.cuda.synchronize()
+    got = {k: v.cpu().double().numpy() for k, v in got.items()}
+    ref = oracle.ssd_scan_bwd(**inp, dy=dy, bidirectional=bidir)
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dD"):
+        assert got[k].shape == ref[k].shape, k
+        _close(got[k], ref[k], k)
+    lrs.ssm_check_device_errors()
