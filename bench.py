@@ -282,7 +282,8 @@ def mode_bytes(w, mode) -> int:
         return w.algorithmic_bytes + xs * esz + 2 * state * 4 + s["H"] * 4
     if w.kind != "diag":
         # backward of the chunked scan: x, dt, B, C, A, D, dy in; dx, ddt, dA, dB, dC, dD out
-        xs, dts, bc = s["Bs"] * s["L"] * s["H"] * s["P"], s["Bs"] * s["L"] * s["H"], s["Bs"] * s["L"] * s["N"]
+        xs, dts = s["Bs"] * s["L"] * s["H"] * s["P"], s["Bs"] * s["L"] * s["H"]
+        bc = s["Bs"] * s["L"] * s.get("groups", 1) * s["N"]
         return (xs * esz + dts * esz + 2 * bc * esz + xs * 4 + xs * 4 + dts * 4 + 2 * bc * 4
                 + 4 * s["H"] * 4)
     # backward of the diagonal scan: x, delta, B, C, A, D, dy in; dx, ddelta, dA, dB, dC, dD out
@@ -498,9 +499,15 @@ def _oracle_sample(w, host, units_per_call_target):
     per_head = L * P * N * dirs
     nb = max(1, min(Bs, int(units_per_call_target // (per_head * H)) or 1))
     nh = H if nb > 1 else max(1, min(H, int(units_per_call_target // per_head)))
+    G = host["B"].shape[2]
+    ng = G
+    if G > 1:   # whole groups only: head h reads group h // (H / G)
+        hpg = H // G
+        ng = max(1, nh // hpg)
+        nh = ng * hpg
     sl = dict(x=host["x"][:nb, :, :nh].contiguous(), dt=host["dt"][:nb, :, :nh].contiguous(),
-              A_head=host["A_head"][:nh].contiguous(), B=host["B"][:nb], C=host["C"][:nb],
-              D=host["D"][:nh].contiguous())
+              A_head=host["A_head"][:nh].contiguous(), B=host["B"][:nb, :, :ng].contiguous(),
+              C=host["C"][:nb, :, :ng].contiguous(), D=host["D"][:nh].contiguous())
     sl = {k: oracle._f64(v) for k, v in sl.items()}
     fn = lambda: oracle.ssd_scan(**sl, bidirectional=s["bidirectional"])
     return fn, nb * L * nh * P * N * dirs, "%d of %d (batch, head) pairs" % (nb * nh, Bs * H)

@@ -50,7 +50,8 @@ class Workload:
             return (2 * Bs * L * ED * ib + 2 * Bs * L * N * ib + ED * N * 4 + ED * 4
                     + Bs * L * ED * 4)
         Bs, L, H, P, N = s["Bs"], s["L"], s["H"], s["P"], s["N"]
-        return (Bs * L * H * P * ib + Bs * L * H * ib + 2 * Bs * L * N * ib + H * 4 + H * 4
+        G = s.get("groups", 1)
+        return (Bs * L * H * P * ib + Bs * L * H * ib + 2 * Bs * L * G * N * ib + H * 4 + H * 4
                 + Bs * L * H * P * 4)
 
 
@@ -66,6 +67,13 @@ WORKLOADS = [
              dict(Bs=4, L=4096, H=32, P=64, N=128, chunk=256, bidirectional=False), seed=3),
     Workload("bissd_bf16_Bs32_L400_H8_P64_N64_Q128", "ssd", "bf16",
              dict(Bs=32, L=400, H=8, P=64, N=64, chunk=128, bidirectional=True), seed=4),
+    # The widened paths at the chunked scan's benchmark shape (not in the
+    # method's table): fp32 inputs, and eight groups of B, C (four heads each).
+    Workload("ssd_f32_Bs4_L4096_H32_P64_N128_Q256", "ssd", "f32",
+             dict(Bs=4, L=4096, H=32, P=64, N=128, chunk=256, bidirectional=False), seed=5),
+    Workload("ssd_bf16_Bs4_L4096_H32_G8_P64_N128_Q256", "ssd", "bf16",
+             dict(Bs=4, L=4096, H=32, P=64, N=128, chunk=256, bidirectional=False, groups=8),
+             seed=6),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 
@@ -138,4 +146,5 @@ def workload_inputs(w: Workload):
     s = w.shape
     if w.kind == "diag":
         return diag_inputs(s["Bs"], s["L"], s["ED"], s["N"], w.dtype, w.seed)
-    return ssd_inputs(s["Bs"], s["L"], s["H"], s["P"], s["N"], w.dtype, w.seed)
+    return ssd_inputs(s["Bs"], s["L"], s["H"], s["P"], s["N"], w.dtype, w.seed,
+                      groups=s.get("groups", 1))
