@@ -195,6 +195,30 @@ def kernels_per_call(w, lrs) -> int:
     return 2 if k > 1 else 1
 
 
+class nvtx_range:
+    """An NVTX range (named in profiler timelines) around a block; a no-op
+    where NVTX is unavailable."""
+
+    def __init__(self, name: str):
+        self.name = name
+
+    def __enter__(self):
+        try:
+            torch.cuda.nvtx.range_push(self.name)
+            self.pushed = True
+        except Exception:
+            self.pushed = False
+        return self
+
+    def __exit__(self, *exc):
+        if self.pushed:
+            try:
+                torch.cuda.nvtx.range_pop()
+            except Exception:
+                pass
+        return False
+
+
 def max_over_ranks(values, world: int, device):
     """Element-wise maximum of per-rank timings over all ranks (the slowest
     rank defines the step time); identity on one rank."""
@@ -353,10 +377,11 @@ def run_ours(args, rank, world, local):
     t_wall0 = time.time()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(args.steps):
-        step(k)
-    e1.record(stream)
+    with nvtx_range("%s %s: %d timed steps" % (w.name, args.mode, args.steps)):
+        e0.record(stream)
+        for k in range(args.steps):
+            step(k)
+        e1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     if world > 1:
@@ -391,14 +416,15 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(k_e2e):
-        for n, t in pinned.items():
-            if t is not None:
-                dbuf[n].copy_(t, non_blocking=True)
-        step(0)
-        y_host.copy_(dbuf["y"], non_blocking=True)
-    f1.record(stream)
+    with nvtx_range("%s %s: %d end-to-end steps" % (w.name, args.mode, k_e2e)):
+        f0.record(stream)
+        for _ in range(k_e2e):
+            for n, t in pinned.items():
+                if t is not None:
+                    dbuf[n].copy_(t, non_blocking=True)
+            step(0)
+            y_host.copy_(dbuf["y"], non_blocking=True)
+        f1.record(stream)
     torch.cuda.synchronize(dev)
     ms_e2e = f0.elapsed_time(f1) if k_e2e else float("nan")
 
