@@ -27,6 +27,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -493,7 +495,9 @@ def run_ours(args, rank, world, local):
         "gpu_launches": args.steps * launches_per_step,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.mode == "fwd":
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        # bufs[0] holds the workload's inputs and the y of its last step
+        line["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds, y_gpu=bufs[0]["y"])
+        line["parity"] = parity
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
@@ -506,7 +510,9 @@ def run_ours(args, rank, world, local):
 
 def _oracle_sample(w, host, units_per_call_target):
     """Slice a contiguous block of channels (diag) or heads (SSD) of every batch
-    row; returns (callable, element-steps it computes, description)."""
+    row; returns (callable, element-steps it computes, description, view), the
+    callable returning the sample's y and view(y) picking the same part of a
+    whole-workload y."""
     import oracle
     s = w.shape
     if w.kind == "diag":
@@ -519,7 +525,7 @@ def _oracle_sample(w, host, units_per_call_target):
         sl = {k: oracle._f64(v) for k, v in sl.items()}
         fn = lambda: oracle.diag_scan(**sl)
         return fn, Bs * L * ne * N, "%d of %d channels (e < %d) of all %d batch rows" % (
-            ne * Bs, Bs * ED, ne, Bs)
+            ne * Bs, Bs * ED, ne, Bs), (lambda y: y[:, :, :ne])
     Bs, L, H, P, N = s["Bs"], s["L"], s["H"], s["P"], s["N"]
     dirs = 2 if s["bidirectional"] else 1
     per_head = L * P * N * dirs
@@ -536,19 +542,35 @@ def _oracle_sample(w, host, units_per_call_target):
               C=host["C"][:nb, :, :ng].contiguous(), D=host["D"][:nh].contiguous())
     sl = {k: oracle._f64(v) for k, v in sl.items()}
     fn = lambda: oracle.ssd_scan(**sl, bidirectional=s["bidirectional"])
-    return fn, nb * L * nh * P * N * dirs, "%d of %d (batch, head) pairs" % (nb * nh, Bs * H)
+    return (fn, nb * L * nh * P * N * dirs, "%d of %d (batch, head) pairs" % (nb * nh, Bs * H),
+            (lambda y: y[:nb, :, :nh]))
 
 
-def cpu_baseline(w, seconds: float):
+def parity_on_sample(w, y_full, ref, view, desc):
+    """The GPU's y against the oracle's on the CPU baseline's sample, with the
+    tolerance of the input type (fp32: 1e-4 * max(1, max|y_ref|); bf16:
+    2e-2 * max|y_ref|)."""
+    got = view(y_full).double().cpu().numpy()
+    err = float(np.max(np.abs(got - ref)))
+    scale = float(np.max(np.abs(ref)))
+    bound = 1e-4 * max(1.0, scale) if w.dtype == "f32" else 2e-2 * scale
+    return {"max_abs_err": err, "ref_max_abs": scale, "bound": bound, "ok": bool(err <= bound),
+            "sample": desc}
+
+
+def cpu_baseline(w, seconds: float, y_gpu=None):
+    """The oracle timed on a sample of the workload; with y_gpu (the GPU's y
+    for the same inputs) also the parity of that sample.  Returns
+    (cpu_baseline, parity or None)."""
     import oracle
     host = workloads.workload_inputs(w)
     cores = oracle.max_threads()
     # Calibrate on a small sample, then size the sample to ~`seconds`.
-    fn, units, _ = _oracle_sample(w, host, 2e6)
+    fn, units, _, _ = _oracle_sample(w, host, 2e6)
     t0 = time.perf_counter()
     fn()
     rate = units / max(1e-6, time.perf_counter() - t0)
-    fn, units, desc = _oracle_sample(w, host, rate * seconds)
+    fn, units, desc, view = _oracle_sample(w, host, rate * seconds)
     # The sample is capped at the whole workload: time one pass, then repeat
     # it until the time budget is filled.
     t0 = time.perf_counter()
@@ -557,11 +579,13 @@ def cpu_baseline(w, seconds: float):
     reps = max(1, min(500, int(round(seconds / max(t_one, 1e-3)))))
     t0 = time.perf_counter()
     for _ in range(reps):
-        fn()
+        ref = fn()
     dt = time.perf_counter() - t0
-    return {"value": units * reps / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "%s, %d pass(es); %.3g element-steps in %.2f s (fp64 sequential C, OpenMP)"
-                      % (desc, reps, units * reps, dt)}
+    cb = {"value": units * reps / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+          "sample": "%s, %d pass(es); %.3g element-steps in %.2f s (fp64 sequential C, OpenMP)"
+                    % (desc, reps, units * reps, dt)}
+    parity = parity_on_sample(w, y_gpu, ref, view, desc) if y_gpu is not None else None
+    return cb, parity
 
 
 def run_reference(args, rank, world):
@@ -572,12 +596,12 @@ def run_reference(args, rank, world):
     host = workloads.workload_inputs(w)
     cores = oracle.max_threads()
     budget = 150.0  # seconds for the whole warm-up + timed run
-    fn, units, _ = _oracle_sample(w, host, 2e6)
+    fn, units, _, _ = _oracle_sample(w, host, 2e6)
     t0 = time.perf_counter()
     fn()
     rate = units / max(1e-6, time.perf_counter() - t0)
     per_step = max(0.05, budget / max(1, args.steps + args.warmup))
-    fn, units, desc = _oracle_sample(w, host, rate * per_step)
+    fn, units, desc, _ = _oracle_sample(w, host, rate * per_step)
     for _ in range(args.warmup):
         fn()
     t0 = time.perf_counter()

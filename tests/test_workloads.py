@@ -1,7 +1,10 @@
 """Host checks of the workload definitions the benchmark and the tests share
 (CPU only): the algorithmic byte count of each workload equals the bytes of
-its inputs plus one fp32 y, and the benchmark's oracle sample of a grouped
-workload keeps whole groups."""
+its inputs plus one fp32 y, the benchmark's oracle sample of a grouped
+workload keeps whole groups, and its parity figure tells a right y from a
+wrong one."""
+import torch
+
 import bench
 import workloads
 
@@ -31,7 +34,23 @@ def test_grouped_oracle_sample_keeps_whole_groups():
     s = w.shape
     per_head = s["L"] * s["P"] * s["N"]
     # a target of 5 heads' work: one batch row, rounded down to one group of 4 heads
-    fn, units, what = bench._oracle_sample(w, host, 5 * per_head)
+    fn, units, what, view = bench._oracle_sample(w, host, 5 * per_head)
     assert units == 4 * per_head
     y = fn()
     assert y.shape == (1, s["L"], 4, s["P"])
+    assert tuple(view(torch.zeros(4, s["L"], s["H"], s["P"])).shape) == y.shape
+
+
+def test_bench_parity_on_sample():
+    """The benchmark's parity figure: the oracle's own y passes, a y off by
+    more than the bf16 bound fails."""
+    w = workloads.BY_NAME["diag_bf16_Bs8_L2048_ED1536_N16"]
+    host = workloads.workload_inputs(w)
+    fn, units, desc, view = bench._oracle_sample(w, host, 2e6)
+    ref = fn()
+    full = torch.zeros(8, 2048, 1536, dtype=torch.float32)
+    view(full)[...] = torch.from_numpy(ref)
+    p = bench.parity_on_sample(w, full, ref, view, desc)
+    assert p["ok"] and p["max_abs_err"] < 1e-5 * p["ref_max_abs"]
+    view(full)[0, 5, 0] += 0.05 * p["ref_max_abs"]
+    assert not bench.parity_on_sample(w, full, ref, view, desc)["ok"]
