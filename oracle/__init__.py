@@ -75,6 +75,10 @@ def _load(path: str | None = None):
         lib.oracle_diag_scan_bwd_range.restype = None
         lib.oracle_ssd_scan_bwd.argtypes = [dp] * 13 + [i64] * 6 + [ctypes.c_int, ctypes.c_int]
         lib.oracle_ssd_scan_bwd.restype = None
+        lib.oracle_ssd_scan_bwd_ex.argtypes = ([dp] * 13 + [i64] * 6 + [ctypes.c_int, dp, ctypes.c_int,
+                                               ctypes.c_int, dbl, dbl, dp, dp, dp, dp, dp,
+                                               ctypes.c_int])
+        lib.oracle_ssd_scan_bwd_ex.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _libs[key] = lib
@@ -234,6 +238,52 @@ def ssd_scan_bwd(x, dt, A_head, B, C, D, dy, bidirectional: bool = False, nthrea
         _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(out["dx"]),
         _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
         Bs, L, H, P, N, G, int(bool(bidirectional)), nthreads)
+    out["dB"] = out["dB"].reshape(shape_bc)
+    out["dC"] = out["dC"].reshape(shape_bc)
+    return out
+
+
+def ssd_scan_bwd_ex(x, dt, A_head, B, C, D, dy, bidirectional: bool = False, dt_bias=None,
+                    dt_softplus: bool = False, dt_limit=None, z=None, h0=None, nthreads: int = 0,
+                    library=None):
+    """Gradients of the SSD scan with its options, in fp64.
+
+    Inputs as in ``ssd_scan`` with the options (``dt`` before the optional
+    bias, softplus and clamp; gate ``z``; initial state ``h0``, single
+    direction only) plus dy.  Returns the keys of ``ssd_scan_bwd`` and
+    dz (like x), ddt_bias (H), dh0 (Bs, H, P, N) -- each None when its option
+    is off; ddt is the gradient with respect to the dt given.
+    """
+    x, dt, A_head, B, C, D, dy, dt_bias, z, h0 = map(
+        _f64, (x, dt, A_head, B, C, D, dy, dt_bias, z, h0))
+    Bs, L, H, P = x.shape
+    shape_bc = B.shape
+    if B.ndim == 3:
+        B, C = B[:, :, None, :], C[:, :, None, :]
+    G, N = B.shape[2], B.shape[3]
+    assert G >= 1 and H % G == 0, "heads must split evenly into the groups of B, C"
+    assert dt.shape == (Bs, L, H) and A_head.shape == (H,) and dy.shape == x.shape
+    assert B.shape == (Bs, L, G, N) and C.shape == (Bs, L, G, N)
+    B, C = np.ascontiguousarray(B), np.ascontiguousarray(C)
+    assert D is None or D.shape == (H,)
+    assert dt_bias is None or dt_bias.shape == (H,)
+    assert z is None or z.shape == x.shape
+    assert h0 is None or h0.shape == (Bs, H, P, N)
+    if bidirectional and h0 is not None:
+        raise ValueError("state input is defined for a single direction only")
+    out = dict(dx=np.zeros((Bs, L, H, P)), ddt=np.zeros((Bs, L, H)), dA=np.zeros(H),
+               dB=np.zeros((Bs, L, G, N)), dC=np.zeros((Bs, L, G, N)),
+               dD=None if D is None else np.zeros(H),
+               dz=None if z is None else np.zeros((Bs, L, H, P)),
+               ddt_bias=None if dt_bias is None else np.zeros(H),
+               dh0=None if h0 is None else np.zeros((Bs, H, P, N)))
+    lim, lo, hi = _limit(dt_limit)
+    _load(library).oracle_ssd_scan_bwd_ex(
+        _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(out["dx"]),
+        _ptr(out["ddt"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+        Bs, L, H, P, N, G, int(bool(bidirectional)), _ptr(dt_bias), int(bool(dt_softplus)), lim,
+        lo, hi, _ptr(z), _ptr(h0), _ptr(out["dz"]), _ptr(out["ddt_bias"]), _ptr(out["dh0"]),
+        nthreads)
     out["dB"] = out["dB"].reshape(shape_bc)
     out["dC"] = out["dC"].reshape(shape_bc)
     return out

@@ -344,16 +344,19 @@ void oracle_diag_scan_bwd_range(const double *x, const double *delta, const doub
  * B, C, dB, dC: (Bs, L, G, N), head h reads group h / (H / G).  All outputs
  * are ACCUMULATED into (the caller zeroes them); dD may be NULL.  The loop
  * over batch rows is the parallel one (a batch row's heads share its dB, dC).
+ * With an initial state H_{-1} = init (P x N, or NULL for zero), the walk
+ * starts from it, and the gradient of the loss with respect to it is
+ * a_0 Gb_0 -- what gb holds when the reverse walk ends (copied to d_init).
  */
 static void ssd_bwd_one_direction(const double *x, const double *dt, double Ah,
                                   const double *B, const double *C, const double *dy,
                                   double *dx, double *ddt, double *dAh, double *dB, double *dC,
                                   int64_t b, int64_t h, int64_t L, int64_t H, int64_t P,
                                   int64_t N, int64_t G, int64_t g, int rev, double *hist,
-                                  double *gb) {
+                                  double *gb, const double *init, double *d_init) {
     const int64_t PN = P * N;
-    /* forward: hist row k + 1 holds H_k; row 0 is the zero initial state */
-    for (int64_t i = 0; i < PN; ++i) hist[i] = 0.0;
+    /* forward: hist row k + 1 holds H_k; row 0 is the initial state */
+    for (int64_t i = 0; i < PN; ++i) hist[i] = init ? init[i] : 0.0;
     for (int64_t k = 0; k < L; ++k) {
         const int64_t t = rev ? L - 1 - k : k;
         const double dtv = dt[(b * L + t) * H + h], a = exp(dtv * Ah);
@@ -394,15 +397,17 @@ static void ssd_bwd_one_direction(const double *x, const double *dt, double Ah,
         ddt[(b * L + t) * H + h] += sdt + Ah * a * sda;
         *dAh += dtv * a * sda;
     }
+    if (d_init)
+        for (int64_t i = 0; i < PN; ++i) d_init[i] = gb[i];
 }
 
-void oracle_ssd_scan_bwd(const double *x, const double *dt, const double *A_head,
+/* The plain scan's gradients, from an initial state h0 (Bs, H, P, N) or
+ * zero, with dh0 (same shape) the gradient with respect to it when given. */
+static void ssd_bwd_core(const double *x, const double *dt, const double *A_head,
                          const double *B, const double *C, const double *D, const double *dy,
                          double *dx, double *ddt, double *dA, double *dB, double *dC,
                          double *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
-                         int64_t G, int bidirectional, int nthreads) {
-    set_threads(nthreads);
-    if (G < 1 || H % G != 0) return;
+                         int64_t G, int bidirectional, const double *h0, double *dh0) {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t b = 0; b < Bs; ++b) {
         double *hist = (double *)malloc((size_t)((L + 1) * P * N) * sizeof(double));
@@ -411,9 +416,12 @@ void oracle_ssd_scan_bwd(const double *x, const double *dt, const double *A_head
         double *lD = (double *)calloc((size_t)H, sizeof(double));
         for (int64_t h = 0; h < H; ++h) {
             const int64_t hg = h / (H / G);   /* the head's group of B, C */
+            const int64_t u = b * H + h;
             for (int dir = 0; dir < (bidirectional ? 2 : 1); ++dir)
                 ssd_bwd_one_direction(x, dt, A_head[h], B, C, dy, dx, ddt, &lA[h], dB, dC, b, h,
-                                      L, H, P, N, G, hg, dir, hist, gb);
+                                      L, H, P, N, G, hg, dir, hist, gb,
+                                      (dir == 0 && h0) ? h0 + u * P * N : NULL,
+                                      (dir == 0 && dh0) ? dh0 + u * P * N : NULL);
             for (int64_t t = 0; t < L; ++t)
                 for (int64_t p = 0; p < P; ++p) {
                     const int64_t i = ((b * L + t) * H + h) * P + p;
@@ -433,4 +441,91 @@ void oracle_ssd_scan_bwd(const double *x, const double *dt, const double *A_head
         free(lA);
         free(lD);
     }
+}
+
+void oracle_ssd_scan_bwd(const double *x, const double *dt, const double *A_head,
+                         const double *B, const double *C, const double *D, const double *dy,
+                         double *dx, double *ddt, double *dA, double *dB, double *dC,
+                         double *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                         int64_t G, int bidirectional, int nthreads) {
+    set_threads(nthreads);
+    if (G < 1 || H % G != 0) return;
+    ssd_bwd_core(x, dt, A_head, B, C, D, dy, dx, ddt, dA, dB, dC, dD, Bs, L, H, P, N, G,
+                 bidirectional, NULL, NULL);
+}
+
+/*
+ * Gradients of the scan with its options ("Some questions of Bi-Mamba2 and
+ * Hydra": the chunked backward returns dz, ddt_bias and the initial
+ * states' gradient besides dx, ddt, dA, dB, dC, dD).  With
+ *   v = dt + dt_bias,  s = softplus(v) (or v),  dte = clamp(s, lo, hi) (or s),
+ *   u = scan(dte) + D x,  y = u * silu(z) (or u),
+ * the chain rule gives, with g = dy * silu(z):
+ *   dz    = dy * u * silu'(z),   silu'(z) = sig(z) (1 + z (1 - sig(z)))
+ *   (dx, d dte, dA, dB, dC, dD, dh0) = the plain scan's gradients for g,
+ *                                        run from h0
+ *   ddt   = d dte * [lo < s < hi] * sig(v)   (each factor if its option is on)
+ *   ddt_bias[h] = sum over (b, t) of ddt.
+ * dt: (Bs, L, H) before the preprocessing; z, dz: like x; h0, dh0:
+ * (Bs, H, P, N), single direction only.  Outputs are overwritten; dz,
+ * ddt_bias, dh0 may be NULL when the matching option is off.
+ */
+void oracle_ssd_scan_bwd_ex(const double *x, const double *dt, const double *A_head,
+                            const double *B, const double *C, const double *D, const double *dy,
+                            double *dx, double *ddt, double *dA, double *dB, double *dC,
+                            double *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                            int64_t G, int bidirectional, const double *dt_bias, int dt_softplus,
+                            int dt_limit, double dt_min, double dt_max, const double *z,
+                            const double *h0, double *dz, double *ddt_bias, double *dh0,
+                            int nthreads) {
+    set_threads(nthreads);
+    if (G < 1 || H % G != 0 || (bidirectional && (h0 || dh0))) return;
+    const int64_t nt = Bs * L * H, nx = nt * P;
+    double *dte = (double *)malloc((size_t)nt * sizeof(double));
+    double *chain = (double *)malloc((size_t)nt * sizeof(double));
+    double *g = (double *)malloc((size_t)nx * sizeof(double));
+    for (int64_t i = 0; i < nt; ++i) {
+        const double v = dt[i] + (dt_bias ? dt_bias[i % H] : 0.0);
+        double s = v, f = 1.0;
+        if (dt_softplus) {
+            s = log1p(exp(v));
+            f = 1.0 / (1.0 + exp(-v));
+        }
+        if (dt_limit) {
+            if (s < dt_min || s > dt_max) f = 0.0;
+            s = fmin(fmax(s, dt_min), dt_max);
+        }
+        dte[i] = s;
+        chain[i] = f;
+    }
+    if (z) {
+        /* the ungated output u, from the same preprocessed dt and h0 */
+        double *u = (double *)malloc((size_t)nx * sizeof(double));
+        oracle_ssd_scan_ex_range(x, dte, A_head, B, C, D, u, Bs, L, H, P, N, G, bidirectional,
+                                 NULL, 0, 0, 0.0, 0.0, NULL, h0, NULL, 0, Bs * H, nthreads);
+        for (int64_t i = 0; i < nx; ++i) {
+            const double sg = 1.0 / (1.0 + exp(-z[i]));
+            g[i] = dy[i] * z[i] * sg;
+            if (dz) dz[i] = dy[i] * u[i] * sg * (1.0 + z[i] * (1.0 - sg));
+        }
+        free(u);
+    } else {
+        memcpy(g, dy, (size_t)nx * sizeof(double));
+    }
+    memset(dx, 0, (size_t)nx * sizeof(double));
+    memset(ddt, 0, (size_t)nt * sizeof(double));
+    memset(dA, 0, (size_t)H * sizeof(double));
+    memset(dB, 0, (size_t)(Bs * L * G * N) * sizeof(double));
+    memset(dC, 0, (size_t)(Bs * L * G * N) * sizeof(double));
+    if (dD) memset(dD, 0, (size_t)H * sizeof(double));
+    ssd_bwd_core(x, dte, A_head, B, C, D, g, dx, ddt, dA, dB, dC, dD, Bs, L, H, P, N, G,
+                 bidirectional, h0, dh0);
+    if (ddt_bias) memset(ddt_bias, 0, (size_t)H * sizeof(double));
+    for (int64_t i = 0; i < nt; ++i) {
+        ddt[i] *= chain[i];                    /* through the clamp and the softplus */
+        if (ddt_bias) ddt_bias[i % H] += ddt[i];
+    }
+    free(dte);
+    free(chain);
+    free(g);
 }

@@ -161,3 +161,101 @@ def test_planted_gradient_mistake_is_caught(name, tmp_path):
     an = oracle.ssd_scan_bwd(**args, dy=dy, bidirectional=bidir, library=lib)
     fd = _fd_grads(args, dy, bidir)    # the real forward oracle
     assert _worst(an, fd) > 1e-6, "planted mistake %s was not caught" % name
+
+
+# ---- gradients of the scan with its options --------------------------------
+
+def _case_opts(seed, Bs, L, H, P, N, G, bidir, opts):
+    rng = _rng(seed)
+    x, dt, A, B, C, D = _rand_ssd(rng, Bs, L, H, P, N)
+    if G > 1:
+        B = rng.standard_normal((Bs, L, G, N)) / np.sqrt(N)
+        C = rng.standard_normal((Bs, L, G, N)) / np.sqrt(N)
+    args = dict(x=x, dt=rng.standard_normal((Bs, L, H)) - 1.0, A_head=A, B=B, C=C, D=D)
+    kw = dict(bidirectional=bidir)
+    if "bias" in opts:
+        args["dt_bias"] = 0.5 * rng.standard_normal(H)
+    if "softplus" in opts:
+        kw["dt_softplus"] = True
+    if "limit" in opts:
+        kw["dt_limit"] = (0.2, 0.8)      # clamps some steps at either bound
+    if "z" in opts:
+        args["z"] = rng.standard_normal(x.shape)
+    if "h0" in opts:
+        args["h0"] = 0.5 * rng.standard_normal((Bs, H, P, N))
+    return args, kw, rng.standard_normal(x.shape)
+
+
+def _fd_grads_opts(args, kw, dy):
+    out = {}
+    for name, base in args.items():
+        if base is None:
+            continue
+        g = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            plus, minus = dict(args), dict(args)
+            p, m = base.copy(), base.copy()
+            p[idx] += EPS
+            m[idx] -= EPS
+            plus[name], minus[name] = p, m
+            lp = float(np.sum(dy * oracle.ssd_scan(**plus, **kw)))
+            lm = float(np.sum(dy * oracle.ssd_scan(**minus, **kw)))
+            g[idx] = (lp - lm) / (2 * EPS)
+        out[{"A_head": "dA", "dt_bias": "ddt_bias"}.get(name, "d" + name)] = g
+    return out
+
+
+OPT_CASES = [
+    # seed, Bs, L, H, P, N, G, bidirectional, options
+    (21, 1, 5, 2, 2, 3, 1, False, ("bias", "softplus", "limit", "z", "h0")),
+    (22, 2, 4, 2, 2, 2, 2, True, ("bias", "softplus", "z")),
+    (23, 1, 6, 1, 3, 2, 1, False, ("softplus", "h0")),
+    (24, 1, 5, 2, 2, 2, 1, True, ("limit", "z")),
+]
+
+
+@pytest.mark.parametrize("seed,Bs,L,H,P,N,G,bidir,opts", OPT_CASES)
+def test_option_gradients_match_finite_differences(seed, Bs, L, H, P, N, G, bidir, opts):
+    """dz, ddt_bias, dh0 and the gradient with respect to the dt given
+    (through the bias, softplus and clamp) against central differences of
+    the forward oracle with the same options."""
+    args, kw, dy = _case_opts(seed, Bs, L, H, P, N, G, bidir, opts)
+    an = oracle.ssd_scan_bwd_ex(**args, dy=dy, **kw)
+    fd = _fd_grads_opts(args, kw, dy)
+    for k in an:
+        assert (an[k] is None) == (k not in fd), k
+    assert _worst({k: an[k] for k in fd}, fd) < 1e-7
+
+
+def test_option_gradients_without_options_equal_plain_ones():
+    args, kw, dy = _case_opts(25, 2, 5, 2, 2, 3, 1, True, ())
+    an = oracle.ssd_scan_bwd_ex(**args, dy=dy, **kw)
+    plain = oracle.ssd_scan_bwd(**args, dy=dy, **kw)
+    for k in plain:
+        assert np.array_equal(an[k], plain[k]), k
+
+
+SSD_BWD_OPT_MUTANTS = {
+    "gate_derivative_drops_term": (
+        "if (dz) dz[i] = dy[i] * u[i] * sg * (1.0 + z[i] * (1.0 - sg));",
+        "if (dz) dz[i] = dy[i] * u[i] * sg;"),
+    "softplus_derivative_dropped": ("f = 1.0 / (1.0 + exp(-v));", "f = 1.0;"),
+    "clamp_passes_gradient": ("if (s < dt_min || s > dt_max) f = 0.0;", "if (0) f = 0.0;"),
+    "backward_ignores_initial_state": ("for (int64_t i = 0; i < PN; ++i) hist[i] = init ? init[i] : 0.0;",
+                                       "for (int64_t i = 0; i < PN; ++i) hist[i] = 0.0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SSD_BWD_OPT_MUTANTS))
+def test_planted_option_gradient_mistake_is_caught(name, tmp_path):
+    old, new = SSD_BWD_OPT_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation site not found: " + old
+    path = str(tmp_path / (name + ".c"))
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.compile_source(path, str(tmp_path / (name + ".so")))
+    args, kw, dy = _case_opts(26, 1, 5, 2, 2, 2, 1, False, ("bias", "softplus", "limit", "z", "h0"))
+    an = oracle.ssd_scan_bwd_ex(**args, dy=dy, **kw, library=lib)
+    fd = _fd_grads_opts(args, kw, dy)   # the real forward oracle
+    assert _worst({k: an[k] for k in fd}, fd) > 1e-6, "planted mistake %s was not caught" % name
