@@ -47,6 +47,11 @@
  * (Bs, L, G, N) and head h reads group h / (H / G); G = 1 is one group
  * shared by all heads.
  *
+ * Gradients (the backward passes [P2] names): reverse mode written out by
+ * hand for the diagonal scan and for the SSD scan, the latter also with its
+ * options (dz, ddt_bias and the initial state's gradient besides dx, ddt,
+ * dA, dB, dC, dD).
+ *
  * All arrays are dense row-major (last index fastest) fp64.
  */
 #include <math.h>
