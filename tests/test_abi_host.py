@@ -191,3 +191,38 @@ def test_ssd_backward_rejects_bad_arguments():
     assert lib.ssd_chunk_scan_bwd(*bad, 1, 8, 2, 64, 64, 1, 0, 1, None) == 3
     # a valid call reaches the device check (no GPU here, or a real launch there)
     assert lib.ssd_chunk_scan_bwd(*([None] * 13), 1, 8, 2, 64, 64, 1, 0, 1, None) == 1
+
+
+def _declarations():
+    """name -> list of parameter declarations, for every SSM_API function."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"SSM_API\s+[^;(]*?\b([a-z_][a-z0-9_]*)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        out[m.group(1)] = params
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    """Each binding's ctypes argument list has the header's parameter count
+    and, parameter by parameter, its kind: pointer, 64-bit or 32-bit integer,
+    float (a 32-bit integer where an int64_t is declared passes garbage high
+    bits)."""
+    decls = _declarations()
+    for name, (argtypes, _) in lrs.SIGNATURES.items():
+        assert name in decls, name
+        params = decls[name]
+        assert len(argtypes) == len(params), (name, len(argtypes), len(params))
+        for decl, at in zip(params, argtypes):
+            if "*" in decl:
+                assert at in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(at, "_type_") and \
+                    issubclass(at, ctypes._Pointer), (name, decl, at)
+            elif "int64_t" in decl:
+                assert at is ctypes.c_int64, (name, decl, at)
+            elif re.search(r"\bint(32_t)?\b|\bssm_status_t\b", decl):   # the enum is an int
+                assert at in (ctypes.c_int, ctypes.c_int32), (name, decl, at)
+            elif "float" in decl:
+                assert at is ctypes.c_float, (name, decl, at)
+            else:
+                raise AssertionError("unclassified parameter %r of %s" % (decl, name))
