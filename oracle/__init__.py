@@ -79,6 +79,9 @@ def _load(path: str | None = None):
                                                ctypes.c_int, dbl, dbl, dp, dp, dp, dp, dp,
                                                ctypes.c_int])
         lib.oracle_ssd_scan_bwd_ex.restype = None
+        lib.oracle_diag_scan_bwd_ex.argtypes = ([dp] * 13 + [i64] * 4 + [dp, ctypes.c_int, ctypes.c_int,
+                                                dbl, dbl, dp, dp, dp, dp, dp, ctypes.c_int])
+        lib.oracle_diag_scan_bwd_ex.restype = None
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         _libs[key] = lib
@@ -167,6 +170,40 @@ def diag_scan_bwd(x, delta, A, B, C, D, dy, nthreads: int = 0, library=None):
         _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(out["dx"]),
         _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
         Bs, L, ED, N, 0, Bs * ED, nthreads)
+    return out
+
+
+def diag_scan_bwd_ex(x, delta, A, B, C, D, dy, dt_bias=None, dt_softplus: bool = False,
+                     dt_limit=None, z=None, h0=None, nthreads: int = 0, library=None):
+    """Gradients of the diagonal scan with its options, in fp64.
+
+    Inputs as in ``diag_scan`` with the options (``delta`` before the
+    optional bias, softplus and clamp; gate ``z``; initial state ``h0``)
+    plus dy.  Returns the keys of ``diag_scan_bwd`` and dz (like x),
+    ddt_bias (ED), dh0 (Bs, ED, N) -- each None when its option is off;
+    ddelta is the gradient with respect to the delta given.
+    """
+    x, delta, A, B, C, D, dy, dt_bias, z, h0 = map(
+        _f64, (x, delta, A, B, C, D, dy, dt_bias, z, h0))
+    Bs, L, ED = x.shape
+    N = A.shape[1]
+    assert delta.shape == x.shape and dy.shape == x.shape and A.shape == (ED, N)
+    assert B.shape == (Bs, L, N) and C.shape == (Bs, L, N)
+    assert dt_bias is None or dt_bias.shape == (ED,)
+    assert z is None or z.shape == x.shape
+    assert h0 is None or h0.shape == (Bs, ED, N)
+    out = dict(dx=np.zeros((Bs, L, ED)), ddelta=np.zeros((Bs, L, ED)), dA=np.zeros((ED, N)),
+               dB=np.zeros((Bs, L, N)), dC=np.zeros((Bs, L, N)),
+               dD=None if D is None else np.zeros(ED),
+               dz=None if z is None else np.zeros((Bs, L, ED)),
+               ddt_bias=None if dt_bias is None else np.zeros(ED),
+               dh0=None if h0 is None else np.zeros((Bs, ED, N)))
+    lim, lo, hi = _limit(dt_limit)
+    _load(library).oracle_diag_scan_bwd_ex(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(out["dx"]),
+        _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+        Bs, L, ED, N, _ptr(dt_bias), int(bool(dt_softplus)), lim, lo, hi, _ptr(z), _ptr(h0),
+        _ptr(out["dz"]), _ptr(out["ddt_bias"]), _ptr(out["dh0"]), nthreads)
     return out
 
 

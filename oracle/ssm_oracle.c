@@ -268,19 +268,22 @@ void oracle_ssd_scan(const double *x, const double *dt, const double *A_head,
  * dB, dC (Bs, L, N) and dD (ED) are ACCUMULATED into (the caller zeroes
  * them); dD may be NULL.
  */
-void oracle_diag_scan_bwd_range(const double *x, const double *delta, const double *A,
-                                const double *B, const double *C, const double *D,
-                                const double *dy, double *dx, double *ddelta, double *dA,
-                                double *dB, double *dC, double *dD, int64_t Bs, int64_t L,
-                                int64_t ED, int64_t N, int64_t c_begin, int64_t c_end,
-                                int nthreads) {
-    set_threads(nthreads);
+/* The diagonal scan's gradients for the channels [c_begin, c_end), from
+ * initial states h0 (Bs, ED, N) or zero; dh0 (same shape, optional) gets the
+ * gradient with respect to h0: a_0 g_0, what g holds when the walk ends. */
+static void diag_bwd_core(const double *x, const double *delta, const double *A,
+                          const double *B, const double *C, const double *D, const double *dy,
+                          double *dx, double *ddelta, double *dA, double *dB, double *dC,
+                          double *dD, int64_t Bs, int64_t L, int64_t ED, int64_t N,
+                          int64_t c_begin, int64_t c_end, const double *h0, double *dh0) {
     if (c_end > Bs * ED) c_end = Bs * ED;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t c = c_begin; c < c_end; ++c) {
         const int64_t b = c / ED, e = c % ED;
         /* forward: the states h_t (t = -1 .. L-1), row t + 1 of hist */
         double *hist = (double *)calloc((size_t)((L + 1) * N), sizeof(double));
+        if (h0)
+            for (int64_t n = 0; n < N; ++n) hist[n] = h0[c * N + n];
         double *g = (double *)calloc((size_t)N, sizeof(double));
         double *lA = (double *)calloc((size_t)N, sizeof(double));
         double *lB = (double *)calloc((size_t)(L * N), sizeof(double));
@@ -312,6 +315,8 @@ void oracle_diag_scan_bwd_range(const double *x, const double *delta, const doub
             ddelta[i] = sdd;
             lD += gy * xv;
         }
+        if (dh0)
+            for (int64_t n = 0; n < N; ++n) dh0[c * N + n] = g[n];
 #pragma omp critical
         {
             for (int64_t n = 0; n < N; ++n) dA[e * N + n] += lA[n];
@@ -327,6 +332,83 @@ void oracle_diag_scan_bwd_range(const double *x, const double *delta, const doub
         free(lB);
         free(lC);
     }
+}
+
+void oracle_diag_scan_bwd_range(const double *x, const double *delta, const double *A,
+                                const double *B, const double *C, const double *D,
+                                const double *dy, double *dx, double *ddelta, double *dA,
+                                double *dB, double *dC, double *dD, int64_t Bs, int64_t L,
+                                int64_t ED, int64_t N, int64_t c_begin, int64_t c_end,
+                                int nthreads) {
+    set_threads(nthreads);
+    diag_bwd_core(x, delta, A, B, C, D, dy, dx, ddelta, dA, dB, dC, dD, Bs, L, ED, N, c_begin,
+                  c_end, NULL, NULL);
+}
+
+/*
+ * Gradients of the diagonal scan with its options, by the same chain rule
+ * as oracle_ssd_scan_bwd_ex: with v = delta + dt_bias[e], s = softplus(v)
+ * (or v), delta_seen = clamp(s) (or s), u = scan(delta_seen) + D x and
+ * y = u silu(z) (or u); g = dy silu(z) enters the plain gradients (run from
+ * h0), dz = dy u silu'(z), ddelta = d delta_seen * [lo < s < hi] * sig(v),
+ * ddt_bias[e] = sum over (b, t) of ddelta, dh0 = the gradient of h0.
+ * delta: (Bs, L, ED) before the preprocessing; z, dz like x; h0, dh0
+ * (Bs, ED, N).  Outputs are overwritten; dz, ddt_bias, dh0 may be NULL.
+ */
+void oracle_diag_scan_bwd_ex(const double *x, const double *delta, const double *A,
+                             const double *B, const double *C, const double *D,
+                             const double *dy, double *dx, double *ddelta, double *dA,
+                             double *dB, double *dC, double *dD, int64_t Bs, int64_t L,
+                             int64_t ED, int64_t N, const double *dt_bias, int dt_softplus,
+                             int dt_limit, double dt_min, double dt_max, const double *z,
+                             const double *h0, double *dz, double *ddt_bias, double *dh0,
+                             int nthreads) {
+    set_threads(nthreads);
+    const int64_t nx = Bs * L * ED;
+    double *dse = (double *)malloc((size_t)nx * sizeof(double));
+    double *chain = (double *)malloc((size_t)nx * sizeof(double));
+    double *g = (double *)malloc((size_t)nx * sizeof(double));
+    for (int64_t i = 0; i < nx; ++i) {
+        const double w = delta[i] + (dt_bias ? dt_bias[i % ED] : 0.0);
+        double sv = w, fac = 1.0;
+        if (dt_softplus) {
+            sv = log1p(exp(w));
+            fac = 1.0 / (1.0 + exp(-w));            /* softplus' = sigmoid */
+        }
+        if (dt_limit) {
+            if (sv < dt_min || sv > dt_max) fac = 0.0;  /* clamped: no gradient */
+            sv = fmin(fmax(sv, dt_min), dt_max);
+        }
+        dse[i] = sv;
+        chain[i] = fac;
+    }
+    if (z) {
+        double *u = (double *)malloc((size_t)nx * sizeof(double));
+        oracle_diag_scan_ex_range(x, dse, A, B, C, D, u, Bs, L, ED, N, NULL, 0, 0, 0.0, 0.0,
+                                  NULL, h0, NULL, 0, Bs * ED, nthreads);
+        for (int64_t i = 0; i < nx; ++i) {
+            const double sgm = 1.0 / (1.0 + exp(-z[i]));
+            g[i] = dy[i] * z[i] * sgm;
+            if (dz) dz[i] = dy[i] * u[i] * sgm * (1.0 + z[i] * (1.0 - sgm));  /* silu' */
+        }
+        free(u);
+    } else {
+        memcpy(g, dy, (size_t)nx * sizeof(double));
+    }
+    memset(dA, 0, (size_t)(ED * N) * sizeof(double));
+    memset(dB, 0, (size_t)(Bs * L * N) * sizeof(double));
+    memset(dC, 0, (size_t)(Bs * L * N) * sizeof(double));
+    if (dD) memset(dD, 0, (size_t)ED * sizeof(double));
+    diag_bwd_core(x, dse, A, B, C, D, g, dx, ddelta, dA, dB, dC, dD, Bs, L, ED, N, 0, Bs * ED, h0,
+                  dh0);
+    if (ddt_bias) memset(ddt_bias, 0, (size_t)ED * sizeof(double));
+    for (int64_t i = 0; i < nx; ++i) {
+        ddelta[i] *= chain[i];                 /* through the clamp and the softplus */
+        if (ddt_bias) ddt_bias[i % ED] += ddelta[i];
+    }
+    free(dse);
+    free(chain);
+    free(g);
 }
 
 /* Gradients of the chunked scalar-decay scan (the SSD form above) for an

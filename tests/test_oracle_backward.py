@@ -91,3 +91,94 @@ def test_planted_gradient_mistake_is_caught(name, tmp_path):
     an = oracle.diag_scan_bwd(x, delta, A, B, C, D, dy, library=lib)
     fd = _fd_grads(x, delta, A, B, C, D, dy)    # the real forward oracle
     assert _worst(an, fd) > 1e-6, "planted mistake %s was not caught" % name
+
+
+# ---- gradients of the scan with its options --------------------------------
+
+def _case_opts(seed, Bs, L, ED, N, opts):
+    rng = _rng(seed)
+    x, _, A, B, C, D = _rand_diag(rng, Bs, L, ED, N)
+    args = dict(x=x, delta=rng.standard_normal(x.shape) - 1.0, A=A, B=B, C=C, D=D)
+    kw = {}
+    if "bias" in opts:
+        args["dt_bias"] = 0.5 * rng.standard_normal(ED)
+    if "softplus" in opts:
+        kw["dt_softplus"] = True
+    if "limit" in opts:
+        kw["dt_limit"] = (0.2, 0.8)      # clamps some steps at either bound
+    if "z" in opts:
+        args["z"] = rng.standard_normal(x.shape)
+    if "h0" in opts:
+        args["h0"] = 0.5 * rng.standard_normal((Bs, ED, N))
+    return args, kw, rng.standard_normal(x.shape)
+
+
+def _fd_grads_opts(args, kw, dy, library=None):
+    out = {}
+    for name, base in args.items():
+        if base is None:
+            continue
+        g = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            plus, minus = dict(args), dict(args)
+            p, m = base.copy(), base.copy()
+            p[idx] += EPS
+            m[idx] -= EPS
+            plus[name], minus[name] = p, m
+            lp = float(np.sum(dy * oracle.diag_scan(**plus, **kw)))
+            lm = float(np.sum(dy * oracle.diag_scan(**minus, **kw)))
+            g[idx] = (lp - lm) / (2 * EPS)
+        out[{"dt_bias": "ddt_bias"}.get(name, "d" + name)] = g
+    return out
+
+
+@pytest.mark.parametrize("seed,shape,opts", [
+    (11, (2, 5, 2, 3), ("bias", "softplus", "limit", "z", "h0")),
+    (12, (1, 6, 3, 2), ("softplus", "z")),
+    (13, (2, 4, 2, 2), ("limit", "h0")),
+    (14, (1, 5, 2, 3), ("bias", "limit")),   # the clamp keeps delta > 0 (in contract)
+])
+def test_option_gradients_match_finite_differences(seed, shape, opts):
+    """dz, ddt_bias, dh0 and the gradient with respect to the delta given
+    (through the bias, softplus and clamp) against central differences of
+    the forward oracle with the same options."""
+    args, kw, dy = _case_opts(seed, *shape, opts)
+    an = oracle.diag_scan_bwd_ex(**args, dy=dy, **kw)
+    fd = _fd_grads_opts(args, kw, dy)
+    for k in an:
+        assert (an[k] is None) == (k not in fd), k
+    assert _worst({k: an[k] for k in fd}, fd) < 1e-7
+
+
+def test_option_gradients_without_options_equal_plain_ones():
+    args, kw, dy = _case_opts(15, 2, 5, 2, 3, ())
+    an = oracle.diag_scan_bwd_ex(**args, dy=dy)
+    plain = oracle.diag_scan_bwd(**args, dy=dy)
+    for k in plain:
+        assert np.array_equal(an[k], plain[k]), k
+
+
+BWD_OPT_MUTANTS = {
+    "gate_derivative_drops_term": (
+        "if (dz) dz[i] = dy[i] * u[i] * sgm * (1.0 + z[i] * (1.0 - sgm));",
+        "if (dz) dz[i] = dy[i] * u[i] * sgm;"),
+    "softplus_derivative_dropped": ("fac = 1.0 / (1.0 + exp(-w));", "fac = 1.0;"),
+    "clamp_passes_gradient": ("if (sv < dt_min || sv > dt_max) fac = 0.0;", "if (0) fac = 0.0;"),
+    "backward_ignores_initial_state": ("for (int64_t n = 0; n < N; ++n) hist[n] = h0[c * N + n];",
+                                       "for (int64_t n = 0; n < N; ++n) hist[n] = 0.0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BWD_OPT_MUTANTS))
+def test_planted_option_gradient_mistake_is_caught(name, tmp_path):
+    old, new = BWD_OPT_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation site not found: " + old
+    path = str(tmp_path / (name + ".c"))
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.compile_source(path, str(tmp_path / (name + ".so")))
+    args, kw, dy = _case_opts(16, 2, 5, 2, 3, ("bias", "softplus", "limit", "z", "h0"))
+    an = oracle.diag_scan_bwd_ex(**args, dy=dy, **kw, library=lib)
+    fd = _fd_grads_opts(args, kw, dy)   # the real forward oracle
+    assert _worst({k: an[k] for k in fd}, fd) > 1e-6, "planted mistake %s was not caught" % name
