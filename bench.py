@@ -2,9 +2,13 @@
 """Benchmark of the selective-scan hot path on GB300.
 
 A step is one call of the scan on one batch of synthetic input resident in
-HBM.  The default workload is the diagonal selective scan with bf16 inputs,
-Bs=8 L=2048 ED=1536 N=16 (the shape the throughput metric is quoted on);
-``--workload`` selects any of the five workloads in ``workloads.py``.
+HBM.  The default workload is the largest of the method's five benchmark
+configurations by element-steps: the chunked scalar-decay (SSD) scan with
+bf16 inputs, Bs=4 L=4096 H=32 P=64 N=128, chunk 256, on the tensor cores;
+``--workload`` selects any workload in ``workloads.py``.  The default run also
+measures every one of the five configurations (``configs`` in the JSON line):
+time per call, throughput, roofline fraction, whole-output parity against
+the fp64 oracle and the oracle's own CPU rate.
 
 Prints ONE JSON line (rank 0).  ``value`` is element-steps/s (Bs*L*ED*N per
 step, ED = H*P for the chunked scan, both directions counted when
@@ -34,7 +38,9 @@ sys.path.insert(0, ROOT)
 
 import workloads  # noqa: E402
 
-DEFAULT_WORKLOAD = "diag_bf16_Bs8_L2048_ED1536_N16"
+DEFAULT_WORKLOAD = "ssd_bf16_Bs4_L4096_H32_P64_N128_Q256"
+# The method's five benchmark configurations, in their order.
+METHOD_CONFIGS = [w.name for w in workloads.WORKLOADS[:5]]
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "scan throughput (Bs·L·ED·N element-steps/s) and HBM GB/s vs roofline, 1 GB300"
 UNIT = "element-steps/s"
@@ -56,6 +62,8 @@ def parse_args():
     p.add_argument("--quick", action="store_true",
                    help="timed steps only: no clock sampling, pre/post roll or e2e leg "
                         "(used for profiler runs)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the leg that measures each of the five benchmark configurations")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target wall time of the CPU oracle sample")
     p.add_argument("--mode", choices=["fwd", "options", "bwd"], default="fwd",
@@ -325,6 +333,150 @@ def out_shape(w):
     return (s["Bs"], s["L"], s["H"], s["P"])
 
 
+L2_POLICY = "inputs rotate over resident sets, > 2x L2 bytes between reuses"
+
+
+def compute_dtype(w) -> str:
+    """Arithmetic type of the path: the diagonal scan computes in fp32 (bf16
+    or fp32 inputs); the chunked scan's products run on bf16 tensor-core
+    operands with fp32 accumulation and state (fp32 inputs: fp32 CUDA cores)."""
+    if w.kind == "diag" or w.dtype == "f32":
+        return "f32"
+    return "bf16"
+
+
+def bench_config(w, mode: str) -> dict:
+    """The ``config`` object of a bench line; both arms print the same one."""
+    return {"workload": w.name, **{k: v for k, v in w.shape.items()}, "mode": mode,
+            "input_dtype": w.dtype, "state_dtype": "f32", "output_dtype": "f32",
+            "l2": L2_POLICY, "parallelism": "replica per GPU (batch shards, no collective)"}
+
+
+def roofline_of(w, mode: str, per_launch_s: float, peaks: dict, with_traffic: bool) -> dict:
+    """Roofline of one call: the diagonal scan against the ALU bound (MUFU
+    ex2), the chunked scan against HBM bandwidth, both of the measured peaks."""
+    call_bytes = mode_bytes(w, mode)
+    hbm_achieved = call_bytes / per_launch_s / 1e9
+    if w.kind == "diag":
+        # One exp2 on the special-function unit and four fp32 operations per
+        # element-step; both the MUFU (32 ex2 / clk / SM) and the FMA pipe
+        # (128 lanes / clk / SM) allow 32 element-steps / clk / SM.
+        alu_peak = ALU_ELEM_PER_CLK_SM * NUM_SMS * peaks["sm_max_mhz"] * 1e6 / 1e12
+        achieved = w.element_steps / per_launch_s / 1e12
+        return {
+            "bound": "alu", "achieved": round(achieved, 4), "peak": round(alu_peak, 4),
+            "unit": "T element-steps/s", "frac": round(achieved / alu_peak, 4),
+            "traffic": ncu_traffic(w.name, w.kind) if (with_traffic and mode == "fwd") else None,
+            "peak_source": "derived: 152 SMs x 32 ex2/clk/SM (MUFU) x sm_max_mhz of "
+                           "MEASURED_PEAKS.json; 1 ex2 + 4 fp32 ops per element-step"
+                           + ("" if mode != "bwd" else
+                              " of the forward scan (the gradients re-run the forward twice "
+                              "and do about twice its work on the way back)"),
+            "hbm": {"achieved_gbs": round(hbm_achieved, 1), "peak_gbs": peaks["hbm_gbs"],
+                    "frac": round(hbm_achieved / peaks["hbm_gbs"], 4),
+                    "algorithmic_bytes_per_launch": call_bytes},
+            "launch_us": round(per_launch_s * 1e6, 3),
+        }
+    return {
+        "bound": "hbm", "achieved": round(hbm_achieved, 1), "peak": peaks["hbm_gbs"],
+        "unit": "GB/s", "frac": round(hbm_achieved / peaks["hbm_gbs"], 4),
+        "traffic": ncu_traffic(w.name, w.kind) if (with_traffic and mode == "fwd") else None,
+        "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+        "algorithmic_bytes_per_launch": call_bytes,
+        "launch_us": round(per_launch_s * 1e6, 3),
+    }
+
+
+def resident_sets(w, host, dev, per_set: int):
+    """Enough copies of the inputs (and a y each) that > 2x L2 bytes pass
+    between two uses of one set (at least three sets)."""
+    import torch
+    nsets = max(3, -(-3 * L2_BYTES // per_set))
+    bufs = []
+    for _ in range(nsets):
+        b = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
+        b["y"] = torch.empty(out_shape(w), dtype=torch.float32, device=dev)
+        bufs.append(b)
+    return bufs
+
+
+def time_steps(step, stream, dev, steps: int, warmup: int) -> float:
+    """Milliseconds for `steps` back-to-back steps, CUDA events on the
+    launching stream, synchronised on both sides."""
+    import torch
+    for i in range(max(3, warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1)
+
+
+def configs_leg(lrs, dev, peaks, seconds_per_config: float = 2.0) -> dict:
+    """Every one of the method's five configurations: time per call (inputs
+    rotating as in the headline), throughput, roofline, the GPU's whole y
+    against the fp64 oracle, and the oracle's rate on this host's cores."""
+    import oracle
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name in METHOD_CONFIGS:
+        w = workloads.BY_NAME[name]
+        host = workloads.workload_inputs(w)
+        per_set = mode_bytes(w, "fwd")
+        bufs = resident_sets(w, host, dev, per_set)
+        nsets = len(bufs)
+        step = make_step(w, lrs, bufs, "fwd")
+        # about 0.2 s of timed GPU work, at least 20 and at most 5000 calls
+        probe_ms = time_steps(step, stream, dev, 5, 3) / 5
+        steps = int(min(5000, max(20, 200.0 / max(probe_ms, 1e-3))))
+        ms = time_steps(step, stream, dev, steps, 3)
+        per_launch_s = ms / 1e3 / steps
+        # the last step used set (steps - 1) % nsets; rerun set 0 for parity
+        step(0)
+        torch.cuda.synchronize(dev)
+        y = bufs[0]["y"].double().cpu().numpy()
+        del step, bufs
+        torch.cuda.empty_cache()
+        # the oracle on the whole workload, repeated to fill the time budget
+        args = {k: oracle._f64(v) for k, v in host.items()}
+        t0 = time.perf_counter()
+        if w.kind == "diag":
+            ref = oracle.diag_scan(**args)
+        else:
+            ref = oracle.ssd_scan(**args, bidirectional=w.shape["bidirectional"])
+        t_one = time.perf_counter() - t0
+        reps = max(1, int(seconds_per_config / max(t_one, 1e-3)))
+        t0 = time.perf_counter()
+        for _ in range(reps - 1):
+            if w.kind == "diag":
+                oracle.diag_scan(**args)
+            else:
+                oracle.ssd_scan(**args, bidirectional=w.shape["bidirectional"])
+        t_all = t_one + (time.perf_counter() - t0)
+        err = float(np.max(np.abs(y - ref)))
+        scale = float(np.max(np.abs(ref)))
+        bound = 1e-4 * max(1.0, scale) if w.dtype == "f32" else 2e-2 * scale
+        out[name] = {
+            "us_per_call": round(per_launch_s * 1e6, 3),
+            "value": w.element_steps / per_launch_s, "unit": UNIT, "steps": steps,
+            "dtype": compute_dtype(w), "roofline": roofline_of(w, "fwd", per_launch_s, peaks, True),
+            "parity": {"max_abs_err": err, "ref_max_abs": scale, "bound": bound,
+                       "ok": bool(err <= bound), "sample": "whole output"},
+            "cpu_baseline": {"value": w.element_steps * reps / t_all, "unit": UNIT,
+                             "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": "whole workload, %d pass(es) in %.2f s "
+                                       "(fp64 sequential C, OpenMP)" % (reps, t_all)},
+            "l2": "%s (%d sets of %.2f MB)" % (L2_POLICY, nsets, per_set / 1e6),
+        }
+    return out
+
+
 def run_ours(args, rank, world, local):
     import torch
     import torch.distributed as dist
@@ -347,12 +499,8 @@ def run_ours(args, rank, world, local):
     if args.mode == "bwd":
         host["dy"] = workloads.grad_output(out_shape(w), seed=shard_seed(w.seed, rank) + 11)
     per_set = mode_bytes(w, args.mode)
-    nsets = max(3, -(-3 * L2_BYTES // per_set))
-    bufs = []
-    for k in range(nsets):
-        b = {n: (t.to(dev) if t is not None else None) for n, t in host.items()}
-        b["y"] = torch.empty(out_shape(w), dtype=torch.float32, device=dev)
-        bufs.append(b)
+    bufs = resident_sets(w, host, dev, per_set)
+    nsets = len(bufs)
     step = make_step(w, lrs, bufs, args.mode)
     stream = torch.cuda.current_stream(dev)
 
@@ -443,49 +591,15 @@ def run_ours(args, rank, world, local):
     else:
         launches_per_step = kernels_per_call(w, lrs)
     per_launch_s = ms / 1e3 / args.steps
-    call_bytes = mode_bytes(w, args.mode)
-    hbm_achieved = call_bytes / per_launch_s / 1e9
-    if w.kind == "diag":
-        # One exp2 on the special-function unit and four fp32 operations per
-        # element-step; both the MUFU (32 ex2 / clk / SM) and the FMA pipe
-        # (128 lanes / clk / SM) allow 32 element-steps / clk / SM.
-        alu_peak = ALU_ELEM_PER_CLK_SM * NUM_SMS * peaks["sm_max_mhz"] * 1e6 / 1e12
-        achieved = w.element_steps / per_launch_s / 1e12
-        roofline = {
-            "bound": "alu", "achieved": round(achieved, 4), "peak": round(alu_peak, 4),
-            "unit": "T element-steps/s", "frac": round(achieved / alu_peak, 4),
-            "traffic": ncu_traffic(w.name, w.kind) if args.mode == "fwd" else None,
-            "peak_source": "derived: 152 SMs x 32 ex2/clk/SM (MUFU) x sm_max_mhz of "
-                           "MEASURED_PEAKS.json; 1 ex2 + 4 fp32 ops per element-step"
-                           + ("" if args.mode != "bwd" else
-                              " of the forward scan (the gradients re-run the forward twice "
-                              "and do about twice its work on the way back)"),
-            "hbm": {"achieved_gbs": round(hbm_achieved, 1), "peak_gbs": peaks["hbm_gbs"],
-                    "frac": round(hbm_achieved / peaks["hbm_gbs"], 4),
-                    "algorithmic_bytes_per_launch": call_bytes},
-            "launch_us": round(per_launch_s * 1e6, 3),
-        }
-    else:
-        roofline = {
-            "bound": "hbm", "achieved": round(hbm_achieved, 1), "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": round(hbm_achieved / peaks["hbm_gbs"], 4),
-            "traffic": ncu_traffic(w.name, w.kind) if args.mode == "fwd" else None,
-            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-            "algorithmic_bytes_per_launch": call_bytes,
-            "launch_us": round(per_launch_s * 1e6, 3),
-        }
-    achieved = hbm_achieved
-    s = w.shape
-    config = {"workload": w.name, **{k: v for k, v in s.items()}, "mode": args.mode,
-              "input_dtype": w.dtype, "state_dtype": "f32", "output_dtype": "f32",
-              "l2": "inputs rotate over %d resident sets (%.0f MB each, > 2x L2 between reuses)"
-                    % (nsets, per_set / 1e6),
-              "parallelism": "replica per GPU (batch shards, no collective)"}
+    roofline = roofline_of(w, args.mode, per_launch_s, peaks, True)
+    achieved = mode_bytes(w, args.mode) / per_launch_s / 1e9
+    config = bench_config(w, args.mode)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded, distributions of the workload definition)",
+        "dtype": compute_dtype(w),
+        "data": "synthetic (seeded, distributions of the workload definition)",
         "config": config,
         "hbm_gbs": round(achieved, 1),
         "roofline": roofline,
@@ -498,6 +612,10 @@ def run_ours(args, rank, world, local):
         # bufs[0] holds the workload's inputs and the y of its last step
         line["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds, y_gpu=bufs[0]["y"])
         line["parity"] = parity
+    if rank == 0 and world == 1 and args.mode == "fwd" and not (args.quick or args.no_configs):
+        del step, bufs, dbuf
+        torch.cuda.empty_cache()
+        line["configs"] = configs_leg(lrs, dev, peaks)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
@@ -615,7 +733,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, distributions of the workload definition)",
-        "config": {"workload": w.name, **{k: v for k, v in s.items()}, "input_dtype": w.dtype},
+        "config": bench_config(w, "fwd"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "each step: " + desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -158,8 +158,9 @@ SSM_API ssm_status_t ssd_chunk_scan_fwd(const void *x, const void *dt,
  *     return SSM_ERR_UNSUPPORTED and launch nothing.  Unidirectional calls
  *     need no scratch.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it once the lookup succeeds; make
+ *     that first call before any stream capture.  A lookup that fails
+ *     returns SSM_ERR_CUDA, caches nothing, and the next call tries again.
  *   - Every call shares the one array: calls that overlap on the GPU (on
  *     different streams, or from different threads) race and give wrong
  *     results.  The array keeps the last call's contents; no call depends

@@ -1510,31 +1510,42 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 namespace {
 constexpr int kMaxDev = 64;
-std::once_flag g_na_once[kMaxDev];
-void *g_na_addr[kMaxDev];
-cudaError_t g_na_err[kMaxDev];
+std::mutex g_na_mutex;
+void *g_na_addr[kMaxDev];   // written once per device, only after a successful lookup
 }  // namespace
 
+// Bytes of the reverse states a bidirectional call keeps; SIZE_MAX when the
+// product does not fit (the caller then rejects the size).
 size_t noalloc_scratch_needed(int64_t Bs, int64_t L, int64_t H, int64_t N, bool bidirectional) {
     const int64_t nc = (L + kQ - 1) / kQ;
     if (!bidirectional || nc <= 1) return 0;
-    return size_t(Bs) * size_t(H) * size_t(nc) * size_t(N / 64) * kStateRegion;
+    const uint64_t f[5] = {uint64_t(Bs), uint64_t(H), uint64_t(nc), uint64_t(N / 64),
+                           uint64_t(kStateRegion)};
+    uint64_t bytes = 1;
+    for (uint64_t v : f) {
+        if (v != 0 && bytes > UINT64_MAX / v) return SIZE_MAX;
+        bytes *= v;
+    }
+    return bytes > uint64_t(SIZE_MAX) ? SIZE_MAX : size_t(bytes);
 }
 
-// Device address of the array: looked up once per device (with that device
-// current) on the first call, since the host-side symbol is not a device
-// address.
+// Device address of the array, looked up with the device current, since the
+// host-side symbol is not a device address.  Only a successful lookup is
+// kept: a call whose lookup failed (for example while an earlier
+// asynchronous error was pending) returns that error, and the next call
+// tries again.
 static cudaError_t noalloc_scratch_address(uint8_t **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-    std::call_once(g_na_once[dev], [dev]() {
+    std::lock_guard<std::mutex> lock(g_na_mutex);
+    if (g_na_addr[dev] == nullptr) {
         void *p = nullptr;
-        g_na_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
         g_na_addr[dev] = p;
-    });
-    if (g_na_err[dev] != cudaSuccess) return g_na_err[dev];
+    }
     *out = static_cast<uint8_t *>(g_na_addr[dev]);
     return cudaSuccess;
 }
