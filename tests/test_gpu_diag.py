@@ -109,25 +109,16 @@ def test_no_D_and_zero_input(cuda_device):
 
 @pytest.mark.parametrize("name", ["diag_bf16_Bs8_L2048_ED1536_N16",
                                   "diag_bf16_Bs16_L1000_ED2560_N16"])
-def test_benchmark_shape_sampled_channels(cuda_device, name):
+def test_benchmark_shape_whole_output(cuda_device, name):
     """Full benchmark size in the launch configuration the benchmark times;
-    the oracle recomputes a spread-out sample of channels one by one."""
+    the whole y against the oracle on the same inputs."""
     w = workloads.BY_NAME[name]
     inp = workloads.workload_inputs(w)
     y = lrs.ssm_scan_fwd(**_to_dev(inp, cuda_device)).cpu().double().numpy()
-    s = w.shape
-    Bs, L, ED = s["Bs"], s["L"], s["ED"]
-    rng = np.random.default_rng(0)
-    chans = sorted(set([0, Bs * ED - 1, ED - 1, ED] + list(rng.integers(0, Bs * ED, 60))))
-    for c in chans:
-        b, e = divmod(int(c), ED)
-        one = dict(x=inp["x"][b:b + 1, :, e:e + 1], delta=inp["delta"][b:b + 1, :, e:e + 1],
-                   A=inp["A"][e:e + 1], B=inp["B"][b:b + 1], C=inp["C"][b:b + 1],
-                   D=inp["D"][e:e + 1])
-        r = oracle.diag_scan(**one)[0, :, 0]
-        err = np.max(np.abs(y[b, :, e] - r))
-        assert err <= TOL_BF16 * np.max(np.abs(r)), (b, e, err)
+    ref = oracle.diag_scan(**inp)
     assert np.all(np.isfinite(y))
+    err = float(np.max(np.abs(y - ref)))
+    assert err <= TOL_BF16 * float(np.max(np.abs(ref))), err
 
 
 def test_deterministic_and_guard_bands(cuda_device):
