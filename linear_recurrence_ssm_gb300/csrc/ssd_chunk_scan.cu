@@ -691,58 +691,72 @@ done:
 }
 
 // ---------------------------------------------------------------------------
-// Warp-specialised kernel (unidirectional)
+// Unidirectional kernel: eight math warps, an MMA-issuing warp, a copying warp
 // ---------------------------------------------------------------------------
-// The same computation as ssd_chunk_scan_kernel for the forward scan, with
-// the work of a tile split between roles that run up to a tile apart and
-// meet only at mbarriers, so that the mask of one tile, the outputs of the
-// previous one and the tensor-core products overlap instead of taking turns:
-//   warpgroup 0 (rows t = 0..127): the per-tile vectors (dt, cumulative sums,
-//     column factors) a tile ahead, then the decay mask of each tile from G;
-//   warpgroup 1 (rows t = 0..127 / state columns n): the fp32 state update
-//     and its bf16 image, the weighted x rows of the next tile, then the
-//     output rows y = Y + e^{cum} Zf (out through a per-warp shared-memory
-//     staging tile; D x is part of Y: warpgroup 0 adds D_h to the diagonal
-//     of the mask);
-//   warp 8, one thread: every tcgen05.mma, as soon as its inputs are ready;
-//   warp 9, one thread: every TMA copy, as soon as its buffer is free.
-// Y and Zf have two accumulators each (by tile parity): the products of tile
-// c + 1 run while warpgroup 1 reads the outputs of tile c.
+// The same computation as ssd_chunk_scan_kernel for the forward scan.  Eight
+// math warps share every per-tile stage: warps w and w + 4 read TMEM lane
+// quarter q = w % 4 (tile rows / state rows 32 q .. 32 q + 31) and split the
+// work of those rows by column halves (hf = w / 4):
+//   the decay mask: row quarter q has causal 32 x 32 blocks sb = 0..q; the
+//     warp takes the blocks with sb % 2 == hf (at most two, so the causal
+//     triangle's work is spread evenly instead of four blocks on one warp);
+//   the weighted x rows, the fp32 state update and its bf16 image, the
+//     output rows y = Y + e^{cum} Zf: columns 32 hf .. 32 hf + 31.
+// Per tile c the warps (1) weigh the x rows of tile c + 1 and compute its
+// mask in registers while Y(c), S_c(c) run on the tensor core, (2) wait for
+// them, update the state (the image of the state entering tile c + 1), store
+// the mask of tile c + 1 into tensor memory -- so Zf(c + 1), Y(c + 1) and
+// S_c(c + 1) start at once -- and (3) write the outputs of tile c while they
+// run.  Warp 8 (one thread) issues every tcgen05.mma as soon as its inputs
+// are ready, warp 9 (one thread) every TMA copy as soon as its buffer is
+// free.  The mask M lives in tensor memory and is the A operand of Y = M X;
+// D x rides on its diagonal.  Y and Zf have two accumulators (by tile
+// parity) so the products of tile c + 1 run while the outputs of tile c are
+// read; the weighted rows Xw are double-buffered, and the buffer of tile c
+// is free once S_c(c) has run, so it stages tile c's output rows.
 namespace ws {
 
-constexpr int kThreads = 384;
-// Registers: the CTA is launched with 168 per thread (65536 / 384 rounded
-// down to a multiple of 8); the issuing warpgroup gives some back and the
-// two math warpgroups take them (setmaxnreg).
+constexpr int kMath = 256;             // math threads (warps 0..7)
+constexpr int kThreads = kMath + 128;  // + warpgroup 2: warp 8 issues MMAs, warp 9 copies
+// Registers: the register file is split between the SM's four schedulers,
+// one warp of each warpgroup per scheduler; the CTA is launched with 168 per
+// thread (3 warps x 32 x 168 <= 16384 per scheduler) and setmaxnreg moves
+// registers from the control warpgroup to the two math warpgroups.
 constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kIssuerRegs = 56;
+constexpr uint32_t kCtrlRegs = 56;
 constexpr uint32_t kMathRegs = 224;
-static_assert(128 * kIssuerRegs + 256 * kMathRegs <= kThreads * kLaunchRegs,
+static_assert(kCtrlRegs + 2 * kMathRegs <= 3 * kLaunchRegs,
               "the register split must fit in what the CTA is launched with");
 constexpr int kSlots = 3;        // per-tile vectors in flight (tile c uses slot c % 3)
+constexpr int kXBufs = 2;        // x tiles in flight (tile c uses buffer c % 2)
 
-// Tensor-memory columns.
-constexpr uint32_t kWsG = 0, kWsY0 = 128, kWsY1 = 192, kWsZ0 = 256, kWsZ1 = 320, kWsS = 384;
+// Tensor-memory columns: G (fp32, 128), Y and Zf by tile parity (fp32, 64
+// each), the chunk state S_c^T (fp32, 64) and the mask M (bf16 pairs, 64).
+constexpr uint32_t kWsG = 0, kWsY0 = 128, kWsY1 = 192, kWsZ0 = 256, kWsZ1 = 320, kWsS = 384,
+                   kWsM = 448;
 
 template <int NB>
 struct __align__(1024) Smem {
     uint8_t C[2][NB][kTile];    // C tiles (double buffered), K-major rows t
     uint8_t B[2][2][kTile];     // B tiles (double buffered); region 1 zero when N = 64
-    uint8_t X[kTile];           // x tile (MN-major B operand of Y)
-    uint8_t Xw[kTile];          // weighted x rows (operand of S_c)
-    uint8_t M[2][kTile];        // masked G (K-major, two 64-wide regions of s)
+    uint8_t X[kXBufs][kTile];   // x tiles (MN-major B operand of Y), tile c in c % 2
+    uint8_t Xw[2][kTile];       // weighted x rows of tile c in c % 2; then its y staging
     uint8_t S[NB][kStateRegion];    // entering state image
-    float ystage[4][32 * 16];       // per output warp: 32 rows x 16 columns of y on their way out
     float cum[kSlots][kQ];
-    float excl[kSlots][kQ];
     float dtv[kSlots][kQ];
     float csf[kSlots][kQ];
     float tot[kSlots];
-    float wsum[kSlots][4];      // warp sums of warpgroup 0's scans
-    uint64_t bar_c[2], bar_b[2], bar_x;              // TMA copies landed
-    uint64_t bar_g, bar_z[2], bar_m2;                // products finished (bar_z by tile parity)
-    uint64_t bar_gfree, bar_mfull, bar_xw, bar_st;   // hand-offs between roles
-    uint64_t bar_vec[kSlots], bar_vfree[kSlots], bar_sync, bar_fin;
+    float wsum[kSlots][4];      // warp sums of the cumulative-sum scan
+    uint64_t bar_c[2], bar_b[2], bar_x[kXBufs];      // TMA copies landed
+    // Products finished and hand-offs.  A parity wait cannot tell phase k
+    // from phase k + 2, so no barrier may complete twice before every waiter
+    // has seen the first: bar_xw and bar_m2 are one per tile parity, because
+    // the weighted rows of tile c + 1 are written before Y(c) is issued, and
+    // the copying thread is the only waiter on bar_m2 that nothing else holds
+    // back; each of the others completes again only after its waiters moved on.
+    uint64_t bar_g, bar_m2[2];
+    uint64_t bar_gfree, bar_mfull, bar_xw[2], bar_st;
+    uint64_t bar_half, bar_all, bar_fin;             // math-warp syncs; error path
     uint32_t tmem_base;
 };
 
@@ -762,15 +776,25 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Row n of an MN-major bf16 state image (64 p, 128-byte swizzle) from the 64
-// fp32 values a thread holds.
-__device__ __forceinline__ void put_state_row(uint8_t *img, int n, const float (&s)[64]) {
+// Half `hf` (32 p) of row n of an MN-major bf16 state image (64 p, 128-byte
+// swizzle) from the 32 fp32 values a thread holds.
+__device__ __forceinline__ void put_state_half(uint8_t *img, int n, int hf, const float (&s)[32]) {
     uint8_t *rowp = img + n * 128;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<uint4 *>(rowp + ((j ^ (n & 7)) << 4)) =
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4 *>(rowp + (((4 * hf + j) ^ (n & 7)) << 4)) =
             make_uint4(pack_bf16(s[8 * j], s[8 * j + 1]), pack_bf16(s[8 * j + 2], s[8 * j + 3]),
                        pack_bf16(s[8 * j + 4], s[8 * j + 5]), pack_bf16(s[8 * j + 6], s[8 * j + 7]));
+}
+
+// a * b for two packed fp32 pairs (one instruction on sm_100-family cores).
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)),
+          "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return *reinterpret_cast<float2 *>(&r);
 }
 
 template <int NB>
@@ -788,6 +812,14 @@ struct Ctx {
         if (!mbar_wait_bounded(&(bar), (ph), cx.abort, kWaitLimitNs)) return false;       \
         (ph) ^= 1u;                                                                       \
     } while (0)
+// The same for barrier i of an array whose phases are the bits of `bits`
+// (a register, where an array indexed at run time would go to local memory).
+#define WS_WAIT_I(bar, bits, i)                                                           \
+    do {                                                                                  \
+        if (!mbar_wait_bounded(&(bar), ((bits) >> (i)) & 1u, cx.abort, kWaitLimitNs))    \
+            return false;                                                                 \
+        (bits) ^= 1u << (i);                                                              \
+    } while (0)
 
 // ---- the issuing thread -------------------------------------------------------------
 template <int NB, bool EXT>
@@ -800,12 +832,12 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
     constexpr uint32_t idZ = idesc_bf16_f32(128, 64, false, true);
     constexpr uint32_t idY = idesc_bf16_f32(128, 64, false, true);
     constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);
-    uint32_t ph_c[2] = {0, 0}, ph_b[2] = {0, 0}, ph_x = 0;
-    uint32_t ph_gfree = 0, ph_mfull = 0, ph_xw = 0, ph_st = 0;
+    uint32_t ph_c = 0, ph_b = 0, ph_x = 0;    // phase bits, one per buffer
+    uint32_t ph_gfree = 0, ph_mfull = 0, ph_xw = 0, ph_st = 0;   // ph_xw: one bit per parity
 
     // S_c^T = B^T (w x): A = B tile read MN-major (128 n rows), B = the weighted x rows.
-    auto issue_s = [&](int bb) {
-        const uint32_t sB = smem_addr(sm.B[bb]), sXw = smem_addr(sm.Xw);
+    auto issue_s = [&](int c) {
+        const uint32_t sB = smem_addr(sm.B[c & 1]), sXw = smem_addr(sm.Xw[c & 1]);
 #pragma unroll
         for (int kk = 0; kk < kQ / 16; ++kk)
             mma_bf16_ss(tmem + kWsS, smem_desc(sB + kk * 2048, kTile, 1024, kSwizzle128B),
@@ -830,17 +862,19 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
                         smem_desc(sS + kk * 2048, kTile, 1024, kSwizzle128B), idZ, kk > 0);
         }
     };
+    // Y = M X: A = the mask in tensor memory (row t, 8 columns = 16 s per
+    // K step), B = the x tile (MN-major: rows s, 64 p).
     auto issue_y = [&](int c) {
-        const uint32_t sM = smem_addr(sm.M), sX = smem_addr(sm.X);
+        const uint32_t sX = smem_addr(sm.X[c % kXBufs]);
         const uint32_t dcol = (c & 1) ? kWsY1 : kWsY0;
 #pragma unroll
         for (int kk = 0; kk < kQ / 16; ++kk)
-            mma_bf16_ss(tmem + dcol, smem_desc(sM + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024, kSwizzle128B),
+            mma_bf16_ts(tmem + dcol, tmem + kWsM + kk * 8,
                         smem_desc(sX + kk * 2048, kTile, 1024, kSwizzle128B), idY, kk > 0);
     };
 
-    WS_WAIT(sm.bar_c[0], ph_c[0]);
-    WS_WAIT(sm.bar_b[0], ph_b[0]);
+    WS_WAIT_I(sm.bar_c[0], ph_c, 0);
+    WS_WAIT_I(sm.bar_b[0], ph_b, 0);
     tc_fence_after_sync();
     issue_g(0);
     mma_commit(&sm.bar_g);
@@ -849,51 +883,49 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
         tc_fence_after_sync();
         issue_z(0);
     }
-    mma_commit(&sm.bar_z[0]);
     // Three streams of products, each issued as soon as its inputs are ready
     // (non-blocking polls, so that a late input of one stream does not hold
     // up another):
-    //   Y(c), S_c(c): mask(c) and weighted rows(c) written, x(c) landed, and
-    //                 G(c), Zf(c) issued before them -- so that the end of
+    //   Y(c), S_c(c): mask(c) stored, weighted rows(c) written, x(c) landed,
+    //                 and G(c), Zf(c) issued before them -- so that the end of
     //                 Y(c), S_c(c) also means the end of everything of tile c;
-    //   G(c):         G(c - 1) read by warpgroup 0, C(c) and B(c) landed;
+    //   G(c):         G(c - 1) read by the math warps, C(c) and B(c) landed;
     //   Zf(c):        state image of tile c written (C(c) landed: G(c) issued).
-    // (The copies are another thread's: issuing them can hold a thread for
-    // thousands of cycles.)
     int y_next = 0, g_next = 1, z_next = 1;
     uint64_t t_idle = 0;
     while (y_next < nc) {
         bool progress = false;
-        if (g_next > y_next && z_next > y_next && mbar_test_wait(&sm.bar_mfull, ph_mfull) &&
-            mbar_test_wait(&sm.bar_xw, ph_xw) && mbar_test_wait(&sm.bar_x, ph_x)) {
-            ph_mfull ^= 1u;
-            ph_xw ^= 1u;
-            ph_x ^= 1u;
-            tc_fence_after_sync();
-            issue_y(y_next);
-            issue_s(y_next & 1);
-            mma_commit(&sm.bar_m2);
-            ++y_next;
-            progress = true;
-        }
-        if (g_next < nc && mbar_test_wait(&sm.bar_gfree, ph_gfree) &&
-            mbar_test_wait(&sm.bar_c[g_next & 1], ph_c[g_next & 1]) &&
-            mbar_test_wait(&sm.bar_b[g_next & 1], ph_b[g_next & 1])) {
-            ph_gfree ^= 1u;
-            ph_c[g_next & 1] ^= 1u;
-            ph_b[g_next & 1] ^= 1u;
-            tc_fence_after_sync();
-            issue_g(g_next & 1);
-            mma_commit(&sm.bar_g);
-            ++g_next;
-            progress = true;
-        }
         if (z_next < nc && g_next > z_next && mbar_test_wait(&sm.bar_st, ph_st)) {
             ph_st ^= 1u;
             tc_fence_after_sync();
             issue_z(z_next & 1);
-            mma_commit(&sm.bar_z[z_next & 1]);
             ++z_next;
+            progress = true;
+        }
+        const int xb = y_next % kXBufs, yp = y_next & 1;
+        if (g_next > y_next && z_next > y_next && mbar_test_wait(&sm.bar_mfull, ph_mfull) &&
+            mbar_test_wait(&sm.bar_xw[yp], (ph_xw >> yp) & 1u) &&
+            mbar_test_wait(&sm.bar_x[xb], (ph_x >> xb) & 1u)) {
+            ph_mfull ^= 1u;
+            ph_xw ^= 1u << yp;
+            ph_x ^= 1u << xb;
+            tc_fence_after_sync();
+            issue_y(y_next);
+            issue_s(y_next);
+            mma_commit(&sm.bar_m2[yp]);
+            ++y_next;
+            progress = true;
+        }
+        if (g_next < nc && mbar_test_wait(&sm.bar_gfree, ph_gfree) &&
+            mbar_test_wait(&sm.bar_c[g_next & 1], (ph_c >> (g_next & 1)) & 1u) &&
+            mbar_test_wait(&sm.bar_b[g_next & 1], (ph_b >> (g_next & 1)) & 1u)) {
+            ph_gfree ^= 1u;
+            ph_c ^= 1u << (g_next & 1);
+            ph_b ^= 1u << (g_next & 1);
+            tc_fence_after_sync();
+            issue_g(g_next & 1);
+            mma_commit(&sm.bar_g);
+            ++g_next;
             progress = true;
         }
         if (progress) {
@@ -912,7 +944,8 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
 // ---- the copying thread --------------------------------------------------------------
 // Every TMA copy, each into a buffer whose previous contents have been used:
 // the end of Y(c), S_c(c) means the end of every product of tile c (the
-// issuing thread orders G(c) and Zf(c) before them).
+// issuing thread orders G(c) and Zf(c) before them), and the math warps are
+// done with x(c) once they have weighed it (S_c(c) reads the weighted rows).
 template <int NB, bool EXT>
 __device__ __forceinline__ bool loader_role(Ctx<NB> &cx, const CUtensorMap *tmC, const CUtensorMap *tmB,
                                             const CUtensorMap *tmX) {
@@ -931,8 +964,9 @@ __device__ __forceinline__ bool loader_role(Ctx<NB> &cx, const CUtensorMap *tmC,
         for (int r = 0; r < NB; ++r) tma_load_4d(sm.C[buf][r], tmC, &sm.bar_c[buf], r * 64, grp, c * kQ, b);
     };
     auto load_x = [&](int c) {
-        mbar_arrive_expect_tx(&sm.bar_x, kTile);
-        tma_load_4d(sm.X, tmX, &sm.bar_x, 0, h, c * kQ, b);
+        const int xb = c % kXBufs;
+        mbar_arrive_expect_tx(&sm.bar_x[xb], kTile);
+        tma_load_4d(sm.X[xb], tmX, &sm.bar_x[xb], 0, h, c * kQ, b);
     };
     load_c(0, 0);
     load_b(0, 0);
@@ -940,11 +974,12 @@ __device__ __forceinline__ bool loader_role(Ctx<NB> &cx, const CUtensorMap *tmC,
     if (nc > 1) {
         load_c(1, 1);
         load_b(1, 1);
+        load_x(1);
     }
     for (int c = 0; c < nc; ++c) {
-        WS_WAIT(sm.bar_m2, ph_m2);
-        if (c + 1 < nc) load_x(c + 1);
+        WS_WAIT_I(sm.bar_m2[c & 1], ph_m2, c & 1);   // every product of tile c done
         if (c + 2 < nc) {
+            load_x(c + 2);
             load_c(c + 2, c & 1);
             load_b(c + 2, c & 1);
         }
@@ -952,314 +987,293 @@ __device__ __forceinline__ bool loader_role(Ctx<NB> &cx, const CUtensorMap *tmC,
     return true;
 }
 
-// ---- warpgroup 0: vectors and decay mask --------------------------------------------
+// ---- the eight math warps -------------------------------------------------------------
 template <int NB, bool EXT>
-__device__ __forceinline__ bool mask_role(Ctx<NB> &cx) {
+__device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
+    constexpr int N = NB * 64;
     auto &sm = cx.sm;
-    const int t = threadIdx.x;          // 0..127: tile row, TMEM lane
-    const int warp = t >> 5;
-    const int tb = warp;                // the warp's 32-row block
-    const uint32_t lane_base = uint32_t(warp * 32) << 16;
-    const int nc = cx.nc, L = cx.L;
-    const float Dh = cx.Dh;
-    const __nv_bfloat16 *dtp = cx.prm.dt + (int64_t(cx.b) * L) * cx.prm.H + cx.h;
-    uint32_t ph_g = 0, ph_m2 = 0, ph_vfree[kSlots] = {0, 0, 0}, ph_sync = 0;
-    // raw dt of row c * kQ + t (loaded a tile ahead); rows past L: 0
-    auto load_dt = [&](int c) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;             // TMEM lane quarter
+    const int hf = warp >> 2;           // column half
+    const int t = q * 32 + lane;        // tile row t, state row n, TMEM lane
+    const uint32_t lane_base = uint32_t(q * 32) << 16;
+    const int nc = cx.nc, L = cx.L, b = cx.b, h = cx.h, H = cx.prm.H;
+    const uint32_t tmem = cx.tmem;
+    const bool is_state = t < N;        // warp-uniform: N is 64 or 128
+    // this warp's mask blocks of row quarter q: sb0 = hf and sb1 = hf + 2
+    const bool own0 = hf <= q, own1 = hf + 2 <= q;
+    uint32_t ph_g = 0, ph_m2 = 0, ph_half = 0, ph_all = 0, ph_x = 0;
+    const __nv_bfloat16 *dtp = cx.prm.dt + (int64_t(b) * L) * H + h;
+    auto load_dt = [&](int c) {      // raw dt of row c * kQ + t; rows past L: 0
         const int r = c * kQ + t;
-        return r < L ? dtp[int64_t(r) * cx.prm.H] : __float2bfloat16(0.0f);
-    };
-    // vectors of tile c into slot c % 3
-    auto tile_prep = [&](int c, __nv_bfloat16 raw) -> bool {
-        const int p = c % kSlots;
-        float dv = 0.0f;
-        if (c * kQ + t < L) {
-            dv = __bfloat162float(raw);
-            if (EXT) {
-                dv += cx.dbias;
-                if (cx.prm.dt_softplus) dv = softplus_fast(dv);
-                if (cx.prm.dt_limit) dv = fminf(fmaxf(dv, cx.prm.dt_min), cx.prm.dt_max);
-            }
-        }
-        const float dA = dv * cx.Ah;
-        // inclusive prefix sum over the 128 rows: warp scan, then the warp totals
-        const int lane = t & 31;
-        float v = dA;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float n = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += n;
-        }
-        if (lane == 31) sm.wsum[p][warp] = v;
-        mbar_arrive(&sm.bar_sync);
-        WS_WAIT(sm.bar_sync, ph_sync);
-        float off = 0.0f, tot = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float s = sm.wsum[p][w];
-            off += (w < warp) ? s : 0.0f;
-            tot += s;
-        }
-        const float cum = v + off;
-        sm.cum[p][t] = cum;
-        sm.excl[p][t] = cum - dA;
-        sm.dtv[p][t] = dv;
-        if (t == 0) sm.tot[p] = tot;
-        __syncwarp();
-        // column factors of the off-diagonal blocks (row s | 31 is in this warp)
-        sm.csf[p][t] = ex2(sm.cum[p][t | 31] - cum) * dv;
-        mbar_arrive(&sm.bar_sync);              // the mask reads other rows' vectors
-        WS_WAIT(sm.bar_sync, ph_sync);
-        mbar_arrive(&sm.bar_vec[p]);
-        return true;
+        return r < L ? dtp[int64_t(r) * H] : __float2bfloat16(0.0f);
     };
 
-    __nv_bfloat16 raw_next = load_dt(0);
-    if (!tile_prep(0, raw_next)) return false;
-    if (nc > 1) raw_next = load_dt(1);
-    for (int c = 0; c < nc; ++c) {
+    // Vectors of tile c into slot c % 3 (cumulative sums of dt A in log2
+    // units, dt, the column factors of the off-diagonal mask blocks, the
+    // tile total): rows t from half 0, then every math warp syncs.
+    auto prep = [&](int c, __nv_bfloat16 raw) -> bool {
+        const int p = c % kSlots;
+        if (hf == 0) {
+            float dv = 0.0f;
+            if (c * kQ + t < L) {
+                dv = __bfloat162float(raw);
+                if (EXT) {
+                    dv += cx.dbias;
+                    if (cx.prm.dt_softplus) dv = softplus_fast(dv);
+                    if (cx.prm.dt_limit) dv = fminf(fmaxf(dv, cx.prm.dt_min), cx.prm.dt_max);
+                }
+            }
+            const float dA = dv * cx.Ah;
+            float v = dA;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += n;
+            }
+            if (lane == 31) sm.wsum[p][q] = v;
+            mbar_arrive(&sm.bar_half);
+            WS_WAIT(sm.bar_half, ph_half);
+            float off = 0.0f, tot = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float s = sm.wsum[p][w];
+                off += (w < q) ? s : 0.0f;
+                tot += s;
+            }
+            const float cum = v + off;
+            sm.cum[p][t] = cum;
+            sm.dtv[p][t] = dv;
+            if (t == 0) sm.tot[p] = tot;
+            __syncwarp();
+            // column factors of the off-diagonal blocks (row s | 31 is in this warp)
+            sm.csf[p][t] = ex2(sm.cum[p][t | 31] - cum) * dv;
+        }
+        mbar_arrive(&sm.bar_all);
+        WS_WAIT(sm.bar_all, ph_all);
+        return true;
+    };
+    // Weighted x rows of tile c: row s = t, columns of half hf.
+    auto weigh = [&](int c) -> bool {
+        const int p = c % kSlots, xb = c % kXBufs;
+        WS_WAIT_I(sm.bar_x[xb], ph_x, xb);
+        const float w = ex2(sm.tot[p] - sm.cum[p][t]) * sm.dtv[p][t];
+        scale_row(sm.X[xb], sm.Xw[c & 1], t, w, hf);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.bar_xw[c & 1]);
+        return true;
+    };
+    // Mask rows t of tile c, this warp's blocks, into registers (bf16 pairs).
+    uint32_t mk[2][16];
+    auto mask = [&](int c) -> bool {
         const int p = c % kSlots;
         const float *cum = sm.cum[p];
         const float *dtv = sm.dtv[p];
         const float cum_t = cum[t];
         WS_WAIT(sm.bar_g, ph_g);
         tc_fence_after_sync();
-        uint32_t packed[4][16];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t gr[2][32];
-            bool need[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int sb = 2 * half + i;
-                need[i] = sb <= tb;
-                if (need[i]) tmem_ld32_async(cx.tmem + lane_base + kWsG + sb * 32, gr[i]);
+        for (int i = 0; i < 2; ++i) {
+            const int sb = hf + 2 * i;
+            const bool own = i == 0 ? own0 : own1;
+            uint32_t gr[32];
+            if (own) {
+                tmem_ld32_async(tmem + lane_base + kWsG + sb * 32, gr);
+                tmem_wait_tie(gr);
             }
-            if (need[0] || need[1]) {
-                tmem_wait_tie(gr[0]);
-                reg_tie(gr[1]);
-            }
-            if (half == 1) {
+            if (i == 1) {
                 tc_fence_before_sync();
                 mbar_arrive(&sm.bar_gfree);     // G may be overwritten now
             }
+            if (!own) continue;
+            if (sb == q) {
+                // diagonal block: direct differences of cumulative sums; the
+                // skip term rides on the diagonal: Y = (M + D_h I) X
+                const float4 *c4 = reinterpret_cast<const float4 *>(cum + sb * 32);
+                const float4 *d4 = reinterpret_cast<const float4 *>(dtv + sb * 32);
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int sb = 2 * half + i;
-                if (!need[i]) {
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 cs = c4[j4], ds = d4[j4];
+                    const float csv[4] = {cs.x, cs.y, cs.z, cs.w};
+                    const float dsv[4] = {ds.x, ds.y, ds.z, ds.w};
+                    float m[4];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) packed[sb][j] = 0u;
-                    continue;
-                }
-                float m[32];
-                if (sb == tb) {
-                    // diagonal block: direct differences of cumulative sums
-                    const float4 *c4 = reinterpret_cast<const float4 *>(cum + sb * 32);
-                    const float4 *d4 = reinterpret_cast<const float4 *>(dtv + sb * 32);
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 cs = c4[j4], ds = d4[j4];
-                        const float csv[4] = {cs.x, cs.y, cs.z, cs.w};
-                        const float dsv[4] = {ds.x, ds.y, ds.z, ds.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int s = sb * 32 + 4 * j4 + q;
-                            const float w = (s <= t) ? ex2(cum_t - csv[q]) : 0.0f;
-                            m[4 * j4 + q] = __uint_as_float(gr[i][4 * j4 + q]) * (w * dsv[q]);
-                        }
+                    for (int k = 0; k < 4; ++k) {
+                        const int s = sb * 32 + 4 * j4 + k;
+                        const float w = (s <= t) ? ex2(cum_t - csv[k]) : 0.0f;
+                        float v = __uint_as_float(gr[4 * j4 + k]) * (w * dsv[k]);
+                        if (s == t) v += cx.Dh;
+                        m[k] = v;
                     }
-                } else {
-                    const float e = ex2(cum_t - cum[sb * 32 + 31]);
-                    const float4 *f4 = reinterpret_cast<const float4 *>(sm.csf[p] + sb * 32);
-#pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 f = f4[j4];
-                        m[4 * j4 + 0] = __uint_as_float(gr[i][4 * j4 + 0]) * (e * f.x);
-                        m[4 * j4 + 1] = __uint_as_float(gr[i][4 * j4 + 1]) * (e * f.y);
-                        m[4 * j4 + 2] = __uint_as_float(gr[i][4 * j4 + 2]) * (e * f.z);
-                        m[4 * j4 + 3] = __uint_as_float(gr[i][4 * j4 + 3]) * (e * f.w);
-                    }
+                    mk[i][2 * j4] = pack_bf16(m[0], m[1]);
+                    mk[i][2 * j4 + 1] = pack_bf16(m[2], m[3]);
                 }
+            } else {
+                // below the diagonal: G * (row factor) * (column factor), both <= 1
+                const float e = ex2(cum_t - cum[sb * 32 + 31]);
+                const float2 ee = make_float2(e, e);
+                const float4 *f4 = reinterpret_cast<const float4 *>(sm.csf[p] + sb * 32);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) packed[sb][j] = pack_bf16(m[2 * j], m[2 * j + 1]);
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 f = f4[j4];
+                    const float2 a = fmul2(fmul2(make_float2(__uint_as_float(gr[4 * j4]),
+                                                             __uint_as_float(gr[4 * j4 + 1])),
+                                                 make_float2(f.x, f.y)), ee);
+                    const float2 bq = fmul2(fmul2(make_float2(__uint_as_float(gr[4 * j4 + 2]),
+                                                              __uint_as_float(gr[4 * j4 + 3])),
+                                                  make_float2(f.z, f.w)), ee);
+                    mk[i][2 * j4] = pack_bf16(a.x, a.y);
+                    mk[i][2 * j4 + 1] = pack_bf16(bq.x, bq.y);
+                }
             }
         }
-        if (c >= 1) WS_WAIT(sm.bar_m2, ph_m2);  // Y(c - 1) has read the mask buffer
-#pragma unroll
-        for (int sb = 0; sb < 4; ++sb) {
-            uint8_t *reg = sm.M[sb >> 1];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int col = (sb & 1) * 32 + q * 8;
-                *reinterpret_cast<uint4 *>(reg + swz(t, col)) =
-                    make_uint4(packed[sb][4 * q], packed[sb][4 * q + 1], packed[sb][4 * q + 2],
-                               packed[sb][4 * q + 3]);
-            }
-        }
-        {   // the skip term rides on the diagonal: Y = (M + D_h I) X
-            __nv_bfloat16 *d = reinterpret_cast<__nv_bfloat16 *>(sm.M[t >> 6] + swz(t, t & 63));
-            *d = __float2bfloat16(__bfloat162float(*d) + Dh);
-        }
-        fence_proxy_async_smem();
+        return true;
+    };
+    // Store this warp's mask blocks into tensor memory (after Y of the
+    // previous tile has read the mask) and hand the mask to the issuer.
+    auto mask_store = [&]() {
+        if (own0) tmem_st_32x32b_x16(tmem + lane_base + kWsM + hf * 16, mk[0]);
+        if (own1) tmem_st_32x32b_x16(tmem + lane_base + kWsM + (hf + 2) * 16, mk[1]);
+        tmem_wait_st();
+        tc_fence_before_sync();
         mbar_arrive(&sm.bar_mfull);
-        if (c + 1 < nc) {
-            const int pn = (c + 1) % kSlots;
-            if (c + 1 >= kSlots) WS_WAIT(sm.bar_vfree[pn], ph_vfree[pn]);   // tile c - 2 is done with them
-            if (!tile_prep(c + 1, raw_next)) return false;
-            if (c + 2 < nc) raw_next = load_dt(c + 2);
+    };
+    const bool gate = EXT && cx.prm.z != nullptr;
+    uint4 zq[4];   // gate row of the tile being written (bf16, 32 values), loaded a tile early
+    auto prefetch_gate = [&](int c) {
+        const int row = c * kQ + t;
+        if (!gate || row >= L) return;
+        const uint4 *zp = reinterpret_cast<const uint4 *>(cx.prm.z + ((size_t(b) * L + row) * H + h) * kP + hf * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) zq[j] = __ldg(zp + j);
+    };
+    // Output rows t of tile c, columns of half hf: y = Y + e^{cum_t} Zf (Y
+    // already holds D x), out through this warp's staging area in the free
+    // weighted-rows buffer of tile c (32 rows x 16 columns, 2 KB).
+    auto epilogue = [&](int c) {
+        const int p = c % kSlots;
+        const bool has_s = c > 0 || has_h0;
+        const float ef = ex2(sm.cum[p][t]);
+        const uint32_t ycol = (c & 1) ? kWsY1 : kWsY0, zcol = (c & 1) ? kWsZ1 : kWsZ0;
+        uint32_t yv[32], zf[32];
+        tmem_ld32_async(tmem + lane_base + ycol + hf * 32, yv);
+        if (has_s) tmem_ld32_async(tmem + lane_base + zcol + hf * 32, zf);
+        tmem_wait_tie(yv);
+        reg_tie(zf);
+        float out[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) out[j] = __uint_as_float(yv[j]);
+        if (has_s) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) out[j] = fmaf(ef, __uint_as_float(zf[j]), out[j]);
         }
+        if (gate && c * kQ + t < L) {   // (rows past L are computed but not stored)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t w4[4] = {zq[j].x, zq[j].y, zq[j].z, zq[j].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 zz = unpack_bf16(w4[k]);
+                    out[8 * j + 2 * k] *= silu_fast(zz.x);
+                    out[8 * j + 2 * k + 1] *= silu_fast(zz.y);
+                }
+            }
+        }
+        // 16 columns at a time through the staging area, so that each store
+        // instruction covers 8 rows x 64 contiguous bytes instead of 32 rows x
+        // 16 bytes.  The 16-byte chunks of a row are XOR-permuted by
+        // (row / 2) % 4: conflict-free in both directions.
+        float *stg = reinterpret_cast<float *>(sm.Xw[c & 1]) + warp * (32 * 16);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int sw = (lane >> 1) & 3;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                reinterpret_cast<float4 *>(stg + lane * 16)[j ^ sw] =
+                    make_float4(out[16 * hh + 4 * j], out[16 * hh + 4 * j + 1],
+                                out[16 * hh + 4 * j + 2], out[16 * hh + 4 * j + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int rr = 8 * k + (lane >> 2), ch = lane & 3;
+                const float4 v = reinterpret_cast<const float4 *>(stg + rr * 16)[ch ^ ((rr >> 1) & 3)];
+                const int trow = c * kQ + q * 32 + rr;
+                if (trow < L)
+                    *reinterpret_cast<float4 *>(cx.prm.y + ((size_t(b) * L + trow) * H + h) * kP +
+                                                hf * 32 + hh * 16 + ch * 4) = v;
+            }
+            __syncwarp();
+        }
+    };
+
+    // ---- prologue -------------------------------------------------------------------
+    {   // the mask blocks above the diagonal stay zero for every tile
+        uint32_t zero[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) zero[j] = 0u;
+        if (!own0) tmem_st_32x32b_x16(tmem + lane_base + kWsM + hf * 16, zero);
+        if (!own1) tmem_st_32x32b_x16(tmem + lane_base + kWsM + (hf + 2) * 16, zero);
+        tmem_wait_st();
     }
-    return true;
-}
-
-// ---- warpgroup 1: state, weighted rows, outputs ---------------------------------------
-template <int NB, bool EXT>
-__device__ __forceinline__ bool output_role(Ctx<NB> &cx, bool has_h0) {
-    constexpr int N = NB * 64;
-    auto &sm = cx.sm;
-    const int r = threadIdx.x - 128;    // 0..127: tile row t, state column n, TMEM lane
-    const int warp = r >> 5;
-    const int lane = r & 31;
-    const uint32_t lane_base = uint32_t(warp * 32) << 16;
-    const int nc = cx.nc, L = cx.L, b = cx.b, h = cx.h, H = cx.prm.H;
-    uint32_t ph_x = 0, ph_m2 = 0, ph_z[2] = {0, 0}, ph_vec[kSlots] = {0, 0, 0};
-    const bool is_state = r < N;        // warp-uniform: N is 64 or 128
-    float st[64];
+    __nv_bfloat16 raw0 = __float2bfloat16(0.0f), raw1 = raw0, raw_next = raw0;
+    if (hf == 0) {
+        raw0 = load_dt(0);
+        if (nc > 1) raw1 = load_dt(1);
+        if (nc > 2) raw_next = load_dt(2);
+    }
+    if (!prep(0, raw0)) return false;
+    if (nc > 1 && !prep(1, raw1)) return false;
+    float st[32];   // state rows n = t, columns p of half hf (fp32)
 #pragma unroll
-    for (int j = 0; j < 64; ++j) st[j] = 0.0f;
-
+    for (int j = 0; j < 32; ++j) st[j] = 0.0f;
     if (has_h0 && is_state) {
-        // column n = r of the initial state (Bs, H, P, N)
-        const float *src = cx.prm.h0 + size_t(cx.bh) * kP * N + r;
+        const float *src = cx.prm.h0 + size_t(cx.bh) * kP * N + size_t(hf * 32) * N + t;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) st[j] = src[size_t(j) * N];
-        put_state_row(&sm.S[0][0], r, st);
+        for (int j = 0; j < 32; ++j) st[j] = src[size_t(j) * N];
+        put_state_half(&sm.S[0][0], t, hf, st);
     }
     fence_proxy_async_smem();
     mbar_arrive(&sm.bar_st);
-
-    auto weigh = [&](int c) -> bool {   // weighted x rows of tile c
-        const int p = c % kSlots;
-        WS_WAIT(sm.bar_vec[p], ph_vec[p]);
-        WS_WAIT(sm.bar_x, ph_x);
-        const float w = ex2(sm.tot[p] - sm.cum[p][r]) * sm.dtv[p][r];
-        scale_row(sm.X, sm.Xw, r, w, 0);
-        scale_row(sm.X, sm.Xw, r, w, 1);
-        fence_proxy_async_smem();
-        mbar_arrive(&sm.bar_xw);
-        return true;
-    };
-    const bool gate = EXT && cx.prm.z != nullptr;
-    // gate rows of tile c (bf16, 64 values), loaded a step early
-    uint4 zq[8];
-    auto prefetch_rows = [&](int c) {
-        const int row = c * kQ + r;
-        if (!gate || row >= L) return;
-        const uint4 *zp = reinterpret_cast<const uint4 *>(cx.prm.z + ((size_t(b) * L + row) * H + h) * kP);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) zq[j] = __ldg(zp + j);
-    };
-    // y rows of tile c from its accumulators (Y already holds D x).
-    auto epilogue = [&](int c) -> bool {
-        const int p = c % kSlots;
-        const int row = c * kQ + r;
-        const bool valid = row < L;
-        const bool has_s = c > 0 || has_h0;
-        const float ef = ex2(sm.cum[p][r]);
-        WS_WAIT(sm.bar_z[c & 1], ph_z[c & 1]);
-        tc_fence_after_sync();
-        const uint32_t ycol = (c & 1) ? kWsY1 : kWsY0, zcol = (c & 1) ? kWsZ1 : kWsZ0;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            uint32_t yv[32], zf[32];
-            tmem_ld32_async(cx.tmem + lane_base + ycol + q * 32, yv);
-            if (has_s) tmem_ld32_async(cx.tmem + lane_base + zcol + q * 32, zf);
-            tmem_wait_tie(yv);
-            reg_tie(zf);
-            float out[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) out[j] = __uint_as_float(yv[j]);
-            if (has_s) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) out[j] = fmaf(ef, __uint_as_float(zf[j]), out[j]);
-            }
-            if (gate && valid) {   // (rows past L are computed but not stored)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 zv = zq[4 * q + j];
-                    const uint32_t w4[4] = {zv.x, zv.y, zv.z, zv.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 zz = unpack_bf16(w4[k]);
-                        out[8 * j + 2 * k] *= silu_fast(zz.x);
-                        out[8 * j + 2 * k + 1] *= silu_fast(zz.y);
-                    }
-                }
-            }
-            // Out through a per-warp staging tile, 16 columns at a time, so
-            // that each store instruction covers 8 rows x 64 contiguous bytes
-            // instead of 32 rows x 16 bytes.  The 16-byte chunks of a row are
-            // XOR-permuted by (row / 2) % 4: conflict-free in both directions.
-            float *stg = sm.ystage[warp];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int sw = (lane >> 1) & 3;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    reinterpret_cast<float4 *>(stg + lane * 16)[j ^ sw] =
-                        make_float4(out[16 * hh + 4 * j], out[16 * hh + 4 * j + 1],
-                                    out[16 * hh + 4 * j + 2], out[16 * hh + 4 * j + 3]);
-                __syncwarp();
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int rr = 8 * k + (lane >> 2), ch = lane & 3;
-                    const float4 v = reinterpret_cast<const float4 *>(stg + rr * 16)[ch ^ ((rr >> 1) & 3)];
-                    const int trow = c * kQ + warp * 32 + rr;
-                    if (trow < L)
-                        *reinterpret_cast<float4 *>(cx.prm.y + ((size_t(b) * L + trow) * H + h) * kP +
-                                                    q * 32 + hh * 16 + ch * 4) = v;
-                }
-                __syncwarp();
-            }
-        }
-        return true;
-    };
-
     if (!weigh(0)) return false;
-    prefetch_rows(0);
+    prefetch_gate(0);
+    if (!mask(0)) return false;
+    mask_store();
+
     for (int c = 0; c < nc; ++c) {
-        WS_WAIT(sm.bar_m2, ph_m2);              // Y(c), S_c(c) done
+        const bool more = c + 1 < nc;
+        if (more) {
+            if (!weigh(c + 1)) return false;
+            if (!mask(c + 1)) return false;
+        }
+        WS_WAIT_I(sm.bar_m2[c & 1], ph_m2, c & 1);   // every product of tile c done
         tc_fence_after_sync();
-        // state passing: column n = r of S_in, then the image of the state
-        // entering tile c + 1 for Zf(c + 1)
+        // state passing: rows n = t of S_in, columns of half hf
         if (is_state) {
-            uint32_t v0[32], v1[32];
-            tmem_ld32_async(cx.tmem + lane_base + kWsS, v0);
-            tmem_ld32_async(cx.tmem + lane_base + kWsS + 32, v1);
-            tmem_wait_tie(v0);
-            reg_tie(v1);
+            uint32_t v[32];
+            tmem_ld32_async(tmem + lane_base + kWsS + hf * 32, v);
+            tmem_wait_tie(v);
             const float e = ex2(sm.tot[c % kSlots]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                st[j] = fmaf(e, st[j], __uint_as_float(v0[j]));
-                st[32 + j] = fmaf(e, st[32 + j], __uint_as_float(v1[j]));
-            }
-            if (c + 1 < nc) put_state_row(&sm.S[0][0], r, st);
+            for (int j = 0; j < 32; ++j) st[j] = fmaf(e, st[j], __uint_as_float(v[j]));
+            if (more) put_state_half(&sm.S[0][0], t, hf, st);
         }
-        if (c + 1 < nc) {
+        if (more) {
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            mbar_arrive(&sm.bar_st);
-            if (!weigh(c + 1)) return false;    // the products of tile c + 1 can start
+            mbar_arrive(&sm.bar_st);            // Zf(c + 1) can start
+            mask_store();                       // Y(c + 1), S_c(c + 1) can start
         }
-        if (!epilogue(c)) return false;
-        mbar_arrive(&sm.bar_vfree[c % kSlots]);
-        if (c + 1 < nc) prefetch_rows(c + 1);
+        epilogue(c);
+        if (more) prefetch_gate(c + 1);
+        if (c + 2 < nc) {
+            if (!prep(c + 2, raw_next)) return false;
+            if (hf == 0 && c + 3 < nc) raw_next = load_dt(c + 3);
+        }
     }
     if (EXT && cx.prm.h_final != nullptr && is_state) {
-        float *dst = cx.prm.h_final + size_t(cx.bh) * kP * N + r;
+        float *dst = cx.prm.h_final + size_t(cx.bh) * kP * N + size_t(hf * 32) * N + t;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) dst[size_t(j) * N] = st[j];
+        for (int j = 0; j < 32; ++j) dst[size_t(j) * N] = st[j];
     }
     return true;
 }
@@ -1281,21 +1295,19 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.bar_c[i], 1);
             mbar_init(&sm.bar_b[i], 1);
-            mbar_init(&sm.bar_z[i], 1);
         }
-        mbar_init(&sm.bar_x, 1);
+        for (int i = 0; i < kXBufs; ++i) mbar_init(&sm.bar_x[i], 1);
         mbar_init(&sm.bar_g, 1);
-        mbar_init(&sm.bar_m2, 1);
+        mbar_init(&sm.bar_m2[0], 1);
+        mbar_init(&sm.bar_m2[1], 1);
         mbar_init(&sm.bar_fin, 1);
-        mbar_init(&sm.bar_gfree, 128);
-        mbar_init(&sm.bar_mfull, 128);
-        mbar_init(&sm.bar_xw, 128);
-        mbar_init(&sm.bar_st, 128);
-        mbar_init(&sm.bar_sync, 128);
-        for (int i = 0; i < kSlots; ++i) {
-            mbar_init(&sm.bar_vec[i], 128);
-            mbar_init(&sm.bar_vfree[i], 128);
-        }
+        mbar_init(&sm.bar_gfree, kMath);
+        mbar_init(&sm.bar_mfull, kMath);
+        mbar_init(&sm.bar_xw[0], kMath);
+        mbar_init(&sm.bar_xw[1], kMath);
+        mbar_init(&sm.bar_st, kMath);
+        mbar_init(&sm.bar_half, kMath / 2);
+        mbar_init(&sm.bar_all, kMath);
         mbar_fence_init();
         prefetch_tmap(&tmC);
         prefetch_tmap(&tmB);
@@ -1325,13 +1337,13 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
     const bool has_h0 = EXT && prm.h0 != nullptr;
 
     bool ok = true;
-    if (warp >= 8) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kIssuerRegs));
+    if (warp < 8) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kMathRegs));
+        ok = math_role<NB, EXT>(cx, has_h0);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
         if (tid == 256) ok = issuer_role<NB, EXT>(cx, has_h0);
         if (tid == 288) ok = loader_role<NB, EXT>(cx, &tmC, &tmB, &tmX);
-    } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kMathRegs));
-        ok = warp < 4 ? mask_role<NB, EXT>(cx) : output_role<NB, EXT>(cx, has_h0);
     }
     if (!ok) {
         abort_flag = 1;
@@ -1352,6 +1364,7 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
     }
 }
 #undef WS_WAIT
+#undef WS_WAIT_I
 
 }  // namespace ws
 
