@@ -717,14 +717,15 @@ done:
 namespace ws {
 
 constexpr int kMath = 256;             // math threads (warps 0..7)
-constexpr int kThreads = kMath + 128;  // + warpgroup 2: warp 8 issues MMAs, warp 9 copies
+constexpr int kThreads = kMath + 128;  // + warpgroup 2: warp 8 issues MMAs, warp 9 copies,
+                                       //   warp 10 computes the per-tile vectors
 // Registers: the register file is split between the SM's four schedulers,
 // one warp of each warpgroup per scheduler; the CTA is launched with 168 per
 // thread (3 warps x 32 x 168 <= 16384 per scheduler) and setmaxnreg moves
 // registers from the control warpgroup to the two math warpgroups.
 constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kCtrlRegs = 56;
-constexpr uint32_t kMathRegs = 224;
+constexpr uint32_t kCtrlRegs = 40;
+constexpr uint32_t kMathRegs = 232;
 static_assert(kCtrlRegs + 2 * kMathRegs <= 3 * kLaunchRegs,
               "the register split must fit in what the CTA is launched with");
 constexpr int kSlots = 3;        // per-tile vectors in flight (tile c uses slot c % 3)
@@ -740,13 +741,13 @@ struct __align__(1024) Smem {
     uint8_t C[2][NB][kTile];    // C tiles (double buffered), K-major rows t
     uint8_t B[2][2][kTile];     // B tiles (double buffered); region 1 zero when N = 64
     uint8_t X[kXBufs][kTile];   // x tiles (MN-major B operand of Y), tile c in c % 2
-    uint8_t Xw[2][kTile];       // weighted x rows of tile c in c % 2; then its y staging
+    uint8_t Xw[2][kTile];       // weighted x rows of tile c in c % 2
     uint8_t S[NB][kStateRegion];    // entering state image
+    float ystage[8][32 * 8];        // per math warp: 32 rows x 8 columns of y on their way out
     float cum[kSlots][kQ];
     float dtv[kSlots][kQ];
     float csf[kSlots][kQ];
     float tot[kSlots];
-    float wsum[kSlots][4];      // warp sums of the cumulative-sum scan
     uint64_t bar_c[2], bar_b[2], bar_x[kXBufs];      // TMA copies landed
     // Products finished and hand-offs.  A parity wait cannot tell phase k
     // from phase k + 2, so no barrier may complete twice before every waiter
@@ -754,9 +755,10 @@ struct __align__(1024) Smem {
     // the weighted rows of tile c + 1 are written before Y(c) is issued, and
     // the copying thread is the only waiter on bar_m2 that nothing else holds
     // back; each of the others completes again only after its waiters moved on.
-    uint64_t bar_g, bar_m2[2];
+    uint64_t bar_g, bar_m2[2], bar_z[2];
     uint64_t bar_gfree, bar_mfull, bar_xw[2], bar_st;
-    uint64_t bar_half, bar_all, bar_fin;             // math-warp syncs; error path
+    uint64_t bar_vec[kSlots];                        // vectors of a slot written
+    uint64_t bar_fin;                                // error path
     uint32_t tmem_base;
 };
 
@@ -883,27 +885,30 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
         tc_fence_after_sync();
         issue_z(0);
     }
+    mma_commit(&sm.bar_z[0]);
     // Three streams of products, each issued as soon as its inputs are ready
     // (non-blocking polls, so that a late input of one stream does not hold
     // up another):
     //   Y(c), S_c(c): mask(c) stored, weighted rows(c) written, x(c) landed,
-    //                 and G(c), Zf(c) issued before them -- so that the end of
-    //                 Y(c), S_c(c) also means the end of everything of tile c;
+    //                 and G(c) issued before them (so the end of Y(c), S_c(c)
+    //                 also means the end of G(c));
     //   G(c):         G(c - 1) read by the math warps, C(c) and B(c) landed;
-    //   Zf(c):        state image of tile c written (C(c) landed: G(c) issued).
+    //   Zf(c):        state image of tile c written (C(c) landed: G(c) issued);
+    //                 its end is signalled on its own barrier, bar_z.
     int y_next = 0, g_next = 1, z_next = 1;
     uint64_t t_idle = 0;
-    while (y_next < nc) {
+    while (y_next < nc || z_next < nc) {
         bool progress = false;
         if (z_next < nc && g_next > z_next && mbar_test_wait(&sm.bar_st, ph_st)) {
             ph_st ^= 1u;
             tc_fence_after_sync();
             issue_z(z_next & 1);
+            mma_commit(&sm.bar_z[z_next & 1]);
             ++z_next;
             progress = true;
         }
         const int xb = y_next % kXBufs, yp = y_next & 1;
-        if (g_next > y_next && z_next > y_next && mbar_test_wait(&sm.bar_mfull, ph_mfull) &&
+        if (g_next > y_next && mbar_test_wait(&sm.bar_mfull, ph_mfull) &&
             mbar_test_wait(&sm.bar_xw[yp], (ph_xw >> yp) & 1u) &&
             mbar_test_wait(&sm.bar_x[xb], (ph_x >> xb) & 1u)) {
             ph_mfull ^= 1u;
@@ -943,15 +948,15 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
 
 // ---- the copying thread --------------------------------------------------------------
 // Every TMA copy, each into a buffer whose previous contents have been used:
-// the end of Y(c), S_c(c) means the end of every product of tile c (the
-// issuing thread orders G(c) and Zf(c) before them), and the math warps are
-// done with x(c) once they have weighed it (S_c(c) reads the weighted rows).
+// the end of Y(c), S_c(c) means the end of G(c) too (issued before them),
+// Zf(c) signals its own end, and the math warps are done with x(c) once
+// they have weighed it (S_c(c) reads the weighted rows).
 template <int NB, bool EXT>
 __device__ __forceinline__ bool loader_role(Ctx<NB> &cx, const CUtensorMap *tmC, const CUtensorMap *tmB,
                                             const CUtensorMap *tmX) {
     auto &sm = cx.sm;
     const int nc = cx.nc, b = cx.b, h = cx.h, grp = cx.grp;
-    uint32_t ph_m2 = 0;
+    uint32_t ph_m2 = 0, ph_z = 0;   // one bit per parity
     auto load_b = [&](int c, int buf) {
         mbar_arrive_expect_tx(&sm.bar_b[buf], NB * kTile);
 #pragma unroll
@@ -977,17 +982,115 @@ __device__ __forceinline__ bool loader_role(Ctx<NB> &cx, const CUtensorMap *tmC,
         load_x(1);
     }
     for (int c = 0; c < nc; ++c) {
-        WS_WAIT_I(sm.bar_m2[c & 1], ph_m2, c & 1);   // every product of tile c done
+        WS_WAIT_I(sm.bar_m2[c & 1], ph_m2, c & 1);   // G(c), Y(c), S_c(c) done
         if (c + 2 < nc) {
             load_x(c + 2);
-            load_c(c + 2, c & 1);
             load_b(c + 2, c & 1);
         }
+        WS_WAIT_I(sm.bar_z[c & 1], ph_z, c & 1);     // Zf(c) done: C(c) read
+        if (c + 2 < nc) load_c(c + 2, c & 1);
+    }
+    return true;
+}
+
+// ---- the vector warp ------------------------------------------------------------------
+// The per-tile vectors, up to two tiles ahead of the math warps: cumulative
+// sums of dt A (log2 units) inside the tile, dt, the column factors of the
+// off-diagonal mask blocks and the tile total.  Lane l holds rows 4 l ..
+// 4 l + 3.  Slot c % 3 held tile c - 3, which the math warps last read right
+// after m2(c - 3) and before their mask store of tile c - 2: the vectors of
+// tile c are written once that store is complete everywhere.
+template <int NB, bool EXT>
+__device__ __forceinline__ bool vector_role(Ctx<NB> &cx) {
+    auto &sm = cx.sm;
+    const int lane = threadIdx.x & 31;
+    const int nc = cx.nc, L = cx.L, H = cx.prm.H;
+    const __nv_bfloat16 *dtp = cx.prm.dt + (int64_t(cx.b) * L) * H + cx.h;
+    uint32_t ph_mfull = 0;
+    float raw[4], nxt[4];
+    auto load = [&](int c, float (&r)[4]) {    // raw dt of rows c kQ + 4 lane + k; past L: 0
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int row = c * kQ + 4 * lane + k;
+            r[k] = row < L ? __bfloat162float(dtp[int64_t(row) * H]) : 0.0f;
+        }
+    };
+    load(0, raw);
+    for (int c = 0; c < nc; ++c) {
+        if (c + 1 < nc) load(c + 1, nxt);
+        if (c >= 2) WS_WAIT(sm.bar_mfull, ph_mfull);   // mask store of tile c - 2 complete
+        const int p = c % kSlots;
+        float dv[4], cs[4], run = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float d = 0.0f;
+            if (c * kQ + 4 * lane + k < L) {    // rows past L: no decay, no input
+                d = raw[k];
+                if (EXT) {
+                    d += cx.dbias;
+                    if (cx.prm.dt_softplus) d = softplus_fast(d);
+                    if (cx.prm.dt_limit) d = fminf(fmaxf(d, cx.prm.dt_min), cx.prm.dt_max);
+                }
+            }
+            dv[k] = d;
+            run += d * cx.Ah;
+            cs[k] = run;
+        }
+        float incl = run;      // inclusive scan of the lane totals
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        const float excl = incl - run;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cs[k] += excl;
+        // column factor of row s: exp2(cum at the end of s's 32-row block - cum_s) dt_s
+        const float end = __shfl_sync(0xffffffffu, cs[3], lane | 7);
+        const float tot = __shfl_sync(0xffffffffu, cs[3], 31);
+        reinterpret_cast<float4 *>(sm.cum[p])[lane] = make_float4(cs[0], cs[1], cs[2], cs[3]);
+        reinterpret_cast<float4 *>(sm.dtv[p])[lane] = make_float4(dv[0], dv[1], dv[2], dv[3]);
+        reinterpret_cast<float4 *>(sm.csf[p])[lane] =
+            make_float4(ex2(end - cs[0]) * dv[0], ex2(end - cs[1]) * dv[1], ex2(end - cs[2]) * dv[2],
+                        ex2(end - cs[3]) * dv[3]);
+        if (lane == 0) sm.tot[p] = tot;
+        mbar_arrive(&sm.bar_vec[p]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) raw[k] = nxt[k];
     }
     return true;
 }
 
 // ---- the eight math warps -------------------------------------------------------------
+// Weighted x rows: half hf (32 p) of row s of the x tile scaled by w into the
+// Xw tile (same swizzle, so 16-byte chunks map in place).
+__device__ __forceinline__ void weigh_half(const uint8_t *X, uint8_t *Xw, int s, float w, int hf) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(X + s * 128);
+    uint4 *dst = reinterpret_cast<uint4 *>(Xw + s * 128);
+    const float2 ww = make_float2(w, w);
+    uint4 v[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) v[jj] = src[(4 * hf + jj) ^ (s & 7)];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        const float2 a = fmul2(unpack_bf16(v[jj].x), ww), b = fmul2(unpack_bf16(v[jj].y), ww);
+        const float2 c = fmul2(unpack_bf16(v[jj].z), ww), d = fmul2(unpack_bf16(v[jj].w), ww);
+        dst[(4 * hf + jj) ^ (s & 7)] =
+            make_uint4(pack_bf16(a.x, a.y), pack_bf16(b.x, b.y), pack_bf16(c.x, c.y), pack_bf16(d.x, d.y));
+    }
+}
+
+// a * x + y for packed fp32 pairs.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 x, float2 y) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)),
+          "l"(*reinterpret_cast<unsigned long long *>(&x)),
+          "l"(*reinterpret_cast<unsigned long long *>(&y)));
+    return *reinterpret_cast<float2 *>(&r);
+}
+
 template <int NB, bool EXT>
 __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     constexpr int N = NB * 64;
@@ -999,93 +1102,46 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     const int nc = cx.nc, L = cx.L, b = cx.b, h = cx.h, H = cx.prm.H;
     const uint32_t tmem = cx.tmem;
-    const bool is_state = t < N;        // warp-uniform: N is 64 or 128
+    const bool is_state = q * 32 < N;   // state rows n = t exist (warp-uniform)
     // this warp's mask blocks of row quarter q: sb0 = hf and sb1 = hf + 2
     const bool own0 = hf <= q, own1 = hf + 2 <= q;
-    uint32_t ph_g = 0, ph_m2 = 0, ph_half = 0, ph_all = 0, ph_x = 0;
-    const __nv_bfloat16 *dtp = cx.prm.dt + (int64_t(b) * L) * H + h;
-    auto load_dt = [&](int c) {      // raw dt of row c * kQ + t; rows past L: 0
-        const int r = c * kQ + t;
-        return r < L ? dtp[int64_t(r) * H] : __float2bfloat16(0.0f);
-    };
+    uint32_t ph_g = 0, ph_m2 = 0, ph_z = 0, ph_x = 0, ph_vec = 0;   // ph_m2, ph_z, ph_x, ph_vec: bits
 
-    // Vectors of tile c into slot c % 3 (cumulative sums of dt A in log2
-    // units, dt, the column factors of the off-diagonal mask blocks, the
-    // tile total): rows t from half 0, then every math warp syncs.
-    auto prep = [&](int c, __nv_bfloat16 raw) -> bool {
-        const int p = c % kSlots;
-        if (hf == 0) {
-            float dv = 0.0f;
-            if (c * kQ + t < L) {
-                dv = __bfloat162float(raw);
-                if (EXT) {
-                    dv += cx.dbias;
-                    if (cx.prm.dt_softplus) dv = softplus_fast(dv);
-                    if (cx.prm.dt_limit) dv = fminf(fmaxf(dv, cx.prm.dt_min), cx.prm.dt_max);
-                }
-            }
-            const float dA = dv * cx.Ah;
-            float v = dA;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float n = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += n;
-            }
-            if (lane == 31) sm.wsum[p][q] = v;
-            mbar_arrive(&sm.bar_half);
-            WS_WAIT(sm.bar_half, ph_half);
-            float off = 0.0f, tot = 0.0f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float s = sm.wsum[p][w];
-                off += (w < q) ? s : 0.0f;
-                tot += s;
-            }
-            const float cum = v + off;
-            sm.cum[p][t] = cum;
-            sm.dtv[p][t] = dv;
-            if (t == 0) sm.tot[p] = tot;
-            __syncwarp();
-            // column factors of the off-diagonal blocks (row s | 31 is in this warp)
-            sm.csf[p][t] = ex2(sm.cum[p][t | 31] - cum) * dv;
-        }
-        mbar_arrive(&sm.bar_all);
-        WS_WAIT(sm.bar_all, ph_all);
-        return true;
-    };
     // Weighted x rows of tile c: row s = t, columns of half hf.
     auto weigh = [&](int c) -> bool {
         const int p = c % kSlots, xb = c % kXBufs;
-        WS_WAIT_I(sm.bar_x[xb], ph_x, xb);
         const float w = ex2(sm.tot[p] - sm.cum[p][t]) * sm.dtv[p][t];
-        scale_row(sm.X[xb], sm.Xw[c & 1], t, w, hf);
+        WS_WAIT_I(sm.bar_x[xb], ph_x, xb);
+        weigh_half(sm.X[xb], sm.Xw[c & 1], t, w, hf);
         fence_proxy_async_smem();
         mbar_arrive(&sm.bar_xw[c & 1]);
         return true;
     };
-    // Mask rows t of tile c, this warp's blocks, into registers (bf16 pairs).
+    // Mask rows t of tile c, this warp's blocks, into registers (bf16 pairs);
+    // the weighted rows of tile c are written while the G rows load.
     uint32_t mk[2][16];
-    auto mask = [&](int c) -> bool {
+    auto weigh_and_mask = [&](int c) -> bool {
         const int p = c % kSlots;
+        WS_WAIT_I(sm.bar_vec[p], ph_vec, p);
+        WS_WAIT(sm.bar_g, ph_g);
+        tc_fence_after_sync();
+        uint32_t gr[2][32];
+        if (own0) tmem_ld32_async(tmem + lane_base + kWsG + hf * 32, gr[0]);
+        if (own1) tmem_ld32_async(tmem + lane_base + kWsG + (hf + 2) * 32, gr[1]);
+        if (!weigh(c)) return false;
+        if (own0) {
+            tmem_wait_tie(gr[0]);
+            reg_tie(gr[1]);
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&sm.bar_gfree);         // G may be overwritten now
         const float *cum = sm.cum[p];
         const float *dtv = sm.dtv[p];
         const float cum_t = cum[t];
-        WS_WAIT(sm.bar_g, ph_g);
-        tc_fence_after_sync();
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int sb = hf + 2 * i;
-            const bool own = i == 0 ? own0 : own1;
-            uint32_t gr[32];
-            if (own) {
-                tmem_ld32_async(tmem + lane_base + kWsG + sb * 32, gr);
-                tmem_wait_tie(gr);
-            }
-            if (i == 1) {
-                tc_fence_before_sync();
-                mbar_arrive(&sm.bar_gfree);     // G may be overwritten now
-            }
-            if (!own) continue;
+            if (!(i == 0 ? own0 : own1)) continue;
             if (sb == q) {
                 // diagonal block: direct differences of cumulative sums; the
                 // skip term rides on the diagonal: Y = (M + D_h I) X
@@ -1101,7 +1157,7 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
                     for (int k = 0; k < 4; ++k) {
                         const int s = sb * 32 + 4 * j4 + k;
                         const float w = (s <= t) ? ex2(cum_t - csv[k]) : 0.0f;
-                        float v = __uint_as_float(gr[4 * j4 + k]) * (w * dsv[k]);
+                        float v = __uint_as_float(gr[i][4 * j4 + k]) * (w * dsv[k]);
                         if (s == t) v += cx.Dh;
                         m[k] = v;
                     }
@@ -1116,11 +1172,11 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 f = f4[j4];
-                    const float2 a = fmul2(fmul2(make_float2(__uint_as_float(gr[4 * j4]),
-                                                             __uint_as_float(gr[4 * j4 + 1])),
+                    const float2 a = fmul2(fmul2(make_float2(__uint_as_float(gr[i][4 * j4]),
+                                                             __uint_as_float(gr[i][4 * j4 + 1])),
                                                  make_float2(f.x, f.y)), ee);
-                    const float2 bq = fmul2(fmul2(make_float2(__uint_as_float(gr[4 * j4 + 2]),
-                                                              __uint_as_float(gr[4 * j4 + 3])),
+                    const float2 bq = fmul2(fmul2(make_float2(__uint_as_float(gr[i][4 * j4 + 2]),
+                                                              __uint_as_float(gr[i][4 * j4 + 3])),
                                                   make_float2(f.z, f.w)), ee);
                     mk[i][2 * j4] = pack_bf16(a.x, a.y);
                     mk[i][2 * j4 + 1] = pack_bf16(bq.x, bq.y);
@@ -1147,25 +1203,25 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) zq[j] = __ldg(zp + j);
     };
-    // Output rows t of tile c, columns of half hf: y = Y + e^{cum_t} Zf (Y
-    // already holds D x), out through this warp's staging area in the free
-    // weighted-rows buffer of tile c (32 rows x 16 columns, 2 KB).
-    auto epilogue = [&](int c) {
-        const int p = c % kSlots;
-        const bool has_s = c > 0 || has_h0;
-        const float ef = ex2(sm.cum[p][t]);
-        const uint32_t ycol = (c & 1) ? kWsY1 : kWsY0, zcol = (c & 1) ? kWsZ1 : kWsZ0;
-        uint32_t yv[32], zf[32];
-        tmem_ld32_async(tmem + lane_base + ycol + hf * 32, yv);
-        if (has_s) tmem_ld32_async(tmem + lane_base + zcol + hf * 32, zf);
-        tmem_wait_tie(yv);
-        reg_tie(zf);
+    // Output rows t of tile c, columns of half hf, from the loaded
+    // accumulators: y = Y + e^{cum_t} Zf (Y already holds D x), out through
+    // this warp's staging area (32 rows x 8 columns at a time), so that each
+    // store instruction writes 16 rows x 32 contiguous bytes.
+    float *stg = sm.ystage[warp];
+    auto epilogue = [&](int c, const uint32_t (&yv)[32], const uint32_t (&zf)[32], bool has_s, float ef) {
         float out[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) out[j] = __uint_as_float(yv[j]);
         if (has_s) {
+            const float2 e2 = make_float2(ef, ef);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) out[j] = fmaf(ef, __uint_as_float(zf[j]), out[j]);
+            for (int j = 0; j < 16; ++j) {
+                const float2 r = ffma2(e2, make_float2(__uint_as_float(zf[2 * j]), __uint_as_float(zf[2 * j + 1])),
+                                       make_float2(__uint_as_float(yv[2 * j]), __uint_as_float(yv[2 * j + 1])));
+                out[2 * j] = r.x;
+                out[2 * j + 1] = r.y;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) out[j] = __uint_as_float(yv[j]);
         }
         if (gate && c * kQ + t < L) {   // (rows past L are computed but not stored)
 #pragma unroll
@@ -1179,28 +1235,23 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
                 }
             }
         }
-        // 16 columns at a time through the staging area, so that each store
-        // instruction covers 8 rows x 64 contiguous bytes instead of 32 rows x
-        // 16 bytes.  The 16-byte chunks of a row are XOR-permuted by
-        // (row / 2) % 4: conflict-free in both directions.
-        float *stg = reinterpret_cast<float *>(sm.Xw[c & 1]) + warp * (32 * 16);
+        // Row r's two 16-byte chunks sit at chunk ^ ((r / 4) % 2): conflict-free
+        // for the row-per-lane writes and the two-lanes-per-row reads.
+        const int wsw = (lane >> 2) & 1;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int sw = (lane >> 1) & 3;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                reinterpret_cast<float4 *>(stg + lane * 16)[j ^ sw] =
-                    make_float4(out[16 * hh + 4 * j], out[16 * hh + 4 * j + 1],
-                                out[16 * hh + 4 * j + 2], out[16 * hh + 4 * j + 3]);
+        for (int r8 = 0; r8 < 4; ++r8) {
+            float4 *row = reinterpret_cast<float4 *>(stg + lane * 8);
+            row[0 ^ wsw] = make_float4(out[8 * r8], out[8 * r8 + 1], out[8 * r8 + 2], out[8 * r8 + 3]);
+            row[1 ^ wsw] = make_float4(out[8 * r8 + 4], out[8 * r8 + 5], out[8 * r8 + 6], out[8 * r8 + 7]);
             __syncwarp();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int rr = 8 * k + (lane >> 2), ch = lane & 3;
-                const float4 v = reinterpret_cast<const float4 *>(stg + rr * 16)[ch ^ ((rr >> 1) & 3)];
+            for (int k = 0; k < 2; ++k) {
+                const int rr = 16 * k + (lane >> 1), ch = lane & 1;
+                const float4 v = reinterpret_cast<const float4 *>(stg + rr * 8)[ch ^ ((rr >> 2) & 1)];
                 const int trow = c * kQ + q * 32 + rr;
                 if (trow < L)
                     *reinterpret_cast<float4 *>(cx.prm.y + ((size_t(b) * L + trow) * H + h) * kP +
-                                                hf * 32 + hh * 16 + ch * 4) = v;
+                                                hf * 32 + r8 * 8 + ch * 4) = v;
             }
             __syncwarp();
         }
@@ -1215,14 +1266,6 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
         if (!own1) tmem_st_32x32b_x16(tmem + lane_base + kWsM + (hf + 2) * 16, zero);
         tmem_wait_st();
     }
-    __nv_bfloat16 raw0 = __float2bfloat16(0.0f), raw1 = raw0, raw_next = raw0;
-    if (hf == 0) {
-        raw0 = load_dt(0);
-        if (nc > 1) raw1 = load_dt(1);
-        if (nc > 2) raw_next = load_dt(2);
-    }
-    if (!prep(0, raw0)) return false;
-    if (nc > 1 && !prep(1, raw1)) return false;
     float st[32];   // state rows n = t, columns p of half hf (fp32)
 #pragma unroll
     for (int j = 0; j < 32; ++j) st[j] = 0.0f;
@@ -1234,41 +1277,45 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     }
     fence_proxy_async_smem();
     mbar_arrive(&sm.bar_st);
-    if (!weigh(0)) return false;
-    prefetch_gate(0);
-    if (!mask(0)) return false;
+    if (!weigh_and_mask(0)) return false;
     mask_store();
+    prefetch_gate(0);
 
     for (int c = 0; c < nc; ++c) {
         const bool more = c + 1 < nc;
-        if (more) {
-            if (!weigh(c + 1)) return false;
-            if (!mask(c + 1)) return false;
-        }
+        if (more && !weigh_and_mask(c + 1)) return false;
         WS_WAIT_I(sm.bar_m2[c & 1], ph_m2, c & 1);   // every product of tile c done
+        tc_fence_after_sync();
+        const int p = c % kSlots;
+        const float e = ex2(sm.tot[p]), ef = ex2(sm.cum[p][t]);
+        const bool has_s = c > 0 || has_h0;
+        // the chunk state and Y of tile c in one round trip
+        uint32_t sv[32], yv[32], zf[32];
+        if (is_state) tmem_ld32_async(tmem + lane_base + kWsS + hf * 32, sv);
+        tmem_ld32_async(tmem + lane_base + ((c & 1) ? kWsY1 : kWsY0) + hf * 32, yv);
+        tmem_wait_tie(yv);
+        reg_tie(sv);
+        // S_c(c) is in registers: Y(c + 1) and S_c(c + 1) may start
+        if (more) mask_store();
+        WS_WAIT_I(sm.bar_z[c & 1], ph_z, c & 1);    // Zf(c) done: the state image is free
         tc_fence_after_sync();
         // state passing: rows n = t of S_in, columns of half hf
         if (is_state) {
-            uint32_t v[32];
-            tmem_ld32_async(tmem + lane_base + kWsS + hf * 32, v);
-            tmem_wait_tie(v);
-            const float e = ex2(sm.tot[c % kSlots]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) st[j] = fmaf(e, st[j], __uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j) st[j] = fmaf(e, st[j], __uint_as_float(sv[j]));
             if (more) put_state_half(&sm.S[0][0], t, hf, st);
         }
         if (more) {
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(&sm.bar_st);            // Zf(c + 1) can start
-            mask_store();                       // Y(c + 1), S_c(c + 1) can start
         }
-        epilogue(c);
+        if (has_s) {
+            tmem_ld32_async(tmem + lane_base + ((c & 1) ? kWsZ1 : kWsZ0) + hf * 32, zf);
+            tmem_wait_tie(zf);
+        }
+        epilogue(c, yv, zf, has_s, ef);
         if (more) prefetch_gate(c + 1);
-        if (c + 2 < nc) {
-            if (!prep(c + 2, raw_next)) return false;
-            if (hf == 0 && c + 3 < nc) raw_next = load_dt(c + 3);
-        }
     }
     if (EXT && cx.prm.h_final != nullptr && is_state) {
         float *dst = cx.prm.h_final + size_t(cx.bh) * kP * N + size_t(hf * 32) * N + t;
@@ -1306,8 +1353,9 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         mbar_init(&sm.bar_xw[0], kMath);
         mbar_init(&sm.bar_xw[1], kMath);
         mbar_init(&sm.bar_st, kMath);
-        mbar_init(&sm.bar_half, kMath / 2);
-        mbar_init(&sm.bar_all, kMath);
+        mbar_init(&sm.bar_z[0], 1);
+        mbar_init(&sm.bar_z[1], 1);
+        for (int i = 0; i < kSlots; ++i) mbar_init(&sm.bar_vec[i], 32);
         mbar_fence_init();
         prefetch_tmap(&tmC);
         prefetch_tmap(&tmB);
@@ -1344,6 +1392,7 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
         if (tid == 256) ok = issuer_role<NB, EXT>(cx, has_h0);
         if (tid == 288) ok = loader_role<NB, EXT>(cx, &tmC, &tmB, &tmX);
+        if (warp == 10) ok = vector_role<NB, EXT>(cx);
     }
     if (!ok) {
         abort_flag = 1;
