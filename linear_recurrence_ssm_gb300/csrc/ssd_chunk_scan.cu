@@ -698,8 +698,9 @@ done:
 // quarter q = w % 4 (tile rows / state rows 32 q .. 32 q + 31) and split the
 // work of those rows by column halves (hf = w / 4):
 //   the decay mask: row quarter q has causal 32 x 32 blocks sb = 0..q; the
-//     warp takes the blocks with sb % 2 == hf (at most two, so the causal
-//     triangle's work is spread evenly instead of four blocks on one warp);
+//     half-0 warp computes the diagonal block (direct exponentials), the
+//     half-1 warp the blocks below it (products of two factors, cheaper), so
+//     no warp has more than about one diagonal block's work;
 //   the weighted x rows, the fp32 state update and its bf16 image, the
 //     output rows y = Y + e^{cum} Zf: columns 32 hf .. 32 hf + 31.
 // Per tile c the warps (1) weigh the x rows of tile c + 1 and compute its
@@ -712,8 +713,9 @@ done:
 // free.  The mask M lives in tensor memory and is the A operand of Y = M X;
 // D x rides on its diagonal.  Y and Zf have two accumulators (by tile
 // parity) so the products of tile c + 1 run while the outputs of tile c are
-// read; the weighted rows Xw are double-buffered, and the buffer of tile c
-// is free once S_c(c) has run, so it stages tile c's output rows.
+// read; the weighted rows Xw are double-buffered, and once S_c(c) has run
+// each warp stages its output rows of tile c in its own part of tile c's
+// buffer (the part it writes again when it weighs tile c + 2).
 namespace ws {
 
 constexpr int kMath = 256;             // math threads (warps 0..7)
@@ -741,9 +743,8 @@ struct __align__(1024) Smem {
     uint8_t C[2][NB][kTile];    // C tiles (double buffered), K-major rows t
     uint8_t B[2][2][kTile];     // B tiles (double buffered); region 1 zero when N = 64
     uint8_t X[kXBufs][kTile];   // x tiles (MN-major B operand of Y), tile c in c % 2
-    uint8_t Xw[2][kTile];       // weighted x rows of tile c in c % 2
+    uint8_t Xw[2][kTile];       // weighted x rows of tile c in c % 2; then tile c's y staging
     uint8_t S[NB][kStateRegion];    // entering state image
-    float ystage[8][32 * 8];        // per math warp: 32 rows x 8 columns of y on their way out
     float cum[kSlots][kQ];
     float dtv[kSlots][kQ];
     float csf[kSlots][kQ];
@@ -897,6 +898,7 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
     //                 its end is signalled on its own barrier, bar_z.
     int y_next = 0, g_next = 1, z_next = 1;
     uint64_t t_idle = 0;
+    uint32_t idle_passes = 0;
     while (y_next < nc || z_next < nc) {
         bool progress = false;
         if (z_next < nc && g_next > z_next && mbar_test_wait(&sm.bar_st, ph_st)) {
@@ -935,9 +937,10 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
         }
         if (progress) {
             t_idle = 0;
-        } else {
-            // (reading the clock on every idle pass also paces the polls,
-            // which otherwise take issue slots from the math warps)
+            idle_passes = 0;
+        } else if ((++idle_passes & 255u) == 0) {
+            // the wall clock is read only now and then: it is slow to read,
+            // and a slow poll answers late to the math warps' hand-offs
             const uint64_t now = globaltimer_ns();
             if (t_idle == 0) t_idle = now;
             else if (now - t_idle > kWaitLimitNs || *cx.abort) return false;
@@ -1103,8 +1106,8 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     const int nc = cx.nc, L = cx.L, b = cx.b, h = cx.h, H = cx.prm.H;
     const uint32_t tmem = cx.tmem;
     const bool is_state = q * 32 < N;   // state rows n = t exist (warp-uniform)
-    // this warp's mask blocks of row quarter q: sb0 = hf and sb1 = hf + 2
-    const bool own0 = hf <= q, own1 = hf + 2 <= q;
+    // mask blocks of row quarter q: half 0 forms the diagonal block sb = q,
+    // half 1 the blocks sb = 0 .. q - 1 below it
     uint32_t ph_g = 0, ph_m2 = 0, ph_z = 0, ph_x = 0, ph_vec = 0;   // ph_m2, ph_z, ph_x, ph_vec: bits
 
     // Weighted x rows of tile c: row s = t, columns of half hf.
@@ -1119,68 +1122,87 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     };
     // Mask rows t of tile c, this warp's blocks, into registers (bf16 pairs);
     // the weighted rows of tile c are written while the G rows load.
-    uint32_t mk[2][16];
+    uint32_t mk[3][16];
     auto weigh_and_mask = [&](int c) -> bool {
         const int p = c % kSlots;
         WS_WAIT_I(sm.bar_vec[p], ph_vec, p);
         WS_WAIT(sm.bar_g, ph_g);
         tc_fence_after_sync();
-        uint32_t gr[2][32];
-        if (own0) tmem_ld32_async(tmem + lane_base + kWsG + hf * 32, gr[0]);
-        if (own1) tmem_ld32_async(tmem + lane_base + kWsG + (hf + 2) * 32, gr[1]);
-        if (!weigh(c)) return false;
-        if (own0) {
-            tmem_wait_tie(gr[0]);
-            reg_tie(gr[1]);
-        }
-        tc_fence_before_sync();
-        mbar_arrive(&sm.bar_gfree);         // G may be overwritten now
         const float *cum = sm.cum[p];
         const float *dtv = sm.dtv[p];
-        const float cum_t = cum[t];
+        const float *csf = sm.csf[p];
+        if (hf == 0) {
+            uint32_t gr[32];
+            tmem_ld32_async(tmem + lane_base + kWsG + q * 32, gr);
+            if (!weigh(c)) return false;
+            tmem_wait_tie(gr);
+            tc_fence_before_sync();
+            mbar_arrive(&sm.bar_gfree);     // G may be overwritten now
+            // diagonal block: direct differences of cumulative sums; the
+            // skip term rides on the diagonal: Y = (M + D_h I) X
+            const float cum_t = cum[t];
+            const float4 *c4 = reinterpret_cast<const float4 *>(cum + q * 32);
+            const float4 *d4 = reinterpret_cast<const float4 *>(dtv + q * 32);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int sb = hf + 2 * i;
-            if (!(i == 0 ? own0 : own1)) continue;
-            if (sb == q) {
-                // diagonal block: direct differences of cumulative sums; the
-                // skip term rides on the diagonal: Y = (M + D_h I) X
-                const float4 *c4 = reinterpret_cast<const float4 *>(cum + sb * 32);
-                const float4 *d4 = reinterpret_cast<const float4 *>(dtv + sb * 32);
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 cs = c4[j4], ds = d4[j4];
+                const float csv[4] = {cs.x, cs.y, cs.z, cs.w};
+                const float dsv[4] = {ds.x, ds.y, ds.z, ds.w};
+                float m[4];
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 cs = c4[j4], ds = d4[j4];
-                    const float csv[4] = {cs.x, cs.y, cs.z, cs.w};
-                    const float dsv[4] = {ds.x, ds.y, ds.z, ds.w};
-                    float m[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int s = sb * 32 + 4 * j4 + k;
-                        const float w = (s <= t) ? ex2(cum_t - csv[k]) : 0.0f;
-                        float v = __uint_as_float(gr[i][4 * j4 + k]) * (w * dsv[k]);
-                        if (s == t) v += cx.Dh;
-                        m[k] = v;
-                    }
-                    mk[i][2 * j4] = pack_bf16(m[0], m[1]);
-                    mk[i][2 * j4 + 1] = pack_bf16(m[2], m[3]);
+                for (int k = 0; k < 4; ++k) {
+                    const int j = 4 * j4 + k;
+                    const float w = (j <= lane) ? ex2(cum_t - csv[k]) : 0.0f;
+                    float v = __uint_as_float(gr[j]) * (w * dsv[k]);
+                    if (j == lane) v += cx.Dh;
+                    m[k] = v;
                 }
-            } else {
-                // below the diagonal: G * (row factor) * (column factor), both <= 1
-                const float e = ex2(cum_t - cum[sb * 32 + 31]);
+                mk[0][2 * j4] = pack_bf16(m[0], m[1]);
+                mk[0][2 * j4 + 1] = pack_bf16(m[2], m[3]);
+            }
+        } else {
+            // blocks below the diagonal: G * (row factor) * (column factor),
+            // both <= 1; the G rows of block i + 1 load while block i is formed
+            const float cum_t = cum[t];
+            auto offdiag = [&](int i, const uint32_t (&g)[32]) {
+                const float e = ex2(cum_t - cum[i * 32 + 31]);
                 const float2 ee = make_float2(e, e);
-                const float4 *f4 = reinterpret_cast<const float4 *>(sm.csf[p] + sb * 32);
+                const float4 *f4 = reinterpret_cast<const float4 *>(csf + i * 32);
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const float4 f = f4[j4];
-                    const float2 a = fmul2(fmul2(make_float2(__uint_as_float(gr[i][4 * j4]),
-                                                             __uint_as_float(gr[i][4 * j4 + 1])),
+                    const float2 a = fmul2(fmul2(make_float2(__uint_as_float(g[4 * j4]), __uint_as_float(g[4 * j4 + 1])),
                                                  make_float2(f.x, f.y)), ee);
-                    const float2 bq = fmul2(fmul2(make_float2(__uint_as_float(gr[i][4 * j4 + 2]),
-                                                              __uint_as_float(gr[i][4 * j4 + 3])),
+                    const float2 bq = fmul2(fmul2(make_float2(__uint_as_float(g[4 * j4 + 2]), __uint_as_float(g[4 * j4 + 3])),
                                                   make_float2(f.z, f.w)), ee);
                     mk[i][2 * j4] = pack_bf16(a.x, a.y);
                     mk[i][2 * j4 + 1] = pack_bf16(bq.x, bq.y);
                 }
+            };
+            uint32_t ga[32], gb[32];
+            if (q >= 1) tmem_ld32_async(tmem + lane_base + kWsG, ga);
+            if (!weigh(c)) return false;
+            if (q >= 1) tmem_wait_tie(ga);
+            if (q >= 2) tmem_ld32_async(tmem + lane_base + kWsG + 32, gb);
+            if (q < 2) {
+                tc_fence_before_sync();
+                mbar_arrive(&sm.bar_gfree);
+            }
+            if (q >= 1) offdiag(0, ga);
+            if (q >= 2) {
+                tmem_wait_tie(gb);
+                if (q >= 3) tmem_ld32_async(tmem + lane_base + kWsG + 64, ga);
+                if (q < 3) {
+                    tc_fence_before_sync();
+                    mbar_arrive(&sm.bar_gfree);
+                }
+                offdiag(1, gb);
+            }
+            if (q >= 3) {
+                tmem_wait_tie(ga);
+                tc_fence_before_sync();
+                mbar_arrive(&sm.bar_gfree);
+                offdiag(2, ga);
             }
         }
         return true;
@@ -1188,8 +1210,13 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     // Store this warp's mask blocks into tensor memory (after Y of the
     // previous tile has read the mask) and hand the mask to the issuer.
     auto mask_store = [&]() {
-        if (own0) tmem_st_32x32b_x16(tmem + lane_base + kWsM + hf * 16, mk[0]);
-        if (own1) tmem_st_32x32b_x16(tmem + lane_base + kWsM + (hf + 2) * 16, mk[1]);
+        if (hf == 0) {
+            tmem_st_32x32b_x16(tmem + lane_base + kWsM + q * 16, mk[0]);
+        } else {
+            if (q >= 1) tmem_st_32x32b_x16(tmem + lane_base + kWsM, mk[0]);
+            if (q >= 2) tmem_st_32x32b_x16(tmem + lane_base + kWsM + 16, mk[1]);
+            if (q >= 3) tmem_st_32x32b_x16(tmem + lane_base + kWsM + 32, mk[2]);
+        }
         tmem_wait_st();
         tc_fence_before_sync();
         mbar_arrive(&sm.bar_mfull);
@@ -1205,9 +1232,10 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     };
     // Output rows t of tile c, columns of half hf, from the loaded
     // accumulators: y = Y + e^{cum_t} Zf (Y already holds D x), out through
-    // this warp's staging area (32 rows x 8 columns at a time), so that each
-    // store instruction writes 16 rows x 32 contiguous bytes.
-    float *stg = sm.ystage[warp];
+    // this warp's part of tile c's weighted-rows buffer (rows 32 q .. 32 q +
+    // 31, the 16-byte chunks 4 hf .. 4 hf + 3 of each, swizzled as the tile:
+    // 32 rows x 16 columns at a time), so that each store instruction writes
+    // 8 rows x 64 contiguous bytes.
     auto epilogue = [&](int c, const uint32_t (&yv)[32], const uint32_t (&zf)[32], bool has_s, float ef) {
         float out[32];
         if (has_s) {
@@ -1235,35 +1263,36 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
                 }
             }
         }
-        // Row r's two 16-byte chunks sit at chunk ^ ((r / 4) % 2): conflict-free
-        // for the row-per-lane writes and the two-lanes-per-row reads.
-        const int wsw = (lane >> 2) & 1;
+        uint8_t *stg = sm.Xw[c & 1] + q * 32 * 128;
 #pragma unroll
-        for (int r8 = 0; r8 < 4; ++r8) {
-            float4 *row = reinterpret_cast<float4 *>(stg + lane * 8);
-            row[0 ^ wsw] = make_float4(out[8 * r8], out[8 * r8 + 1], out[8 * r8 + 2], out[8 * r8 + 3]);
-            row[1 ^ wsw] = make_float4(out[8 * r8 + 4], out[8 * r8 + 5], out[8 * r8 + 6], out[8 * r8 + 7]);
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<float4 *>(stg + lane * 128 + (((4 * hf + j) ^ (lane & 7)) << 4)) =
+                    make_float4(out[16 * hh + 4 * j], out[16 * hh + 4 * j + 1], out[16 * hh + 4 * j + 2],
+                                out[16 * hh + 4 * j + 3]);
             __syncwarp();
+            // lanes 4 i .. 4 i + 3 read row 4 i + k (i = 0..7): the rows one
+            // instruction reads differ in bit 2, so their chunks do not collide
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int rr = 16 * k + (lane >> 1), ch = lane & 1;
-                const float4 v = reinterpret_cast<const float4 *>(stg + rr * 8)[ch ^ ((rr >> 2) & 1)];
+            for (int k = 0; k < 4; ++k) {
+                const int rr = 4 * (lane >> 2) + k, ch = lane & 3;
+                const float4 v = *reinterpret_cast<const float4 *>(stg + rr * 128 + (((4 * hf + ch) ^ (rr & 7)) << 4));
                 const int trow = c * kQ + q * 32 + rr;
                 if (trow < L)
                     *reinterpret_cast<float4 *>(cx.prm.y + ((size_t(b) * L + trow) * H + h) * kP +
-                                                hf * 32 + r8 * 8 + ch * 4) = v;
+                                                hf * 32 + hh * 16 + ch * 4) = v;
             }
             __syncwarp();
         }
     };
 
     // ---- prologue -------------------------------------------------------------------
-    {   // the mask blocks above the diagonal stay zero for every tile
+    if (hf == 0) {   // the mask blocks above the diagonal stay zero for every tile
         uint32_t zero[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) zero[j] = 0u;
-        if (!own0) tmem_st_32x32b_x16(tmem + lane_base + kWsM + hf * 16, zero);
-        if (!own1) tmem_st_32x32b_x16(tmem + lane_base + kWsM + (hf + 2) * 16, zero);
+        for (int sb = q + 1; sb < 4; ++sb) tmem_st_32x32b_x16(tmem + lane_base + kWsM + sb * 16, zero);
         tmem_wait_st();
     }
     float st[32];   // state rows n = t, columns p of half hf (fp32)
