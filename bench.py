@@ -195,11 +195,16 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def kernels_per_call(w, lrs) -> int:
-    """Kernels one library call launches: the chunked scan is one kernel; the
+    """Kernels one library call launches: the unidirectional chunked scan is
+    one kernel, the bidirectional one two (chunk states, then outputs) for
+    sequences of at most four 128-row tiles with N = 64 and one otherwise; the
     diagonal scan is one, or two when the library splits the sequence into
     time segments (segment pass + carry pass)."""
     if w.kind != "diag":
-        return 1
+        s = w.shape
+        short_bidir = (s["bidirectional"] and w.dtype == "bf16" and s["N"] == 64 and s["P"] == 64
+                       and (s["L"] + 127) // 128 <= 4)
+        return 2 if short_bidir else 1
     s = w.shape
     _, _, k = lrs.ssm_scan_fwd_plan(s["Bs"], s["L"], s["ED"], s["N"], w.dtype == "bf16")
     return 2 if k > 1 else 1

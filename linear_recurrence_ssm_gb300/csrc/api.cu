@@ -45,6 +45,9 @@ cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *
                    const float *D, float *y, int64_t Bs, int64_t L, int64_t H, int64_t P,
                    int64_t N, bool bidir, const ScanOpts *opt, cudaStream_t st);
 }
+namespace bidir {
+cudaError_t take_device_error(unsigned int *out);
+}
 namespace ssd {
 cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
                    const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
@@ -366,9 +369,10 @@ ssm_status_t ssm_check_device_errors(void *stream) {
     ssm_status_t s = current_device(&dev);
     if (s != SSM_OK) return s;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSM_ERR_CUDA;
-    unsigned int flag = 0;
+    unsigned int flag = 0, flag_bi = 0;
     if (ssm::ssd::take_device_error(&flag) != cudaSuccess) return SSM_ERR_CUDA;
-    return flag ? SSM_ERR_DEVICE_TIMEOUT : SSM_OK;
+    if (ssm::bidir::take_device_error(&flag_bi) != cudaSuccess) return SSM_ERR_CUDA;
+    return (flag | flag_bi) ? SSM_ERR_DEVICE_TIMEOUT : SSM_OK;
 }
 
 ssm_status_t ssm_selftest_wait_timeout(void *stream) {

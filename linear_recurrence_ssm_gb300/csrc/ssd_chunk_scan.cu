@@ -41,6 +41,13 @@
 #include "tc_ptx.cuh"
 
 namespace ssm {
+namespace bidir {
+bool supported(int64_t L, int64_t P, int64_t N);
+cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float *A_head,
+                   const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
+                   int64_t Bs, int64_t L, int64_t H, int num_sms, const ScanOpts *opt,
+                   cudaStream_t stream);
+}  // namespace bidir
 namespace ssd {
 
 using namespace ssm::tc;
@@ -1577,9 +1584,11 @@ cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float 
                    const __nv_bfloat16 *Bm, const __nv_bfloat16 *Cm, const float *D, float *y,
                    int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N, int64_t chunk,
                    bool bidirectional, int num_sms, cudaStream_t stream, const Options *opt) {
-    (void)num_sms;
     (void)chunk;
     if (P != kP) return cudaErrorNotSupported;
+    // short bidirectional sequences: independent per-tile passes (ssd_bidir.cu)
+    if (bidirectional && bidir::supported(L, P, N))
+        return bidir::launch(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, num_sms, opt, stream);
     if (N == 64)
         return launch_nb<1>(x, dt, A_head, Bm, Cm, D, y, Bs, L, H, bidirectional, stream, nullptr, opt);
     if (N == 128)
