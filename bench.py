@@ -99,13 +99,24 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 
 def kernel_source_hash(kind: str) -> str:
+    """Hash of the sources of the kernels a workload kind runs: "diag", "ssd"
+    (the unidirectional tensor-core kernel) or "bissd" (the short-sequence
+    bidirectional passes)."""
     csrc = os.path.join(ROOT, "linear_recurrence_ssm_gb300", "csrc")
-    srcs = ["diag_scan.cuh", "diag_scan.cu"] if kind == "diag" else ["ssd_chunk_scan.cu", "tc_ptx.cuh"]
+    srcs = {"diag": ["diag_scan.cuh", "diag_scan.cu"],
+            "ssd": ["ssd_chunk_scan.cu", "tc_ptx.cuh"],
+            "bissd": ["ssd_bidir.cu", "tc_ptx.cuh"]}[kind]
     h = hashlib.sha256()
     for p in [os.path.join(csrc, f) for f in srcs] + [os.path.join(csrc, "ssm_common.cuh")]:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def source_kind(w) -> str:
+    if w.kind == "diag":
+        return "diag"
+    return "bissd" if kernels_per_call(w, None) == 2 else "ssd"
 
 
 def ncu_traffic(workload: str, kind: str):
@@ -371,7 +382,7 @@ def roofline_of(w, mode: str, per_launch_s: float, peaks: dict, with_traffic: bo
         return {
             "bound": "alu", "achieved": round(achieved, 4), "peak": round(alu_peak, 4),
             "unit": "T element-steps/s", "frac": round(achieved / alu_peak, 4),
-            "traffic": ncu_traffic(w.name, w.kind) if (with_traffic and mode == "fwd") else None,
+            "traffic": ncu_traffic(w.name, source_kind(w)) if (with_traffic and mode == "fwd") else None,
             "peak_source": "derived: 152 SMs x 32 ex2/clk/SM (MUFU) x sm_max_mhz of "
                            "MEASURED_PEAKS.json; 1 ex2 + 4 fp32 ops per element-step"
                            + ("" if mode != "bwd" else
@@ -385,7 +396,7 @@ def roofline_of(w, mode: str, per_launch_s: float, peaks: dict, with_traffic: bo
     return {
         "bound": "hbm", "achieved": round(hbm_achieved, 1), "peak": peaks["hbm_gbs"],
         "unit": "GB/s", "frac": round(hbm_achieved / peaks["hbm_gbs"], 4),
-        "traffic": ncu_traffic(w.name, w.kind) if (with_traffic and mode == "fwd") else None,
+        "traffic": ncu_traffic(w.name, source_kind(w)) if (with_traffic and mode == "fwd") else None,
         "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
         "algorithmic_bytes_per_launch": call_bytes,
         "launch_us": round(per_launch_s * 1e6, 3),

@@ -272,12 +272,16 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
             }
             const float dlx = dl * xv;
             if constexpr (SPLIT) {
+                // (rows past the segment hold delta = 0: they leave the sum
+                // unchanged and cannot make the minimum negative)
                 dsum += dl;
-                dmin = (t < tl) ? fminf(dmin, dl) : dmin;
+                dmin = fminf(dmin, dl);
             }
             // Products with the step's delta and delta*x are formed two states
             // at a time (packed fp32x2 multiply: one issue slot for two), the
-            // state update and the readout as scalar fused multiply-adds.
+            // state update and the readout as scalar fused multiply-adds
+            // (packed fused multiply-adds measured slower here: they hold the
+            // FMA pipe longer than two scalar ones).
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             const float2 dl2 = make_float2(dl, dl), dlx2 = make_float2(dlx, dlx);
 #pragma unroll

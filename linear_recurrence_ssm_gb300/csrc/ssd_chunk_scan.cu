@@ -766,7 +766,7 @@ struct __align__(1024) Smem {
     uint64_t bar_g, bar_m2[2], bar_z[2];
     uint64_t bar_gfree, bar_mfull, bar_xw[2], bar_st;
     uint64_t bar_vec[kSlots];                        // vectors of a slot written
-    uint64_t bar_fin;                                // error path
+    uint64_t bar_fin[2];                             // error path (one per issuing thread)
     uint32_t tmem_base;
 };
 
@@ -840,19 +840,9 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
     const uint32_t tmem = cx.tmem;
     constexpr uint32_t idG = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idZ = idesc_bf16_f32(128, 64, false, true);
-    constexpr uint32_t idY = idesc_bf16_f32(128, 64, false, true);
-    constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);
-    uint32_t ph_c = 0, ph_b = 0, ph_x = 0;    // phase bits, one per buffer
-    uint32_t ph_gfree = 0, ph_mfull = 0, ph_xw = 0, ph_st = 0;   // ph_xw: one bit per parity
+    uint32_t ph_c = 0, ph_b = 0;              // phase bits, one per buffer
+    uint32_t ph_gfree = 0, ph_st = 0;
 
-    // S_c^T = B^T (w x): A = B tile read MN-major (128 n rows), B = the weighted x rows.
-    auto issue_s = [&](int c) {
-        const uint32_t sB = smem_addr(sm.B[c & 1]), sXw = smem_addr(sm.Xw[c & 1]);
-#pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk)
-            mma_bf16_ss(tmem + kWsS, smem_desc(sB + kk * 2048, kTile, 1024, kSwizzle128B),
-                        smem_desc(sXw + kk * 2048, kTile, 1024, kSwizzle128B), idS, kk > 0);
-    };
     auto issue_g = [&](int buf) {
         const uint32_t sC = smem_addr(sm.C[buf]), sB = smem_addr(sm.B[buf]);
 #pragma unroll
@@ -872,17 +862,6 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
                         smem_desc(sS + kk * 2048, kTile, 1024, kSwizzle128B), idZ, kk > 0);
         }
     };
-    // Y = M X: A = the mask in tensor memory (row t, 8 columns = 16 s per
-    // K step), B = the x tile (MN-major: rows s, 64 p).
-    auto issue_y = [&](int c) {
-        const uint32_t sX = smem_addr(sm.X[c % kXBufs]);
-        const uint32_t dcol = (c & 1) ? kWsY1 : kWsY0;
-#pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk)
-            mma_bf16_ts(tmem + dcol, tmem + kWsM + kk * 8,
-                        smem_desc(sX + kk * 2048, kTile, 1024, kSwizzle128B), idY, kk > 0);
-    };
-
     WS_WAIT_I(sm.bar_c[0], ph_c, 0);
     WS_WAIT_I(sm.bar_b[0], ph_b, 0);
     tc_fence_after_sync();
@@ -894,19 +873,16 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
         issue_z(0);
     }
     mma_commit(&sm.bar_z[0]);
-    // Three streams of products, each issued as soon as its inputs are ready
+    // Two streams of products, each issued as soon as its inputs are ready
     // (non-blocking polls, so that a late input of one stream does not hold
-    // up another):
-    //   Y(c), S_c(c): mask(c) stored, weighted rows(c) written, x(c) landed,
-    //                 and G(c) issued before them (so the end of Y(c), S_c(c)
-    //                 also means the end of G(c));
+    // up the other); Y(c) and S_c(c) are issued by another thread:
     //   G(c):         G(c - 1) read by the math warps, C(c) and B(c) landed;
     //   Zf(c):        state image of tile c written (C(c) landed: G(c) issued);
     //                 its end is signalled on its own barrier, bar_z.
-    int y_next = 0, g_next = 1, z_next = 1;
+    int g_next = 1, z_next = 1;
     uint64_t t_idle = 0;
     uint32_t idle_passes = 0;
-    while (y_next < nc || z_next < nc) {
+    while (g_next < nc || z_next < nc) {
         bool progress = false;
         if (z_next < nc && g_next > z_next && mbar_test_wait(&sm.bar_st, ph_st)) {
             ph_st ^= 1u;
@@ -914,20 +890,6 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
             issue_z(z_next & 1);
             mma_commit(&sm.bar_z[z_next & 1]);
             ++z_next;
-            progress = true;
-        }
-        const int xb = y_next % kXBufs, yp = y_next & 1;
-        if (g_next > y_next && mbar_test_wait(&sm.bar_mfull, ph_mfull) &&
-            mbar_test_wait(&sm.bar_xw[yp], (ph_xw >> yp) & 1u) &&
-            mbar_test_wait(&sm.bar_x[xb], (ph_x >> xb) & 1u)) {
-            ph_mfull ^= 1u;
-            ph_xw ^= 1u << yp;
-            ph_x ^= 1u << xb;
-            tc_fence_after_sync();
-            issue_y(y_next);
-            issue_s(y_next);
-            mma_commit(&sm.bar_m2[yp]);
-            ++y_next;
             progress = true;
         }
         if (g_next < nc && mbar_test_wait(&sm.bar_gfree, ph_gfree) &&
@@ -952,6 +914,46 @@ __device__ __forceinline__ bool issuer_role(Ctx<NB> &cx, bool has_h0) {
             if (t_idle == 0) t_idle = now;
             else if (now - t_idle > kWaitLimitNs || *cx.abort) return false;
         }
+    }
+    return true;
+}
+
+// ---- the thread issuing Y and S_c ---------------------------------------------------------
+// Y(c), S_c(c) once mask(c) is stored, the weighted rows of tile c are
+// written and x(c) has landed.  The math warps store mask(c) after reading
+// G(c), so G(c) has ended by then, and the end of Y(c), S_c(c) also means
+// the end of G(c).  (A thread of its own: the mask hand-off is on the
+// per-tile chain, and a thread that also polls the other streams answers
+// it late.)
+template <int NB, bool EXT>
+__device__ __forceinline__ bool issuer_ys_role(Ctx<NB> &cx) {
+    auto &sm = cx.sm;
+    const int nc = cx.nc;
+    const uint32_t tmem = cx.tmem;
+    constexpr uint32_t idY = idesc_bf16_f32(128, 64, false, true);
+    constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);
+    uint32_t ph_mfull = 0, ph_xw = 0, ph_x = 0;   // ph_xw, ph_x: one bit per buffer
+    for (int c = 0; c < nc; ++c) {
+        const int xb = c % kXBufs, yp = c & 1;
+        WS_WAIT(sm.bar_mfull, ph_mfull);
+        WS_WAIT_I(sm.bar_xw[yp], ph_xw, yp);
+        WS_WAIT_I(sm.bar_x[xb], ph_x, xb);
+        tc_fence_after_sync();
+        // Y = M X: A = the mask in tensor memory (row t, 8 columns = 16 s per
+        // K step), B = the x tile (MN-major: rows s, 64 p)
+        const uint32_t sX = smem_addr(sm.X[xb]);
+        const uint32_t dcol = (c & 1) ? kWsY1 : kWsY0;
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk)
+            mma_bf16_ts(tmem + dcol, tmem + kWsM + kk * 8,
+                        smem_desc(sX + kk * 2048, kTile, 1024, kSwizzle128B), idY, kk > 0);
+        // S_c^T = B^T (w x): A = B tile read MN-major (128 n rows), B = the weighted x rows
+        const uint32_t sB = smem_addr(sm.B[c & 1]), sXw = smem_addr(sm.Xw[c & 1]);
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk)
+            mma_bf16_ss(tmem + kWsS, smem_desc(sB + kk * 2048, kTile, 1024, kSwizzle128B),
+                        smem_desc(sXw + kk * 2048, kTile, 1024, kSwizzle128B), idS, kk > 0);
+        mma_commit(&sm.bar_m2[yp]);
     }
     return true;
 }
@@ -1383,7 +1385,8 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         mbar_init(&sm.bar_g, 1);
         mbar_init(&sm.bar_m2[0], 1);
         mbar_init(&sm.bar_m2[1], 1);
-        mbar_init(&sm.bar_fin, 1);
+        mbar_init(&sm.bar_fin[0], 1);
+        mbar_init(&sm.bar_fin[1], 1);
         mbar_init(&sm.bar_gfree, kMath);
         mbar_init(&sm.bar_mfull, kMath);
         mbar_init(&sm.bar_xw[0], kMath);
@@ -1429,17 +1432,19 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         if (tid == 256) ok = issuer_role<NB, EXT>(cx, has_h0);
         if (tid == 288) ok = loader_role<NB, EXT>(cx, &tmC, &tmB, &tmX);
         if (warp == 10) ok = vector_role<NB, EXT>(cx);
+        if (tid == 352) ok = issuer_ys_role<NB, EXT>(cx);
     }
     if (!ok) {
         abort_flag = 1;
         atomicOr(&g_device_error, 1u);
     }
-    if (!ok && tid == 256) {
-        // products still in flight after a timeout: give them a bounded
-        // chance to finish before the tensor memory is released
-        mma_commit(&sm.bar_fin);
+    if (!ok && (tid == 256 || tid == 352)) {
+        // products still in flight after a timeout: give each issuing
+        // thread's a bounded chance to finish before the tensor memory is released
+        uint64_t *fin = &sm.bar_fin[tid == 352];
+        mma_commit(fin);
         volatile int never = 0;
-        (void)mbar_wait_bounded(&sm.bar_fin, 0, &never, 100000000ull);
+        (void)mbar_wait_bounded(fin, 0, &never, 100000000ull);
     }
     tc_fence_before_sync();
     __syncthreads();
