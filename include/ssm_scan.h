@@ -76,7 +76,7 @@ typedef enum {
  *   x, delta : (Bs, L, ED) fp32        A : (ED, N) fp32
  *   B, C     : (Bs, L, N)  fp32        D : (ED) fp32 or NULL
  *   y        : (Bs, L, ED) fp32 output
- * Supported: 1 <= N <= 64.  Every pointer must be 4-byte aligned
+ * Supported: 1 <= N <= 256.  Every pointer must be 4-byte aligned
  * (SSM_ERR_ALIGNMENT otherwise).  Any Bs, L, ED >= 1.
  */
 SSM_API ssm_status_t ssm_scan_fwd(const float *x, const float *delta, const float *A,
@@ -119,8 +119,8 @@ SSM_API ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED,
  *   D  : (H) fp32 or NULL          y  : (Bs, L, H, P) fp32 output
  *   chunk : time-chunk length Q of the chunked algorithm.
  *   bidirectional : 0 = forward scan; != 0 = forward + reversed scan + D x.
- * Supported: P in {16, 32, 64, 128}, N in {32, 64, 128, 256} with
- * P * N <= 16384; chunk in {64, 128, 256}; any Bs, L, H >= 1 (L need not be
+ * Supported: P and N in {16, 32, 64, 128, 256}; chunk in {64, 128, 256};
+ * any Bs, L, H >= 1 (L need not be
  * a multiple of chunk).  x, B, C and y must be 16-byte aligned, dt aligned
  * to its element size (SSM_ERR_ALIGNMENT otherwise).  bf16 inputs with
  * P == 64 and N in {64, 128} run on the tensor cores (tcgen05); every other

@@ -139,7 +139,7 @@ ssm_status_t diag_entry(const Tin *x, const Tin *delta, const float *A, const Ti
     if (!x || !delta || !A || !B || !C || !y) return SSM_ERR_INVALID_ARG;
     if (!sizes_ok({Bs, L, ED}) || !sizes_ok({Bs, L, N}) || !sizes_ok({ED, N}))
         return SSM_ERR_INVALID_ARG;
-    if (N > 64) return SSM_ERR_UNSUPPORTED;
+    if (N > 256) return SSM_ERR_UNSUPPORTED;
     if (L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
     const size_t es = sizeof(Tin);
     if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
@@ -352,7 +352,7 @@ ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED, int64_t N, int
     if (!states_per_thread || !lanes_per_channel || !time_segments) return SSM_ERR_INVALID_ARG;
     if (!sizes_ok({Bs, L, ED}) || !sizes_ok({Bs, L, N}) || !sizes_ok({ED, N}))
         return SSM_ERR_INVALID_ARG;
-    if (N > 64) return SSM_ERR_UNSUPPORTED;
+    if (N > 256) return SSM_ERR_UNSUPPORTED;
     if (L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
     DeviceInfo dev;
     ssm_status_t s = current_device(&dev);

@@ -16,8 +16,12 @@ namespace diag {
 // segments K (each >= 128 steps) that give >= 1.8 warps per scheduler, and
 // fewer states per lane only if even 8 segments are not enough.  A plan that
 // would need a second wave of CTAs is never chosen.
+static int padded_states(int64_t N) {
+    return N <= 16 ? 16 : (N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256)));
+}
+
 static Plan choose_plan(int64_t Bs, int64_t L, int64_t ED, int N, int num_sms, int max_ctas_per_sm) {
-    const int NP = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
+    const int NP = padded_states(N);
     const double schedulers = 4.0 * num_sms;
     auto make = [&](int s, int k) {
         int64_t seg = (L + k - 1) / k;
@@ -52,7 +56,7 @@ static Plan choose_plan(int64_t Bs, int64_t L, int64_t ED, int N, int num_sms, i
 
 // The decomposition used for a shape: (S, G, K) and the segment length.
 Plan plan_for(int64_t Bs, int64_t L, int64_t ED, int64_t N, int esz, int num_sms) {
-    const int NP = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
+    const int NP = padded_states(N);
     // CTAs per SM allowed by shared memory (228 KB per SM, 1 KB reserved per
     // CTA) for the 16-states-per-thread split, capped at 16.
     const int et = kThreads / (NP / 16);

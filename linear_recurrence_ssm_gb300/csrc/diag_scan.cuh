@@ -649,6 +649,8 @@ static cudaError_t dispatch_sg(int S, int G, const Tin *x, const Tin *dlt, const
         SSM_DIAG_CASE(16, 2)
         SSM_DIAG_CASE(8, 4)
         SSM_DIAG_CASE(16, 4)
+        SSM_DIAG_CASE(16, 8)
+        SSM_DIAG_CASE(16, 16)
     }
 #undef SSM_DIAG_CASE
     return cudaErrorInvalidValue;

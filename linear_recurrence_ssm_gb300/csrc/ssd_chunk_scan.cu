@@ -28,10 +28,16 @@
 // w'_s = dt_s exp(excl_s).  Both directions read each tile of x, dt, B, C in
 // place -- no reversed copy of any input is materialised.
 //
-// One CTA of 128 threads owns one (b, h) and walks its tiles in order; thread
-// t owns tile row t (and TMEM lane t).  Thread 0 issues the TMA copies and
-// the tensor-core MMAs; every wait is bounded in time and reports through an
-// error word instead of hanging.
+// Three kernels compute it.  The unidirectional scan runs on a warp-
+// specialised kernel (ws::ssd_ws_kernel below): eight math warps, an
+// MMA-issuing thread each for the G / Zf and the Y / S_c streams, a copying
+// thread and a warp for the per-tile vectors.  Short bidirectional sequences
+// (at most four tiles, N = 64) run as two passes over independent tiles
+// (ssd_bidir.cu).  Every other bidirectional call runs on
+// ssd_chunk_scan_kernel: one CTA of 128 threads owns one (b, h) and walks its
+// tiles in order; thread t owns tile row t (and TMEM lane t), and thread 0
+// issues the TMA copies and the tensor-core MMAs.  Every wait is bounded in
+// time and reports through an error word instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -100,7 +106,7 @@ struct Params {
     const float *D;
     float *y;
     uint8_t *rstate;   // reverse entering states, [Bs*H][nc][NB * kStateRegion] (bidirectional)
-    int L, H, nc, bidir;
+    int L, H, nc;
     // options (kernels built with them only): dt <- clamp(softplus(dt + bias)),
     // y <- y * silu(z), initial / final state (Bs, H, P, N) fp32
     const float *dt_bias;
@@ -203,6 +209,11 @@ __device__ __forceinline__ void store_state_bf16(uint8_t (*img)[kStateRegion], i
         }                                                                                 \
     } while (0)
 
+// The bidirectional scan for sequences the two-pass kernels do not take:
+// first the reverse sweep from the last tile (entering states R_in of every
+// tile, stored bf16 in scratch), then the forward sweep with the outputs.
+// (The options that go with state input / output are not accepted with the
+// bidirectional scan, so neither appears here.)
 template <int NB, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
@@ -223,13 +234,11 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     const int h = bh % prm.H;
     const int L = prm.L;
     const int nc = prm.nc;
-    const bool bidir = prm.bidir != 0;
     const int grp = h / (prm.H / prm.G);          // this head's group of B, C
     const float Ah = prm.A[h] * SSM_LOG2E;        // decays are exp2 of log2e-scaled sums
     const float Dh = prm.D ? prm.D[h] : 0.0f;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const size_t rstride = size_t(NB) * kStateRegion;
-    const bool has_h0 = EXT && prm.h0 != nullptr;
 
     if (tid == 0) {
         abort_flag = 0;
@@ -327,7 +336,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             // (Rows r, r' are in the same warp as s.)
             const int s = row;
             sm.csf[p][s] = ex2(sm.cum[p][s | 31] - cum) * dv;
-            if (bidir) sm.csr[p][s] = ex2(cum - dA - sm.excl[p][s & ~31]) * dv;
+            sm.csr[p][s] = ex2(cum - dA - sm.excl[p][s & ~31]) * dv;
         }
         *tot_out = tot;
     };
@@ -377,7 +386,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     float st[32];   // rows [32 wg, 32 wg + 32) of this thread's state column (n = row), fp32
 
     // ---------------- reverse sweep: entering states of the reverse scan -------------
-    if (bidir) {
+    {
 #pragma unroll
         for (int p = 0; p < 32; ++p) st[p] = 0.0f;
         if (tid == 0) {
@@ -426,17 +435,10 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     // update, so that the mask pass of tile c + 1 can start at once.
 #pragma unroll
     for (int p = 0; p < 32; ++p) st[p] = 0.0f;
-    if (has_h0 && row < N) {
-        // initial state, rows [32 wg, 32 wg + 32) of column n = row
-        const float *src = prm.h0 + (size_t(bh) * kP + wg * 32) * N + row;
-#pragma unroll
-        for (int p = 0; p < 32; ++p) st[p] = src[size_t(p) * N];
-        store_state_bf16<NB>(sm.S, row, wg * 32, *reinterpret_cast<float(*)[32]>(st));
-    }
     fence_proxy_async_smem();
     if (tid == 0) {
         load_x(0, 0);
-        load_c(0, bidir && nc > 1);
+        load_c(0, nc > 1);
         load_b(0, 0);
         if (nc > 1) {
             load_b(1, 1);
@@ -456,21 +458,21 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
     if (tid == 0) {
         tc_fence_after_sync();
         issue_g(0);
-        issue_z(has_h0, bidir && nc > 1);
+        issue_z(false, nc > 1);
         mma_commit(&sm.bar_g);
     }
     for (int c = 0; c < nc; ++c) {
         const int c0 = c * kQ;
         const int par = c & 1;      // buffers and per-tile vectors of tile c
         const bool more = c + 1 < nc;
-        const bool has_s = c > 0 || has_h0;
-        const bool has_r = bidir && (c < nc - 1);
+        const bool has_s = c > 0;
+        const bool has_r = c < nc - 1;
         // The previous tile's output rows staged in the mask buffer must have
         // been read by their store before the mask pass overwrites it.
         if (tid == 0) bulk_wait_read0();
         SSM_CTA_WAIT(sm.bar_g, ph_g);          // G, Zf, Zr of tile c; C and R buffers free
         tc_fence_after_sync();
-        if (tid == 0 && more) load_c(c + 1, bidir && (c + 1 < nc - 1));
+        if (tid == 0 && more) load_c(c + 1, c + 1 < nc - 1);
 
         // Decay mask on row t of G -> bf16 M (K-major, swizzled).
         {
@@ -480,24 +482,19 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             const float *excl = sm.excl[par];
             const float *dtv = sm.dtv[par];
             const float cum_t = cum[t], excl_t = excl[t];
-            // Blocks {0, 3} to warpgroup 0 and {1, 2} to warpgroup 1: the causal
-            // (and diagonal) work of every row warp is then split evenly.
+            // Blocks {0, 3} to warpgroup 0 and {1, 2} to warpgroup 1 (every
+            // block of the two-sided mask is needed).
             const int sbs[2] = {wg == 0 ? 0 : 1, wg == 0 ? 3 : 2};
-            const bool need0 = (sbs[0] <= tb) || (bidir && sbs[0] >= tb);
-            const bool need1 = (sbs[1] <= tb) || (bidir && sbs[1] >= tb);
             uint32_t gr[2][32];
-            if (need0) tmem_ld32_async(tmem + lane_base + kColG + sbs[0] * 32, gr[0]);
-            if (need1) tmem_ld32_async(tmem + lane_base + kColG + sbs[1] * 32, gr[1]);
-            if (need0 || need1) {
-                tmem_wait_tie(gr[0]);
-                reg_tie(gr[1]);
-            }
+            tmem_ld32_async(tmem + lane_base + kColG + sbs[0] * 32, gr[0]);
+            tmem_ld32_async(tmem + lane_base + kColG + sbs[1] * 32, gr[1]);
+            tmem_wait_tie(gr[0]);
+            reg_tie(gr[1]);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int sb = sbs[i];
-                const bool need = i == 0 ? need0 : need1;
                 uint32_t packed[16];
-                if (need) {
+                {
                     float m[32];
                     if (sb == tb) {
                         // diagonal block: direct differences of cumulative sums
@@ -507,7 +504,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
 #pragma unroll
                         for (int j4 = 0; j4 < 8; ++j4) {
                             const float4 cs = c4[j4], ds = d4[j4];
-                            const float4 es = bidir ? e4[j4] : cs;
+                            const float4 es = e4[j4];
                             const float csv[4] = {cs.x, cs.y, cs.z, cs.w};
                             const float esv[4] = {es.x, es.y, es.z, es.w};
                             const float dsv[4] = {ds.x, ds.y, ds.z, ds.w};
@@ -515,7 +512,7 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                             for (int q = 0; q < 4; ++q) {
                                 const int s = sb * 32 + 4 * j4 + q;
                                 float w = (s <= t) ? ex2(cum_t - csv[q]) : 0.0f;
-                                if (bidir && s >= t) w += ex2(esv[q] - excl_t);
+                                if (s >= t) w += ex2(esv[q] - excl_t);
                                 m[4 * j4 + q] = __uint_as_float(gr[i][4 * j4 + q]) * (w * dsv[q]);
                             }
                         }
@@ -535,9 +532,6 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
                     }
 #pragma unroll
                     for (int j = 0; j < 16; ++j) packed[j] = pack_bf16(m[2 * j], m[2 * j + 1]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) packed[j] = 0u;
                 }
                 uint8_t *reg = sm.M[sb >> 1];
 #pragma unroll
@@ -663,18 +657,11 @@ ssd_chunk_scan_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_cons
             if (c + 2 < nc) load_x(c + 2, par);
             if (more) {
                 tc_fence_after_sync();
-                issue_z(true, bidir && (c + 1 < nc - 1));
+                issue_z(true, c + 1 < nc - 1);
                 mma_commit(&sm.bar_g);
             }
         }
         tot_cur = tot_nxt;
-    }
-    // Final state: after the last tile st holds the state after row L - 1
-    // (rows past L have dt = 0 and leave it unchanged).
-    if (EXT && prm.h_final != nullptr && row < N) {
-        float *dst = prm.h_final + (size_t(bh) * kP + wg * 32) * N + row;
-#pragma unroll
-        for (int p = 0; p < 32; ++p) dst[size_t(p) * N] = st[p];
     }
     }
 
@@ -1522,7 +1509,6 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
     prm.L = int(L);
     prm.H = int(H);
     prm.nc = int((L + kQ - 1) / kQ);
-    prm.bidir = bidir ? 1 : 0;
     const Options none{};
     const Options &o = opt ? *opt : none;
     prm.dt_bias = o.dt_bias;

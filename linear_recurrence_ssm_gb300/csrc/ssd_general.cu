@@ -1,19 +1,24 @@
 // ssd_general.cu -- the chunked scalar-decay ("SSD") scan on CUDA cores, for
 // the shapes and input types the tensor-core kernel (ssd_chunk_scan.cu: bf16,
-// P = 64, N in {64, 128}) does not take: fp32 inputs, P in {16, 32, 64, 128},
-// N in {32, 64, 128, 256}.
+// P = 64, N in {64, 128}) does not take: fp32 inputs, P and N in
+// {16, 32, 64, 128, 256}.
 //
 // Per (b, h), with H_t the P x N state,
 //     H_t = exp(dt_t A_h) H_{t-1} + dt_t x_t (outer) B_t,   y_t = H_t C_t + D_h x_t,
-// walked sequentially over t with the state in registers: a CTA of 256
-// threads owns one (b, h); warp w holds rows p = w, w + 8, ... and lane l
-// columns n = l, l + 32, ... of the state.  y_t[p] is a sum over n: the
-// warp's lanes reduce it with shuffles each step.  The inputs of kT steps
+// walked sequentially over t with the state in registers.  Rows p of the
+// state are independent of one another (they share only dt, B and C), so the
+// P rows are cut into slices of PS = min(P, 128) rows (64 when N = 256, to
+// keep at most 64 state values per thread) and a CTA of 256 threads owns one
+// slice of one (b, h); warp w holds rows p0 + w, p0 + w + 8, ... and lane l
+// columns n = l, l + 32, ... of the state (lanes l >= N idle when N = 16).
+// y_t[p] is a sum over n: the warp's lanes reduce it with shuffles each step.  The inputs of kT steps
 // are staged in shared memory one tile ahead.  The bidirectional scan runs
 // a second pass from the last step that adds its part to y.  The scan
 // options (dt bias / softplus / clamp, silu gate, initial and final state,
 // groups of B and C) are applied as in the tensor-core kernel.
 #include "ssm_common.cuh"
+
+#include <algorithm>
 
 namespace ssm {
 namespace ssd_general {
@@ -27,6 +32,7 @@ struct Args {
     const float *A, *D, *dt_bias, *h0;
     float *y, *h_final;
     int L, H, P, N, G;
+    int slices;       // CTAs per (b, h): row slices of PS = kWarps * PW rows
     float dt_min, dt_max;
     int dt_softplus, dt_limit;
 };
@@ -39,24 +45,25 @@ struct Tile {
     float dt[kT];
 };
 
-// Stage the x, B, C rows of steps [t0, t0 + kT) (in walk order: `rev`
-// walks backwards) of one (b, h) with 16-byte asynchronous copies (rows are
-// multiples of 16 bytes; the entry points require 16-byte aligned x, B, C).
-// Rows outside [0, L) are zero filled.
+// Stage the x (columns [p0, p0 + ps) of the row), B, C rows of steps
+// [t0, t0 + kT) (in walk order: `rev` walks backwards) of one (b, h) with
+// 16-byte asynchronous copies (slices and rows are multiples of 16 bytes; the
+// entry points require 16-byte aligned x, B, C).  Rows outside [0, L) are
+// zero filled.
 template <typename Tin>
 __device__ __forceinline__ void stage_rows(Tile<Tin> &s, const Args &a, int64_t b, int h, int g,
-                                           int t0, bool rev) {
+                                           int p0, int ps, int t0, bool rev) {
     constexpr int EPC = 16 / sizeof(Tin);
     const Tin *x = static_cast<const Tin *>(a.x);
     const Tin *Bm = static_cast<const Tin *>(a.B);
     const Tin *Cm = static_cast<const Tin *>(a.C);
-    const int cpx = a.P / EPC, cpn = a.N / EPC;
+    const int cpx = ps / EPC, cpn = a.N / EPC;
     for (int i = threadIdx.x; i < kT * cpx; i += kThreads) {
         const int k = i / cpx, c = i % cpx;
         const int t = rev ? a.L - 1 - (t0 + k) : t0 + k;
         const bool ok = t0 + k < a.L;
-        cp_async16(&s.x[k][c * EPC], x + (ok ? ((b * a.L + t) * a.H + h) * a.P + c * EPC : 0),
-                   ok ? 16 : 0);
+        cp_async16(&s.x[k][c * EPC],
+                   x + (ok ? ((b * a.L + t) * a.H + h) * a.P + p0 + c * EPC : 0), ok ? 16 : 0);
     }
     for (int i = threadIdx.x; i < kT * cpn; i += kThreads) {
         const int k = i / cpn, c = i % cpn;
@@ -90,7 +97,9 @@ ssd_general_kernel(Args a, int pass, int gate_now) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Tile<Tin> *tiles = reinterpret_cast<Tile<Tin> *>(smem_raw);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int bh = blockIdx.x;
+    constexpr int PS = kWarps * PW;              // rows of this CTA's slice
+    const int bh = blockIdx.x / a.slices;
+    const int p0 = (blockIdx.x % a.slices) * PS;
     const int64_t b = bh / a.H;
     const int h = bh % a.H;
     const int g = h / (a.H / a.G);
@@ -105,12 +114,12 @@ ssd_general_kernel(Args a, int pass, int gate_now) {
     for (int i = 0; i < PW; ++i)
 #pragma unroll
         for (int j = 0; j < NL; ++j) {
-            const int p = w + kWarps * i, n = lane + 32 * j;
-            st[i][j] = (a.h0 && !rev) ? a.h0[((int64_t(bh) * a.P) + p) * a.N + n] : 0.0f;
+            const int p = p0 + w + kWarps * i, n = lane + 32 * j;
+            st[i][j] = (a.h0 && !rev && n < a.N) ? a.h0[((int64_t(bh) * a.P) + p) * a.N + n] : 0.0f;
         }
 
     const int ntiles = (a.L + kT - 1) / kT;
-    stage_rows<Tin>(tiles[0], a, b, h, g, 0, rev);
+    stage_rows<Tin>(tiles[0], a, b, h, g, p0, PS, 0, rev);
     cp_async_commit();
     if (threadIdx.x < kT) tiles[0].dt[threadIdx.x] = load_dt<Tin>(a, b, h, 0, rev, dbias);
     cp_async_wait<0>();
@@ -120,7 +129,7 @@ ssd_general_kernel(Args a, int pass, int gate_now) {
         // the next tile's copies run while this one is used
         float dnext = 0.0f;
         if (k + 1 < ntiles) {
-            stage_rows<Tin>(tiles[(k + 1) & 1], a, b, h, g, (k + 1) * kT, rev);
+            stage_rows<Tin>(tiles[(k + 1) & 1], a, b, h, g, p0, PS, (k + 1) * kT, rev);
             dnext = load_dt<Tin>(a, b, h, (k + 1) * kT, rev, dbias);
         }
         cp_async_commit();
@@ -131,8 +140,10 @@ ssd_general_kernel(Args a, int pass, int gate_now) {
             float bv[NL], cv[NL];
 #pragma unroll
             for (int q = 0; q < NL; ++q) {
-                bv[q] = to_f32(s.B[j][lane + 32 * q]);
-                cv[q] = to_f32(s.C[j][lane + 32 * q]);
+                // (N = 16: lanes past N hold no state and add nothing)
+                const bool n_ok = NL > 1 || lane + 32 * q < a.N;
+                bv[q] = n_ok ? to_f32(s.B[j][lane + 32 * q]) : 0.0f;
+                cv[q] = n_ok ? to_f32(s.C[j][lane + 32 * q]) : 0.0f;
             }
             float yp[PW];
 #pragma unroll
@@ -150,16 +161,16 @@ ssd_general_kernel(Args a, int pass, int gate_now) {
             for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
                 for (int i = 0; i < PW; ++i) yp[i] += __shfl_xor_sync(0xffffffffu, yp[i], o);
-            // lane i of the warp writes row p = w + 8 i
+            // lane i of the warp writes row p = p0 + w + 8 i
             const int t = rev ? a.L - 1 - (k * kT + j) : k * kT + j;
 #pragma unroll
             for (int i = 0; i < PW; ++i) {
                 if (lane == i) {
-                    const int p = w + kWarps * i;
-                    const int64_t o = ((b * a.L + t) * a.H + h) * a.P + p;
+                    const int pl = w + kWarps * i;
+                    const int64_t o = ((b * a.L + t) * a.H + h) * a.P + p0 + pl;
                     float v = yp[i];
                     if (rev) v += a.y[o];                       // forward part, written by pass 0
-                    else v = fmaf(Dh, to_f32(s.x[j][p]), v);
+                    else v = fmaf(Dh, to_f32(s.x[j][pl]), v);
                     if (gate_now && zg) v *= silu_fast(to_f32(zg[o]));
                     a.y[o] = v;
                 }
@@ -174,8 +185,8 @@ ssd_general_kernel(Args a, int pass, int gate_now) {
         for (int i = 0; i < PW; ++i)
 #pragma unroll
             for (int j = 0; j < NL; ++j) {
-                const int p = w + kWarps * i, n = lane + 32 * j;
-                a.h_final[((int64_t(bh) * a.P) + p) * a.N + n] = st[i][j];
+                const int p = p0 + w + kWarps * i, n = lane + 32 * j;
+                if (n < a.N) a.h_final[((int64_t(bh) * a.P) + p) * a.N + n] = st[i][j];
             }
     }
 }
@@ -196,6 +207,7 @@ static cudaError_t run(const Args &a, int64_t grid, bool bidir, cudaStream_t st)
 template <typename Tin, int PW>
 static cudaError_t run_pw(const Args &a, int64_t grid, bool bidir, cudaStream_t st) {
     switch (a.N) {
+        case 16:
         case 32: return run<Tin, PW, 1>(a, grid, bidir, st);
         case 64: return run<Tin, PW, 2>(a, grid, bidir, st);
         case 128: return run<Tin, PW, 4>(a, grid, bidir, st);
@@ -206,20 +218,22 @@ static cudaError_t run_pw(const Args &a, int64_t grid, bool bidir, cudaStream_t 
     return cudaErrorNotSupported;
 }
 
-// Shapes this path takes: P in {16, 32, 64, 128}, N in {32, 64, 128, 256},
-// P * N <= 16384.
-bool supported(int64_t P, int64_t N) {
-    const bool p_ok = P == 16 || P == 32 || P == 64 || P == 128;
-    const bool n_ok = N == 32 || N == 64 || N == 128 || N == 256;
-    return p_ok && n_ok && P * N <= 16384;
+static bool pow2_16_256(int64_t v) {
+    return v == 16 || v == 32 || v == 64 || v == 128 || v == 256;
 }
+
+// Shapes this path takes: P and N in {16, 32, 64, 128, 256}.
+bool supported(int64_t P, int64_t N) { return pow2_16_256(P) && pow2_16_256(N); }
 
 template <typename Tin>
 cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *Bm, const Tin *Cm,
                    const float *D, float *y, int64_t Bs, int64_t L, int64_t H, int64_t P,
                    int64_t N, bool bidir, const ScanOpts *opt, cudaStream_t st) {
     if (!supported(P, N)) return cudaErrorNotSupported;
-    const int64_t grid = Bs * H;
+    // slice height: at most 64 state values per thread (16 rows per warp of
+    // up to 4 columns, or 8 rows of 8 columns when N = 256)
+    const int64_t ps = std::min<int64_t>(P, N == 256 ? 64 : 128);
+    const int64_t grid = Bs * H * (P / ps);
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const ScanOpts none{};
     const ScanOpts &o = opt ? *opt : none;
@@ -229,9 +243,10 @@ cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *
     a.y = y; a.h_final = o.h_final;
     a.L = int(L); a.H = int(H); a.P = int(P); a.N = int(N);
     a.G = o.ngroups > 1 ? o.ngroups : 1;
+    a.slices = int(P / ps);
     a.dt_min = o.dt_min; a.dt_max = o.dt_max;
     a.dt_softplus = o.dt_softplus; a.dt_limit = o.dt_limit;
-    switch (P) {
+    switch (ps) {
         case 16: return run_pw<Tin, 2>(a, grid, bidir, st);
         case 32: return run_pw<Tin, 4>(a, grid, bidir, st);
         case 64: return run_pw<Tin, 8>(a, grid, bidir, st);

@@ -67,7 +67,7 @@ def test_diag_rejects_bad_arguments(fn):
     assert diag(fn, ED=-3) == 1
     assert diag(fn, N=0) == 1
     assert diag(fn, Bs=2 ** 40, L=2 ** 40) == 1      # element count overflows int64
-    assert diag(fn, N=65) == 2
+    assert diag(fn, N=257) == 2
     ptrs = [P] * 7
     ptrs[6] = P_ODD                       # y not 4-byte aligned
     assert diag(fn, ptrs) == 3
@@ -80,10 +80,11 @@ def test_ssd_rejects_bad_arguments():
     assert ssd(L=0) == 1
     assert ssd(chunk=0) == 1
     assert ssd(P_=48) == 2
-    assert ssd(P_=256) == 2
+    assert ssd(P_=512) == 2
+    assert ssd(P_=8) == 2
     assert ssd(N=48) == 2
-    assert ssd(N=16) == 2
-    assert ssd(P_=128, N=256) == 2        # P * N above 16384
+    assert ssd(N=8) == 2
+    assert ssd(N=512) == 2
     assert ssd(chunk=96) == 2
     ptrs = [P] * 7
     ptrs[3] = P_ODD                       # B not 16-byte aligned

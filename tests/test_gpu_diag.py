@@ -49,7 +49,11 @@ def _check(y_gpu, ref, dtype):
     (1, 45, 24, 5),       # N not a multiple of 4 (padded states)
     (2, 40, 72, 17),      # N just above 16
     (1, 70, 136, 32),
-    (1, 50, 40, 64),      # largest N
+    (1, 50, 40, 64),
+    (2, 45, 40, 100),     # 128 padded states: 8 lanes per channel
+    (1, 70, 24, 128),
+    (2, 37, 20, 200),     # 256 padded states: 16 lanes per channel, 8 channels per CTA
+    (1, 40, 16, 256),     # largest N
     (2, 31, 70, 16),      # ED*esize not a multiple of 16 (unvectorised loads for bf16)
     (1, 29, 3, 7),        # tiny odd shapes
 ])

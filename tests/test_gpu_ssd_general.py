@@ -1,8 +1,9 @@
 """GPU parity of the chunked scan's CUDA-core path against the fp64 oracle.
 
 Shapes and input types outside the tensor-core kernel (bf16, P = 64,
-N in {64, 128}) run on the CUDA-core kernel: P in {16, 32, 64, 128},
-N in {32, 64, 128, 256} (P * N <= 16384) and fp32 inputs.  Tolerances as for
+N in {64, 128}) run on the CUDA-core kernel: P and N in {16, 32, 64, 128,
+256} and fp32 inputs.  P = 256 (and P = 128 with N = 256) is cut into row
+slices owned by separate CTAs; N = 16 leaves half of each warp's lanes idle.  Tolerances as for
 the scans: 1e-4 * max(1, max|ref|) for fp32 inputs, 2e-2 * max|ref| for bf16.
 """
 import numpy as np
@@ -41,6 +42,11 @@ def _dev(d, dev):
     (1, 90, 1, 64, 256),
     (2, 17, 2, 16, 256),
     (1, 300, 2, 64, 128),     # the tensor-core shape, fp32 inputs take this path
+    (2, 90, 2, 64, 16),       # N = 16
+    (1, 70, 2, 256, 16),      # two 128-row slices, N = 16
+    (1, 100, 2, 256, 64),
+    (1, 130, 1, 128, 256),    # two 64-row slices
+    (1, 60, 1, 256, 256),     # four 64-row slices, largest state
 ])
 def test_general_path_matches_oracle(cuda_device, dtype, bidir, Bs, L, H, P, N):
     if dtype == "bf16" and P == 64 and N in (64, 128):
@@ -68,6 +74,20 @@ def test_general_path_with_options_and_groups(cuda_device, dtype):
     torch.cuda.synchronize()
     _close(y, ref, dtype)
     _close(hf, href, dtype, "h_final")
+
+
+@pytest.mark.parametrize("P,N", [(256, 16), (256, 256)])
+def test_general_path_row_slices_with_state_io(cuda_device, P, N):
+    """Initial and final states indexed by the slice's rows."""
+    Bs, L, H = 1, 75, 2
+    inp = workloads.ssd_inputs(Bs, L, H, P, N, "f32", seed=P + N)
+    opt = workloads.option_inputs((Bs, L, H, P), (Bs, L, H), H, (Bs, H, P, N), "f32", P + N + 1)
+    ref, href = oracle.ssd_scan(**inp, h0=opt["h0"], return_final_state=True)
+    y, hf = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), h0=opt["h0"].to(cuda_device),
+                                   return_final_state=True)
+    torch.cuda.synchronize()
+    _close(y, ref, "f32")
+    _close(hf, href, "f32", "h_final")
 
 
 def test_general_path_bidirectional_gate(cuda_device):
