@@ -108,9 +108,25 @@ def kernel_source_hash(kind: str) -> str:
             "bissd": ["ssd_bidir.cu", "tc_ptx.cuh"]}[kind]
     h = hashlib.sha256()
     for p in [os.path.join(csrc, f) for f in srcs] + [os.path.join(csrc, "ssm_common.cuh")]:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
+
+
+def _code_only(src: str) -> str:
+    """C++ source without comments and blank lines (a comment edit leaves the
+    compiled kernel, and so the recorded counters, valid)."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    lines = []
+    for line in src.splitlines():
+        # drop a // comment unless the // sits inside a string literal
+        cut = line.find("//")
+        if cut >= 0 and line[:cut].count('"') % 2 == 0:
+            line = line[:cut]
+        line = line.rstrip()
+        if line.strip():
+            lines.append(line)
+    return "\n".join(lines)
 
 
 def source_kind(w) -> str:

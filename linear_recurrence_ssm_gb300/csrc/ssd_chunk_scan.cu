@@ -702,9 +702,9 @@ done:
 // them, update the state (the image of the state entering tile c + 1), store
 // the mask of tile c + 1 into tensor memory -- so Zf(c + 1), Y(c + 1) and
 // S_c(c + 1) start at once -- and (3) write the outputs of tile c while they
-// run.  Warp 8 (one thread) issues every tcgen05.mma as soon as its inputs
-// are ready, warp 9 (one thread) every TMA copy as soon as its buffer is
-// free.  The mask M lives in tensor memory and is the A operand of Y = M X;
+// run.  Two threads issue the tcgen05.mma products as soon as their inputs
+// are ready -- warp 8 the G and Zf streams, warp 11 the Y and S_c products --
+// and warp 9 (one thread) every TMA copy as soon as its buffer is free.  The mask M lives in tensor memory and is the A operand of Y = M X;
 // D x rides on its diagonal.  Y and Zf have two accumulators (by tile
 // parity) so the products of tile c + 1 run while the outputs of tile c are
 // read; the weighted rows Xw are double-buffered, and once S_c(c) has run
@@ -713,8 +713,9 @@ done:
 namespace ws {
 
 constexpr int kMath = 256;             // math threads (warps 0..7)
-constexpr int kThreads = kMath + 128;  // + warpgroup 2: warp 8 issues MMAs, warp 9 copies,
-                                       //   warp 10 computes the per-tile vectors
+constexpr int kThreads = kMath + 128;  // + warpgroup 2: warp 8 issues G and Zf, warp 9 copies,
+                                       //   warp 10 computes the per-tile vectors, warp 11
+                                       //   issues Y and S_c
 // Registers: the register file is split between the SM's four schedulers,
 // one warp of each warpgroup per scheduler; the CTA is launched with 168 per
 // thread (3 warps x 32 x 168 <= 16384 per scheduler) and setmaxnreg moves
