@@ -708,8 +708,8 @@ done:
 // D x rides on its diagonal.  Y and Zf have two accumulators (by tile
 // parity) so the products of tile c + 1 run while the outputs of tile c are
 // read; the weighted rows Xw are double-buffered, and once S_c(c) has run
-// each warp stages its output rows of tile c in its own part of tile c's
-// buffer (the part it writes again when it weighs tile c + 2).
+// the outputs of tile c are staged in tile c's buffer and leave by TMA
+// stores, so that no warp waits on its global stores.
 namespace ws {
 
 constexpr int kMath = 256;             // math threads (warps 0..7)
@@ -754,6 +754,8 @@ struct __align__(1024) Smem {
     uint64_t bar_g, bar_m2[2], bar_z[2];
     uint64_t bar_gfree, bar_mfull, bar_xw[2], bar_st;
     uint64_t bar_vec[kSlots];                        // vectors of a slot written
+    uint64_t bar_pair[4];                            // the two warps of a lane quarter: their
+                                                     //   output stores have read the staging
     uint64_t bar_fin[2];                             // error path (one per issuing thread)
     uint32_t tmem_base;
 };
@@ -803,6 +805,7 @@ struct Ctx {
     float Ah, Dh, dbias;
     uint32_t tmem;
     volatile int *abort;
+    const CUtensorMap *tmY;   // y (fp32), box 16 p x 32 rows, 64-byte swizzle
 };
 
 #define WS_WAIT(bar, ph)                                                                  \
@@ -1107,10 +1110,21 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     // half 1 the blocks sb = 0 .. q - 1 below it
     uint32_t ph_g = 0, ph_m2 = 0, ph_z = 0, ph_x = 0, ph_vec = 0;   // ph_m2, ph_z, ph_x, ph_vec: bits
 
-    // Weighted x rows of tile c: row s = t, columns of half hf.
+    // Weighted x rows of tile c: row s = t, columns of half hf.  The buffer
+    // held the output staging of tile c - 2, whose rows 32 q .. 32 q + 31
+    // both warps of this lane quarter used: each waits until its own stores
+    // have read it, then for the other warp.
+    uint32_t ph_pair = 0;
     auto weigh = [&](int c) -> bool {
         const int p = c % kSlots, xb = c % kXBufs;
         const float w = ex2(sm.tot[p] - sm.cum[p][t]) * sm.dtv[p][t];
+        if (c >= 2) {
+            if (lane == 0) {
+                bulk_wait_read0();
+                mbar_arrive(&sm.bar_pair[q]);
+            }
+            WS_WAIT(sm.bar_pair[q], ph_pair);
+        }
         WS_WAIT_I(sm.bar_x[xb], ph_x, xb);
         weigh_half(sm.X[xb], sm.Xw[c & 1], t, w, hf);
         fence_proxy_async_smem();
@@ -1260,27 +1274,30 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
                 }
             }
         }
-        uint8_t *stg = sm.Xw[c & 1] + q * 32 * 128;
+        // Out by TMA stores: rows 32 q .. 32 q + 31 of tile c's weighted-rows
+        // buffer (read by S_c(c), which has finished) hold two 2 KB boxes,
+        // one per warp of the lane quarter: 32 rows x 16 columns (64-byte
+        // rows, 64-byte swizzle: 16-byte chunk j of row r at j ^ (r / 2 % 4)),
+        // written twice (columns 0..15, then 16..31 of the warp's half).
+        // Rows past L are not written by the store.
+        uint8_t *box = sm.Xw[c & 1] + q * 4096 + hf * 2048;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
+            if (hh == 1) {
+                if (lane == 0) bulk_wait_read0();   // the first store has read the box
+                __syncwarp();
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<float4 *>(stg + lane * 128 + (((4 * hf + j) ^ (lane & 7)) << 4)) =
+                *reinterpret_cast<float4 *>(box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
                     make_float4(out[16 * hh + 4 * j], out[16 * hh + 4 * j + 1], out[16 * hh + 4 * j + 2],
                                 out[16 * hh + 4 * j + 3]);
+            fence_proxy_async_smem();
             __syncwarp();
-            // lanes 4 i .. 4 i + 3 read row 4 i + k (i = 0..7): the rows one
-            // instruction reads differ in bit 2, so their chunks do not collide
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int rr = 4 * (lane >> 2) + k, ch = lane & 3;
-                const float4 v = *reinterpret_cast<const float4 *>(stg + rr * 128 + (((4 * hf + ch) ^ (rr & 7)) << 4));
-                const int trow = c * kQ + q * 32 + rr;
-                if (trow < L)
-                    *reinterpret_cast<float4 *>(cx.prm.y + ((size_t(b) * L + trow) * H + h) * kP +
-                                                hf * 32 + hh * 16 + ch * 4) = v;
+            if (lane == 0) {
+                tma_store_4d(cx.tmY, box, hf * 32 + hh * 16, h, c * kQ + q * 32, b);
+                bulk_commit();
             }
-            __syncwarp();
         }
     };
 
@@ -1354,7 +1371,8 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
 template <int NB, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Params prm) {
+              const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+              const __grid_constant__ Params prm) {
     extern __shared__ uint8_t smem_raw[];
     Smem<NB> &sm = *reinterpret_cast<Smem<NB> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1383,10 +1401,12 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         mbar_init(&sm.bar_z[0], 1);
         mbar_init(&sm.bar_z[1], 1);
         for (int i = 0; i < kSlots; ++i) mbar_init(&sm.bar_vec[i], 32);
+        for (int i = 0; i < 4; ++i) mbar_init(&sm.bar_pair[i], 2);
         mbar_fence_init();
         prefetch_tmap(&tmC);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmX);
+        prefetch_tmap(&tmY);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -1404,7 +1424,7 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
     tc_fence_after_sync();
 
     Ctx<NB> cx{sm, prm, bh / prm.H, bh % prm.H, 0, bh, prm.L, prm.nc, 0.0f, 0.0f, 0.0f,
-               sm.tmem_base, &abort_flag};
+               sm.tmem_base, &abort_flag, &tmY};
     cx.grp = cx.h / (prm.H / prm.G);
     cx.Ah = prm.A[cx.h] * SSM_LOG2E;
     cx.Dh = prm.D ? prm.D[cx.h] : 0.0f;
@@ -1422,6 +1442,7 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         if (warp == 10) ok = vector_role<NB, EXT>(cx);
         if (tid == 352) ok = issuer_ys_role<NB, EXT>(cx);
     }
+    if (warp < 8 && (tid & 31) == 0) bulk_wait0();   // the output stores are complete
     if (!ok) {
         abort_flag = 1;
         atomicOr(&g_device_error, 1u);
@@ -1467,13 +1488,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 static bool make_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
                      const cuuint64_t *strides_bytes, const cuuint32_t *box,
-                     CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                     CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(m, dtype, cuuint32_t(rank), const_cast<void *>(base),
                     dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1530,13 +1552,20 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
     static_assert(sizeof(Smem<NB>) + 1024 <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
     static_assert(sizeof(ws::Smem<NB>) + 1024 <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
     auto kern = opt ? ssd_chunk_scan_kernel<NB, true> : ssd_chunk_scan_kernel<NB, false>;
-    using WsKern = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);
+    using WsKern = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                            const Params);
     WsKern wkern = nullptr;
     if (use_ws) {
         wkern = opt ? ws::ssd_ws_kernel<NB, true> : ws::ssd_ws_kernel<NB, false>;
         smem = sizeof(ws::Smem<NB>) + 1024;
     }
     cudaError_t err;
+    // the warp-specialised kernel stores y in boxes of 16 p x 32 rows
+    CUtensorMap tmYw;
+    const cuuint32_t boxyw[4] = {16, 1, 32, 1};
+    if (wkern && !make_map(&tmYw, y, 4, dx, sy, boxyw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                           CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
     if (wkern) {
         err = cudaFuncSetAttribute(wkern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err != cudaSuccess) return err;
@@ -1561,7 +1590,7 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
         prm.rstate = static_cast<uint8_t *>(scratch);
     }
     if (wkern)
-        wkern<<<dim3(unsigned(grid)), dim3(ws::kThreads), smem, stream>>>(tmC, tmB, tmX, prm);
+        wkern<<<dim3(unsigned(grid)), dim3(ws::kThreads), smem, stream>>>(tmC, tmB, tmX, tmYw, prm);
     else
         kern<<<dim3(unsigned(grid)), dim3(kThreads), smem, stream>>>(tmC, tmB, tmX, tmY, prm);
     err = cudaGetLastError();
