@@ -101,26 +101,26 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ===========================================================================
-// Pass 1: chunk states of every tile (persistent)
+// Pass 1: chunk states of every tile (one tile per CTA)
 // ===========================================================================
 struct __align__(1024) StateSmem {
-    uint8_t Bt[2][kTile];      // B tiles by tile parity (rows s, 64 n)
-    uint8_t Zr[kTile];         // zeros: rows n = 64..127 of the A operand (M = 128)
-    uint8_t X[2][kTile];       // x tiles by tile parity; weighted forward in place; then Sf staging
+    uint8_t Bt[kTile];         // B tile (rows s, 64 n)
+    uint8_t X[kTile];          // x tile; weighted forward in place; then Sf staging
     uint8_t XR[kTile];         // x weighted reverse; then Sr staging
     float wsum[4];
-    uint64_t bar_ld[2], bar_mma;
+    uint64_t bar_ld, bar_mma;
     uint32_t tmem_base;
 };
 
-// CTAs of 128 threads (thread t owns tile row t and TMEM lane t), two per SM,
-// each walking tiles blockIdx.x, blockIdx.x + gridDim.x, ..; the copies of a
-// tile are issued two tiles ahead.  Per tile D (128 x 128) = B^T [w_f x | w_r x]
-// with A = the B tile read MN-major (rows n; rows 64..127 the zero tile),
-// B = the two weighted x tiles (N = 128: p of the forward, then of the
+// One CTA of 128 threads per tile (thread t owns tile row t and TMEM lane t),
+// four per SM (about 50 KB of shared memory, 128 TMEM columns each), so that
+// the copies of every tile of a wave are in flight at once.  D (128 x 128) =
+// B^T [w_f x | w_r x] with A = the B tile read MN-major (rows n 0..63; rows
+// 64..127 of A read the x tile -- they only feed rows of D that are never
+// read), B = the two weighted x tiles (N = 128: p of the forward, then of the
 // reverse direction); rows n < 64 of D go to scratch through bulk copies.
 template <bool EXT>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(128, 4)
 bidir_state_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ Params prm) {
     extern __shared__ uint8_t smem_raw[];
@@ -128,160 +128,124 @@ bidir_state_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int nc = prm.nc, L = prm.L, H = prm.H;
-    const int nk = (prm.units - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);
+    const int bh = int(blockIdx.x) / nc, c = int(blockIdx.x) % nc;
+    const int b = bh / H, h = bh % H;
     volatile int never = 0;
 
     if (t == 0) {
-        mbar_init(&sm.bar_ld[0], 1);
-        mbar_init(&sm.bar_ld[1], 1);
+        mbar_init(&sm.bar_ld, 1);
         mbar_init(&sm.bar_mma, 1);
         mbar_fence_init();
-        prefetch_tmap(&tmB);
-        prefetch_tmap(&tmX);
+        mbar_arrive_expect_tx(&sm.bar_ld, 2 * kTile);
+        tma_load_4d(sm.Bt, &tmB, &sm.bar_ld, 0, h / (H / prm.G), c * kQ, b);
+        tma_load_4d(sm.X, &tmX, &sm.bar_ld, 0, h, c * kQ, b);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 128);
         tmem_relinquish();
     }
-    for (int i = t; i < int(kTile / 16); i += 128) reinterpret_cast<uint4 *>(sm.Zr)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
+    // the tile's cumulative sums (row t), rows past L: dt = 0
+    const int r = c * kQ + t;
+    const float dv = r < L ? prep_dt<EXT>(__bfloat162float(prm.dt[(int64_t(b) * L + r) * H + h]), prm,
+                                          (EXT && prm.dt_bias) ? prm.dt_bias[h] : 0.0f)
+                           : 0.0f;
+    const float dA = dv * prm.A[h] * SSM_LOG2E;
+    float v = dA;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) sm.wsum[warp] = v;
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
-    auto unit = [&](int k, int &bh, int &c, int &b, int &h) {
-        const int u = blockIdx.x + k * gridDim.x;
-        bh = u / nc;
-        c = u % nc;
-        b = bh / H;
-        h = bh % H;
-    };
-    auto load = [&](int k) {      // thread 0: B and x of the k-th tile into buffer k % 2
-        int bh, c, b, h;
-        unit(k, bh, c, b, h);
-        const int buf = k & 1;
-        mbar_arrive_expect_tx(&sm.bar_ld[buf], 2 * kTile);
-        tma_load_4d(sm.Bt[buf], &tmB, &sm.bar_ld[buf], 0, h / (H / prm.G), c * kQ, b);
-        tma_load_4d(sm.X[buf], &tmX, &sm.bar_ld[buf], 0, h, c * kQ, b);
-    };
-    if (t == 0) {
-        load(0);
-        if (nk > 1) load(1);
+    float off = 0.0f, tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        off += (w < warp) ? sm.wsum[w] : 0.0f;
+        tot += sm.wsum[w];
     }
-    auto raw_dt = [&](int k) {   // raw dt of row t of the k-th tile; rows past L: 0
-        int bh, c, b, h;
-        unit(k, bh, c, b, h);
-        const int r = c * kQ + t;
-        return r < L ? __bfloat162float(prm.dt[(int64_t(b) * L + r) * H + h]) : 0.0f;
-    };
-    bool ok = true;
-    uint32_t ph_ld = 0, ph_mma = 0;   // ph_ld: one bit per buffer
-    float raw = raw_dt(0);
-    for (int k = 0; k < nk && ok; ++k) {
-        int bh, c, b, h;
-        unit(k, bh, c, b, h);
-        const int buf = k & 1;
-        // the tile's cumulative sums (row t), rows past L: dt = 0
-        const int r = c * kQ + t;
-        const float dv = r < L ? prep_dt<EXT>(raw, prm, (EXT && prm.dt_bias) ? prm.dt_bias[h] : 0.0f) : 0.0f;
-        if (k + 1 < nk) raw = raw_dt(k + 1);
-        const float dA = dv * prm.A[h] * SSM_LOG2E;
-        float v = dA;
+    const float cum = v + off, excl = cum - dA;
+    bool ok = mbar_wait_bounded(&sm.bar_ld, 0, &never, kWaitLimitNs);
+    if (ok) {
+        // row t: the reverse weights into XR, the forward weights in place
+        // (same swizzle: 16-byte chunks map one to one)
+        const float wf = ex2(tot - cum) * dv, wr = ex2(excl) * dv;
+        const float2 f2 = make_float2(wf, wf), r2 = make_float2(wr, wr);
+        uint4 *src = reinterpret_cast<uint4 *>(sm.X + t * 128);
+        uint4 *dst = reinterpret_cast<uint4 *>(sm.XR + t * 128);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float n = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += n;
+        for (int jj = 0; jj < 8; ++jj) {
+            const int j = jj ^ (t & 7);      // (rows of a warp hit different banks)
+            const uint4 x4 = src[j];
+            const float2 a = unpack_bf16(x4.x), bb = unpack_bf16(x4.y), cc = unpack_bf16(x4.z),
+                         dd = unpack_bf16(x4.w);
+            float2 p0 = fmul2(a, r2), p1 = fmul2(bb, r2), p2 = fmul2(cc, r2), p3 = fmul2(dd, r2);
+            dst[j] = make_uint4(pack_bf16(p0.x, p0.y), pack_bf16(p1.x, p1.y), pack_bf16(p2.x, p2.y),
+                                pack_bf16(p3.x, p3.y));
+            p0 = fmul2(a, f2), p1 = fmul2(bb, f2), p2 = fmul2(cc, f2), p3 = fmul2(dd, f2);
+            src[j] = make_uint4(pack_bf16(p0.x, p0.y), pack_bf16(p1.x, p1.y), pack_bf16(p2.x, p2.y),
+                                pack_bf16(p3.x, p3.y));
         }
-        if (lane == 31) sm.wsum[warp] = v;
-        __syncthreads();
-        float off = 0.0f, tot = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            off += (w < warp) ? sm.wsum[w] : 0.0f;
-            tot += sm.wsum[w];
-        }
-        const float cum = v + off, excl = cum - dA;
-        ok = mbar_wait_bounded(&sm.bar_ld[buf], (ph_ld >> buf) & 1u, &never, kWaitLimitNs);
-        ph_ld ^= 1u << buf;
-        if (ok) {
-            // row t: the reverse weights into XR, the forward weights in place
-            // (same swizzle: 16-byte chunks map one to one)
-            const float wf = ex2(tot - cum) * dv, wr = ex2(excl) * dv;
-            const float2 f2 = make_float2(wf, wf), r2 = make_float2(wr, wr);
-            uint4 *src = reinterpret_cast<uint4 *>(sm.X[buf] + t * 128);
-            uint4 *dst = reinterpret_cast<uint4 *>(sm.XR + t * 128);
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const int j = jj ^ (t & 7);      // (rows of a warp hit different banks)
-                const uint4 x4 = src[j];
-                const float2 a = unpack_bf16(x4.x), bb = unpack_bf16(x4.y), cc = unpack_bf16(x4.z),
-                             dd = unpack_bf16(x4.w);
-                float2 p0 = fmul2(a, r2), p1 = fmul2(bb, r2), p2 = fmul2(cc, r2), p3 = fmul2(dd, r2);
-                dst[j] = make_uint4(pack_bf16(p0.x, p0.y), pack_bf16(p1.x, p1.y), pack_bf16(p2.x, p2.y),
-                                    pack_bf16(p3.x, p3.y));
-                p0 = fmul2(a, f2), p1 = fmul2(bb, f2), p2 = fmul2(cc, f2), p3 = fmul2(dd, f2);
-                src[j] = make_uint4(pack_bf16(p0.x, p0.y), pack_bf16(p1.x, p1.y), pack_bf16(p2.x, p2.y),
-                                    pack_bf16(p3.x, p3.y));
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        if (__syncthreads_or(!ok)) ok = false;
-        if (ok && t == 0) {
-            tc_fence_after_sync();
-            constexpr uint32_t idS = idesc_bf16_f32(128, 128, true, true);
-            const uint32_t sB = smem_addr(sm.Bt[buf]), sX = smem_addr(sm.X[buf]);
-            const uint32_t lboA = smem_addr(sm.Zr) - sB, lboB = smem_addr(sm.XR) - sX;
-#pragma unroll
-            for (int kk = 0; kk < kQ / 16; ++kk)
-                mma_bf16_ss(tmem, smem_desc(sB + kk * 2048, lboA, 1024, kSwizzle128B),
-                            smem_desc(sX + kk * 2048, lboB, 1024, kSwizzle128B), idS, kk > 0);
-            mma_commit(&sm.bar_mma);
-        }
-        if (ok) ok = mbar_wait_bounded(&sm.bar_mma, ph_mma, &never, kWaitLimitNs);
-        ph_mma ^= 1u;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    if (__syncthreads_or(!ok)) ok = false;
+    bool issued = false;   // (thread 0)
+    if (ok && t == 0) {
+        issued = true;
         tc_fence_after_sync();
-        if (__syncthreads_or(!ok)) ok = false;
-        if (!ok) break;
+        constexpr uint32_t idS = idesc_bf16_f32(128, 128, true, true);
+        const uint32_t sB = smem_addr(sm.Bt), sX = smem_addr(sm.X);
+        const uint32_t lboA = smem_addr(sm.X) - sB, lboB = smem_addr(sm.XR) - sX;
+#pragma unroll
+        for (int kk = 0; kk < kQ / 16; ++kk)
+            mma_bf16_ss(tmem, smem_desc(sB + kk * 2048, lboA, 1024, kSwizzle128B),
+                        smem_desc(sX + kk * 2048, lboB, 1024, kSwizzle128B), idS, kk > 0);
+        mma_commit(&sm.bar_mma);
+    }
+    if (ok) ok = mbar_wait_bounded(&sm.bar_mma, 0, &never, kWaitLimitNs);
+    tc_fence_after_sync();
+    if (__syncthreads_or(!ok)) ok = false;
+    if (ok) {
         // lanes n = t < 64: Sf, Sr rows as bf16, staged (swizzled chunks) in
-        // the free x buffers, then two bulk copies of 8 KB
+        // the x buffers (the product has read them), then two bulk copies of 8 KB
         if (warp < 2) {
             const uint32_t lb = uint32_t(warp * 32) << 16;
+            uint32_t vv[2][32];
+            tmem_ld32_async(tmem + lb, vv[0]);
+            tmem_ld32_async(tmem + lb + 32, vv[1]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                uint32_t vv[32];
-                tmem_ld32_async(tmem + lb + q * 32, vv);
-                tmem_wait_tie(vv);
-                uint4 *row = reinterpret_cast<uint4 *>((q < 2 ? sm.X[buf] : sm.XR) + t * 128);
+                tmem_wait_tie(vv[q & 1]);
+                uint4 *row = reinterpret_cast<uint4 *>((q < 2 ? sm.X : sm.XR) + t * 128);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     row[((q & 1) * 4 + j) ^ (t & 7)] = make_uint4(
-                        pack_bf16(__uint_as_float(vv[8 * j]), __uint_as_float(vv[8 * j + 1])),
-                        pack_bf16(__uint_as_float(vv[8 * j + 2]), __uint_as_float(vv[8 * j + 3])),
-                        pack_bf16(__uint_as_float(vv[8 * j + 4]), __uint_as_float(vv[8 * j + 5])),
-                        pack_bf16(__uint_as_float(vv[8 * j + 6]), __uint_as_float(vv[8 * j + 7])));
+                        pack_bf16(__uint_as_float(vv[q & 1][8 * j]), __uint_as_float(vv[q & 1][8 * j + 1])),
+                        pack_bf16(__uint_as_float(vv[q & 1][8 * j + 2]), __uint_as_float(vv[q & 1][8 * j + 3])),
+                        pack_bf16(__uint_as_float(vv[q & 1][8 * j + 4]), __uint_as_float(vv[q & 1][8 * j + 5])),
+                        pack_bf16(__uint_as_float(vv[q & 1][8 * j + 6]), __uint_as_float(vv[q & 1][8 * j + 7])));
+                if (q < 2) tmem_ld32_async(tmem + lb + (q + 2) * 32, vv[q & 1]);
             }
         }
         fence_proxy_async_smem();
-        tc_fence_before_sync();
         __syncthreads();
         if (t == 0) {
-            bulk_store(prm.chunk + ((size_t(bh) * 2 + 0) * nc + c) * kState, sm.X[buf], kState);
+            bulk_store(prm.chunk + ((size_t(bh) * 2 + 0) * nc + c) * kState, sm.X, kState);
             bulk_store(prm.chunk + ((size_t(bh) * 2 + 1) * nc + c) * kState, sm.XR, kState);
             bulk_commit();
             prm.tot[size_t(bh) * kMaxTiles + c] = tot;
-            bulk_wait_read0();            // X[buf] and XR may be overwritten
-            if (k + 2 < nk) load(k + 2);
+            bulk_wait0();                 // the states have been written
         }
-        __syncthreads();                  // XR is free for the next tile's weights
-    }
-    if (!ok && t == 0) {
+    } else if (t == 0) {
         atomicOr(&g_device_error, 1u);
         // a product may still be in flight: give it a bounded chance to finish
         mma_commit(&sm.bar_mma);
-        (void)mbar_wait_bounded(&sm.bar_mma, ph_mma, &never, 100000000ull);
+        (void)mbar_wait_bounded(&sm.bar_mma, issued ? 1u : 0u, &never, 100000000ull);
     }
-    if (t == 0) bulk_wait0();             // the states have been written
     pdl_launch_dependents();
     tc_fence_before_sync();
     __syncthreads();
@@ -1007,9 +971,8 @@ cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float 
         if (err == cudaSuccess && fa.numRegs < int(kLaunchRegs)) err = cudaErrorNotSupported;
     }
     if (err == cudaSuccess) {
-        // pass 1: two CTAs per SM, each walking its tiles
-        const int64_t g1 = units64 < 2 * int64_t(num_sms) ? units64 : 2 * int64_t(num_sms);
-        kst<<<dim3(unsigned(g1)), dim3(128), smem_st, stream>>>(tmB, tmX, prm);
+        // pass 1: one CTA per tile
+        kst<<<dim3(unsigned(units64)), dim3(128), smem_st, stream>>>(tmB, tmX, prm);
         err = cudaGetLastError();
     }
     if (err == cudaSuccess) {
