@@ -43,7 +43,7 @@ bool supported(int64_t P, int64_t N);
 template <typename Tin>
 cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *Bm, const Tin *Cm,
                    const float *D, float *y, int64_t Bs, int64_t L, int64_t H, int64_t P,
-                   int64_t N, bool bidir, const ScanOpts *opt, cudaStream_t st);
+                   int64_t N, bool bidir, int num_sms, const ScanOpts *opt, cudaStream_t st);
 }
 namespace bidir {
 cudaError_t take_device_error(unsigned int *out);
@@ -206,11 +206,11 @@ ssm_status_t ssd_entry(const void *x, const void *dt, const float *A_head, const
             return from_cuda(ssm::ssd_general::launch<bf>(
                 static_cast<const bf *>(x), static_cast<const bf *>(dt), A_head,
                 static_cast<const bf *>(B), static_cast<const bf *>(C), D, y, Bs, L, H, P, N,
-                bidirectional != 0, opts ? &o : nullptr, st));
+                bidirectional != 0, dev.num_sms, opts ? &o : nullptr, st));
         return from_cuda(ssm::ssd_general::launch<float>(
             static_cast<const float *>(x), static_cast<const float *>(dt), A_head,
             static_cast<const float *>(B), static_cast<const float *>(C), D, y, Bs, L, H, P, N,
-            bidirectional != 0, opts ? &o : nullptr, st));
+            bidirectional != 0, dev.num_sms, opts ? &o : nullptr, st));
     }
     if (noalloc)
         return from_cuda(ssm::ssd::launch_noalloc(static_cast<const bf *>(x),

@@ -37,11 +37,13 @@ struct Args {
     int dt_softplus, dt_limit;
 };
 
-template <typename Tin>
+// The staged rows of kT steps: the slice's x columns, B and C rows padded
+// to the 32 NL states the kernel instance holds.
+template <typename Tin, int PW, int NL>
 struct Tile {
-    Tin x[kT][128];
-    Tin B[kT][256];
-    Tin C[kT][256];
+    Tin x[kT][8 * PW];
+    Tin B[kT][32 * NL];
+    Tin C[kT][32 * NL];
     float dt[kT];
 };
 
@@ -50,8 +52,8 @@ struct Tile {
 // 16-byte asynchronous copies (slices and rows are multiples of 16 bytes; the
 // entry points require 16-byte aligned x, B, C).  Rows outside [0, L) are
 // zero filled.
-template <typename Tin>
-__device__ __forceinline__ void stage_rows(Tile<Tin> &s, const Args &a, int64_t b, int h, int g,
+template <typename Tin, typename TileT>
+__device__ __forceinline__ void stage_rows(TileT &s, const Args &a, int64_t b, int h, int g,
                                            int p0, int ps, int t0, bool rev) {
     constexpr int EPC = 16 / sizeof(Tin);
     const Tin *x = static_cast<const Tin *>(a.x);
@@ -95,7 +97,8 @@ template <typename Tin, int PW, int NL>
 __global__ void __launch_bounds__(kThreads)
 ssd_general_kernel(Args a, int pass, int gate_now) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    Tile<Tin> *tiles = reinterpret_cast<Tile<Tin> *>(smem_raw);
+    using TileT = Tile<Tin, PW, NL>;
+    TileT *tiles = reinterpret_cast<TileT *>(smem_raw);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     constexpr int PS = kWarps * PW;              // rows of this CTA's slice
     const int bh = blockIdx.x / a.slices;
@@ -125,7 +128,7 @@ ssd_general_kernel(Args a, int pass, int gate_now) {
     cp_async_wait<0>();
     __syncthreads();
     for (int k = 0; k < ntiles; ++k) {
-        Tile<Tin> &s = tiles[k & 1];
+        TileT &s = tiles[k & 1];
         // the next tile's copies run while this one is used
         float dnext = 0.0f;
         if (k + 1 < ntiles) {
@@ -193,7 +196,7 @@ ssd_general_kernel(Args a, int pass, int gate_now) {
 
 template <typename Tin, int PW, int NL>
 static cudaError_t run(const Args &a, int64_t grid, bool bidir, cudaStream_t st) {
-    const int smem = int(2 * sizeof(Tile<Tin>));
+    const int smem = int(2 * sizeof(Tile<Tin, PW, NL>));
     auto kern = ssd_general_kernel<Tin, PW, NL>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
@@ -228,11 +231,13 @@ bool supported(int64_t P, int64_t N) { return pow2_16_256(P) && pow2_16_256(N); 
 template <typename Tin>
 cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *Bm, const Tin *Cm,
                    const float *D, float *y, int64_t Bs, int64_t L, int64_t H, int64_t P,
-                   int64_t N, bool bidir, const ScanOpts *opt, cudaStream_t st) {
+                   int64_t N, bool bidir, int num_sms, const ScanOpts *opt, cudaStream_t st) {
     if (!supported(P, N)) return cudaErrorNotSupported;
     // slice height: at most 64 state values per thread (16 rows per warp of
-    // up to 4 columns, or 8 rows of 8 columns when N = 256)
-    const int64_t ps = std::min<int64_t>(P, N == 256 ? 64 : 128);
+    // up to 4 columns, or 8 rows of 8 columns when N = 256), and narrower
+    // slices (down to 16 rows) while there are fewer than two CTAs per SM
+    int64_t ps = std::min<int64_t>(P, N == 256 ? 64 : 128);
+    while (ps > 16 && Bs * H * (P / ps) < 2 * int64_t(num_sms)) ps /= 2;
     const int64_t grid = Bs * H * (P / ps);
     if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const ScanOpts none{};
@@ -257,11 +262,11 @@ cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *
 
 template cudaError_t launch<float>(const float *, const float *, const float *, const float *,
                                    const float *, const float *, float *, int64_t, int64_t, int64_t,
-                                   int64_t, int64_t, bool, const ScanOpts *, cudaStream_t);
+                                   int64_t, int64_t, bool, int, const ScanOpts *, cudaStream_t);
 template cudaError_t launch<__nv_bfloat16>(const __nv_bfloat16 *, const __nv_bfloat16 *,
                                            const float *, const __nv_bfloat16 *,
                                            const __nv_bfloat16 *, const float *, float *, int64_t,
-                                           int64_t, int64_t, int64_t, int64_t, bool,
+                                           int64_t, int64_t, int64_t, int64_t, bool, int,
                                            const ScanOpts *, cudaStream_t);
 
 }  // namespace ssd_general
