@@ -15,6 +15,11 @@ step, ED = H*P for the chunked scan, both directions counted when
 bidirectional) over all ranks.  Inputs rotate over several resident sets so
 no step finds its inputs in L2 (> 2x L2 bytes between reuses).
 
+``e2e`` is the same metric through the public API with host buffers: each
+step copies its inputs from pinned host memory, makes the call and copies y
+back to pinned host memory, the three on three streams over a few device
+buffer sets so that one step's copies overlap its neighbours' calls.
+
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
 same workload on this host's cores (the reference arm).
 """
@@ -365,6 +370,7 @@ def out_shape(w):
     return (s["Bs"], s["L"], s["H"], s["P"])
 
 
+E2E_SETS = 3          # device buffer sets the end-to-end leg cycles through
 L2_POLICY = "inputs rotate over resident sets, > 2x L2 bytes between reuses"
 
 
@@ -579,20 +585,45 @@ def run_ours(args, rank, world, local):
     sampler.stop()
     clocks = sampler.summary(t_wall0 - 0.6, t_wall1 + 0.4)
 
-    # End to end through the public API with host buffers: pinned H2D of the
-    # step's inputs, the call, D2H of y, every step.
+    # End to end through the public API with host buffers: every step copies
+    # its inputs from pinned host memory, makes the call and copies y back to
+    # pinned host memory.  The three run on three streams over NB device
+    # buffer sets, so that the copies of one step overlap the calls of its
+    # neighbours (a set is refilled only once its previous call has read it
+    # and its previous y has been copied out).
     pinned = {n: (t.pin_memory() if t is not None else None) for n, t in host.items()}
     y_host = torch.empty(out_shape(w), dtype=torch.float32).pin_memory()
-    dbuf = bufs[0]
     h2d = sum(t.numel() * t.element_size() for t in pinned.values() if t is not None)
     d2h = y_host.numel() * 4
     k_e2e = 0 if (args.quick or args.mode == "bwd") else max(1, min(args.steps, 200))
-    for _ in range(0 if args.quick else 2):
-        for n, t in pinned.items():
-            if t is not None:
-                dbuf[n].copy_(t, non_blocking=True)
-        step(0)
-        y_host.copy_(dbuf["y"], non_blocking=True)
+    nb = min(nsets, E2E_SETS)
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    in_done = [torch.cuda.Event() for _ in range(nb)]
+    comp_done = [torch.cuda.Event() for _ in range(nb)]
+    out_done = [torch.cuda.Event() for _ in range(nb)]
+
+    def e2e_step(k):
+        j = k % nb
+        with torch.cuda.stream(s_in):
+            if k >= nb:
+                s_in.wait_event(comp_done[j])      # the call of step k - nb has read set j
+            for n, t in pinned.items():
+                if t is not None:
+                    bufs[j][n].copy_(t, non_blocking=True)
+            in_done[j].record(s_in)
+        stream.wait_event(in_done[j])
+        if k >= nb:
+            stream.wait_event(out_done[j])         # y of step k - nb has left set j
+        step(j)
+        comp_done[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[j])
+            y_host.copy_(bufs[j]["y"], non_blocking=True)
+            out_done[j].record(s_out)
+
+    for k in range(0 if args.quick else 2 * nb):
+        e2e_step(k)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -600,12 +631,12 @@ def run_ours(args, rank, world, local):
     f1 = torch.cuda.Event(enable_timing=True)
     with nvtx_range("%s %s: %d end-to-end steps" % (w.name, args.mode, k_e2e)):
         f0.record(stream)
-        for _ in range(k_e2e):
-            for n, t in pinned.items():
-                if t is not None:
-                    dbuf[n].copy_(t, non_blocking=True)
-            step(0)
-            y_host.copy_(dbuf["y"], non_blocking=True)
+        s_in.wait_event(f0)
+        s_out.wait_event(f0)
+        for k in range(k_e2e):
+            e2e_step(k)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
         f1.record(stream)
     torch.cuda.synchronize(dev)
     ms_e2e = f0.elapsed_time(f1) if k_e2e else float("nan")
@@ -637,7 +668,9 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": k_e2e},
+                "d2h_bytes_per_step": d2h, "steps": k_e2e,
+                "pipeline": "H2D, call and D2H of each step on three streams over %d device "
+                            "buffer sets" % nb},
         "gpu_launches": args.steps * launches_per_step,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.mode == "fwd":
@@ -645,7 +678,7 @@ def run_ours(args, rank, world, local):
         line["cpu_baseline"], parity = cpu_baseline(w, args.cpu_seconds, y_gpu=bufs[0]["y"])
         line["parity"] = parity
     if rank == 0 and world == 1 and args.mode == "fwd" and not (args.quick or args.no_configs):
-        del step, bufs, dbuf
+        del step, bufs
         torch.cuda.empty_cache()
         line["configs"] = configs_leg(lrs, dev, peaks)
     if world > 1:
