@@ -137,46 +137,64 @@ ssd_general_kernel(Args a, int pass, int gate_now) {
         }
         cp_async_commit();
         const int steps = min(kT, a.L - k * kT);
-        for (int j = 0; j < steps; ++j) {
-            const float d = s.dt[j];
-            const float dec = ex2(d * A2);
-            float bv[NL], cv[NL];
+        // Batches of kBatch steps: each lane keeps its partial sums of the
+        // batch's PW rows (32 values), then one reduce-scatter over the warp
+        // (31 shuffles) leaves lane l with the whole sum of value l = (step,
+        // row) -- so the shuffle latencies overlap and each lane writes one
+        // output.  Rows past L have dt = 0 and zero inputs: the state passes
+        // through them unchanged, and their outputs are not written.
+        constexpr int kBatch = 32 / PW;
+#pragma unroll 1
+        for (int j0 = 0; j0 < kT; j0 += kBatch) {
+            if (j0 >= steps) break;
+            float v[32];
 #pragma unroll
-            for (int q = 0; q < NL; ++q) {
-                // (N = 16: lanes past N hold no state and add nothing)
-                const bool n_ok = NL > 1 || lane + 32 * q < a.N;
-                bv[q] = n_ok ? to_f32(s.B[j][lane + 32 * q]) : 0.0f;
-                cv[q] = n_ok ? to_f32(s.C[j][lane + 32 * q]) : 0.0f;
-            }
-            float yp[PW];
-#pragma unroll
-            for (int i = 0; i < PW; ++i) {
-                const float dx = d * to_f32(s.x[j][w + kWarps * i]);
-                float acc = 0.0f;
+            for (int jj = 0; jj < kBatch; ++jj) {
+                const int j = j0 + jj;
+                const float d = s.dt[j];
+                const float dec = ex2(d * A2);
+                float bv[NL], cv[NL];
 #pragma unroll
                 for (int q = 0; q < NL; ++q) {
-                    st[i][q] = fmaf(dec, st[i][q], dx * bv[q]);
-                    acc = fmaf(st[i][q], cv[q], acc);
+                    // (N = 16: lanes past N hold no state and add nothing)
+                    const bool n_ok = NL > 1 || lane + 32 * q < a.N;
+                    bv[q] = n_ok ? to_f32(s.B[j][lane + 32 * q]) : 0.0f;
+                    cv[q] = n_ok ? to_f32(s.C[j][lane + 32 * q]) : 0.0f;
                 }
-                yp[i] = acc;
+#pragma unroll
+                for (int i = 0; i < PW; ++i) {
+                    const float dx = d * to_f32(s.x[j][w + kWarps * i]);
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < NL; ++q) {
+                        st[i][q] = fmaf(dec, st[i][q], dx * bv[q]);
+                        acc = fmaf(st[i][q], cv[q], acc);
+                    }
+                    v[jj * PW + i] = acc;
+                }
             }
+            // reduce-scatter: at distance o the lanes with bit o set keep the
+            // upper half of their values, the others the lower half
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
+            for (int o = 16, half = 16; o > 0; o >>= 1, half >>= 1) {
+                const bool up = (lane & o) != 0;
 #pragma unroll
-                for (int i = 0; i < PW; ++i) yp[i] += __shfl_xor_sync(0xffffffffu, yp[i], o);
-            // lane i of the warp writes row p = p0 + w + 8 i
-            const int t = rev ? a.L - 1 - (k * kT + j) : k * kT + j;
-#pragma unroll
-            for (int i = 0; i < PW; ++i) {
-                if (lane == i) {
-                    const int pl = w + kWarps * i;
-                    const int64_t o = ((b * a.L + t) * a.H + h) * a.P + p0 + pl;
-                    float v = yp[i];
-                    if (rev) v += a.y[o];                       // forward part, written by pass 0
-                    else v = fmaf(Dh, to_f32(s.x[j][pl]), v);
-                    if (gate_now && zg) v *= silu_fast(to_f32(zg[o]));
-                    a.y[o] = v;
+                for (int e = 0; e < half; ++e) {
+                    const float send = up ? v[e] : v[e + half];
+                    const float keep = up ? v[e + half] : v[e];
+                    v[e] = keep + __shfl_xor_sync(0xffffffffu, send, o);
                 }
+            }
+            // lane l: value l = (step j0 + l / PW, row w + 8 (l % PW))
+            const int j = j0 + lane / PW, pl = w + kWarps * (lane % PW);
+            if (j < steps) {
+                const int t = rev ? a.L - 1 - (k * kT + j) : k * kT + j;
+                const int64_t o = ((b * a.L + t) * a.H + h) * a.P + p0 + pl;
+                float val = v[0];
+                if (rev) val += a.y[o];                       // forward part, written by pass 0
+                else val = fmaf(Dh, to_f32(s.x[j][pl]), val);
+                if (gate_now && zg) val *= silu_fast(to_f32(zg[o]));
+                a.y[o] = val;
             }
         }
         cp_async_wait<0>();
