@@ -142,3 +142,17 @@ def test_bounded_wait_reports_timeout(cuda_device):
     y = lrs.ssd_chunk_scan_fwd(**{k: v.to(cuda_device) for k, v in inp.items()})
     torch.cuda.synchronize()
     _check(y, oracle.ssd_scan(**inp))
+
+
+@pytest.mark.parametrize("L", [1, 2, 127, 129, 384, 511, 512, 513])
+@pytest.mark.parametrize("groups", [1, 2])
+def test_short_bidirectional_boundaries(cuda_device, L, groups):
+    """The bidirectional scan with N = 64 runs as two passes over independent
+    tiles for up to four 128-row tiles (L <= 512) and on the single-role
+    kernel beyond: both sides of that boundary, one and two rows into a
+    tile, and groups of B, C, against the oracle."""
+    Bs, H = 2, 4
+    inp = workloads.ssd_inputs(Bs, L, H, 64, 64, "bf16", seed=L + 7 * groups, groups=groups)
+    ref = oracle.ssd_scan(**inp, bidirectional=True)
+    y = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=128, bidirectional=True)
+    _check(y, ref)

@@ -111,3 +111,22 @@ def test_fp32_inputs_at_the_ssd_workload_size_sampled(cuda_device):
     for u in (5, 6):
         b, h = divmod(u, s["H"])
         _close(torch.from_numpy(y[b, :, h]), ref[b, :, h], "f32", "y head %d" % u)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("Bs,L,H,P,N", [
+    (4, 37, 80, 128, 64),    # 320 (b, h): 128-row slices, 16 rows per warp
+    (2, 50, 160, 64, 128),   # 320 (b, h): 64-row slices, 8 rows per warp
+    (2, 45, 160, 32, 32),    # 320 (b, h): 32-row slices, 4 rows per warp
+])
+def test_general_path_wide_slices(cuda_device, dtype, Bs, L, H, P, N):
+    """Shapes with enough (b, h) pairs that the rows are not cut below the
+    register limit, so each warp holds 4 to 16 rows of the state."""
+    if dtype == "bf16" and P == 64 and N in (64, 128):
+        pytest.skip("the tensor-core kernel's shape")
+    inp = workloads.ssd_inputs(Bs, L, H, P, N, dtype, seed=L + P)
+    for bidir in (False, True):
+        ref = oracle.ssd_scan(**inp, bidirectional=bidir)
+        y = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=128, bidirectional=bidir)
+        torch.cuda.synchronize()
+        _close(y, ref, dtype)
