@@ -289,6 +289,39 @@ SSM_API ssm_status_t ssd_chunk_scan_bwd(const void *x, const void *dt, const flo
                                         int bidirectional, int input_bf16, void *stream);
 
 /*
+ * Gradients of the chunked scalar-decay scan with its options (the scan of
+ * ssd_chunk_scan_fwd_ex): besides the outputs of ssd_chunk_scan_bwd, the
+ * gradients the chunked backward of "Some questions of Bi-Mamba2 and Hydra"
+ * (Bi-Mamba2 issue 1) returns for its options:
+ *   dz       : (Bs, L, H, P) fp32, overwritten -- required when opts->z is set
+ *   ddt_bias : (H) fp32, overwritten when opts->dt_bias is set (may be NULL)
+ *   dh0      : (Bs, H, P, N) fp32, overwritten when opts->h0 is set (may be NULL)
+ * dt is given before the options (bias, softplus, clamp) and ddt is the
+ * gradient with respect to it; where the clamp is active ddt is 0.  With
+ * v = dt + dt_bias, s = softplus(v) (or v), dte = clamp(s) (or s),
+ * u = scan(dte) + D x and y = u silu(z): dz = dy u silu'(z), the scan's
+ * gradients are taken for dy silu(z) from h0, and ddt = d dte [lo <= s <= hi]
+ * sig(v).  opts->ngroups gives the groups of B, C; opts->h_final must be NULL
+ * (SSM_ERR_INVALID_ARG); h0 with the bidirectional scan: SSM_ERR_UNSUPPORTED.
+ * Support and the remaining rules as ssd_chunk_scan_bwd; x, B, C must be
+ * 16-byte aligned, z aligned to its element size.  Computed on CUDA cores by
+ * composition: the options' elementwise steps, the forward scan without z
+ * (for u), the plain gradients and one kernel for the terms of h0; bf16
+ * inputs are widened to fp32 first.  Takes stream-ordered scratch of about
+ * (2 Bs L H + [bf16] Bs L H P + 2 Bs L G N + [z] 2 Bs L H P + [h0] Bs H L) * 4
+ * bytes besides that of ssd_chunk_scan_bwd.  ddt_bias is summed in a fixed
+ * order; dA_head, dB, dC, dD are formed with atomic additions.
+ */
+SSM_API ssm_status_t ssd_chunk_scan_bwd_ex(const void *x, const void *dt, const float *A_head,
+                                           const void *B, const void *C, const float *D,
+                                           const float *dy, float *dx, float *ddt,
+                                           float *dA_head, float *dB, float *dC, float *dD,
+                                           float *dz, float *ddt_bias, float *dh0, int64_t Bs,
+                                           int64_t L, int64_t H, int64_t P, int64_t N,
+                                           int bidirectional, int input_bf16,
+                                           const ssm_scan_options_t *opts, void *stream);
+
+/*
  * Synchronise `stream` and report whether a kernel of this library running on
  * the current device gave up a bounded wait (SSM_ERR_DEVICE_TIMEOUT) since
  * the previous check; the record is cleared by the call.  Kernels never hang

@@ -55,6 +55,8 @@ SIGNATURES = {
     "ssm_scan_fwd_ex": ([_VP] * 7 + [_I64] * 4 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
     "ssm_scan_bwd": ([_VP] * 13 + [_I64] * 4 + [ctypes.c_int, _VP], ctypes.c_int),
     "ssd_chunk_scan_bwd": ([_VP] * 13 + [_I64] * 6 + [ctypes.c_int, ctypes.c_int, _VP], ctypes.c_int),
+    "ssd_chunk_scan_bwd_ex": ([_VP] * 16 + [_I64] * 5 + [ctypes.c_int, ctypes.c_int, _VP, _VP],
+                              ctypes.c_int),
     "ssd_chunk_scan_fwd_ex": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, ctypes.c_int, _VP, _VP],
                               ctypes.c_int),
     "ssm_check_device_errors": ([_VP], ctypes.c_int),
@@ -302,10 +304,13 @@ def ssm_scan_bwd(x, delta, A, B, C, D, dy):
     return g
 
 
-def ssd_chunk_scan_bwd(x, dt, A_head, B, C, D, dy, bidirectional: bool = False):
-    """Gradients of the chunked scan (no options) for the upstream gradient
-    dy (fp32, shaped like y): dict(dx, ddt, dA, dB, dC, dD) as fp32 tensors
-    (dB, dC shaped like B, C; dD is None when D is None)."""
+def ssd_chunk_scan_bwd(x, dt, A_head, B, C, D, dy, bidirectional: bool = False, **options):
+    """Gradients of the chunked scan for the upstream gradient dy (fp32,
+    shaped like y): dict(dx, ddt, dA, dB, dC, dD) as fp32 tensors (dB, dC
+    shaped like B, C; dD is None when D is None).  With the forward scan's
+    options (dt_bias, dt_softplus, dt_limit, z, h0) the dict also holds dz,
+    ddt_bias and dh0 (None when the matching option is off), and ddt is the
+    gradient with respect to dt before the options."""
     import torch
     dev = x.device
     if dev.type != "cuda":
@@ -330,6 +335,23 @@ def ssd_chunk_scan_bwd(x, dt, A_head, B, C, D, dy, bidirectional: bool = False):
     g = dict(dx=torch.empty((Bs, L, H, P), **f32), ddt=torch.empty((Bs, L, H), **f32),
              dA=torch.empty(H, **f32), dB=torch.empty(bc, **f32), dC=torch.empty(bc, **f32),
              dD=None if D is None else torch.empty(H, **f32))
+    bad = set(options) - (set(_OPTION_KEYS) - {"return_final_state"})
+    if bad:
+        raise TypeError("unknown options: %s" % sorted(bad))
+    if options:
+        o, _, keep = _options(x, H, (Bs, H, P, N), dev, ngroups=G, **options)
+        g["dz"] = torch.empty((Bs, L, H, P), **f32) if options.get("z") is not None else None
+        g["ddt_bias"] = torch.empty(H, **f32) if options.get("dt_bias") is not None else None
+        g["dh0"] = torch.empty((Bs, H, P, N), **f32) if options.get("h0") is not None else None
+        st = library().ssd_chunk_scan_bwd_ex(
+            _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(g["dx"]),
+            _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+            _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dh0"]), Bs, L, H, P, N,
+            int(bool(bidirectional)), int(x.dtype == torch.bfloat16), ctypes.byref(o),
+            _stream(dev))
+        if st != 0:
+            raise SsmError("ssd_chunk_scan_bwd_ex", st)
+        return g
     st = library().ssd_chunk_scan_bwd(
         _ptr(x), _ptr(dt), _ptr(A_head), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(g["dx"]),
         _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),

@@ -38,6 +38,14 @@ cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *
                    float *dC, float *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
                    int64_t G, bool bidir, cudaStream_t st);
 }
+namespace ssd_bwd_ex {
+template <typename Tin>
+cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *Bm, const Tin *Cm,
+                   const float *D, const float *dy, float *dx, float *ddt, float *dA, float *dB,
+                   float *dC, float *dD, float *dz, float *ddt_bias, float *dh0, int64_t Bs,
+                   int64_t L, int64_t H, int64_t P, int64_t N, int64_t G, bool bidir,
+                   const ScanOpts &o, int num_sms, cudaStream_t st);
+}
 namespace ssd_general {
 bool supported(int64_t P, int64_t N);
 template <typename Tin>
@@ -344,6 +352,55 @@ ssm_status_t ssd_chunk_scan_bwd(const void *x, const void *dt, const float *A_he
         static_cast<const float *>(x), static_cast<const float *>(dt), A_head,
         static_cast<const float *>(B), static_cast<const float *>(C), D, dy, dx, ddt, dA_head, dB,
         dC, dD, Bs, L, H, P, N, ngroups, bidirectional != 0, st));
+}
+
+ssm_status_t ssd_chunk_scan_bwd_ex(const void *x, const void *dt, const float *A_head,
+                                   const void *B, const void *C, const float *D, const float *dy,
+                                   float *dx, float *ddt, float *dA_head, float *dB, float *dC,
+                                   float *dD, float *dz, float *ddt_bias, float *dh0, int64_t Bs,
+                                   int64_t L, int64_t H, int64_t P, int64_t N, int bidirectional,
+                                   int input_bf16, const ssm_scan_options_t *opts, void *stream) {
+    if (!x || !dt || !A_head || !B || !C || !dy || !dx || !ddt || !dA_head || !dB || !dC)
+        return SSM_ERR_INVALID_ARG;
+    const int64_t G = (opts && opts->ngroups > 1) ? opts->ngroups : 1;
+    if ((opts && opts->ngroups < 0) || !sizes_ok({Bs, L, H, P}) || !sizes_ok({Bs, L, G, N}) ||
+        !sizes_ok({Bs, H, L, P, N}))
+        return SSM_ERR_INVALID_ARG;
+    if (opts && opts->h_final) return SSM_ERR_INVALID_ARG;       // an output of the forward only
+    if (opts && opts->z && !dz) return SSM_ERR_INVALID_ARG;
+    if (bidirectional && opts && opts->h0) return SSM_ERR_UNSUPPORTED;
+    if (!ssm::ssd_bwd::supported(P, N) || H % G != 0 || Bs * H > INT_MAX || L > INT_MAX)
+        return SSM_ERR_UNSUPPORTED;
+    const size_t es = input_bf16 ? 2 : 4;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(dt, es) ||
+        !aligned(A_head, 4) || (D && !aligned(D, 4)) || !aligned(dy, 4) || !aligned(dx, 4) ||
+        !aligned(ddt, 4) || !aligned(dA_head, 4) || !aligned(dB, 4) || !aligned(dC, 4) ||
+        (dD && !aligned(dD, 4)) || (dz && !aligned(dz, 4)) || (ddt_bias && !aligned(ddt_bias, 4)) ||
+        (dh0 && !aligned(dh0, 4)))
+        return SSM_ERR_ALIGNMENT;
+    ssm_status_t s = check_options(opts, es);
+    if (s != SSM_OK) return s;
+    DeviceInfo dev;
+    s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    ssm::ScanOpts o{};
+    if (opts)
+        o = ssm::ScanOpts{opts->dt_bias, opts->z, opts->h0, nullptr, opts->dt_min,
+                          opts->dt_max, opts->dt_softplus, opts->dt_limit, opts->ngroups};
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    using bf = __nv_bfloat16;
+    float *dzo = o.z ? dz : nullptr;
+    float *dbo = o.dt_bias ? ddt_bias : nullptr;
+    float *dho = o.h0 ? dh0 : nullptr;
+    if (input_bf16)
+        return from_cuda(ssm::ssd_bwd_ex::launch<bf>(
+            static_cast<const bf *>(x), static_cast<const bf *>(dt), A_head,
+            static_cast<const bf *>(B), static_cast<const bf *>(C), D, dy, dx, ddt, dA_head, dB, dC,
+            dD, dzo, dbo, dho, Bs, L, H, P, N, G, bidirectional != 0, o, dev.num_sms, st));
+    return from_cuda(ssm::ssd_bwd_ex::launch<float>(
+        static_cast<const float *>(x), static_cast<const float *>(dt), A_head,
+        static_cast<const float *>(B), static_cast<const float *>(C), D, dy, dx, ddt, dA_head, dB,
+        dC, dD, dzo, dbo, dho, Bs, L, H, P, N, G, bidirectional != 0, o, dev.num_sms, st));
 }
 
 ssm_status_t ssm_scan_fwd_plan(int64_t Bs, int64_t L, int64_t ED, int64_t N, int input_bf16,
