@@ -263,6 +263,32 @@ SSM_API ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float 
                                   int64_t ED, int64_t N, int input_bf16, void *stream);
 
 /*
+ * Gradients of the diagonal scan with its options (the scan of
+ * ssm_scan_fwd_ex): besides the outputs of ssm_scan_bwd,
+ *   dz       : (Bs, L, ED) fp32, overwritten -- required when opts->z is set
+ *   ddt_bias : (ED) fp32, overwritten when opts->dt_bias is set (may be NULL)
+ *   dh0      : (Bs, ED, N) fp32, overwritten when opts->h0 is set (may be NULL)
+ * delta is given before the options (bias, softplus, clamp) and ddelta is the
+ * gradient with respect to it (0 where the clamp is active); the chain rule
+ * as for ssd_chunk_scan_bwd_ex, per channel.  opts->h_final must be NULL
+ * (SSM_ERR_INVALID_ARG); groups are an SSD option (SSM_ERR_UNSUPPORTED).
+ * Support and the remaining rules as ssm_scan_bwd (N <= 16).  Computed on
+ * CUDA cores by composition: the options' elementwise steps, the forward scan
+ * without z (for the ungated output), the plain gradients and one kernel for
+ * the terms of h0; bf16 inputs are widened to fp32 first.  Takes
+ * stream-ordered scratch of about (2 + [bf16] 1 + [z] 2 + [h0] 1) Bs L ED * 4
+ * (+ [bf16] 2 Bs L N * 4) bytes besides that of ssm_scan_bwd.  ddt_bias is
+ * summed in a fixed order; dA, dB, dC, dD are formed with atomic additions.
+ */
+SSM_API ssm_status_t ssm_scan_bwd_ex(const void *x, const void *delta, const float *A,
+                                     const void *B, const void *C, const float *D,
+                                     const float *dy, float *dx, float *ddelta, float *dA,
+                                     float *dB, float *dC, float *dD, float *dz,
+                                     float *ddt_bias, float *dh0, int64_t Bs, int64_t L,
+                                     int64_t ED, int64_t N, int input_bf16,
+                                     const ssm_scan_options_t *opts, void *stream);
+
+/*
  * Gradients of the chunked scalar-decay scan (ssd_chunk_scan_fwd_ex without
  * options; unidirectional or bidirectional, groups of B, C): given dy, the
  * gradient of a loss with respect to y, writes the gradients with respect to

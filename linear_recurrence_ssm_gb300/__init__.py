@@ -55,6 +55,7 @@ SIGNATURES = {
     "ssm_scan_fwd_ex": ([_VP] * 7 + [_I64] * 4 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
     "ssm_scan_bwd": ([_VP] * 13 + [_I64] * 4 + [ctypes.c_int, _VP], ctypes.c_int),
     "ssd_chunk_scan_bwd": ([_VP] * 13 + [_I64] * 6 + [ctypes.c_int, ctypes.c_int, _VP], ctypes.c_int),
+    "ssm_scan_bwd_ex": ([_VP] * 16 + [_I64] * 4 + [ctypes.c_int, _VP, _VP], ctypes.c_int),
     "ssd_chunk_scan_bwd_ex": ([_VP] * 16 + [_I64] * 5 + [ctypes.c_int, ctypes.c_int, _VP, _VP],
                               ctypes.c_int),
     "ssd_chunk_scan_fwd_ex": ([_VP] * 7 + [_I64] * 6 + [ctypes.c_int, ctypes.c_int, _VP, _VP],
@@ -272,10 +273,13 @@ def ssd_chunk_scan_fwd(x, dt, A_head, B, C, D=None, chunk: int = 256,
     return y
 
 
-def ssm_scan_bwd(x, delta, A, B, C, D, dy):
+def ssm_scan_bwd(x, delta, A, B, C, D, dy, **options):
     """Gradients of the diagonal scan for the upstream gradient dy (fp32,
     shaped like y): dict(dx, ddelta, dA, dB, dC, dD) as fp32 tensors (dD is
-    None when D is None)."""
+    None when D is None).  With the forward scan's options (dt_bias,
+    dt_softplus, dt_limit, z, h0) the dict also holds dz, ddt_bias and dh0
+    (None when the matching option is off), and ddelta is the gradient with
+    respect to delta before the options."""
     import torch
     dev = x.device
     if dev.type != "cuda":
@@ -295,6 +299,22 @@ def ssm_scan_bwd(x, delta, A, B, C, D, dy):
     g = dict(dx=torch.empty((Bs, L, ED), **f32), ddelta=torch.empty((Bs, L, ED), **f32),
              dA=torch.empty((ED, N), **f32), dB=torch.empty((Bs, L, N), **f32),
              dC=torch.empty((Bs, L, N), **f32), dD=None if D is None else torch.empty(ED, **f32))
+    bad = set(options) - (set(_OPTION_KEYS) - {"return_final_state"})
+    if bad:
+        raise TypeError("unknown options: %s" % sorted(bad))
+    if options:
+        o, _, keep = _options(x, ED, (Bs, ED, N), dev, **options)
+        g["dz"] = torch.empty((Bs, L, ED), **f32) if options.get("z") is not None else None
+        g["ddt_bias"] = torch.empty(ED, **f32) if options.get("dt_bias") is not None else None
+        g["dh0"] = torch.empty((Bs, ED, N), **f32) if options.get("h0") is not None else None
+        st = library().ssm_scan_bwd_ex(
+            _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dy), _ptr(g["dx"]),
+            _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
+            _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dh0"]), Bs, L, ED, N,
+            int(x.dtype == torch.bfloat16), ctypes.byref(o), _stream(dev))
+        if st != 0:
+            raise SsmError("ssm_scan_bwd_ex", st)
+        return g
     st = library().ssm_scan_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dy),
                                 _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]),
                                 _ptr(g["dC"]), _ptr(g["dD"]), Bs, L, ED, N,

@@ -38,6 +38,14 @@ cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *
                    float *dC, float *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
                    int64_t G, bool bidir, cudaStream_t st);
 }
+namespace diag_bwd_ex {
+template <typename Tin>
+cudaError_t launch(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
+                   const float *D, const float *dy, float *dx, float *ddelta, float *dA, float *dB,
+                   float *dC, float *dD, float *dz, float *ddt_bias, float *dh0, int64_t Bs,
+                   int64_t L, int64_t ED, int64_t N, const ScanOpts &o, int num_sms,
+                   cudaStream_t st);
+}
 namespace ssd_bwd_ex {
 template <typename Tin>
 cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *Bm, const Tin *Cm,
@@ -318,6 +326,52 @@ ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float *A, cons
         static_cast<const float *>(x), static_cast<const float *>(delta), A,
         static_cast<const float *>(B), static_cast<const float *>(C), D, dy, dx, ddelta, dA, dB,
         dC, dD, Bs, L, ED, N, dev.num_sms, st));
+}
+
+ssm_status_t ssm_scan_bwd_ex(const void *x, const void *delta, const float *A, const void *B,
+                             const void *C, const float *D, const float *dy, float *dx,
+                             float *ddelta, float *dA, float *dB, float *dC, float *dD, float *dz,
+                             float *ddt_bias, float *dh0, int64_t Bs, int64_t L, int64_t ED,
+                             int64_t N, int input_bf16, const ssm_scan_options_t *opts,
+                             void *stream) {
+    if (!x || !delta || !A || !B || !C || !dy || !dx || !ddelta || !dA || !dB || !dC)
+        return SSM_ERR_INVALID_ARG;
+    if (!sizes_ok({Bs, L, ED}) || !sizes_ok({Bs, L, N}) || !sizes_ok({ED, N}))
+        return SSM_ERR_INVALID_ARG;
+    if (opts && opts->h_final) return SSM_ERR_INVALID_ARG;       // an output of the forward only
+    if (opts && opts->z && !dz) return SSM_ERR_INVALID_ARG;
+    if (opts && opts->ngroups > 1) return SSM_ERR_UNSUPPORTED;  // groups: SSD only
+    if (N > 16 || Bs > 65535 || L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    const size_t es = input_bf16 ? 2 : 4;
+    if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
+        !aligned(A, 4) || (D && !aligned(D, 4)) || !aligned(dy, 4) || !aligned(dx, 4) ||
+        !aligned(ddelta, 4) || !aligned(dA, 4) || !aligned(dB, 4) || !aligned(dC, 4) ||
+        (dD && !aligned(dD, 4)) || (dz && !aligned(dz, 4)) || (ddt_bias && !aligned(ddt_bias, 4)) ||
+        (dh0 && !aligned(dh0, 4)))
+        return SSM_ERR_ALIGNMENT;
+    ssm_status_t s = check_options(opts, es);
+    if (s != SSM_OK) return s;
+    DeviceInfo dev;
+    s = current_device(&dev);
+    if (s != SSM_OK) return s;
+    ssm::ScanOpts o{};
+    if (opts)
+        o = ssm::ScanOpts{opts->dt_bias, opts->z, opts->h0, nullptr, opts->dt_min,
+                          opts->dt_max, opts->dt_softplus, opts->dt_limit, 1};
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    using bf = __nv_bfloat16;
+    float *dzo = o.z ? dz : nullptr;
+    float *dbo = o.dt_bias ? ddt_bias : nullptr;
+    float *dho = o.h0 ? dh0 : nullptr;
+    if (input_bf16)
+        return from_cuda(ssm::diag_bwd_ex::launch<bf>(
+            static_cast<const bf *>(x), static_cast<const bf *>(delta), A,
+            static_cast<const bf *>(B), static_cast<const bf *>(C), D, dy, dx, ddelta, dA, dB, dC,
+            dD, dzo, dbo, dho, Bs, L, ED, N, o, dev.num_sms, st));
+    return from_cuda(ssm::diag_bwd_ex::launch<float>(
+        static_cast<const float *>(x), static_cast<const float *>(delta), A,
+        static_cast<const float *>(B), static_cast<const float *>(C), D, dy, dx, ddelta, dA, dB,
+        dC, dD, dzo, dbo, dho, Bs, L, ED, N, o, dev.num_sms, st));
 }
 
 ssm_status_t ssd_chunk_scan_bwd(const void *x, const void *dt, const float *A_head, const void *B,
