@@ -248,11 +248,15 @@ SSM_API ssm_status_t ssd_chunk_scan_fwd_ex(const void *x, const void *dt,
  *   dA         : (ED, N) fp32,  dB, dC : (Bs, L, N) fp32,  dD : (ED) fp32
  *                (zeroed by the call, then accumulated; dD may be NULL)
  * x, delta, B, C are fp32 (input_bf16 == 0) or bf16; A, D, dy are fp32.
- * Supported: N <= 16 (SSM_ERR_UNSUPPORTED otherwise), Bs <= 65535.  dx and
- * ddelta are deterministic; dA, dB, dC, dD are sums formed with atomic
- * additions, so their last bits may differ between runs.  Takes a
+ * Supported: N <= 256 (SSM_ERR_UNSUPPORTED otherwise), Bs <= 65535.  More
+ * than 16 states are taken in groups of 16 (the recurrence is separate per
+ * state): one gradient pass per group, dx and ddelta summed over the groups.
+ * dx and ddelta are deterministic; dA, dB, dC, dD are sums formed with
+ * atomic additions, so their last bits may differ between runs.  Takes a
  * stream-ordered scratch buffer of ceil(L/16)*Bs*ED*64 bytes for the
- * re-computation checkpoints.
+ * re-computation checkpoints, and for N > 16 another of about
+ * (2 Bs L ED + 2 Bs L 16 + 2 ED 16) * 4 + 2 Bs L 16 * elem bytes for one
+ * group's columns and its dx, ddelta.
  * Alignment: every pointer to its element size; dy, dx, ddelta, dA, dB, dC,
  * dD to 4 bytes.
  */
@@ -272,7 +276,7 @@ SSM_API ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float 
  * gradient with respect to it (0 where the clamp is active); the chain rule
  * as for ssd_chunk_scan_bwd_ex, per channel.  opts->h_final must be NULL
  * (SSM_ERR_INVALID_ARG); groups are an SSD option (SSM_ERR_UNSUPPORTED).
- * Support and the remaining rules as ssm_scan_bwd (N <= 16).  Computed on
+ * Support and the remaining rules as ssm_scan_bwd (N <= 256).  Computed on
  * CUDA cores by composition: the options' elementwise steps, the forward scan
  * without z (for the ungated output), the plain gradients and one kernel for
  * the terms of h0; bf16 inputs are widened to fp32 first.  Takes

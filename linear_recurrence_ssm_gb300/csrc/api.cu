@@ -305,7 +305,7 @@ ssm_status_t ssm_scan_bwd(const void *x, const void *delta, const float *A, cons
         return SSM_ERR_INVALID_ARG;
     if (!sizes_ok({Bs, L, ED}) || !sizes_ok({Bs, L, N}) || !sizes_ok({ED, N}))
         return SSM_ERR_INVALID_ARG;
-    if (N > 16 || Bs > 65535 || L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    if (N > 256 || Bs > 65535 || L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
     const size_t es = input_bf16 ? 2 : 4;
     if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
         !aligned(A, 4) || (D && !aligned(D, 4)) || !aligned(dy, 4) || !aligned(dx, 4) ||
@@ -341,7 +341,7 @@ ssm_status_t ssm_scan_bwd_ex(const void *x, const void *delta, const float *A, c
     if (opts && opts->h_final) return SSM_ERR_INVALID_ARG;       // an output of the forward only
     if (opts && opts->z && !dz) return SSM_ERR_INVALID_ARG;
     if (opts && opts->ngroups > 1) return SSM_ERR_UNSUPPORTED;  // groups: SSD only
-    if (N > 16 || Bs > 65535 || L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
+    if (N > 256 || Bs > 65535 || L > INT_MAX || ED > INT_MAX) return SSM_ERR_UNSUPPORTED;
     const size_t es = input_bf16 ? 2 : 4;
     if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
         !aligned(A, 4) || (D && !aligned(D, 4)) || !aligned(dy, 4) || !aligned(dx, 4) ||

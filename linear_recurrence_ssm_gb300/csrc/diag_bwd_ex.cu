@@ -36,12 +36,13 @@ namespace diag_bwd_ex {
 
 using namespace grad_opts;
 constexpr int kCh = 128;   // channels per CTA (one thread each)
-constexpr int kMaxN = 16;
+constexpr int kMaxN = 16;  // states held in registers per walk
 
 // The terms of h0: one thread per channel e of batch row blockIdx.y, walking
-// t; the dC_t[n] terms are summed over the warp's channels with shuffles and
-// added with one atomic per warp; q_t goes to scratch and a backward walk
-// forms its suffix sums.
+// t once per group of kMaxN states (their exponentials in registers); the
+// dC_t[n] terms are summed over the warp's channels with shuffles and added
+// with one atomic per warp; q_t, summed over the groups, goes to scratch and
+// a backward walk forms its suffix sums.
 __global__ void __launch_bounds__(kCh)
 h0_terms_kernel(const float *__restrict__ Cm, const float *__restrict__ g,
                 const float *__restrict__ dlt, const float *__restrict__ A,
@@ -50,49 +51,55 @@ h0_terms_kernel(const float *__restrict__ Cm, const float *__restrict__ g,
                 int L, int ED, int N) {
     const int b = blockIdx.y, e = blockIdx.x * kCh + threadIdx.x, lane = threadIdx.x & 31;
     const bool ok = e < ED;
-    float hv[kMaxN], a2[kMaxN], acc[kMaxN], dA_acc[kMaxN];
-#pragma unroll
-    for (int n = 0; n < kMaxN; ++n) {
-        const bool on = ok && n < N;
-        hv[n] = on ? h0[(size_t(b) * ED + e) * N + n] : 0.0f;
-        a2[n] = on ? A[size_t(e) * N + n] * SSM_LOG2E : 0.0f;
-        acc[n] = 0.0f;
-        dA_acc[n] = 0.0f;
-    }
-    double csum = 0.0;
-    for (int t = 0; t < L; ++t) {
-        const size_t i = (size_t(b) * L + t) * ED + e;
-        float gv = 0.0f;
-        if (ok) {
-            csum += double(dlt[i]);
-            gv = g[i];
-        }
-        const float cs = float(csum);
-        float qv = 0.0f;
+    for (int n0 = 0; n0 < N; n0 += kMaxN) {
+        const int nc = N - n0 < kMaxN ? N - n0 : kMaxN;
+        float hv[kMaxN], a2[kMaxN], acc[kMaxN], dA_acc[kMaxN];
 #pragma unroll
         for (int n = 0; n < kMaxN; ++n) {
-            if (n >= N) break;
-            const float c = Cm[(size_t(b) * L + t) * N + n];
-            const float E = ok ? ex2(a2[n] * cs) : 0.0f;
-            const float eh = E * hv[n];
-            acc[n] = fmaf(gv * c, E, acc[n]);
-            dA_acc[n] = fmaf(gv * c * cs, eh, dA_acc[n]);
-            qv = fmaf(c * a2[n], eh, qv);
-            // dC_t[n]: this warp's channels, then one atomic
-            float dc = gv * eh;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dc += __shfl_xor_sync(0xffffffffu, dc, o);
-            if (lane == 0 && dc != 0.0f) atomicAdd(&dC[(size_t(b) * L + t) * N + n], dc);
+            const bool on = ok && n < nc;
+            hv[n] = on ? h0[(size_t(b) * ED + e) * N + n0 + n] : 0.0f;
+            a2[n] = on ? A[size_t(e) * N + n0 + n] * SSM_LOG2E : 0.0f;
+            acc[n] = 0.0f;
+            dA_acc[n] = 0.0f;
         }
-        if (ok) q[i] = gv * qv * float(1.0 / SSM_LOG2E);   // (a2 carries log2 e)
+        double csum = 0.0;
+        for (int t = 0; t < L; ++t) {
+            const size_t i = (size_t(b) * L + t) * ED + e;
+            float gv = 0.0f;
+            if (ok) {
+                csum += double(dlt[i]);
+                gv = g[i];
+            }
+            const float cs = float(csum);
+            float qv = 0.0f;
+#pragma unroll
+            for (int n = 0; n < kMaxN; ++n) {
+                if (n >= nc) break;
+                const float c = Cm[(size_t(b) * L + t) * N + n0 + n];
+                const float E = ok ? ex2(a2[n] * cs) : 0.0f;
+                const float eh = E * hv[n];
+                acc[n] = fmaf(gv * c, E, acc[n]);
+                dA_acc[n] = fmaf(gv * c * cs, eh, dA_acc[n]);
+                qv = fmaf(c * a2[n], eh, qv);
+                // dC_t[n]: this warp's channels, then one atomic
+                float dc = gv * eh;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) dc += __shfl_xor_sync(0xffffffffu, dc, o);
+                if (lane == 0 && dc != 0.0f) atomicAdd(&dC[(size_t(b) * L + t) * N + n0 + n], dc);
+            }
+            // (a2 carries log2 e)
+            if (ok) q[i] = (n0 == 0 ? 0.0f : q[i]) + gv * qv * float(1.0 / SSM_LOG2E);
+        }
+        if (ok) {
+#pragma unroll
+            for (int n = 0; n < kMaxN; ++n) {
+                if (n >= nc) break;
+                if (dh0) dh0[(size_t(b) * ED + e) * N + n0 + n] = acc[n];
+                atomicAdd(&dA[size_t(e) * N + n0 + n], dA_acc[n]);
+            }
+        }
     }
     if (!ok) return;
-#pragma unroll
-    for (int n = 0; n < kMaxN; ++n) {
-        if (n >= N) break;
-        if (dh0) dh0[(size_t(b) * ED + e) * N + n] = acc[n];
-        atomicAdd(&dA[size_t(e) * N + n], dA_acc[n]);
-    }
     float run = 0.0f;
     for (int t = L - 1; t >= 0; --t) {
         const size_t i = (size_t(b) * L + t) * ED + e;

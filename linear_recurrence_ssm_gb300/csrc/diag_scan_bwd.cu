@@ -1,4 +1,5 @@
-// diag_scan_bwd.cu -- gradients of the diagonal selective scan (N <= 16).
+// diag_scan_bwd.cu -- gradients of the diagonal selective scan (N <= 256;
+// more than 16 states in groups of 16, see launch_bwd).
 //
 // Forward: h_t = a_t h_{t-1} + delta_t B_t x_t with a_t[n] = exp(delta_t A[e,n]),
 // y_t = C_t . h_t + D[e] x_t.  Given dy, the adjoint of the state runs
@@ -262,11 +263,12 @@ diag_bwd_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt, const fl
     }
 }
 
+// The gradients for at most kNP states.
 template <typename Tin>
-cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
-                       const float *D, const float *dy, float *dx, float *ddelta, float *dA,
-                       float *dB, float *dC, float *dD, int64_t Bs, int64_t L, int64_t ED,
-                       int64_t N, int num_sms, cudaStream_t st) {
+cudaError_t launch_bwd16(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm,
+                         const Tin *Cm, const float *D, const float *dy, float *dx,
+                         float *ddelta, float *dA, float *dB, float *dC, float *dD, int64_t Bs,
+                         int64_t L, int64_t ED, int64_t N, int num_sms, cudaStream_t st) {
     if (N > kNP) return cudaErrorNotSupported;
     if (Bs > 65535) return cudaErrorInvalidConfiguration;
     // parameter gradients are sums: start from zero
@@ -302,6 +304,109 @@ cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *
                                                dC, dD, int(Bs), int(L), int(ED), int(N));
             err = cudaGetLastError();
         }
+    }
+    cudaError_t e2 = cudaFreeAsync(scratch, st);
+    return err != cudaSuccess ? err : e2;
+}
+
+// More than kNP states.  The recurrence is separate per state n: y is a sum
+// over n, so dx and ddelta are sums over groups of states, while dA, dB, dC
+// hold one column per state and D enters once.  So the states are taken in
+// groups of kNP: each group's columns of A, B and C are gathered into
+// contiguous scratch, its gradients formed by launch_bwd16 (D and dD with the
+// first group only), its columns of dA, dB, dC scattered back, and its dx,
+// ddelta added to the first group's in group order (deterministic).
+namespace {
+constexpr int kElemThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kElemThreads)
+gather_cols(const T *__restrict__ src, T *__restrict__ dst, int64_t rows, int N, int n0, int ng) {
+    const int64_t n = rows * ng;
+    for (int64_t i = blockIdx.x * int64_t(kElemThreads) + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * kElemThreads) {
+        const int64_t r = i / ng;
+        dst[i] = src[r * N + n0 + (i - r * ng)];
+    }
+}
+
+__global__ void __launch_bounds__(kElemThreads)
+scatter_cols(const float *__restrict__ src, float *__restrict__ dst, int64_t rows, int N, int n0,
+             int ng) {
+    const int64_t n = rows * ng;
+    for (int64_t i = blockIdx.x * int64_t(kElemThreads) + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * kElemThreads) {
+        const int64_t r = i / ng;
+        dst[r * N + n0 + (i - r * ng)] = src[i];
+    }
+}
+
+__global__ void __launch_bounds__(kElemThreads)
+add_into(float *__restrict__ dst, const float *__restrict__ src, int64_t n) {
+    for (int64_t i = blockIdx.x * int64_t(kElemThreads) + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * kElemThreads)
+        dst[i] += src[i];
+}
+
+unsigned elem_grid(int64_t n, int num_sms) {
+    const int64_t want = (n + kElemThreads - 1) / kElemThreads;
+    const int64_t cap = int64_t(num_sms) * 8;
+    return unsigned(want < 1 ? 1 : (want < cap ? want : cap));
+}
+}  // namespace
+
+template <typename Tin>
+cudaError_t launch_bwd(const Tin *x, const Tin *dlt, const float *A, const Tin *Bm, const Tin *Cm,
+                       const float *D, const float *dy, float *dx, float *ddelta, float *dA,
+                       float *dB, float *dC, float *dD, int64_t Bs, int64_t L, int64_t ED,
+                       int64_t N, int num_sms, cudaStream_t st) {
+    if (N <= kNP)
+        return launch_bwd16<Tin>(x, dlt, A, Bm, Cm, D, dy, dx, ddelta, dA, dB, dC, dD, Bs, L, ED, N,
+                                 num_sms, st);
+    if (Bs > 65535) return cudaErrorInvalidConfiguration;
+    const int64_t rows = Bs * L, nx = rows * ED;
+    auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+    const size_t bytes = up(size_t(ED) * kNP * 4) * 2 + up(size_t(rows) * kNP * sizeof(Tin)) * 2 +
+                         up(size_t(rows) * kNP * 4) * 2 + up(size_t(nx) * 4) * 2;
+    void *scratch = nullptr;
+    cudaError_t err = cudaMallocAsync(&scratch, bytes, st);
+    if (err != cudaSuccess) return err;
+    char *cur = static_cast<char *>(scratch);
+    auto take = [&](size_t b) { char *p = cur; cur += up(b); return p; };
+    float *Ag = reinterpret_cast<float *>(take(size_t(ED) * kNP * 4));
+    float *dAg = reinterpret_cast<float *>(take(size_t(ED) * kNP * 4));
+    Tin *Bg = reinterpret_cast<Tin *>(take(size_t(rows) * kNP * sizeof(Tin)));
+    Tin *Cg = reinterpret_cast<Tin *>(take(size_t(rows) * kNP * sizeof(Tin)));
+    float *dBg = reinterpret_cast<float *>(take(size_t(rows) * kNP * 4));
+    float *dCg = reinterpret_cast<float *>(take(size_t(rows) * kNP * 4));
+    float *dxg = reinterpret_cast<float *>(take(size_t(nx) * 4));
+    float *ddg = reinterpret_cast<float *>(take(size_t(nx) * 4));
+    for (int64_t n0 = 0; n0 < N && err == cudaSuccess; n0 += kNP) {
+        const int ng = int(N - n0 < kNP ? N - n0 : kNP);
+        const bool first = n0 == 0;
+        gather_cols<float><<<elem_grid(ED * ng, num_sms), kElemThreads, 0, st>>>(A, Ag, ED, int(N),
+                                                                               int(n0), ng);
+        gather_cols<Tin><<<elem_grid(rows * ng, num_sms), kElemThreads, 0, st>>>(Bm, Bg, rows,
+                                                                               int(N), int(n0), ng);
+        gather_cols<Tin><<<elem_grid(rows * ng, num_sms), kElemThreads, 0, st>>>(Cm, Cg, rows,
+                                                                               int(N), int(n0), ng);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) break;
+        err = launch_bwd16<Tin>(x, dlt, Ag, Bg, Cg, first ? D : nullptr, dy, first ? dx : dxg,
+                                first ? ddelta : ddg, dAg, dBg, dCg, first ? dD : nullptr, Bs, L,
+                                ED, ng, num_sms, st);
+        if (err != cudaSuccess) break;
+        scatter_cols<<<elem_grid(ED * ng, num_sms), kElemThreads, 0, st>>>(dAg, dA, ED, int(N),
+                                                                           int(n0), ng);
+        scatter_cols<<<elem_grid(rows * ng, num_sms), kElemThreads, 0, st>>>(dBg, dB, rows, int(N),
+                                                                             int(n0), ng);
+        scatter_cols<<<elem_grid(rows * ng, num_sms), kElemThreads, 0, st>>>(dCg, dC, rows, int(N),
+                                                                             int(n0), ng);
+        if (!first) {
+            add_into<<<elem_grid(nx, num_sms), kElemThreads, 0, st>>>(dx, dxg, nx);
+            add_into<<<elem_grid(nx, num_sms), kElemThreads, 0, st>>>(ddelta, ddg, nx);
+        }
+        err = cudaGetLastError();
     }
     cudaError_t e2 = cudaFreeAsync(scratch, st);
     return err != cudaSuccess ? err : e2;

@@ -165,7 +165,7 @@ def test_groups_are_validated():
 def test_backward_rejects_bad_arguments():
     lib = lrs.library()
     p13 = [P] * 13
-    assert lib.ssm_scan_bwd(*p13, 1, 8, 8, 17, 0, None) == 2       # N > 16
+    assert lib.ssm_scan_bwd(*p13, 1, 8, 8, 257, 0, None) == 2      # N > 256
     bad = list(p13)
     bad[6] = None                                                  # dy
     assert lib.ssm_scan_bwd(*bad, 1, 8, 8, 4, 0, None) == 1

@@ -38,6 +38,10 @@ def _close(got, ref, dtype, what):
     (1, 45, 24, 5),       # padded states
     (2, 33, 70, 16),
     (1, 600, 128, 16),    # long sequence
+    (2, 70, 96, 17),      # two groups of states, the second of one state
+    (2, 50, 64, 32),      # two full groups
+    (1, 90, 40, 40),      # three groups, the last ragged
+    (1, 20, 16, 256),     # the largest state count: 16 groups
 ])
 def test_gradients_match_oracle(cuda_device, dtype, Bs, L, ED, N):
     inp = workloads.diag_inputs(Bs, L, ED, N, dtype, seed=2 * L + ED + N)
@@ -63,7 +67,7 @@ def test_gradients_without_D(cuda_device):
 
 
 def test_unsupported_state_count(cuda_device):
-    inp = workloads.diag_inputs(1, 16, 8, 17, "f32", seed=1)
+    inp = workloads.diag_inputs(1, 16, 8, 257, "f32", seed=1)
     dy = workloads.grad_output((1, 16, 8), seed=2)
     with pytest.raises(lrs.SsmError):
         lrs.ssm_scan_bwd(**{k: v.to(cuda_device) for k, v in inp.items()}, dy=dy.to(cuda_device))

@@ -78,6 +78,12 @@ def test_option_gradients_match_oracle(cuda_device, dtype, opts):
     (1, 1, 8, 16),        # L = 1
     (1, 45, 24, 5),       # padded states
     (2, 600, 130, 16),    # long sequence (split into time segments), ragged channel tile
+    (2, 60, 48, 40),      # three groups of states, the last ragged
 ])
 def test_option_gradients_shapes(cuda_device, Bs, L, ED, N):
     _run(Bs, L, ED, N, "f32", {"bias", "softplus", "z", "h0"}, seed=L + ED + N)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_option_gradients_many_states(cuda_device, dtype):
+    _run(1, 40, 32, 64, dtype, {"bias", "softplus", "limit", "z", "h0"}, seed=91)

@@ -51,6 +51,7 @@ def _dev(d, dev):
     (1, 45, 24, 5),       # padded states
     (1, 600, 128, 16),    # split into time segments (carry pass)
     (2, 3000, 128, 7),
+    (2, 50, 64, 40),      # more than 16 states (padded to 64)
 ])
 def test_diag_all_options(cuda_device, dtype, Bs, L, ED, N):
     inp, opt = _diag_case(Bs, L, ED, N, dtype, seed=L + ED + N)
