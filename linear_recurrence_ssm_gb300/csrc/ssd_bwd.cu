@@ -29,6 +29,14 @@
 #include "ssm_common.cuh"
 
 namespace ssm {
+namespace ssd_bwd_chunk {   // the chunked form (ssd_bwd_chunk.cu)
+bool supported(int64_t P, int64_t N);
+template <typename Tin>
+cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *Bm, const Tin *Cm,
+                   const float *D, const float *dy, float *dx, float *ddt, float *dA, float *dB,
+                   float *dC, float *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
+                   int64_t G, bool bidir, cudaStream_t st);
+}  // namespace ssd_bwd_chunk
 namespace ssd_bwd {
 
 constexpr int kThreads = 256;
@@ -335,6 +343,11 @@ cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *
                    float *dC, float *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
                    int64_t G, bool bidir, cudaStream_t st) {
     if (!supported(P, N) || G < 1 || H % G != 0) return cudaErrorNotSupported;
+    // P = 64, N = 64 or 128: the chunked form (its dx stores are 16-byte wide)
+    if (ssd_bwd_chunk::supported(P, N) && Bs * H <= 65535 &&
+        reinterpret_cast<uintptr_t>(dx) % 16 == 0)
+        return ssd_bwd_chunk::launch<Tin>(x, dt, A_head, Bm, Cm, D, dy, dx, ddt, dA, dB, dC, dD, Bs,
+                                          L, H, P, N, G, bidir, st);
     const int64_t grid = Bs * H;
     if (grid > 0x7fffffff || L > 0x7fffffff) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaMemsetAsync(dA, 0, size_t(H) * sizeof(float), st);
