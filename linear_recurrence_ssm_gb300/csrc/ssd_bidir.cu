@@ -957,8 +957,10 @@ cudaError_t launch(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, const float 
     prm.chunk = static_cast<uint8_t *>(scratch);
     prm.tot = reinterpret_cast<float *>(prm.chunk + size_t(Bs) * size_t(H) * 2 * nc * kState);
 
-    auto kst = opt ? bidir_state_kernel<true> : bidir_state_kernel<false>;
-    auto kout = opt ? bidir_out_kernel<true> : bidir_out_kernel<false>;
+    // the plain kernels unless an option is on (groups alone need none)
+    const bool ext = opt && (opt->dt_bias || opt->dt_softplus || opt->dt_limit || opt->z);
+    auto kst = ext ? bidir_state_kernel<true> : bidir_state_kernel<false>;
+    auto kout = ext ? bidir_out_kernel<true> : bidir_out_kernel<false>;
     const size_t smem_st = sizeof(StateSmem) + 1024, smem_out = sizeof(OutSmem) + 1024;
     static_assert(sizeof(OutSmem) + 1024 <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
     err = cudaFuncSetAttribute(kst, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_st));

@@ -787,6 +787,16 @@ __device__ __forceinline__ void put_state_half(uint8_t *img, int n, int hf, cons
                        pack_bf16(s[8 * j + 4], s[8 * j + 5]), pack_bf16(s[8 * j + 6], s[8 * j + 7]));
 }
 
+// silu(z) = z sigmoid(z), sigmoid(z) = (1 + tanh(z / 2)) / 2: one
+// special-function instruction (the hardware tanh approximation, relative
+// error about 2^-11) instead of an exponential and a reciprocal.  The gate
+// multiplies an fp32 output that came through bf16 operands.
+__device__ __forceinline__ float silu_tanh(float z) {
+    float th;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * z));
+    return z * fmaf(0.5f, th, 0.5f);
+}
+
 // a * b for two packed fp32 pairs (one instruction on sm_100-family cores).
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
     unsigned long long r;
@@ -1094,7 +1104,7 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 x, float2 y) {
     return *reinterpret_cast<float2 *>(&r);
 }
 
-template <int NB, bool EXT>
+template <int NB, bool EXT, bool GATE>
 __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     constexpr int N = NB * 64;
     auto &sm = cx.sm;
@@ -1232,9 +1242,12 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
         tc_fence_before_sync();
         mbar_arrive(&sm.bar_mfull);
     };
-    const bool gate = EXT && cx.prm.z != nullptr;
-    uint4 zq[4];   // gate row of the tile being written (bf16, 32 values), loaded a tile early
-    auto prefetch_gate = [&](int c) {
+    const bool gate = GATE && cx.prm.z != nullptr;
+    // gate row of tile c (bf16, 32 values), loaded in iteration c after the
+    // mask of tile c + 1 is formed (the registers are not held through the
+    // mask phase) and used by the epilogue of tile c
+    uint4 zq[4];
+    auto load_gate = [&](int c) {
         const int row = c * kQ + t;
         if (!gate || row >= L) return;
         const uint4 *zp = reinterpret_cast<const uint4 *>(cx.prm.z + ((size_t(b) * L + row) * H + h) * kP + hf * 32);
@@ -1247,7 +1260,8 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     // 31, the 16-byte chunks 4 hf .. 4 hf + 3 of each, swizzled as the tile:
     // 32 rows x 16 columns at a time), so that each store instruction writes
     // 8 rows x 64 contiguous bytes.
-    auto epilogue = [&](int c, const uint32_t (&yv)[32], const uint32_t (&zf)[32], bool has_s, float ef) {
+    auto epilogue = [&](int c, const uint32_t (&yv)[32], const uint32_t (&zf)[32], bool has_s,
+                        float ef) -> bool {
         float out[32];
         if (has_s) {
             const float2 e2 = make_float2(ef, ef);
@@ -1269,8 +1283,8 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const float2 zz = unpack_bf16(w4[k]);
-                    out[8 * j + 2 * k] *= silu_fast(zz.x);
-                    out[8 * j + 2 * k + 1] *= silu_fast(zz.y);
+                    out[8 * j + 2 * k] *= silu_tanh(zz.x);
+                    out[8 * j + 2 * k + 1] *= silu_tanh(zz.y);
                 }
             }
         }
@@ -1299,6 +1313,7 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
                 bulk_commit();
             }
         }
+        return true;
     };
 
     // ---- prologue -------------------------------------------------------------------
@@ -1322,11 +1337,11 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     mbar_arrive(&sm.bar_st);
     if (!weigh_and_mask(0)) return false;
     mask_store();
-    prefetch_gate(0);
 
     for (int c = 0; c < nc; ++c) {
         const bool more = c + 1 < nc;
         if (more && !weigh_and_mask(c + 1)) return false;
+        load_gate(c);
         WS_WAIT_I(sm.bar_m2[c & 1], ph_m2, c & 1);   // every product of tile c done
         tc_fence_after_sync();
         const int p = c % kSlots;
@@ -1357,8 +1372,7 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
             tmem_ld32_async(tmem + lane_base + ((c & 1) ? kWsZ1 : kWsZ0) + hf * 32, zf);
             tmem_wait_tie(zf);
         }
-        epilogue(c, yv, zf, has_s, ef);
-        if (more) prefetch_gate(c + 1);
+        if (!epilogue(c, yv, zf, has_s, ef)) return false;
     }
     if (EXT && cx.prm.h_final != nullptr && is_state) {
         float *dst = cx.prm.h_final + size_t(cx.bh) * kP * N + size_t(hf * 32) * N + t;
@@ -1368,7 +1382,9 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     return true;
 }
 
-template <int NB, bool EXT>
+// GATE (only with EXT): the silu gate z is compiled in (its rows, loaded a
+// tile ahead, take registers the other options do not need).
+template <int NB, bool EXT, bool GATE>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
@@ -1434,7 +1450,7 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
     bool ok = true;
     if (warp < 8) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kMathRegs));
-        ok = math_role<NB, EXT>(cx, has_h0);
+        ok = math_role<NB, EXT, GATE>(cx, has_h0);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
         if (tid == 256) ok = issuer_role<NB, EXT>(cx, has_h0);
@@ -1551,12 +1567,16 @@ static cudaError_t launch_nb(const __nv_bfloat16 *x, const __nv_bfloat16 *dt, co
     size_t smem = sizeof(Smem<NB>) + 1024;
     static_assert(sizeof(Smem<NB>) + 1024 <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
     static_assert(sizeof(ws::Smem<NB>) + 1024 <= 227 * 1024, "shared memory of one CTA exceeds 227 KB");
-    auto kern = opt ? ssd_chunk_scan_kernel<NB, true> : ssd_chunk_scan_kernel<NB, false>;
+    // the plain kernels unless an option is on (groups alone need none)
+    const bool ext = opt && (opt->dt_bias || opt->dt_softplus || opt->dt_limit || opt->z ||
+                             opt->h0 || opt->h_final);
+    auto kern = ext ? ssd_chunk_scan_kernel<NB, true> : ssd_chunk_scan_kernel<NB, false>;
     using WsKern = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                             const Params);
     WsKern wkern = nullptr;
     if (use_ws) {
-        wkern = opt ? ws::ssd_ws_kernel<NB, true> : ws::ssd_ws_kernel<NB, false>;
+        wkern = !ext ? ws::ssd_ws_kernel<NB, false, false>
+                     : (opt->z ? ws::ssd_ws_kernel<NB, true, true> : ws::ssd_ws_kernel<NB, true, false>);
         smem = sizeof(ws::Smem<NB>) + 1024;
     }
     cudaError_t err;
