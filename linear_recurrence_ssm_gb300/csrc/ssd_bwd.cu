@@ -343,9 +343,11 @@ cudaError_t launch(const Tin *x, const Tin *dt, const float *A_head, const Tin *
                    float *dC, float *dD, int64_t Bs, int64_t L, int64_t H, int64_t P, int64_t N,
                    int64_t G, bool bidir, cudaStream_t st) {
     if (!supported(P, N) || G < 1 || H % G != 0) return cudaErrorNotSupported;
-    // P = 64, N = 64 or 128: the chunked form (its dx stores are 16-byte wide)
-    if (ssd_bwd_chunk::supported(P, N) && Bs * H <= 65535 &&
-        reinterpret_cast<uintptr_t>(dx) % 16 == 0)
+    // P = 64, N = 64 or 128: the chunked form (its reads of x, dy, B, C are
+    // 16 bytes wide)
+    auto a16 = [](const void *q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+    if (ssd_bwd_chunk::supported(P, N) && Bs * H <= 65535 && a16(dx) && a16(x) && a16(dy) &&
+        a16(Bm) && a16(Cm))
         return ssd_bwd_chunk::launch<Tin>(x, dt, A_head, Bm, Cm, D, dy, dx, ddt, dA, dB, dC, dD, Bs,
                                           L, H, P, N, G, bidir, st);
     const int64_t grid = Bs * H;

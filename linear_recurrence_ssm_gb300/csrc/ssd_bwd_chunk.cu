@@ -71,10 +71,14 @@ __device__ __forceinline__ int colj(int tj, int c) {
 // contiguous) else a[k sa + i]; B(k, j) = b[j sb + k] if BK else b[k sb + j]
 // (BK requires IL).  Loads are float4 along the contiguous index, four k at a
 // time, except B with j contiguous and IL: four scalars per k.
-template <int TN, bool AK, bool BK, bool IL>
+template <int K, int TN, bool AK, bool BK, bool IL>
 __device__ __forceinline__ void mm(float (&acc)[4][TN], const float *a, int sa, const float *b,
-                                   int sb, int K, int i0, int tj) {
+                                   int sb, int i0, int tj) {
     static_assert(!BK || IL, "k-contiguous B operands are read interleaved");
+    static_assert(K % 4 == 0, "K is taken four at a time");
+    // (K known at compile time: the loop is unrolled, so the loads of the
+    // next four k overlap the multiply-adds of these)
+#pragma unroll 4
     for (int k = 0; k < K; k += 4) {
         float av[4][4];   // av[r][kk] = A(i0 + r, k + kk)
         if (AK) {
@@ -136,37 +140,62 @@ __device__ __forceinline__ float row_sum16(float v) {
     return v;
 }
 
+// 16 bytes of Tin as fp32 (8 bf16 or 4 floats) into shared memory.
+__device__ __forceinline__ void put16(float *dst, uint4 v, const __nv_bfloat16 *) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        dst[2 * i] = __uint_as_float(w[i] << 16);
+        dst[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void put16(float *dst, uint4 v, const float *) {
+    *reinterpret_cast<uint4 *>(dst) = v;
+}
+
 // Rows of chunk k (walk order) into shared memory: x, dy [Q][P], B, C
-// [Q][N] (fp32, padded rows), dt [Q]; rows past L are zero.
+// [Q][N] (fp32, padded rows), dt [Q]; rows past L are zero.  Global reads
+// are 16 bytes wide (x, dy, B, C are 16-byte aligned: checked by the caller).
 template <typename Tin, int N>
 __device__ __forceinline__ void load_chunk(const Args<Tin> &a, int dir, int b, int h, int g,
                                            int k, float *X, float *DY, float *Bs, float *Cs,
                                            float *dtv, bool with_dy, bool with_b, bool with_c) {
     constexpr int ldP = kP + kPad, ldN = N + kPad;
+    constexpr int EV = 16 / sizeof(Tin);   // input elements per 16 bytes
     const int L = a.L, H = a.H, G = a.G;
-    for (int i = threadIdx.x; i < kQ * kP; i += kThreads) {
-        const int r = i / kP, p = i % kP;
+    for (int i = threadIdx.x; i < kQ * kP / EV; i += kThreads) {
+        const int r = i / (kP / EV), p = (i % (kP / EV)) * EV;
         const int lam = k * kQ + r;
-        float xv = 0.0f, dv = 0.0f;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (lam < L) {
             const size_t o = (size_t(b) * L + walk_row(lam, L, dir)) * H + h;
-            xv = to_f32(a.x[o * kP + p]);
-            if (with_dy) dv = a.dy[o * kP + p];
+            v = *reinterpret_cast<const uint4 *>(a.x + o * kP + p);
         }
-        X[r * ldP + p] = xv;
-        if (with_dy) DY[r * ldP + p] = dv;
+        put16(X + r * ldP + p, v, a.x);
     }
-    for (int i = threadIdx.x; i < kQ * N; i += kThreads) {
-        const int r = i / N, n = i % N;
+    if (with_dy) {
+        for (int i = threadIdx.x; i < kQ * kP / 4; i += kThreads) {
+            const int r = i / (kP / 4), p = (i % (kP / 4)) * 4;
+            const int lam = k * kQ + r;
+            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (lam < L) {
+                const size_t o = (size_t(b) * L + walk_row(lam, L, dir)) * H + h;
+                v = *reinterpret_cast<const float4 *>(a.dy + o * kP + p);
+            }
+            *reinterpret_cast<float4 *>(DY + r * ldP + p) = v;
+        }
+    }
+    for (int i = threadIdx.x; i < kQ * N / EV; i += kThreads) {
+        const int r = i / (N / EV), n = (i % (N / EV)) * EV;
         const int lam = k * kQ + r;
-        float bv = 0.0f, cv = 0.0f;
+        uint4 bv = make_uint4(0u, 0u, 0u, 0u), cv = bv;
         if (lam < L) {
             const size_t o = ((size_t(b) * L + walk_row(lam, L, dir)) * G + g) * N + n;
-            if (with_b) bv = to_f32(a.B[o]);
-            if (with_c) cv = to_f32(a.C[o]);
+            if (with_b) bv = *reinterpret_cast<const uint4 *>(a.B + o);
+            if (with_c) cv = *reinterpret_cast<const uint4 *>(a.C + o);
         }
-        if (with_b) Bs[r * ldN + n] = bv;
-        if (with_c) Cs[r * ldN + n] = cv;
+        if (with_b) put16(Bs + r * ldN + n, bv, a.B);
+        if (with_c) put16(Cs + r * ldN + n, cv, a.C);
     }
     for (int r = threadIdx.x; r < kQ; r += kThreads) {
         const int lam = k * kQ + r;
@@ -219,7 +248,7 @@ chunk_local_kernel(const Args<Tin> a, int dir) {
     const size_t base = (size_t(bh) * a.nc + k) * kP * N;
     float acc[4][TN];
     zero(acc);
-    mm<TN, false, false, false>(acc, X, ldP, Bs, ldN, kQ, i0, tj);   // A(p, s) = X[s][p], B(s, n) = B[s][n]
+    mm<kQ, TN, false, false, false>(acc, X, ldP, Bs, ldN, i0, tj);   // A(p, s) = X[s][p], B(s, n) = B[s][n]
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -227,7 +256,7 @@ chunk_local_kernel(const Args<Tin> a, int dir) {
             *reinterpret_cast<float4 *>(a.Sx + base + (i0 + r) * N + 4 * tj + 64 * c4) =
                 make_float4(acc[r][4 * c4], acc[r][4 * c4 + 1], acc[r][4 * c4 + 2], acc[r][4 * c4 + 3]);
     zero(acc);
-    mm<TN, false, false, false>(acc, DY, ldP, Cs, ldN, kQ, i0, tj);  // A(p, u) = DY[u][p], B(u, n) = C[u][n]
+    mm<kQ, TN, false, false, false>(acc, DY, ldP, Cs, ldN, i0, tj);  // A(p, u) = DY[u][p], B(u, n) = C[u][n]
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -322,7 +351,7 @@ chunk_grad_kernel(const Args<Tin> a, int dir) {
     {
         float acc[4][4];
         zero(acc);
-        mm<4, true, true, true>(acc, Cs, ldN, Bs, ldN, N, i0, tj);   // A(u, n) = C[u][n], B(n, s) = B[s][n]
+        mm<N, 4, true, true, true>(acc, Cs, ldN, Bs, ldN, i0, tj);   // A(u, n) = C[u][n], B(n, s) = B[s][n]
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -331,7 +360,7 @@ chunk_grad_kernel(const Args<Tin> a, int dir) {
                 GL[u * ldQ + s] = u >= s ? acc[r][c] * ex2(cum[u] - cum[s]) : 0.0f;
             }
         zero(acc);
-        mm<4, true, true, true>(acc, DY, ldP, X, ldP, kP, i0, tj);   // A(u, p) = dy[u][p], B(p, s) = x[s][p]
+        mm<kP, 4, true, true, true>(acc, DY, ldP, X, ldP, i0, tj);   // A(u, p) = dy[u][p], B(p, s) = x[s][p]
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -346,8 +375,8 @@ chunk_grad_kernel(const Args<Tin> a, int dir) {
         float v[4][4], w[4][4];
         zero(v);
         zero(w);
-        mm<4, false, false, true>(v, GL, ldQ, DY, ldP, kQ, i0, tj);  // A(s, u) = GL[u][s], B(u, p) = dy[u][p]
-        mm<4, true, true, true>(w, Bs, ldN, Gi, ldN, N, i0, tj);     // A(s, n) = B[s][n], B(n, p) = Gin[p][n]
+        mm<kQ, 4, false, false, true>(v, GL, ldQ, DY, ldP, i0, tj);  // A(s, u) = GL[u][s], B(u, p) = dy[u][p]
+        mm<N, 4, true, true, true>(w, Bs, ldN, Gi, ldN, i0, tj);     // A(s, n) = B[s][n], B(n, p) = Gin[p][n]
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int s = i0 + r, lam = k * kQ + s;
@@ -376,8 +405,8 @@ chunk_grad_kernel(const Args<Tin> a, int dir) {
         float u1[4][TN], u2[4][TN];
         zero(u1);
         zero(u2);
-        mm<TN, false, false, false>(u1, WL, ldQ, Cs, ldN, kQ, i0, tj);  // A(s, u) = WL[u][s], B(u, n) = C[u][n]
-        mm<TN, true, false, false>(u2, X, ldP, Gi, ldN, kP, i0, tj);    // A(s, p) = x[s][p], B(p, n) = Gin[p][n]
+        mm<kQ, TN, false, false, false>(u1, WL, ldQ, Cs, ldN, i0, tj);  // A(s, u) = WL[u][s], B(u, n) = C[u][n]
+        mm<kP, TN, true, false, false>(u2, X, ldP, Gi, ldN, i0, tj);    // A(s, p) = x[s][p], B(p, n) = Gin[p][n]
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int s = i0 + r, lam = k * kQ + s;
@@ -401,8 +430,8 @@ chunk_grad_kernel(const Args<Tin> a, int dir) {
         float u1[4][TN], u2[4][TN];
         zero(u1);
         zero(u2);
-        mm<TN, true, false, false>(u1, WL, ldQ, Bs, ldN, kQ, i0, tj);   // A(t, s) = WL[t][s] dt_s, B(s, n) = B[s][n]
-        mm<TN, true, false, false>(u2, DY, ldP, S, ldN, kP, i0, tj);    // A(t, p) = dy[t][p], B(p, n) = S[p][n]
+        mm<kQ, TN, true, false, false>(u1, WL, ldQ, Bs, ldN, i0, tj);   // A(t, s) = WL[t][s] dt_s, B(s, n) = B[s][n]
+        mm<kP, TN, true, false, false>(u2, DY, ldP, S, ldN, i0, tj);    // A(t, p) = dy[t][p], B(p, n) = S[p][n]
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = i0 + r, lam = k * kQ + t;
@@ -417,8 +446,8 @@ chunk_grad_kernel(const Args<Tin> a, int dir) {
         float y1[4][4], y2[4][4];
         zero(y1);
         zero(y2);
-        mm<4, true, false, true>(y1, GL, ldQ, X, ldP, kQ, i0, tj);    // A(t, s) = GL[t][s] dt_s, B(s, p) = x[s][p]
-        mm<4, true, true, true>(y2, Cs, ldN, S, ldN, N, i0, tj);      // A(t, n) = C[t][n], B(n, p) = S[p][n]
+        mm<kQ, 4, true, false, true>(y1, GL, ldQ, X, ldP, i0, tj);    // A(t, s) = GL[t][s] dt_s, B(s, p) = x[s][p]
+        mm<N, 4, true, true, true>(y2, Cs, ldN, S, ldN, i0, tj);      // A(t, n) = C[t][n], B(n, p) = S[p][n]
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int t = i0 + r, lam = k * kQ + t;
