@@ -167,7 +167,9 @@ ssm_status_t diag_entry(const Tin *x, const Tin *delta, const float *A, const Ti
     DeviceInfo dev;
     s = current_device(&dev);
     if (s != SSM_OK) return s;
-    if (opts) {
+    // the plain kernels unless an option is on
+    if (opts && (opts->dt_bias || opts->dt_softplus || opts->dt_limit || opts->z || opts->h0 ||
+                 opts->h_final)) {
         const ssm::ScanOpts ex{opts->dt_bias, opts->z, opts->h0, opts->h_final,
                                opts->dt_min, opts->dt_max, opts->dt_softplus, opts->dt_limit, 1};
         return from_cuda(ssm::diag::launch_ext<Tin>(x, delta, A, B, C, D, y, Bs, L, ED, N,

@@ -166,7 +166,8 @@ def test_ssd_state_io_rejected_when_bidirectional(cuda_device):
 
 
 def test_plain_entry_points_unchanged_by_empty_options(cuda_device):
-    """dt_softplus=False alone selects the option kernels; the result matches the plain call."""
+    """Options that turn nothing on (dt_softplus=False alone) run the plain
+    kernels: the same bits as the plain call."""
     inp = workloads.diag_inputs(2, 300, 64, 16, "bf16", seed=4)
     d = _dev(inp, cuda_device)
     y0 = lrs.ssm_scan_fwd(**d)
@@ -177,7 +178,7 @@ def test_plain_entry_points_unchanged_by_empty_options(cuda_device):
     z1 = lrs.ssd_chunk_scan_fwd(**ds, dt_softplus=False)
     torch.cuda.synchronize()
     for a, b in ((y0, y1), (z0, z1)):
-        assert float((a - b).abs().max()) <= 1e-6 * float(a.abs().max())
+        assert torch.equal(a, b)
 
 
 @pytest.mark.parametrize("Bs,L,H,N,G,bidir", [
