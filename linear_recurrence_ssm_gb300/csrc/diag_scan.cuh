@@ -588,13 +588,40 @@ diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
                 }
             }
         }
-        if (e_ok) {
+        if (e_ok && !(EXT && ex.no_y)) {
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
                 const int t = RW * w + r;
                 float v = acc[r];
                 if (EXT && zg) v *= silu(to_f32(s_z[slot][t * CW + lane]));   // the output gate
                 if (t < tl && v != 0.0f) atomicAdd(y + (b * L + t0 + t) * ED + e, v);
+            }
+        }
+        if (EXT && ex.ckpt && e_ok) {
+            // checkpoints (the state entering every 16th step) of this
+            // segment were written from a zero entering state: add the
+            // carried part, exp(A (delta summed before the step)) h_in
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int t = RW * w + r;
+                if (((t0 + t) & 15) != 0 || t >= tl) continue;
+                const float exc = cum[r] - d[r];
+                float4 *dst = reinterpret_cast<float4 *>(
+                    ex.ckpt + ((int64_t((t0 + t) >> 4) * Bs + b) * ED + e) * 16);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float cv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int n = 4 * j + q;
+                        cv[q] = ((live >> n) & 1u)
+                                    ? __uint_as_float(__float_as_uint(ex2(fmaf(A2[n], exc, lh[n]))) ^ sg[n])
+                                    : 0.0f;
+                    }
+                    float4 v4 = dst[j];
+                    v4.x += cv[0]; v4.y += cv[1]; v4.z += cv[2]; v4.w += cv[3];
+                    dst[j] = v4;
+                }
             }
         }
         cum_run += tile_sum;
@@ -669,8 +696,9 @@ cudaError_t launch_impl(const Tin *x, const Tin *dlt, const float *A, const Tin 
                         const Tin *Cm, const float *D, float *y, int64_t Bs, int64_t L,
                         int64_t ED, int64_t N, int num_sms, const Ext &ex, cudaStream_t st) {
     const int esz = int(sizeof(Tin));
-    // checkpointing for the gradients needs the true state at every step: one segment
-    Plan p = (EXT && ex.ckpt) ? Plan{16, 1, 1, int(L)} : plan_for(Bs, L, ED, N, esz, num_sms);
+    // checkpointing for the gradients (N <= 16): the time split too, the carry
+    // pass adding the carried state to a later segment's checkpoints
+    Plan p = (EXT && ex.ckpt && N > 16) ? Plan{16, 1, 1, int(L)} : plan_for(Bs, L, ED, N, esz, num_sms);
     const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(dlt) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(Bm) % 16 == 0) &&
