@@ -55,6 +55,7 @@ template <typename Tin>
 struct Shared {
     float hist[kSeg][kNP][kCh];           // state entering each step of the segment
     float red[kWarps][kSeg][2 * kNP];     // per-warp sums of dB_t, dC_t over the warp's channels
+    float fB[kSeg][kNP], fC[kSeg][kNP];   // the segment's B, C rows in fp32 (converted once)
     Stage<Tin> st[2];
 };
 
@@ -169,6 +170,12 @@ diag_bwd_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt, const fl
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();                              // segment k staged everywhere
+        // B, C rows of the segment in fp32, once, instead of at every use
+        for (int i = tid; i < kSeg * kNP; i += kThreads) {
+            sm.fB[i / kNP][i % kNP] = to_f32(s.B[i / kNP][i % kNP]);
+            sm.fC[i / kNP][i % kNP] = to_f32(s.C[i / kNP][i % kNP]);
+        }
+        __syncthreads();
         const int t0 = k * kSeg;
         const int tl = min(kSeg, L - t0);
         float h[kSpl];
@@ -184,7 +191,7 @@ diag_bwd_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt, const fl
             for (int i = 0; i < kSpl; ++i) {
                 const int n = q * kSpl + i;
                 sm.hist[j][n][cl] = h[i];
-                h[i] = fmaf(ex2(dl * A2[i]), h[i], dlx * to_f32(s.B[j][n]));
+                h[i] = fmaf(ex2(dl * A2[i]), h[i], dlx * sm.fB[j][n]);
             }
         }
         // backward over the segment
@@ -195,7 +202,7 @@ diag_bwd_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt, const fl
 #pragma unroll
             for (int i = 0; i < kSpl; ++i) {
                 const int n = q * kSpl + i;
-                const float bv = to_f32(s.B[j][n]), cv = to_f32(s.C[j][n]);
+                const float bv = sm.fB[j][n], cv = sm.fC[j][n];
                 const float a = ex2(dl * A2[i]);
                 const float hp = sm.hist[j][n][cl];
                 g[i] = fmaf(gy, cv, g[i]);                      // g_t
