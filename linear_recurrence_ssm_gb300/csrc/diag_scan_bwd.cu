@@ -185,6 +185,8 @@ diag_bwd_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt, const fl
             h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
         }
         // forward over the segment: keep the entering state of every step
+        // (unrolled by 4: the next steps' exponentials overlap this step's chain)
+#pragma unroll 4
         for (int j = 0; j < tl; ++j) {
             const float dl = to_f32(s.d[j][cl]), dlx = dl * to_f32(s.x[j][cl]);
 #pragma unroll
@@ -195,6 +197,7 @@ diag_bwd_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt, const fl
             }
         }
         // backward over the segment
+#pragma unroll 4
         for (int j = tl - 1; j >= 0; --j) {
             const float dl = to_f32(s.d[j][cl]), xv = to_f32(s.x[j][cl]);
             const float gy = s.dy[j][cl];                 // zero past ED
