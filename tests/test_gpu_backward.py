@@ -71,3 +71,23 @@ def test_unsupported_state_count(cuda_device):
     dy = workloads.grad_output((1, 16, 8), seed=2)
     with pytest.raises(lrs.SsmError):
         lrs.ssm_scan_bwd(**{k: v.to(cuda_device) for k, v in inp.items()}, dy=dy.to(cuda_device))
+
+
+@pytest.mark.parametrize("a_scale", [1e-3, -1e-3])
+def test_split_checkpoints_with_slow_or_growing_decay(cuda_device, a_scale):
+    """A shape the forward splits into time segments (few channels, a long
+    sequence): the checkpointing pass runs split, and the carry pass adds the
+    carried state to the later segments' checkpoints.  With |A| tiny the
+    carried part never decays below the cut-off (positive A: the cut-off is
+    off), so every checkpoint of a later segment is corrected."""
+    Bs, L, ED, N = 1, 1200, 64, 16
+    inp = workloads.diag_inputs(Bs, L, ED, N, "f32", seed=41)
+    inp["A"] = a_scale * torch.rand(ED, N, generator=torch.Generator().manual_seed(3))
+    dy = workloads.grad_output((Bs, L, ED), seed=42)
+    ref = oracle.diag_scan_bwd(**inp, dy=dy)
+    dev = {k: v.to(cuda_device) for k, v in inp.items()}
+    got = lrs.ssm_scan_bwd(**dev, dy=dy.to(cuda_device))
+    torch.cuda.synchronize()
+    for k in ("dx", "ddelta", "dA", "dB", "dC", "dD"):
+        _close(got[k], ref[k], "f32", k)
+    lrs.ssm_check_device_errors()
