@@ -134,10 +134,18 @@ def _code_only(src: str) -> str:
     return "\n".join(lines)
 
 
+def short_bidir(w) -> bool:
+    """Whether the library runs this SSD workload on the short-sequence
+    bidirectional passes: bf16, P = N = 64, at most four 128-row tiles."""
+    s = w.shape
+    return (w.kind != "diag" and s["bidirectional"] and w.dtype == "bf16" and s["N"] == 64
+            and s["P"] == 64 and (s["L"] + 127) // 128 <= 4)
+
+
 def source_kind(w) -> str:
     if w.kind == "diag":
         return "diag"
-    return "bissd" if kernels_per_call(w, None) == 2 else "ssd"
+    return "bissd" if short_bidir(w) else "ssd"
 
 
 def ncu_traffic(workload: str, kind: str):
@@ -233,10 +241,7 @@ def kernels_per_call(w, lrs) -> int:
     diagonal scan is one, or two when the library splits the sequence into
     time segments (segment pass + carry pass)."""
     if w.kind != "diag":
-        s = w.shape
-        short_bidir = (s["bidirectional"] and w.dtype == "bf16" and s["N"] == 64 and s["P"] == 64
-                       and (s["L"] + 127) // 128 <= 4)
-        return 2 if short_bidir else 1
+        return 2 if short_bidir(w) else 1
     s = w.shape
     _, _, k = lrs.ssm_scan_fwd_plan(s["Bs"], s["L"], s["ED"], s["N"], w.dtype == "bf16")
     return 2 if k > 1 else 1
@@ -648,9 +653,10 @@ def run_ours(args, rank, world, local):
     e2e_value = units * k_e2e * world / (ms_e2e / 1e3) if k_e2e else None
     peaks = load_peaks()
     if args.mode == "bwd":
-        # diagonal: checkpointing forward + reverse pass; chunked: state pass +
-        # reverse pass per direction
-        launches_per_step = 2 if w.kind == "diag" else 2 * (2 if w.shape["bidirectional"] else 1)
+        # diagonal: checkpointing forward + reverse pass; chunked (P = 64, N =
+        # 64 or 128): chunk-local states, the pass over chunks, the per-chunk
+        # gradients and the finishing sums, per direction
+        launches_per_step = 2 if w.kind == "diag" else 4 * (2 if w.shape["bidirectional"] else 1)
     else:
         launches_per_step = kernels_per_call(w, lrs)
     per_launch_s = ms / 1e3 / args.steps
