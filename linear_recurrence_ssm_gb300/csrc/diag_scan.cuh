@@ -146,6 +146,11 @@ diag_scan_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt,
     constexpr int NP = Sh::NP;
     static_assert(S % 4 == 0, "states per thread must be a multiple of 4");
 
+    // With a time split the carry pass follows as a programmatic dependent
+    // launch: it may start once every CTA of this pass has started, stage its
+    // first inputs, and wait (griddepcontrol.wait) for this grid's results.
+    if constexpr (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Tin *sx = reinterpret_cast<Tin *>(smem_raw);     // [kStages][TT][ET]
     Tin *sd = sx + kStages * Sh::raw_x;              // [kStages][TT][ET]
@@ -464,6 +469,9 @@ diag_fixup_kernel(const Tin *__restrict__ dlt, const float *__restrict__ A,
 
     // h_in for states 4w..4w+3 of channel `lane`, shared as log2|h_in| and
     // sign.  All summary loads are issued before the fold uses them.
+    // The main pass's results (summaries, y, checkpoints) are read only
+    // after it has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     bool mono = summ.dmin[(int64_t(seg) * Bs + b) * ED + ec] >= 0.0f;
     {
         float a2[4], hin[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -651,13 +659,23 @@ static cudaError_t launch_one(const Tin *x, const Tin *dlt, const float *A, cons
     if (err != cudaSuccess || !SPLIT) return err;
     const dim3 fgrid(unsigned((ED + kFixCh - 1) / kFixCh), unsigned(Bs), unsigned(K - 1));
     const bool yvec = (reinterpret_cast<uintptr_t>(y) % 16 == 0) && (ED % 4 == 0);
+    // a programmatic dependent launch: its prologue overlaps the main pass's tail
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = fgrid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int Bsi = int(Bs);
     if (VEC && yvec)
-        diag_fixup_kernel<Tin, true, EXT><<<fgrid, dim3(kThreads), 0, stream>>>(
-            dlt, A, Cm, y, int(Bs), L, ED, N, seg_len, summ, ex);
-    else
-        diag_fixup_kernel<Tin, false, EXT><<<fgrid, dim3(kThreads), 0, stream>>>(
-            dlt, A, Cm, y, int(Bs), L, ED, N, seg_len, summ, ex);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, diag_fixup_kernel<Tin, true, EXT>, dlt, A, Cm, y, Bsi, L, ED, N,
+                                  seg_len, summ, ex);
+    return cudaLaunchKernelEx(&cfg, diag_fixup_kernel<Tin, false, EXT>, dlt, A, Cm, y, Bsi, L, ED, N,
+                              seg_len, summ, ex);
 }
 
 template <typename Tin, bool VEC, bool SPLIT, bool EXT>

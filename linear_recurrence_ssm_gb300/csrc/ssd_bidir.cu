@@ -131,6 +131,12 @@ bidir_state_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
     const int bh = int(blockIdx.x) / nc, c = int(blockIdx.x) % nc;
     const int b = bh / H, h = bh % H;
     volatile int never = 0;
+    // The output pass may be launched as soon as every CTA of this one has
+    // started: what it does before its griddepcontrol.wait (barriers, tensor
+    // memory, the first x, B, C copies) reads nothing this pass writes, and
+    // that wait returns only once this grid has completed and its writes
+    // (the bulk stores included) are visible.
+    pdl_launch_dependents();
 
     if (t == 0) {
         mbar_init(&sm.bar_ld, 1);
@@ -238,7 +244,7 @@ bidir_state_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
             bulk_store(prm.chunk + ((size_t(bh) * 2 + 1) * nc + c) * kState, sm.XR, kState);
             bulk_commit();
             prm.tot[size_t(bh) * kMaxTiles + c] = tot;
-            bulk_wait0();                 // the states have been written
+            bulk_wait_read0();            // the stores have read the staging (shared memory)
         }
     } else if (t == 0) {
         atomicOr(&g_device_error, 1u);
@@ -246,7 +252,6 @@ bidir_state_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
         mma_commit(&sm.bar_mma);
         (void)mbar_wait_bounded(&sm.bar_mma, issued ? 1u : 0u, &never, 100000000ull);
     }
-    pdl_launch_dependents();
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
