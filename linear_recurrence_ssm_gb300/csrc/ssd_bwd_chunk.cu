@@ -331,15 +331,17 @@ chunk_grad_kernel(const Args<Tin> a, int dir) {
     const int tid = threadIdx.x, lane = tid & 31, ti = tid >> 4, tj = tid & 15, i0 = 4 * ti;
     const float Dh = (dir == 0 && a.D) ? a.D[h] : 0.0f;
 
-    load_chunk<Tin, N>(a, dir, b, h, g, k, X, DY, Bs, Cs, dtv, true, true, true);
-    {   // the entering state and the incoming adjoint, [p][n]
+    {   // the entering state and the incoming adjoint, [p][n]: asynchronous
+        // copies, first needed after the masked products below
         const size_t base = (size_t(bh) * a.nc + k) * kP * N;
         for (int i = tid; i < kP * N / 4; i += kThreads) {
             const int p = (4 * i) / N, n = (4 * i) % N;
-            *reinterpret_cast<float4 *>(S + p * ldN + n) = *reinterpret_cast<const float4 *>(a.Sx + base + 4 * i);
-            *reinterpret_cast<float4 *>(Gi + p * ldN + n) = *reinterpret_cast<const float4 *>(a.Ux + base + 4 * i);
+            cp_async16(S + p * ldN + n, a.Sx + base + 4 * i, 16);
+            cp_async16(Gi + p * ldN + n, a.Ux + base + 4 * i, 16);
         }
+        cp_async_commit();
     }
+    load_chunk<Tin, N>(a, dir, b, h, g, k, X, DY, Bs, Cs, dtv, true, true, true);
     __syncthreads();
     chunk_cumsum(dtv, a.A[h] * SSM_LOG2E, cum, wtot);
     const float tot = cum[kQ - 1];
@@ -369,6 +371,7 @@ chunk_grad_kernel(const Args<Tin> a, int dir) {
                 WL[u * ldQ + s] = u >= s ? acc[r][c] * ex2(cum[u] - cum[s]) : 0.0f;
             }
     }
+    cp_async_wait<0>();                  // this thread's copies of S and Gin have landed
     __syncthreads();
     // v = GL^T dY + eo o (B Gin^T): dx and ddt1 = x . v
     {
