@@ -40,6 +40,7 @@ constexpr int kSeg = 16;              // steps per checkpointed segment (the for
 constexpr int kThreads = 128;      // 32 channels per CTA: small CTAs spread over the SMs evenly (measured: 1.17x faster than 64)
 constexpr int kCh = kThreads / kLanes;    // channels per CTA
 constexpr int kWarps = kThreads / 32;
+static_assert(kSpl == 4, "a lane's states are moved as one float4");
 
 // Inputs of one segment, staged in shared memory.
 template <typename Tin>
@@ -53,7 +54,10 @@ struct Stage {
 
 template <typename Tin>
 struct Shared {
-    float hist[kSeg][kNP][kCh];           // state entering each step of the segment
+    // state entering each step of the segment, [step][channel][state]: a
+    // lane's four states are one 16-byte access, and the eight lanes of a
+    // quarter-warp (two channels) cover 128 contiguous bytes
+    float hist[kSeg][kCh][kNP];
     float red[kWarps][kSeg][2 * kNP];     // per-warp sums of dB_t, dC_t over the warp's channels
     float fB[kSeg][kNP], fC[kSeg][kNP];   // the segment's B, C rows in fp32 (converted once)
     Stage<Tin> st[2];
@@ -189,12 +193,11 @@ diag_bwd_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt, const fl
 #pragma unroll 4
         for (int j = 0; j < tl; ++j) {
             const float dl = to_f32(s.d[j][cl]), dlx = dl * to_f32(s.x[j][cl]);
+            *reinterpret_cast<float4 *>(&sm.hist[j][cl][q * kSpl]) = make_float4(h[0], h[1], h[2], h[3]);
+            const float4 b4 = *reinterpret_cast<const float4 *>(&sm.fB[j][q * kSpl]);
+            const float bb[kSpl] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-            for (int i = 0; i < kSpl; ++i) {
-                const int n = q * kSpl + i;
-                sm.hist[j][n][cl] = h[i];
-                h[i] = fmaf(ex2(dl * A2[i]), h[i], dlx * sm.fB[j][n]);
-            }
+            for (int i = 0; i < kSpl; ++i) h[i] = fmaf(ex2(dl * A2[i]), h[i], dlx * bb[i]);
         }
         // backward over the segment
 #pragma unroll 4
@@ -202,12 +205,16 @@ diag_bwd_kernel(const Tin *__restrict__ x, const Tin *__restrict__ dlt, const fl
             const float dl = to_f32(s.d[j][cl]), xv = to_f32(s.x[j][cl]);
             const float gy = s.dy[j][cl];                 // zero past ED
             float sdx = 0.0f, sdd = 0.0f, vb[kSpl], vc[kSpl];
+            const float4 b4 = *reinterpret_cast<const float4 *>(&sm.fB[j][q * kSpl]);
+            const float4 c4 = *reinterpret_cast<const float4 *>(&sm.fC[j][q * kSpl]);
+            const float4 h4 = *reinterpret_cast<const float4 *>(&sm.hist[j][cl][q * kSpl]);
+            const float bb[kSpl] = {b4.x, b4.y, b4.z, b4.w}, cc[kSpl] = {c4.x, c4.y, c4.z, c4.w},
+                        hh[kSpl] = {h4.x, h4.y, h4.z, h4.w};
 #pragma unroll
             for (int i = 0; i < kSpl; ++i) {
-                const int n = q * kSpl + i;
-                const float bv = sm.fB[j][n], cv = sm.fC[j][n];
+                const float bv = bb[i], cv = cc[i];
                 const float a = ex2(dl * A2[i]);
-                const float hp = sm.hist[j][n][cl];
+                const float hp = hh[i];
                 g[i] = fmaf(gy, cv, g[i]);                      // g_t
                 sdx = fmaf(g[i] * dl, bv, sdx);
                 sdd = fmaf(g[i], fmaf(An[i] * a, hp, bv * xv), sdd);
