@@ -156,3 +156,17 @@ def test_short_bidirectional_boundaries(cuda_device, L, groups):
     ref = oracle.ssd_scan(**inp, bidirectional=True)
     y = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=128, bidirectional=True)
     _check(y, ref)
+
+
+def test_short_bidirectional_many_tiles_per_cta(cuda_device):
+    """4096 tiles of 128 rows on the persistent output pass: each CTA walks
+    about 27 tiles, so every barrier phase and double buffer of the two
+    passes wraps many times (the benchmark size gives about 7).  Sequences are
+    independent, so batch rows from both ends (the first and the last CTAs'
+    tiles) are checked against the oracle run on those rows alone."""
+    Bs, L, H, N = 128, 512, 8, 64
+    inp = workloads.ssd_inputs(Bs, L, H, 64, N, "bf16", seed=31)
+    y = lrs.ssd_chunk_scan_fwd(**_dev(inp, cuda_device), chunk=128, bidirectional=True)
+    for rows in (slice(0, 3), slice(Bs // 2, Bs // 2 + 2), slice(Bs - 3, Bs)):
+        sub = {k: (v[rows] if v is not None and v.dim() > 1 else v) for k, v in inp.items()}
+        _check(y[rows], oracle.ssd_scan(**sub, bidirectional=True))
