@@ -54,3 +54,28 @@ def test_bench_parity_on_sample():
     assert p["ok"] and p["max_abs_err"] < 1e-5 * p["ref_max_abs"]
     view(full)[0, 5, 0] += 0.05 * p["ref_max_abs"]
     assert not bench.parity_on_sample(w, full, ref, view, desc)["ok"]
+
+
+def test_kernel_bookkeeping_of_the_benchmark():
+    """Which kernels a workload runs, as the benchmark counts them: the
+    short bidirectional SSD (bf16, P = N = 64, at most four 128-row tiles) is
+    two passes and hashes the sources of ssd_bidir.cu; every other SSD
+    workload is one kernel and hashes the tensor-core scan's sources."""
+    by = workloads.BY_NAME
+    short = by["bissd_bf16_Bs32_L400_H8_P64_N64_Q128"]
+    uni = by["ssd_bf16_Bs4_L4096_H32_P64_N128_Q256"]
+    assert bench.short_bidir(short) and not bench.short_bidir(uni)
+    assert bench.kernels_per_call(short, None) == 2
+    assert bench.kernels_per_call(uni, None) == 1
+    assert bench.source_kind(short) == "bissd" and bench.source_kind(uni) == "ssd"
+    assert bench.source_kind(by["diag_bf16_Bs8_L2048_ED1536_N16"]) == "diag"
+    for w in workloads.WORKLOADS:
+        if w.kind != "diag" and w.shape["bidirectional"]:
+            s = w.shape
+            fits = w.dtype == "bf16" and s["N"] == 64 and s["P"] == 64 and (s["L"] + 127) // 128 <= 4
+            assert bench.short_bidir(w) == fits, w.name
+    # the hashes of the three kernel families differ and ignore comments
+    hashes = {k: bench.kernel_source_hash(k) for k in ("diag", "ssd", "bissd")}
+    assert len(set(hashes.values())) == 3
+    assert (bench._code_only("int a; // note\n\n/* block */ int b;")
+            == bench._code_only("int a;\n/* another comment */ int b;  // x"))
