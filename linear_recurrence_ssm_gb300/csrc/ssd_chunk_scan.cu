@@ -1348,8 +1348,11 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
         const float e = ex2(sm.tot[p]), ef = ex2(sm.cum[p][t]);
         const bool has_s = c > 0 || has_h0;
         // the chunk state and Y of tile c in one round trip
+        // (with N = 64 the lanes of quarters 2, 3 hold S_c rows 64..127, which
+        // are exact zeros -- the B operand's upper rows are zero: their state
+        // stays zero, and loading it keeps the code the same for every warp)
         uint32_t sv[32], yv[32], zf[32];
-        if (is_state) tmem_ld32_async(tmem + lane_base + kWsS + hf * 32, sv);
+        tmem_ld32_async(tmem + lane_base + kWsS + hf * 32, sv);
         tmem_ld32_async(tmem + lane_base + ((c & 1) ? kWsY1 : kWsY0) + hf * 32, yv);
         tmem_wait_tie(yv);
         reg_tie(sv);
@@ -1358,11 +1361,9 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
         WS_WAIT_I(sm.bar_z[c & 1], ph_z, c & 1);    // Zf(c) done: the state image is free
         tc_fence_after_sync();
         // state passing: rows n = t of S_in, columns of half hf
-        if (is_state) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) st[j] = fmaf(e, st[j], __uint_as_float(sv[j]));
-            if (more) put_state_half(&sm.S[0][0], t, hf, st);
-        }
+        for (int j = 0; j < 32; ++j) st[j] = fmaf(e, st[j], __uint_as_float(sv[j]));
+        if (is_state && more) put_state_half(&sm.S[0][0], t, hf, st);
         if (more) {
             fence_proxy_async_smem();
             tc_fence_before_sync();
