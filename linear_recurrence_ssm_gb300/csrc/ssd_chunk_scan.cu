@@ -1243,16 +1243,15 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
         mbar_arrive(&sm.bar_mfull);
     };
     const bool gate = GATE && cx.prm.z != nullptr;
-    // gate row of tile c (bf16, 32 values), loaded in iteration c after the
-    // mask of tile c + 1 is formed (the registers are not held through the
-    // mask phase) and used by the epilogue of tile c
-    uint4 zq[4];
+    // gate row of tile c (bf16, 32 values = 64 bytes): prefetched into L1 in
+    // iteration c after the mask of tile c + 1 is formed, and read in the
+    // epilogue of tile c, so that no registers hold it through the state update
+    auto gate_row = [&](int c) {
+        return reinterpret_cast<const uint4 *>(cx.prm.z + ((size_t(b) * L + c * kQ + t) * H + h) * kP + hf * 32);
+    };
     auto load_gate = [&](int c) {
-        const int row = c * kQ + t;
-        if (!gate || row >= L) return;
-        const uint4 *zp = reinterpret_cast<const uint4 *>(cx.prm.z + ((size_t(b) * L + row) * H + h) * kP + hf * 32);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) zq[j] = __ldg(zp + j);
+        if (!gate || c * kQ + t >= L) return;
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(gate_row(c)));
     };
     // Output rows t of tile c, columns of half hf, from the loaded
     // accumulators: y = Y + e^{cum_t} Zf (Y already holds D x), out through
@@ -1277,6 +1276,10 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
             for (int j = 0; j < 32; ++j) out[j] = __uint_as_float(yv[j]);
         }
         if (gate && c * kQ + t < L) {   // (rows past L are computed but not stored)
+            const uint4 *zp = gate_row(c);
+            uint4 zq[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) zq[j] = __ldg(zp + j);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t w4[4] = {zq[j].x, zq[j].y, zq[j].z, zq[j].w};
