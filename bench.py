@@ -445,7 +445,9 @@ def resident_sets(w, host, dev, per_set: int):
 
 def time_steps(step, stream, dev, steps: int, warmup: int) -> float:
     """Milliseconds for `steps` back-to-back steps, CUDA events on the
-    launching stream, synchronised on both sides."""
+    launching stream, synchronised on both sides; raises if a kernel gave up
+    a bounded wait meanwhile (its output would be wrong)."""
+    import linear_recurrence_ssm_gb300 as lrs
     import torch
     for i in range(max(3, warmup)):
         step(i)
@@ -457,6 +459,7 @@ def time_steps(step, stream, dev, steps: int, warmup: int) -> float:
         step(k)
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    lrs.ssm_check_device_errors(dev)
     return e0.elapsed_time(e1)
 
 
@@ -589,6 +592,7 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize(dev)
     sampler.stop()
     clocks = sampler.summary(t_wall0 - 0.6, t_wall1 + 0.4)
+    lrs.ssm_check_device_errors(dev)   # no kernel gave up a bounded wait
 
     # End to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory, makes the call and copies y back to
@@ -644,6 +648,7 @@ def run_ours(args, rank, world, local):
         stream.wait_stream(s_out)
         f1.record(stream)
     torch.cuda.synchronize(dev)
+    lrs.ssm_check_device_errors(dev)
     ms_e2e = f0.elapsed_time(f1) if k_e2e else float("nan")
 
     ms, ms_e2e = max_over_ranks([ms, ms_e2e], world, dev)

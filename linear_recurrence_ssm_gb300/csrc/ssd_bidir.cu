@@ -301,6 +301,7 @@ struct __align__(1024) OutSmem {
     uint64_t bar_g, bar_y[2], bar_z[2];                  // products finished
     uint64_t bar_gfree, bar_mfull, bar_zfree, bar_st[2], bar_sbfree;   // math -> issue / copy
     uint64_t bar_vec[kSlots], bar_fin[2];
+    uint64_t bar_slot[kSlots];                           // math warps done with a vector slot
     uint32_t tmem_base;
 };
 
@@ -507,14 +508,19 @@ __device__ __forceinline__ bool loader_role(Ctx &cx, const CUtensorMap *tmC, con
 // Per-tile vectors up to two tiles ahead (lane l: rows 4 l .. 4 l + 3):
 // cumulative sums of dt A (log2 units), their exclusive form, dt, the column
 // factors of the off-diagonal mask blocks in both directions, the total.
-// Slot k % 3 held tile k - 3, last read before the mask store of tile k - 2.
+// Slot k % 3 held tile k - 3: the math warps signal their last read of it on
+// the slot's own barrier.  (A parity wait on the mask stores instead could
+// alias: with this warp held up -- by a slow dt load, say -- the math warps
+// could complete the stores of tiles k - 2 and k - 1 first, and the wait for
+// the first would then wait for the store of tile k, which needs this warp.
+// A slot's barrier cannot complete again before this warp writes the slot.)
 template <bool EXT>
 __device__ __forceinline__ bool vector_role(Ctx &cx) {
     auto &sm = cx.sm;
     const Params &prm = cx.prm;
     const int lane = threadIdx.x & 31;
     const int nk = cx.nk, L = prm.L, H = prm.H;
-    uint32_t ph_mfull = 0;
+    uint32_t ph_slot = 0;   // one bit per slot
     float raw[4], nxt[4];
     auto load = [&](int k, float (&rr)[4]) {
         const Unit un = unit_of(prm, k);
@@ -528,11 +534,11 @@ __device__ __forceinline__ bool vector_role(Ctx &cx) {
     load(0, raw);
     for (int k = 0; k < nk; ++k) {
         if (k + 1 < nk) load(k + 1, nxt);
-        if (k >= 2) BI_WAIT(sm.bar_mfull, ph_mfull);   // mask store of tile k - 2 complete
+        const int p = k % kSlots;
+        if (k >= kSlots) BI_WAIT_I(sm.bar_slot[p], ph_slot, p);   // tile k - 3 done with slot p
         const Unit un = unit_of(prm, k);
         const float Ah = prm.A[un.h] * SSM_LOG2E;
         const float bias = (EXT && prm.dt_bias) ? prm.dt_bias[un.h] : 0.0f;
-        const int p = k % kSlots;
         float dv[4], cs[4], da[4], run = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -741,12 +747,16 @@ __device__ __forceinline__ bool math_role(Ctx &cx, const CUtensorMap *tmY) {
     for (int k = 0; k < nk; ++k) {
         const bool more = k + 1 < nk;
         const Unit un = unit_of(prm, k);
+        if (gate && un.c * kQ + t < L)   // the gate row of tile k, read by its epilogue below
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(
+                prm.z + ((size_t(un.b) * L + un.c * kQ + t) * H + un.h) * kP + hf * 32));
         if (more && !mask(k + 1)) return false;
         BI_WAIT_I(sm.bar_y[k & 1], ph_y, k & 1);   // G(k), Y(k) done
         BI_WAIT_I(sm.bar_z[k & 1], ph_z, k & 1);   // Z(k) done
         tc_fence_after_sync();
         const int p = k % kSlots;
         const float ef = ex2(sm.cum[p][t]), er = ex2(sm.tot[p] - sm.excl[p][t]);
+        arrive(&sm.bar_slot[p]);             // tile k's vectors are read for the last time
         uint32_t yv[32], zf[32], zr[32];
         tmem_ld32_async(tmem + lane_base + ((k & 1) ? kColY1 : kColY0) + hf * 32, yv);
         tmem_ld32_async(tmem + lane_base + kColZ + hf * 32, zf);
@@ -829,7 +839,10 @@ bidir_out_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         mbar_init(&sm.bar_sbfree, kMath);
         mbar_init(&sm.bar_fin[0], 1);
         mbar_init(&sm.bar_fin[1], 1);
-        for (int i = 0; i < kSlots; ++i) mbar_init(&sm.bar_vec[i], 32);
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&sm.bar_vec[i], 32);
+            mbar_init(&sm.bar_slot[i], kMath);
+        }
         mbar_fence_init();
         prefetch_tmap(&tmC);
         prefetch_tmap(&tmB);

@@ -752,7 +752,7 @@ struct __align__(1024) Smem {
     // the copying thread is the only waiter on bar_m2 that nothing else holds
     // back; each of the others completes again only after its waiters moved on.
     uint64_t bar_g, bar_m2[2], bar_z[2];
-    uint64_t bar_gfree, bar_mfull, bar_xw[2], bar_st;
+    uint64_t bar_gfree, bar_mfull[2], bar_xw[2], bar_st;   // bar_mfull[c & 1]: mask of tile c stored
     uint64_t bar_vec[kSlots];                        // vectors of a slot written
     uint64_t bar_pair[4];                            // the two warps of a lane quarter: their
                                                      //   output stores have read the staging
@@ -933,10 +933,10 @@ __device__ __forceinline__ bool issuer_ys_role(Ctx<NB> &cx) {
     const uint32_t tmem = cx.tmem;
     constexpr uint32_t idY = idesc_bf16_f32(128, 64, false, true);
     constexpr uint32_t idS = idesc_bf16_f32(128, 64, true, true);
-    uint32_t ph_mfull = 0, ph_xw = 0, ph_x = 0;   // ph_xw, ph_x: one bit per buffer
+    uint32_t ph_mfull = 0, ph_xw = 0, ph_x = 0;   // one bit per buffer
     for (int c = 0; c < nc; ++c) {
         const int xb = c % kXBufs, yp = c & 1;
-        WS_WAIT(sm.bar_mfull, ph_mfull);
+        WS_WAIT_I(sm.bar_mfull[yp], ph_mfull, yp);
         WS_WAIT_I(sm.bar_xw[yp], ph_xw, yp);
         WS_WAIT_I(sm.bar_x[xb], ph_x, xb);
         tc_fence_after_sync();
@@ -1012,14 +1012,20 @@ __device__ __forceinline__ bool loader_role(Ctx<NB> &cx, const CUtensorMap *tmC,
 // off-diagonal mask blocks and the tile total.  Lane l holds rows 4 l ..
 // 4 l + 3.  Slot c % 3 held tile c - 3, which the math warps last read right
 // after m2(c - 3) and before their mask store of tile c - 2: the vectors of
-// tile c are written once that store is complete everywhere.
+// tile c are written once that store is complete everywhere.  The mask
+// stores alternate between two barriers, so that this wait cannot alias: the
+// barrier of tile c - 2 completes next with the store of tile c, which needs
+// the vectors this warp is about to write.  (With one barrier a parity wait
+// could: were this warp held up, by a slow dt load say, the stores of tiles
+// c - 2 and c - 1 could both complete first, and the wait would then stand
+// for the store of tile c.)
 template <int NB, bool EXT>
 __device__ __forceinline__ bool vector_role(Ctx<NB> &cx) {
     auto &sm = cx.sm;
     const int lane = threadIdx.x & 31;
     const int nc = cx.nc, L = cx.L, H = cx.prm.H;
     const __nv_bfloat16 *dtp = cx.prm.dt + (int64_t(cx.b) * L) * H + cx.h;
-    uint32_t ph_mfull = 0;
+    uint32_t ph_mfull = 0;   // one bit per mask barrier
     float raw[4], nxt[4];
     auto load = [&](int c, float (&r)[4]) {    // raw dt of rows c kQ + 4 lane + k; past L: 0
 #pragma unroll
@@ -1031,7 +1037,7 @@ __device__ __forceinline__ bool vector_role(Ctx<NB> &cx) {
     load(0, raw);
     for (int c = 0; c < nc; ++c) {
         if (c + 1 < nc) load(c + 1, nxt);
-        if (c >= 2) WS_WAIT(sm.bar_mfull, ph_mfull);   // mask store of tile c - 2 complete
+        if (c >= 2) WS_WAIT_I(sm.bar_mfull[c & 1], ph_mfull, c & 1);   // mask of tile c - 2 stored
         const int p = c % kSlots;
         float dv[4], cs[4], run = 0.0f;
 #pragma unroll
@@ -1230,7 +1236,7 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     };
     // Store this warp's mask blocks into tensor memory (after Y of the
     // previous tile has read the mask) and hand the mask to the issuer.
-    auto mask_store = [&]() {
+    auto mask_store = [&](int c) {
         if (hf == 0) {
             tmem_st_32x32b_x16(tmem + lane_base + kWsM + q * 16, mk[0]);
         } else {
@@ -1240,7 +1246,7 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
         }
         tmem_wait_st();
         tc_fence_before_sync();
-        mbar_arrive(&sm.bar_mfull);
+        mbar_arrive(&sm.bar_mfull[c & 1]);
     };
     const bool gate = GATE && cx.prm.z != nullptr;
     // gate row of tile c (bf16, 32 values = 64 bytes): prefetched into L1 in
@@ -1339,7 +1345,7 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
     fence_proxy_async_smem();
     mbar_arrive(&sm.bar_st);
     if (!weigh_and_mask(0)) return false;
-    mask_store();
+    mask_store(0);
 
     for (int c = 0; c < nc; ++c) {
         const bool more = c + 1 < nc;
@@ -1360,7 +1366,7 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
         tmem_wait_tie(yv);
         reg_tie(sv);
         // S_c(c) is in registers: Y(c + 1) and S_c(c + 1) may start
-        if (more) mask_store();
+        if (more) mask_store(c + 1);
         WS_WAIT_I(sm.bar_z[c & 1], ph_z, c & 1);    // Zf(c) done: the state image is free
         tc_fence_after_sync();
         // state passing: rows n = t of S_in, columns of half hf
@@ -1414,7 +1420,7 @@ ssd_ws_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         mbar_init(&sm.bar_fin[0], 1);
         mbar_init(&sm.bar_fin[1], 1);
         mbar_init(&sm.bar_gfree, kMath);
-        mbar_init(&sm.bar_mfull, kMath);
+        for (int i = 0; i < 2; ++i) mbar_init(&sm.bar_mfull[i], kMath);
         mbar_init(&sm.bar_xw[0], kMath);
         mbar_init(&sm.bar_xw[1], kMath);
         mbar_init(&sm.bar_st, kMath);
