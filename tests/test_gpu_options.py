@@ -209,3 +209,33 @@ def test_ssd_groups_with_options(cuda_device):
     torch.cuda.synchronize()
     _close(y, ref, "bf16", "y")
     _close(hf, href, "bf16", "h_final")
+
+
+@pytest.mark.parametrize("Bs,L,H,N,chunk,bidir,calls", [
+    (4, 4096, 32, 128, 256, False, 800),   # the SSD benchmark shape
+    (32, 400, 8, 64, 128, True, 2000),     # the short bidirectional benchmark shape
+])
+def test_ssd_repeated_calls_with_options_stay_exact(cuda_device, Bs, L, H, N, chunk, bidir, calls):
+    """Back-to-back calls at a benchmark shape, with every option the
+    direction allows: no kernel gives up a bounded wait, and every call
+    writes the same bits.  The hand-offs between a kernel's warp roles must
+    not depend on how far one role runs ahead of another (a parity wait that
+    could alias showed up as an abandoned wait about once in 2000 calls)."""
+    inp, opt = _ssd_case(Bs, L, H, N, seed=5)
+    d = _dev(inp, cuda_device)
+    kw = dict(chunk=chunk, bidirectional=bidir, dt_bias=opt["dt_bias"].to(cuda_device),
+              dt_softplus=True, dt_limit=LIMIT, z=opt["z"].to(cuda_device))
+    if not bidir:
+        kw.update(h0=opt["h0"].to(cuda_device))
+    y = torch.empty(Bs, L, H, 64, dtype=torch.float32, device=cuda_device)
+    lrs.ssd_chunk_scan_fwd(**d, y=y, **kw)
+    y0 = y.clone()
+    for i in range(calls):
+        if i % 100 == 0:
+            y.fill_(float("nan"))   # a call that wrote nothing cannot pass
+        lrs.ssd_chunk_scan_fwd(**d, y=y, **kw)
+        if i % 100 == 99:
+            assert torch.equal(y, y0), "call %d differs from the first" % i
+    lrs.ssm_check_device_errors(cuda_device)
+    assert torch.equal(y, y0)
+    assert bool(torch.isfinite(y0).all())
