@@ -88,10 +88,11 @@ struct DeviceInfo {
     int num_sms = 0;
 };
 
-std::once_flag g_dev_once[kMaxDevices];
+std::mutex g_dev_mutex;
+bool g_dev_known[kMaxDevices];   // set only once the attribute queries succeeded
 DeviceInfo g_dev[kMaxDevices];
 
-// Device attributes, queried once per device.  A device that is not
+// Device attributes, kept per device once a query has succeeded.  A device that is not
 // compute capability 10.3 cannot run this library's sm_103a code.
 ssm_status_t current_device(DeviceInfo *out) {
     int dev = -1;
@@ -99,15 +100,21 @@ ssm_status_t current_device(DeviceInfo *out) {
         cudaGetLastError();
         return SSM_ERR_NO_DEVICE;
     }
-    std::call_once(g_dev_once[dev], [dev]() {
-        int major = 0, minor = 0, sms = 0;
-        bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
-                  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
-                  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
-        g_dev[dev].ok = ok && major == 10 && minor == 3;
-        g_dev[dev].num_sms = sms;
-    });
-    *out = g_dev[dev];
+    {
+        // a failed query is not kept: the next call asks again
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        if (!g_dev_known[dev]) {
+            int major = 0, minor = 0, sms = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return SSM_ERR_NO_DEVICE;
+            g_dev[dev].ok = major == 10 && minor == 3;
+            g_dev[dev].num_sms = sms;
+            g_dev_known[dev] = true;
+        }
+        *out = g_dev[dev];
+    }
     return out->ok ? SSM_OK : SSM_ERR_NO_DEVICE;
 }
 

@@ -30,6 +30,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ssm_common.cuh"
@@ -893,17 +894,20 @@ bidir_out_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
 // ===========================================================================
 // Host side
 // ===========================================================================
+// The driver's tensor-map encoder.  Only a successful lookup is kept: after
+// a failed one the next call asks the driver again.
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, []() {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &qr) == cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_acquire);
+    if (fn != nullptr) return fn;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess) {
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cached.store(fn, std::memory_order_release);
+    }
     return fn;
 }
 
