@@ -1159,16 +1159,20 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
         const float *cum = sm.cum[p];
         const float *dtv = sm.dtv[p];
         const float *csf = sm.csf[p];
+        const float cum_t = cum[t];
+        // The first G block of this warp (half 0: the diagonal block; half 1:
+        // block 0, when the quarter has blocks below the diagonal) loads
+        // while the x rows are weighed: one weighing call site for both halves.
+        uint32_t ga[32];
+        const bool ld0 = hf == 0 || q >= 1;
+        if (ld0) tmem_ld32_async(tmem + lane_base + kWsG + (hf == 0 ? q * 32 : 0), ga);
+        if (!weigh(c)) return false;
+        if (ld0) tmem_wait_tie(ga);
         if (hf == 0) {
-            uint32_t gr[32];
-            tmem_ld32_async(tmem + lane_base + kWsG + q * 32, gr);
-            if (!weigh(c)) return false;
-            tmem_wait_tie(gr);
             tc_fence_before_sync();
             mbar_arrive(&sm.bar_gfree);     // G may be overwritten now
             // diagonal block: direct differences of cumulative sums; the
             // skip term rides on the diagonal: Y = (M + D_h I) X
-            const float cum_t = cum[t];
             const float4 *c4 = reinterpret_cast<const float4 *>(cum + q * 32);
             const float4 *d4 = reinterpret_cast<const float4 *>(dtv + q * 32);
 #pragma unroll
@@ -1181,7 +1185,7 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
                 for (int k = 0; k < 4; ++k) {
                     const int j = 4 * j4 + k;
                     const float w = (j <= lane) ? ex2(cum_t - csv[k]) : 0.0f;
-                    float v = __uint_as_float(gr[j]) * (w * dsv[k]);
+                    float v = __uint_as_float(ga[j]) * (w * dsv[k]);
                     if (j == lane) v += cx.Dh;
                     m[k] = v;
                 }
@@ -1191,7 +1195,6 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
         } else {
             // blocks below the diagonal: G * (row factor) * (column factor),
             // both <= 1; the G rows of block i + 1 load while block i is formed
-            const float cum_t = cum[t];
             auto offdiag = [&](int i, const uint32_t (&g)[32]) {
                 const float e = ex2(cum_t - cum[i * 32 + 31]);
                 const float2 ee = make_float2(e, e);
@@ -1207,10 +1210,7 @@ __device__ __forceinline__ bool math_role(Ctx<NB> &cx, bool has_h0) {
                     mk[i][2 * j4 + 1] = pack_bf16(bq.x, bq.y);
                 }
             };
-            uint32_t ga[32], gb[32];
-            if (q >= 1) tmem_ld32_async(tmem + lane_base + kWsG, ga);
-            if (!weigh(c)) return false;
-            if (q >= 1) tmem_wait_tie(ga);
+            uint32_t gb[32];
             if (q >= 2) tmem_ld32_async(tmem + lane_base + kWsG + 32, gb);
             if (q < 2) {
                 tc_fence_before_sync();
