@@ -715,12 +715,13 @@ __device__ __forceinline__ bool math_role(Ctx &cx, const CUtensorMap *tmY) {
                 mkd[2 * j4 + 1] = pack_bf16(m[2], m[3]);
             }
         }
+        // one call site for the first off-diagonal block of either half
         if (hf == 0) {
             tc_fence_before_sync();
             arrive(&sm.bar_gfree);
-            offdiag(0, ob0, ga);
-        } else {
-            offdiag(0, ob1, ga);
+        }
+        offdiag(0, hf == 0 ? ob0 : ob1, ga);
+        if (hf == 1) {
             tmem_wait_tie(gb);
             tc_fence_before_sync();
             arrive(&sm.bar_gfree);
@@ -730,12 +731,8 @@ __device__ __forceinline__ bool math_role(Ctx &cx, const CUtensorMap *tmY) {
     };
     auto mask_store = [&]() {
         tmem_st_32x32b_x8(tmem + lane_base + kColM + q * 16 + hf * 8, mkd);
-        if (hf == 0) {
-            tmem_st_32x32b_x16(tmem + lane_base + kColM + ob0 * 16, mk[0]);
-        } else {
-            tmem_st_32x32b_x16(tmem + lane_base + kColM + ob1 * 16, mk[0]);
-            tmem_st_32x32b_x16(tmem + lane_base + kColM + ob2 * 16, mk[1]);
-        }
+        tmem_st_32x32b_x16(tmem + lane_base + kColM + (hf == 0 ? ob0 : ob1) * 16, mk[0]);
+        if (hf == 1) tmem_st_32x32b_x16(tmem + lane_base + kColM + ob2 * 16, mk[1]);
         tmem_wait_st();
         tc_fence_before_sync();
         arrive(&sm.bar_mfull);
